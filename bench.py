@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the Q8_0 Llama forward on GB300.
+
+Workload (one "step"): the 135M-shaped Q8_0 Llama with random weights
+(seed 0), a fresh KV cache, one 203-token prefill of uniform random ids, then
+128 greedy decode steps — the task of the candle page "速度"
+(两边量的是同一件事: 203-token prefill + 128 greedy decode steps, repeated
+with a fresh cache). The headline metric is decode tokens/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl ours (default): the CUDA library; device-timed with CUDA events on the
+library's stream, inputs resident in HBM; plus an end-to-end number through
+the host API, per-kernel timing, the 7B-shape GEMV roofline and the CPU
+oracle baseline. --impl reference: the CPU oracle on this host's cores on the
+same workload, each step a bounded sample (prefill + a few decode steps).
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the model does not shard); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s + ms/token; Q8_0 GEMV HBM GB/s vs peak (Q8_0 Llama, 1 GB300)"
+PROMPT_LEN = 203
+DECODE_STEPS = 128
+SEED = 0
+# The pages' number for this task and metric: Q8_0 decode 7.40 ms/token on an
+# M2 Max CPU ("速度", CPU GGUF：decode 快，prefill 慢). Context, not the target.
+PAGES_DECODE_MS = 7.40
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2 ** 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# multi-rank plumbing (replicas)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (x itself at world == 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, elapsed_s: float, world: int, device=None) -> tuple[float, float]:
+    """Whole-job throughput: units of all ranks / the slowest rank's time."""
+    t = max_over_ranks(elapsed_s, world, device)
+    return units_per_rank * world / t, t
+
+
+# ----------------------------------------------------------------------------
+# peaks and clocks
+# ----------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d:
+                    v = d[key]
+                    return float(v["value"] if isinstance(v, dict) else v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"lq8_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        try:
+            self.fh.close()
+        except Exception:
+            pass
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle legs
+# ----------------------------------------------------------------------------
+
+def oracle_model():
+    from oracle import q8_oracle as O
+    from q8_quantized_llama_gb300 import synth
+    cfg = dict(synth.MODEL_135M)
+    t = {}
+    for name, w, kind in synth.iter_model_weights_f32(cfg, SEED):
+        t[name] = O.quantize_q8_0(w) if kind == "matrix" else w
+    return O, cfg, O.ModelWeights(cfg, t, weight_cache="f64")
+
+
+def oracle_step(O, model, prompt, n_decode):
+    """Prefill + n_decode greedy steps on the oracle; returns (prefill_s, decode_s)."""
+    t0 = time.perf_counter()
+    logits = model.forward(prompt, 0)
+    t1 = time.perf_counter()
+    nxt = O.argmax_lowest(logits)
+    pos = len(prompt)
+    for _ in range(n_decode):
+        nxt = O.argmax_lowest(model.forward([nxt], pos))
+        pos += 1
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def cpu_baseline_worker(seconds: float):
+    """Runs in a fresh interpreter: the oracle on a bounded sample of the workload."""
+    from q8_quantized_llama_gb300 import synth
+    O, cfg, model = oracle_model()
+    prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
+    t_start = time.perf_counter()
+    p_s, _ = oracle_step(O, model, prompt, 0)
+    nxt = O.argmax_lowest(model.forward(prompt, 0))
+    pos, n, d_s = PROMPT_LEN, 0, 0.0
+    while n < DECODE_STEPS and time.perf_counter() - t_start < seconds:
+        t0 = time.perf_counter()
+        nxt = O.argmax_lowest(model.forward([nxt], pos))
+        d_s += time.perf_counter() - t0
+        pos += 1
+        n += 1
+    print(json.dumps({"value": n / d_s, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                      "prefill_tok_s": PROMPT_LEN / p_s,
+                      "sample": f"135M Q8_0 oracle (numpy f64): one 203-token prefill and the first {n} of the "
+                                f"128 greedy decode steps"}))
+
+
+def run_cpu_baseline(seconds: float):
+    env = dict(os.environ)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
+                        "--cpu-baseline-seconds", str(seconds)], capture_output=True, text=True, env=env,
+                       timeout=600)
+    for line in r.stdout.splitlines()[::-1]:
+        if line.startswith("{"):
+            return json.loads(line)
+    return {"value": None, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": "failed: " + r.stderr[-300:]}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from q8_quantized_llama_gb300 import synth
+    O, cfg, model = oracle_model()
+    prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
+    n_dec = 2
+    for _ in range(args.warmup):
+        oracle_step(O, model, prompt, n_dec)
+    pre, dec = [], []
+    for _ in range(args.steps):
+        p_s, d_s = oracle_step(O, model, prompt, n_dec)
+        pre.append(p_s)
+        dec.append(d_s)
+    value = n_dec * args.steps / sum(dec)
+    sample = (f"135M Q8_0 oracle (numpy f64) per step: one 203-token prefill + the first {n_dec} of the 128 "
+              f"greedy decode steps")
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1000 * (sum(pre) + sum(dec)) / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": "135M-shaped Q8_0 Llama seed 0, 203-token random prompt prefill + greedy decode",
+                      "prompt": PROMPT_LEN, "decode_steps_per_step": n_dec},
+           "decode_ms_per_token": 1000 * sum(dec) / (n_dec * args.steps),
+           "prefill_tok_s": PROMPT_LEN * args.steps / sum(pre),
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def gpu_model(torch, B, synth, device):
+    cfg = dict(synth.MODEL_135M)
+    t = {}
+    for name, w, kind in synth.iter_model_weights_f32(cfg, SEED):
+        dw = torch.from_numpy(w).to(device)
+        if kind == "matrix":
+            q = torch.empty((w.shape[0], w.shape[1] // 32 * 34), dtype=torch.uint8, device=device)
+            B.llama_q8_quantize(dw, w.shape[0], w.shape[1], q, torch.cuda.current_stream().cuda_stream)
+            t[name] = q
+        else:
+            t[name] = dw
+    torch.cuda.synchronize()
+    model = B.Model(cfg, t, device=device.index, on_device=True)
+    del t
+    torch.cuda.empty_cache()
+    return cfg, model
+
+
+def gemv_7b_roofline(torch, B, synth, device, peak):
+    """The Q8_0 GEMV at the 7B shape [1,4096]x[4096,14336], timed with CUDA
+    events over back-to-back launches that rotate through 8 weight copies
+    (8 x 62.4 MB > L2), so every launch streams its matrix from HBM."""
+    rows, k = 14336, 4096
+    w = synth.weight_matrix_f32(rows, k, 1)
+    dw = torch.from_numpy(w).to(device)
+    q = torch.empty((rows, k // 32 * 34), dtype=torch.uint8, device=device)
+    B.llama_q8_quantize(dw, rows, k, q)
+    nbytes = B.llama_q8_packed_bytes(rows, k)
+    copies = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(8)]
+    for c in copies:
+        B.llama_q8_pack(q, rows, k, c)
+    del dw, q
+    x = torch.from_numpy(synth.normal_f32((1, k), 1, 7)).to(device)
+    y = torch.empty((1, rows), dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream()
+    for i in range(16):
+        B.llama_q8_matmul(copies[i % 8], rows, k, x, 1, y, s.cuda_stream)
+    n = 400
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for i in range(n):
+        B.llama_q8_matmul(copies[i % 8], rows, k, x, 1, y, s.cuda_stream)
+    e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000 / n
+    algo = rows * k * 34 / 32 + 4 * k + 4 * rows
+    gbs = algo / (us * 1e-6) / 1e9
+    del copies
+    torch.cuda.empty_cache()
+    return {"kernel": "q8_gemv_kernel<EPI_STORE>", "shape": "[1,4096]x[4096,14336]", "us": us,
+            "algorithmic_bytes": algo, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        dist_init(world, "nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from q8_quantized_llama_gb300 import binding as B
+    from q8_quantized_llama_gb300 import synth
+    B.lib()
+    peak, peak_kind = hbm_peak()
+    cfg, model = gpu_model(torch, B, synth, device)
+    prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
+    d_prompt = torch.from_numpy(prompt).to(device)
+    d_next = torch.zeros(1, dtype=torch.int32, device=device)
+    d_out = torch.zeros(DECODE_STEPS, dtype=torch.int32, device=device)
+    stream = torch.cuda.ExternalStream(model.stream(), device=device)
+
+    def one_step():
+        model.prefill_async(d_prompt, PROMPT_LEN, 0, d_next)
+        model.decode_async(DECODE_STEPS, d_out)
+
+    for _ in range(args.warmup):
+        one_step()
+    model.sync()
+    ref_tokens = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches0 = model.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            model.prefill_async(d_prompt, PROMPT_LEN, 0, d_next)
+            ev[i][1].record(stream)
+            model.decode_async(DECODE_STEPS, d_out)
+            ev[i][2].record(stream)
+        model.sync()
+        torch.cuda.synchronize()
+    barrier(world)
+    gpu_launches = model.launch_count() - launches0
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(pre_ms) + sum(dec_ms)
+    tokens = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
+    assert np.array_equal(tokens, ref_tokens), "decode tokens changed between repetitions"
+    value, t_max = aggregate_throughput(DECODE_STEPS * args.steps, sum(dec_ms) / 1000, world, device)
+    clk = clocks.summary()
+
+    # end to end through the host API: the pages' loop, one synchronous call per token
+    e2e_dec = []
+    for i in range(args.warmup + args.steps):
+        nxt = model.forward_argmax(prompt, 0)
+        t0 = time.perf_counter()
+        pos = PROMPT_LEN
+        for _ in range(DECODE_STEPS):
+            nxt = model.forward_argmax([nxt], pos)
+            pos += 1
+        if i >= args.warmup:
+            e2e_dec.append(time.perf_counter() - t0)
+    e2e_value, _ = aggregate_throughput(DECODE_STEPS * args.steps, sum(e2e_dec), world, device)
+
+    # per-kernel timing of the decode step (eager launches with event pairs)
+    model.forward_argmax(prompt, 0)
+    prof = model.profile_decode(DECODE_STEPS)
+    step_ms = sum(v[1] for v in prof.values()) / DECODE_STEPS
+    dom_name = max(prof, key=lambda k: prof[k][1])
+    dl, dms, dbytes = prof[dom_name]
+    dom_gbs = (dbytes / dl) / (dms / dl * 1e-3) / 1e9
+    weights_bytes = sum(v[2] for k, v in prof.items() if k != "attn_decode") / DECODE_STEPS
+    kv_bytes = prof["attn_decode"][2] / DECODE_STEPS
+
+    out = None
+    if rank == 0:
+        gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
+        dec_tok_ms = [d / DECODE_STEPS for d in dec_ms]
+        out = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": value / (1000.0 / PAGES_DECODE_MS),
+            "vs_baseline_ref": "pages' M2 Max CPU Q8_0 decode, 7.40 ms/token (context only)",
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "135M-shaped Q8_0 Llama (30x576, 9/3 heads, FFN 1536, vocab 49152, seed 0): "
+                                   "203-token random prompt prefill + 128 greedy decode steps, fresh KV cache",
+                       "prompt": PROMPT_LEN, "decode_steps": DECODE_STEPS,
+                       "l2": "inputs larger than L2: each decode step streams 142.9 MB of Q8_0 weights"},
+            "decode_ms_per_token": {"min": min(dec_tok_ms), "median": statistics.median(dec_tok_ms)},
+            "prefill_ms": {"min": min(pre_ms), "median": statistics.median(pre_ms)},
+            "prefill_tok_s": PROMPT_LEN * args.steps / (sum(pre_ms) / 1000),
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "path": "llama_q8_forward_argmax per token (host ids in, host token out, one sync per token)",
+                    "h2d_bytes_per_step": 4 * (PROMPT_LEN + DECODE_STEPS),
+                    "d2h_bytes_per_step": 16 * (1 + DECODE_STEPS)},
+            "gpu_launches": gpu_launches,
+            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": dom_gbs / peak, "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "traffic": None,
+                         "note": "algorithmic bytes per launch / mean event-timed launch duration, eager decode"},
+            "decode_step_roofline": {"weights_bytes": weights_bytes, "kv_bytes_mean": kv_bytes,
+                                     "roofline_us": (weights_bytes + kv_bytes) / (peak * 1e9) * 1e6,
+                                     "graph_step_us": 1000 * statistics.median(dec_tok_ms),
+                                     "frac": ((weights_bytes + kv_bytes) / (peak * 1e9) * 1e6)
+                                     / (1000 * statistics.median(dec_tok_ms))},
+            "kernels": {k: {"launches": v[0], "ms": v[1], "gbs": (v[2] / (v[1] * 1e-3) / 1e9) if v[1] else None,
+                            "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items()},
+            "gemv_7b": gemv7,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)
+    model.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out))
+
+
+def main():
+    args = parse_args()
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker(args.cpu_baseline_seconds)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+/*
+ * llama_q8.h — C ABI of the GB300 (sm_103a) Q8_0 Llama forward.
+ *
+ * One forward pass of a Q8_0-quantised Llama, as described on the candle
+ * 0.11.0 documentation pages "量化 llama 的一次前向" (quantized-llama),
+ * "生成一个 token" (one-token) and "速度" (speed):
+ *   - ModelWeights::from_gguf keeps the projections in Q8_0, dequantises the
+ *     embedding, and uses the embedding as the output head when the file has
+ *     no output.weight ("生成一个 token", section 建模型：按名字取张量);
+ *   - forward(ids, index_pos) returns logits for the last position only,
+ *     builds a causal mask only when T > 1, drops the KV cache when
+ *     index_pos == 0 and appends to it otherwise ("量化 llama 的一次前向",
+ *     sections forward：mask 什么时候建 and forward_attn：自己拼 KV);
+ *   - the rotary table holds 4096 positions and index_pos + T > 4096 is an
+ *     error (same page, section from_gguf：键名写死了 llama.);
+ *   - clear_kv_cache drops the cache (same page, section 换 prompt 要不要
+ *     clear_kv_cache).
+ *
+ * Conventions for every call:
+ *   - Every call returns a llama_q8_status. On any error nothing is launched
+ *     and the context state (cached length, KV cache) is unchanged, except
+ *     LQ8_ERR_CUDA, after which the context only accepts llama_q8_free.
+ *   - "host" pointers are ordinary or pinned CPU memory; "device" pointers
+ *     are CUDA device memory on the context's device. The caller owns every
+ *     pointer it passes; the library copies what it needs and keeps no
+ *     caller pointer after a call returns.
+ *   - Model calls run on the context's own CUDA stream and are synchronous
+ *     unless the name ends in _async (those enqueue and return).
+ *   - Batch size is 1 (the pages' forward ignores the batch dimension).
+ *   - Activations, the KV cache and logits are f32; weights are Q8_0.
+ *   - All kernels are written for sm_103a; there is no CPU fallback. A call
+ *     on a machine without such a GPU returns LQ8_ERR_CUDA.
+ */
+#ifndef LLAMA_Q8_H
+#define LLAMA_Q8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum llama_q8_status {
+    LQ8_OK = 0,
+    LQ8_ERR_ARG = 1,         /* NULL pointer, non-positive size, inconsistent config */
+    LQ8_ERR_POS = 2,         /* index_pos is neither 0 nor the number of cached positions */
+    LQ8_ERR_CTX = 3,         /* index_pos + T exceeds max_seq (4096 on the pages) */
+    LQ8_ERR_TOKEN = 4,       /* a token id outside [0, n_vocab) */
+    LQ8_ERR_CUDA = 5,        /* a CUDA runtime call or a kernel launch failed */
+    LQ8_ERR_OOM = 6,         /* device or pinned-host allocation failed */
+    LQ8_ERR_STATE = 7,       /* context already failed, or call order violated */
+    LQ8_ERR_UNSUPPORTED = 8  /* shape outside what the kernels implement */
+} llama_q8_status;
+
+/* Q8_0 block: 32 consecutive weights of one row along the input dimension,
+ * stored as an IEEE fp16 scale d (little-endian) followed by 32 int8 codes,
+ * 34 bytes; w = d * q. A [rows, k] matrix is rows * (k / 32) blocks, row-major.
+ * The pages fix the 34-bytes-per-32-weights size through the GGUF byte counts
+ * ("生成一个 token", 实验程序 and 读 GGUF; "速度", CPU GGUF). */
+#define LLAMA_Q8_BLOCK 32
+#define LLAMA_Q8_BLOCK_BYTES 34
+
+typedef struct llama_q8_config {
+    int32_t n_layer;      /* llama.block_count, 30 for the 135M model */
+    int32_t n_embd;       /* llama.embedding_length (hidden), multiple of 32 */
+    int32_t n_head;       /* llama.attention.head_count */
+    int32_t n_head_kv;    /* llama.attention.head_count_kv; n_head % n_head_kv == 0, ratio <= 8 */
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t n_ff;         /* llama.feed_forward_length, multiple of 32 */
+    int32_t n_vocab;
+    int32_t max_seq;      /* rotary table rows and KV capacity; the pages use 4096 */
+    float rms_eps;        /* 1e-5 */
+    float rope_theta;     /* 10000 */
+    int32_t tied_output;  /* 1: the head is token_embd (no output.weight) */
+} llama_q8_config;
+
+typedef struct llama_q8_layer_weights {
+    const float* attn_norm;   /* [n_embd] f32 */
+    const float* ffn_norm;    /* [n_embd] f32 */
+    const void* attn_q;       /* Q8_0 [n_head*head_dim, n_embd] */
+    const void* attn_k;       /* Q8_0 [n_head_kv*head_dim, n_embd] */
+    const void* attn_v;       /* Q8_0 [n_head_kv*head_dim, n_embd] */
+    const void* attn_output;  /* Q8_0 [n_embd, n_head*head_dim] */
+    const void* ffn_gate;     /* Q8_0 [n_ff, n_embd] */
+    const void* ffn_up;       /* Q8_0 [n_ff, n_embd] */
+    const void* ffn_down;     /* Q8_0 [n_embd, n_ff] */
+} llama_q8_layer_weights;
+
+typedef struct llama_q8_weights {
+    const void* token_embd;    /* Q8_0 [n_vocab, n_embd] */
+    const float* output_norm;  /* [n_embd] f32 */
+    const void* output;        /* Q8_0 [n_vocab, n_embd]; NULL when tied_output */
+    const llama_q8_layer_weights* layers;  /* host array of n_layer entries */
+    int32_t on_device;         /* 0: tensor pointers are host memory; 1: device memory */
+} llama_q8_weights;
+
+typedef struct llama_q8_ctx llama_q8_ctx;
+
+/* Build a context on CUDA device `device`: copy and repack every tensor into
+ * the library's device layout, build the rotary cos/sin table
+ * [max_seq, head_dim/2] (angle p * theta^(-2i/head_dim), computed in double,
+ * stored f32), allocate the KV cache [n_layer][n_head_kv][max_seq][head_dim]
+ * for K and for V, and create the context's stream. `*out` receives the
+ * context, owned by the caller until llama_q8_free. Errors: LQ8_ERR_ARG,
+ * LQ8_ERR_UNSUPPORTED, LQ8_ERR_OOM, LQ8_ERR_CUDA ("量化 llama 的一次前向",
+ * from_gguf). */
+llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights* w,
+                              int32_t device, llama_q8_ctx** out);
+
+/* forward(ids, index_pos): run T tokens (host ids[T]) starting at position
+ * index_pos and write the f32 logits of the LAST position to host
+ * logits[n_vocab]. index_pos == 0 drops the cache first; otherwise index_pos
+ * must equal the number of cached positions (LQ8_ERR_POS) — a deliberate
+ * tightening of the pages, where a wrong index_pos is silent when T == 1
+ * ("量化 llama 的一次前向", index_pos 传错). index_pos + T > max_seq gives
+ * LQ8_ERR_CTX; T <= 0 gives LQ8_ERR_ARG; an id outside [0, n_vocab) gives
+ * LQ8_ERR_TOKEN. Checked in that order: ARG, TOKEN, CTX, POS. T == 1 runs
+ * the captured CUDA-graph decode step; T > 1 runs the prefill kernels with
+ * the causal mask. */
+llama_q8_status llama_q8_forward(llama_q8_ctx* ctx, const int32_t* ids, int32_t T,
+                                 int32_t index_pos, float* logits);
+
+/* As llama_q8_forward, but returns only the greedy next token (argmax of the
+ * last position's logits, lowest index on ties) in host *next. */
+llama_q8_status llama_q8_forward_argmax(llama_q8_ctx* ctx, const int32_t* ids, int32_t T,
+                                        int32_t index_pos, int32_t* next);
+
+/* The generation loop of "生成一个 token" (实验程序): prefill the host
+ * prompt[T] at position 0, then n_decode greedy decode steps, each feeding
+ * back the previous token. out_ids (host, n_decode + 1 entries) receives the
+ * token chosen by the prefill followed by one token per decode step. The
+ * decode steps replay the CUDA graph back to back with the token fed back on
+ * the device; the host reads the tokens once at the end. Requires
+ * T + n_decode <= max_seq (LQ8_ERR_CTX). */
+llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int32_t T,
+                                  int32_t n_decode, int32_t* out_ids);
+
+/* Device-resident variants for callers that keep ids on the GPU. They enqueue
+ * on the context's stream and return at once; llama_q8_sync waits.
+ * prefill_async: device d_ids[T] at index_pos (same position rules as
+ * llama_q8_forward, checked on the host); writes the greedy token to device
+ * *d_next and keeps it as the token the next decode step consumes.
+ * decode_async: n_steps decode steps starting from that token; device
+ * d_out[n_steps] receives one token per step. Ids in device memory are not
+ * seen by the host: an out-of-range id is clamped to 0 by the embedding
+ * kernel and reported as LQ8_ERR_TOKEN by the next llama_q8_sync. */
+llama_q8_status llama_q8_prefill_async(llama_q8_ctx* ctx, const int32_t* d_ids, int32_t T,
+                                       int32_t index_pos, int32_t* d_next);
+llama_q8_status llama_q8_decode_async(llama_q8_ctx* ctx, int32_t n_steps, int32_t* d_out);
+llama_q8_status llama_q8_sync(llama_q8_ctx* ctx);
+
+/* clear_kv_cache: cached length := 0. Frees nothing (the cache is
+ * preallocated); the next forward must use index_pos 0. */
+llama_q8_status llama_q8_reset(llama_q8_ctx* ctx);
+
+/* Release every device and host resource of ctx. NULL is accepted. */
+llama_q8_status llama_q8_free(llama_q8_ctx* ctx);
+
+/* Number of cached positions (the value index_pos must take next). */
+llama_q8_status llama_q8_cache_len(const llama_q8_ctx* ctx, int32_t* len);
+
+/* Copy cached K and V rows [pos0, pos0 + n) of one layer to host buffers
+ * k_out, v_out, each [n_head_kv][n][head_dim] f32 (K is stored after RoPE).
+ * Requires pos0 + n <= cached length. */
+llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0, int32_t n,
+                                 float* k_out, float* v_out);
+
+/* The context's CUDA stream (a cudaStream_t), for recording events around
+ * the _async calls. */
+void* llama_q8_stream(llama_q8_ctx* ctx);
+
+/* Number of kernel launches one decode step makes (the CUDA-graph nodes). */
+int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx);
+
+/* Cumulative number of kernel launches this context has issued; a CUDA-graph
+ * decode step counts as its llama_q8_decode_kernel_count() kernels. */
+int64_t llama_q8_launch_count(const llama_q8_ctx* ctx);
+
+/* Per-kernel timing of the decode step, in the spirit of the per-span self
+ * times on "量化 llama 的一次前向" (一个 decode 步里时间去了哪): runs n_steps
+ * greedy decode steps EAGERLY (the same kernels the graph holds, one launch
+ * at a time, a CUDA event pair around each launch on the context stream),
+ * continuing from the current cached length and advancing it like
+ * llama_q8_decode_async. For each kernel family it reports the launches, the
+ * summed event time and the algorithmic bytes (weights read once, activations,
+ * KV rows read, outputs written). stats: host array of max_stats entries;
+ * *n_stats receives the number of families. Requires a non-empty cache and
+ * cached length + n_steps <= max_seq. */
+typedef struct llama_q8_kernel_stat {
+    char name[32];
+    int32_t launches;
+    double ms;
+    double bytes;
+} llama_q8_kernel_stat;
+llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llama_q8_kernel_stat* stats,
+                                        int32_t max_stats, int32_t* n_stats);
+
+const char* llama_q8_status_str(llama_q8_status s);
+
+/* ---------------------------------------------------------------------------
+ * Device-level entry points (kernel workloads). All data pointers are device
+ * memory; `stream` is a cudaStream_t (NULL = legacy default stream). They
+ * enqueue and return.
+ * ------------------------------------------------------------------------- */
+
+/* Quantise f32 w[rows][k] (k % 32 == 0) to Q8_0 blocks out[rows][k/32][34]
+ * with the rule d = max|w|/127 (f32), q = round(w/d) (f32 IEEE division,
+ * ties away from zero, clamp +-127, d == 0 -> 0), d stored as fp16 (round to
+ * nearest even). The pages only fix the block size through byte counts;
+ * this rule is the block format's definition the build follows. */
+llama_q8_status llama_q8_quantize(const float* w, int64_t rows, int64_t k, void* out,
+                                  void* stream);
+
+/* Bytes of the library's device layout for a [rows, k] Q8_0 matrix
+ * (rows padded to a multiple of 32; same 34 bytes per block otherwise). */
+size_t llama_q8_packed_bytes(int64_t rows, int64_t k);
+
+/* Repack Q8_0 blocks q8[rows][k/32][34] into the device layout used by
+ * llama_q8_matmul: packed must hold llama_q8_packed_bytes(rows, k) bytes. */
+llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* packed,
+                              void* stream);
+
+/* QMatMul forward: y[m][rows] = x[m][k] . W[rows][k]^T with W the packed Q8_0
+ * matrix, f32 x and y, f32 accumulation. m == 1 runs the matrix-vector kernel,
+ * m > 1 the matrix-matrix kernel (the dispatch "生成一个 token" describes for
+ * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32). */
+llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
+                                int64_t m, float* y, void* stream);
+
+/* Grouped-query attention over a KV cache: for each of T queries at
+ * positions index_pos + t, out = softmax(q k^T / sqrt(head_dim) + mask) v,
+ * query head h reading KV head h / (n_head / n_head_kv). q[T][n_head][head_dim];
+ * k_cache, v_cache [n_head_kv][cache_stride][head_dim] with positions
+ * [0, index_pos + T) filled; out[T][n_head][head_dim]. T == 1: the split-KV
+ * decode kernel, no mask; T > 1: the causal prefill kernel, query t sees
+ * positions <= index_pos + t ("量化 llama 的一次前向", forward：mask 什么时候建).
+ * workspace: device scratch of llama_q8_attention_workspace_bytes(...) bytes
+ * (split-KV partial results and completion counters); its counters must be
+ * zero before the first call and are left zero by every call; calls sharing a
+ * workspace must not overlap on the GPU. */
+size_t llama_q8_attention_workspace_bytes(int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                                          int32_t cache_stride);
+llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const float* v_cache,
+                                   int32_t T, int32_t index_pos, int32_t n_head,
+                                   int32_t n_head_kv, int32_t head_dim, int32_t cache_stride,
+                                   float* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLAMA_Q8_H */

@@ -1,0 +1,286 @@
+// Grouped-query attention over the preallocated KV cache.
+//
+// Decode (T = 1): the fused single-token kernel the pages describe for the
+// Metal path ("生成一个 token", prefill 和 decode：同一个 forward，不同的路:
+// q k^T, scale, softmax and the product with v in one kernel, the query heads
+// of a group sharing their KV head inside it). Here the cache is split into
+// 64-position chunks, one CTA per (KV head, chunk), all query heads of the
+// group handled by that CTA so each K/V row is read from HBM once; the last
+// CTA of a KV head (completion counter) merges the chunk results with the
+// usual max/sum rescaling. No repeat_kv copy and no cat.
+//
+// Prefill (T > 1): a causal flash-style kernel, one CTA per (query head,
+// 32-query tile), streaming 32-position K/V tiles through shared memory with
+// an online softmax; query t sees positions <= index_pos + t ("量化 llama 的一次
+// 前向", forward：mask 什么时候建 — the mask is a predicate here, never built).
+#include "kernels.cuh"
+
+namespace lq8 {
+
+constexpr int kChunk = 64;       // positions per decode CTA
+constexpr int kDecThreads = 128;
+constexpr int kMaxGroup = 8;
+
+static inline int max_splits_for(int cache_stride) { return (cache_stride + kChunk - 1) / kChunk; }
+
+size_t attn_workspace_bytes(int n_head, int n_head_kv, int head_dim, int cache_stride) {
+    const int G = n_head / n_head_kv;
+    const size_t ms = (size_t)max_splits_for(cache_stride);
+    size_t counters = ((size_t)n_head_kv * 4 + 255) / 256 * 256;
+    size_t ml = ((size_t)n_head_kv * ms * G * 2 * 4 + 255) / 256 * 256;
+    size_t o = (size_t)n_head_kv * ms * G * head_dim * 4;
+    return counters + ml + o;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
+    const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int n_head,
+    int n_kv, int cache_stride, int kv_len_host, const DevState* st, float scale, float* __restrict__ out,
+    unsigned int* counters, float* part_ml, float* part_o, int max_splits) {
+    extern __shared__ float4 sm4[];
+    float* Ks = reinterpret_cast<float*>(sm4);      // [kChunk][HD + 4]
+    float* Vs = Ks + kChunk * (HD + 4);             // [kChunk][HD]
+    float* Qs = Vs + kChunk * HD;                   // [G][HD]
+    float* Ps = Qs + kMaxGroup * HD;                // [G][kChunk]
+    __shared__ float s_m[kMaxGroup], s_l[kMaxGroup];
+    __shared__ int s_last;
+
+    const int kh = blockIdx.x, split = blockIdx.y;
+    const int G = n_head / n_kv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kv_len = st ? st->pos + 1 : kv_len_host;
+    const int n_splits = (kv_len + kChunk - 1) / kChunk;
+    if (split >= n_splits) return;
+    const int j0 = split * kChunk;
+    const int n = min(kChunk, kv_len - j0);
+
+    for (int i = tid; i < G * HD; i += kDecThreads) Qs[i] = q[(int64_t)kh * G * HD + i];
+    const float4* kb = reinterpret_cast<const float4*>(kc + ((int64_t)kh * cache_stride + j0) * HD);
+    const float4* vb = reinterpret_cast<const float4*>(vc + ((int64_t)kh * cache_stride + j0) * HD);
+    for (int f = tid; f < n * (HD / 4); f += kDecThreads) {
+        const int row = f / (HD / 4), c = f % (HD / 4);
+        *reinterpret_cast<float4*>(Ks + row * (HD + 4) + c * 4) = kb[f];
+        reinterpret_cast<float4*>(Vs)[f] = vb[f];
+    }
+    __syncthreads();
+
+    if (tid < n) {
+        const float* kr = Ks + tid * (HD + 4);
+        for (int g = 0; g < G; ++g) {
+            const float* qg = Qs + g * HD;
+            float s = 0.0f;
+#pragma unroll
+            for (int d = 0; d < HD; d += 4) {
+                const float4 kk = *reinterpret_cast<const float4*>(kr + d);
+                const float4 qq = *reinterpret_cast<const float4*>(qg + d);
+                s = fmaf(qq.x, kk.x, s); s = fmaf(qq.y, kk.y, s);
+                s = fmaf(qq.z, kk.z, s); s = fmaf(qq.w, kk.w, s);
+            }
+            Ps[g * kChunk + tid] = s * scale;
+        }
+    }
+    __syncthreads();
+
+    for (int g = warp; g < G; g += kDecThreads / 32) {
+        const float a = lane < n ? Ps[g * kChunk + lane] : -INFINITY;
+        const float b = lane + 32 < n ? Ps[g * kChunk + lane + 32] : -INFINITY;
+        const float mx = warp_max(fmaxf(a, b));
+        const float ea = lane < n ? expf(a - mx) : 0.0f;
+        const float eb = lane + 32 < n ? expf(b - mx) : 0.0f;
+        Ps[g * kChunk + lane] = ea;
+        Ps[g * kChunk + lane + 32] = eb;
+        const float l = warp_sum(ea + eb);
+        if (lane == 0) { s_m[g] = mx; s_l[g] = l; }
+    }
+    __syncthreads();
+
+    const int64_t pbase = ((int64_t)kh * max_splits + split) * G;
+    for (int o = tid; o < G * HD; o += kDecThreads) {
+        const int g = o / HD, d = o % HD;
+        const float* pg = Ps + g * kChunk;
+        float acc = 0.0f;
+        for (int j = 0; j < n; ++j) acc = fmaf(pg[j], Vs[j * HD + d], acc);
+        if (n_splits == 1) {
+            out[((int64_t)kh * G + g) * HD + d] = acc / s_l[g];
+        } else {
+            part_o[(pbase + g) * HD + d] = acc;
+        }
+    }
+    if (n_splits == 1) return;
+    if (tid < G) {
+        part_ml[(pbase + tid) * 2 + 0] = s_m[tid];
+        part_ml[(pbase + tid) * 2 + 1] = s_l[tid];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&counters[kh], 1u);
+        s_last = (ticket == (unsigned)(n_splits - 1));
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int o = tid; o < G * HD; o += kDecThreads) {
+        const int g = o / HD, d = o % HD;
+        float M = -INFINITY;
+        for (int s = 0; s < n_splits; ++s)
+            M = fmaxf(M, __ldcg(part_ml + (((int64_t)kh * max_splits + s) * G + g) * 2));
+        float L = 0.0f, acc = 0.0f;
+        for (int s = 0; s < n_splits; ++s) {
+            const int64_t pb = ((int64_t)kh * max_splits + s) * G + g;
+            const float w = expf(__ldcg(part_ml + pb * 2) - M);
+            L = fmaf(w, __ldcg(part_ml + pb * 2 + 1), L);
+            acc = fmaf(w, __ldcg(part_o + pb * HD + d), acc);
+        }
+        out[((int64_t)kh * G + g) * HD + d] = acc / L;
+    }
+    if (tid == 0) atomicExch(&counters[kh], 0u);
+}
+
+static constexpr size_t decode_smem_bytes(int hd) {
+    return (size_t)(kChunk * (hd + 4) + kChunk * hd + kMaxGroup * hd + kMaxGroup * kChunk) * 4;
+}
+
+cudaError_t init_attention_attributes() {
+    cudaError_t err = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)decode_smem_bytes(64));
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)decode_smem_bytes(128));
+}
+
+template <int HD>
+static cudaError_t attn_decode_launch(const float* q, const float* kc, const float* vc, int n_head,
+                                      int n_kv, int cache_stride, int kv_len, const DevState* st,
+                                      float* out, void* ws, cudaStream_t s) {
+    const int ms = max_splits_for(cache_stride);
+    const int G = n_head / n_kv;
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    unsigned int* counters = reinterpret_cast<unsigned int*>(w);
+    size_t off = ((size_t)n_kv * 4 + 255) / 256 * 256;
+    float* part_ml = reinterpret_cast<float*>(w + off);
+    off += ((size_t)n_kv * ms * G * 2 * 4 + 255) / 256 * 256;
+    float* part_o = reinterpret_cast<float*>(w + off);
+    const size_t smem = decode_smem_bytes(HD);
+    const int grid_y = st ? ms : (kv_len + kChunk - 1) / kChunk;
+    const float scale = 1.0f / sqrtf((float)HD);
+    attn_decode_kernel<HD><<<dim3(n_kv, grid_y), kDecThreads, smem, s>>>(
+        q, kc, vc, n_head, n_kv, cache_stride, kv_len, st, scale, out, counters, part_ml, part_o, ms);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float* v_cache, int n_head,
+                               int n_head_kv, int head_dim, int cache_stride, int kv_len,
+                               const DevState* st, float* out, void* workspace, cudaStream_t s) {
+    if (head_dim == 64)
+        return attn_decode_launch<64>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, workspace, s);
+    if (head_dim == 128)
+        return attn_decode_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, workspace, s);
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Prefill
+// ---------------------------------------------------------------------------
+constexpr int kQTile = 32;
+constexpr int kKTile = 32;
+
+template <int HD>
+__global__ void __launch_bounds__(128) attn_prefill_kernel(const float* __restrict__ q, const float* __restrict__ kc,
+                                                           const float* __restrict__ vc, int T, int index_pos,
+                                                           int n_head, int n_kv, int cache_stride, float scale,
+                                                           float* __restrict__ out) {
+    constexpr int DS = HD / 4;  // dims per thread
+    __shared__ __align__(16) float Ks[kKTile][HD + 4];
+    __shared__ __align__(16) float Vs[kKTile][HD + 4];
+    const int h = blockIdx.x, qt = blockIdx.y;
+    const int G = n_head / n_kv, kh = h / G;
+    const int tid = threadIdx.x, r = tid >> 2, c = tid & 3;
+    const int i = qt * kQTile + r;
+    float qv[DS], o[DS];
+#pragma unroll
+    for (int d = 0; d < DS; ++d) {
+        qv[d] = i < T ? q[((int64_t)i * n_head + h) * HD + c * DS + d] : 0.0f;
+        o[d] = 0.0f;
+    }
+    float m = -INFINITY, l = 0.0f;
+    const int kv_end = index_pos + min(T, (qt + 1) * kQTile);
+    const float* kbase = kc + (int64_t)kh * cache_stride * HD;
+    const float* vbase = vc + (int64_t)kh * cache_stride * HD;
+    for (int j0 = 0; j0 < kv_end; j0 += kKTile) {
+        const int nt = min(kKTile, kv_end - j0);
+        for (int f = tid; f < kKTile * (HD / 4); f += 128) {
+            const int row = f / (HD / 4), cc = f % (HD / 4);
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+            if (row < nt) {
+                kv = *reinterpret_cast<const float4*>(kbase + (int64_t)(j0 + row) * HD + cc * 4);
+                vv = *reinterpret_cast<const float4*>(vbase + (int64_t)(j0 + row) * HD + cc * 4);
+            }
+            *reinterpret_cast<float4*>(&Ks[row][cc * 4]) = kv;
+            *reinterpret_cast<float4*>(&Vs[row][cc * 4]) = vv;
+        }
+        __syncthreads();
+        float s[kKTile];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < kKTile; ++jj) {
+            float p = 0.0f;
+#pragma unroll
+            for (int d = 0; d < DS; d += 4) {
+                const float4 kk = *reinterpret_cast<const float4*>(&Ks[jj][c * DS + d]);
+                p = fmaf(qv[d], kk.x, p); p = fmaf(qv[d + 1], kk.y, p);
+                p = fmaf(qv[d + 2], kk.z, p); p = fmaf(qv[d + 3], kk.w, p);
+            }
+            p += __shfl_xor_sync(0xffffffffu, p, 1);
+            p += __shfl_xor_sync(0xffffffffu, p, 2);
+            const int j = j0 + jj;
+            const bool vis = (jj < nt) && (j <= index_pos + i) && (i < T);
+            s[jj] = vis ? p * scale : -INFINITY;
+            mt = fmaxf(mt, s[jj]);
+        }
+        const float m_new = fmaxf(m, mt);
+        if (m_new != -INFINITY) {
+            const float corr = expf(m - m_new);
+            l *= corr;
+#pragma unroll
+            for (int d = 0; d < DS; ++d) o[d] *= corr;
+#pragma unroll
+            for (int jj = 0; jj < kKTile; ++jj) {
+                const float p = expf(s[jj] - m_new);
+                l += p;
+#pragma unroll
+                for (int d = 0; d < DS; d += 4) {
+                    const float4 vv = *reinterpret_cast<const float4*>(&Vs[jj][c * DS + d]);
+                    o[d] = fmaf(p, vv.x, o[d]); o[d + 1] = fmaf(p, vv.y, o[d + 1]);
+                    o[d + 2] = fmaf(p, vv.z, o[d + 2]); o[d + 3] = fmaf(p, vv.w, o[d + 3]);
+                }
+            }
+            m = m_new;
+        }
+        __syncthreads();
+    }
+    if (i < T) {
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int d = 0; d < DS; ++d) out[((int64_t)i * n_head + h) * HD + c * DS + d] = o[d] * inv;
+    }
+}
+
+cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache, int T,
+                                int index_pos, int n_head, int n_head_kv, int head_dim, int cache_stride,
+                                float* out, cudaStream_t s) {
+    dim3 grid(n_head, (T + kQTile - 1) / kQTile);
+    const float scale = 1.0f / sqrtf((float)head_dim);
+    if (head_dim == 64) {
+        attn_prefill_kernel<64><<<grid, 128, 0, s>>>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv,
+                                                    cache_stride, scale, out);
+    } else if (head_dim == 128) {
+        attn_prefill_kernel<128><<<grid, 128, 0, s>>>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv,
+                                                     cache_stride, scale, out);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lq8

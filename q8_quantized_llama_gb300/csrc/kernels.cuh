@@ -1,0 +1,82 @@
+// Internal interface between the runtime (runtime.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace lq8 {
+
+// Device-resident step state. The decode step reads pos and token from here,
+// so one captured CUDA graph serves every decode position; the lm_head
+// epilogue writes the greedy token back and advances pos.
+struct DevState {
+    int32_t pos;    // position of the token being processed (decode)
+    int32_t token;  // token the next decode step embeds
+    int32_t n_out;  // tokens written to out_ids so far
+    int32_t err;    // 0, or a llama_q8_status raised on the device
+};
+
+enum Epi : int {
+    EPI_STORE = 0,     // y[t][n] = acc
+    EPI_RESIDUAL = 1,  // y[t][n] += acc            (O-proj, down-proj)
+    EPI_QKV = 2,       // rope_i on q/k rows, q -> q_out, k/v -> KV cache at pos
+    EPI_SILU = 3,      // rows interleaved gate/up: a[t][n/2] = silu(g) * u
+    EPI_ARGMAX = 4     // logits[n] = acc; greedy token -> state / out_ids
+};
+
+struct EpiArgs {
+    float* y = nullptr;  // STORE / RESIDUAL output, row stride ldy
+    int ldy = 0;
+    // QKV
+    float* q_out = nullptr;  // [m][q_rows]
+    float* k_cache = nullptr;  // layer base, [n_head_kv][max_seq][head_dim]
+    float* v_cache = nullptr;
+    int q_rows = 0, kv_rows = 0, head_dim = 0, max_seq = 0;
+    const float* rope_cos = nullptr;  // [max_seq][head_dim/2]
+    const float* rope_sin = nullptr;
+    int pos0 = 0;                     // position of the first token (when state == nullptr)
+    const DevState* state = nullptr;  // decode: position read from the device
+    // SILU
+    float* a_out = nullptr;
+    int lda = 0;
+    // ARGMAX
+    float* logits = nullptr;
+    unsigned long long* best_key = nullptr;  // zero between launches
+    unsigned int* done_count = nullptr;      // zero between launches
+    DevState* st = nullptr;
+    int32_t* out_ids = nullptr;
+    int pos_after = -1;  // >= 0: state->pos := pos_after; < 0: state->pos += 1
+};
+
+// quant.cu
+cudaError_t launch_quantize(const float* w, int64_t rows, int64_t k, uint8_t* out, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* q8, int64_t rows, int64_t k, uint8_t* packed_base,
+                        int64_t dst_rows, int64_t row_offset, int64_t row_stride, cudaStream_t s);
+cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const DevState* st_token,
+                         DevState* st_err, float* x, int n_vocab, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y,
+                           cudaStream_t s);
+cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
+
+// gemv.cu (m == 1)
+cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
+                        const EpiArgs& e, cudaStream_t s);
+// gemm.cu (m > 1)
+cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
+                        const EpiArgs& e, cudaStream_t s);
+
+// attention.cu
+size_t attn_workspace_bytes(int n_head, int n_head_kv, int head_dim, int max_seq);
+cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float* v_cache,
+                               int n_head, int n_head_kv, int head_dim, int cache_stride,
+                               int kv_len, const DevState* st, float* out, void* workspace,
+                               cudaStream_t s);
+cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache,
+                                int T, int index_pos, int n_head, int n_head_kv, int head_dim,
+                                int cache_stride, float* out, cudaStream_t s);
+
+PackedQ8 packed_view(const uint8_t* base, int64_t rows, int64_t k);
+
+}  // namespace lq8

@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads and exports every symbol include/llama_q8.h
+declares; argument checks that need no GPU return their status codes."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+from tests.gpu_helpers import built_lib
+
+
+@pytest.fixture(scope="module")
+def B():
+    built_lib()
+    from q8_quantized_llama_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "llama_q8.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(llama_q8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_lists_the_binding_exports(B):
+    assert sorted(B.EXPORTS) == _declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = C.CDLL(B.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(B):
+    for s in range(9):
+        assert B.status_str(s)
+    assert B.status_str(0) == "ok"
+
+
+def test_null_arguments_rejected_without_a_gpu(B):
+    L = B.lib()
+    out = C.c_void_p()
+    assert L.llama_q8_load(None, None, 0, C.byref(out)) == B.LQ8_ERR_ARG
+    assert L.llama_q8_forward(None, None, 1, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_forward_argmax(None, None, 1, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_generate(None, None, 1, 1, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_reset(None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_free(None) == B.LQ8_OK
+    assert L.llama_q8_quantize(None, 1, 32, None, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_matmul(None, 1, 32, None, 1, None, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_attention(None, None, None, 1, 0, 9, 3, 64, 4096, None, None, 0, None) == B.LQ8_ERR_ARG
+
+
+def test_config_validation_without_a_gpu(B):
+    import numpy as np
+    from q8_quantized_llama_gb300 import synth
+    cfg = dict(synth.MODEL_135M, n_layer=1)
+    dummy = np.zeros(64, np.uint8)
+    t = {n: dummy for n, _, _ in synth.model_tensor_specs(cfg)}
+    for bad, status in [(dict(head_dim=96), B.LQ8_ERR_UNSUPPORTED), (dict(n_embd=500), B.LQ8_ERR_UNSUPPORTED),
+                        (dict(n_head_kv=4), B.LQ8_ERR_ARG), (dict(n_layer=0), B.LQ8_ERR_ARG),
+                        (dict(tied_output=0), B.LQ8_ERR_ARG)]:
+        c = B.make_config(dict(cfg, **bad))
+        w, keep = B.make_weights(cfg, t, on_device=False)
+        out = C.c_void_p()
+        assert B.lib().llama_q8_load(C.byref(c), C.byref(w), 0, C.byref(out)) == status, bad
+
+
+def test_size_queries(B):
+    assert B.llama_q8_packed_bytes(576, 576) == 576 * 576 + 576 * 18 * 2
+    assert B.llama_q8_packed_bytes(1, 32) == 32 * 32 + (256 - 32 * 32 % 256) % 256 + 32 * 2
+    assert B.llama_q8_packed_bytes(10, 31) == 0
+    assert B.llama_q8_attention_workspace_bytes(9, 3, 64, 4096) > 0
+    assert B.llama_q8_attention_workspace_bytes(9, 4, 64, 4096) == 0

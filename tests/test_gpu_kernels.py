@@ -1,0 +1,169 @@
+"""Kernel parity through the C ABI against the CPU oracle: Q8_0 quantiser
+(bit-exact), Q8_0 matmul (the linear sweep shapes of the 135M model plus the
+7B GEMV shapes), GQA attention (decode and causal prefill)."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import q8_oracle as O
+from q8_quantized_llama_gb300 import synth
+from tests.gpu_helpers import binding, gpu_quantize, require_gpu, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -24  # f32 unit roundoff
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+# ------------------------------------------------------------------ quantiser
+
+def _golden_blocks():
+    from tests.test_oracle_pins import _hand_blocks
+    return _hand_blocks()
+
+
+def test_quantize_hand_blocks_bit_exact():
+    cases = _golden_blocks()
+    w = np.stack([c["w"] for c in cases])
+    got = gpu_quantize(w).cpu().numpy()
+    for i, c in enumerate(cases):
+        np.testing.assert_array_equal(got[i], c["bytes"], err_msg=c["name"])
+
+
+@pytest.mark.parametrize("rows,k,scale", [(576, 576, 0.02), (1536, 576, 0.02), (576, 1536, 0.02),
+                                          (49152, 576, 0.02), (7, 32, 3.0), (33, 96, 1e-3),
+                                          (64, 4096, 0.02)])
+def test_quantize_bit_exact_vs_oracle(rows, k, scale):
+    w = synth.normal_f32((rows, k), 42, rows * 7 + k, std=scale)
+    w[0, :32] = 0.0                          # an all-zero block
+    w[min(1, rows - 1), 32 - 1] = 1e-30      # tiny values
+    np.testing.assert_array_equal(gpu_quantize(w).cpu().numpy(), O.quantize_q8_0(w))
+
+
+def test_quantize_ties_and_extremes():
+    rng = np.random.default_rng(0)
+    # exact half-way ratios: w = (j + 0.5) * d for d = amax/127 with amax a power of two
+    amax = np.float32(1.0)
+    d = np.float32(amax / np.float32(127))
+    blocks = []
+    for j in range(0, 126, 4):
+        b = np.zeros(32, np.float32)
+        b[0] = amax
+        b[1:5] = np.float32((np.arange(j, j + 4) + 0.5) * np.float64(d))
+        b[5:9] = -b[1:5]
+        b[9:] = rng.uniform(-1, 1, 23).astype(np.float32)
+        blocks.append(b)
+    w = np.stack(blocks)
+    np.testing.assert_array_equal(gpu_quantize(w).cpu().numpy(), O.quantize_q8_0(w))
+
+
+# ------------------------------------------------------------------ matmul
+
+def _packed(wq_dev, rows, k):
+    B = binding()
+    packed = torch.empty(B.llama_q8_packed_bytes(rows, k), dtype=torch.uint8, device="cuda")
+    B.llama_q8_pack(wq_dev, rows, k, packed)
+    return packed
+
+
+def _matmul_case(rows, k, m, seed):
+    B = binding()
+    w = synth.weight_matrix_f32(rows, k, seed, stream=rows + k)
+    x = synth.normal_f32((m, k), seed, stream=m * 131 + k)
+    wq = gpu_quantize(w)
+    np.testing.assert_array_equal(wq.cpu().numpy(), O.quantize_q8_0(w))
+    packed = _packed(wq, rows, k)
+    dx = to_dev(x)
+    dy = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    B.llama_q8_matmul(packed, rows, k, dx, m, dy)
+    torch.cuda.synchronize()
+    got = dy.cpu().numpy().astype(np.float64)
+    wd = O.dequantize_q8_0(O.quantize_q8_0(w), rows, k).astype(np.float64)
+    ref = x.astype(np.float64) @ wd.T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(wd).T
+    # f32 accumulation: the matrix-vector kernel sums 32-code blocks, then at
+    # most k/256 blocks per warp, then 8 warp partials; the matrix-matrix
+    # kernel sums the k products in one chain. Bound = (chain + 8) u sum|w x|.
+    chain = (k // 256 + 40) if m == 1 else (k + 8)
+    tol = (chain + 8) * U * mag + 1e-30
+    assert np.all(np.isfinite(got))
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} elements off; max err {np.max(np.abs(got - ref))}"
+
+
+@pytest.mark.parametrize("rows,k", [(576, 576), (192, 576), (1536, 576), (576, 1536), (49152, 576)])
+@pytest.mark.parametrize("m", [1, 8, 203])
+def test_matmul_linear_sweep_135m(rows, k, m):
+    _matmul_case(rows, k, m, seed=2)
+
+
+@pytest.mark.parametrize("rows,k", [(4096, 4096), (14336, 4096), (4096, 14336)])
+def test_matvec_7b_shapes(rows, k):
+    _matmul_case(rows, k, 1, seed=3)
+
+
+@pytest.mark.parametrize("rows,k,m", [(1, 32, 1), (33, 64, 1), (7, 32, 3), (100, 96, 65), (31, 4096, 2)])
+def test_matmul_ragged_edges(rows, k, m):
+    _matmul_case(rows, k, m, seed=4)
+
+
+# ------------------------------------------------------------------ attention
+
+def _attention_case(T, index_pos, nh, nkv, hd, stride, seed):
+    B = binding()
+    kv_len = index_pos + T
+    q = synth.normal_f32((T, nh, hd), seed, 1)
+    kc = synth.normal_f32((nkv, stride, hd), seed, 2)
+    vc = synth.normal_f32((nkv, stride, hd), seed, 3)
+    kc[:, kv_len:] = np.nan  # positions past kv_len must not be read
+    vc[:, kv_len:] = np.nan
+    ws_bytes = B.llama_q8_attention_workspace_bytes(nh, nkv, hd, stride)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((T, nh, hd), float("nan"), dtype=torch.float32, device="cuda")
+    dq, dk, dv = to_dev(q), to_dev(kc), to_dev(vc)
+    B.llama_q8_attention(dq, dk, dv, T, index_pos, nh, nkv, hd, stride, out, ws, ws_bytes)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    k = np.transpose(kc[:, :kv_len], (1, 0, 2))
+    v = np.transpose(vc[:, :kv_len], (1, 0, 2))
+    mask = None if T == 1 else O.build_causal_mask(T, index_pos)
+    ref = O.attention(q, k, v, mask)
+    # Score error <= hd u sum|q k| * scale propagates through exp; the output
+    # is a convex combination of v rows: tolerance 2e-4 max|v| covers the
+    # worst case for N(0,1) inputs at hd <= 128.
+    tol = 2e-4 * float(np.max(np.abs(v)))
+    assert np.all(np.isfinite(got))
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= tol, (err, tol)
+    # the workspace counters are left at zero for the next call
+    assert int(ws[:4 * nkv].view(torch.int32).abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("kv_len", [1, 32, 63, 64, 65, 256, 331, 1024, 4096])
+def test_attention_decode_135m(kv_len):
+    _attention_case(1, kv_len - 1, 9, 3, 64, 4096, seed=kv_len)
+
+
+@pytest.mark.parametrize("kv_len", [32, 1024, 4096])
+def test_attention_decode_7b(kv_len):
+    _attention_case(1, kv_len - 1, 32, 8, 128, 4096, seed=kv_len + 1)
+
+
+@pytest.mark.parametrize("T,index_pos", [(203, 0), (64, 512), (2, 0), (13, 33), (33, 0)])
+def test_attention_prefill_135m(T, index_pos):
+    _attention_case(T, index_pos, 9, 3, 64, 4096, seed=T + index_pos)
+
+
+@pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8)])
+def test_attention_prefill_7b(T, index_pos):
+    _attention_case(T, index_pos, 32, 8, 128, 4096, seed=T * 3 + index_pos)
+
+
+def test_attention_two_calls_reuse_workspace():
+    for kv in (700, 130):
+        _attention_case(1, kv - 1, 9, 3, 64, 1024, seed=kv)

@@ -1,0 +1,159 @@
+"""End-to-end parity of the 135M-shaped Q8_0 Llama through the C ABI against
+the CPU oracle: the 13 + 20 generation run, the 203 + 128 run, the KV cache
+after RoPE, the index_pos rules of the boundary, and the device-resident API."""
+import numpy as np
+import pytest
+
+from oracle import q8_oracle as O
+from q8_quantized_llama_gb300 import synth
+from tests.gpu_helpers import (binding, gpu_model_tensors, logits_close, oracle_model_tensors, require_gpu,
+                               torch)
+
+pytestmark = pytest.mark.gpu
+
+CFG = dict(synth.MODEL_135M)
+V = CFG["n_vocab"]
+
+
+@pytest.fixture(scope="module")
+def m135():
+    require_gpu()
+    B = binding()
+    host = synth.model_weights_f32(CFG, 0)
+    dev_t = gpu_model_tensors(CFG, 0, host)
+    ora_t = oracle_model_tensors(CFG, 0, host)
+    for name, t in dev_t.items():     # the GPU quantiser matches the oracle's bytes
+        if ora_t[name].dtype == np.uint8:
+            np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
+    model = B.Model(CFG, dev_t, on_device=True)
+    del dev_t
+    torch.cuda.empty_cache()
+    oracle = O.ModelWeights(CFG, ora_t, weight_cache="f64")
+    yield model, oracle
+    model.close()
+
+
+def _check_run(model, oracle, prompt, n_decode):
+    """Greedy run step by step on both sides: identical tokens, logits within tol."""
+    ora_ids, ora_logits = oracle.generate(prompt, n_decode)
+    logits = model.forward(prompt, 0)
+    ok, err, bound = logits_close(logits, ora_logits[0])
+    assert ok, ("prefill", err, bound)
+    got = [int(np.argmax(logits))]
+    pos = len(prompt)
+    for step in range(1, n_decode + 1):
+        logits = model.forward([got[-1]], pos)
+        pos += 1
+        ok, err, bound = logits_close(logits, ora_logits[step])
+        assert ok, (step, err, bound)
+        got.append(int(np.argmax(logits)))
+    assert got == ora_ids
+    return ora_ids
+
+
+def test_generation_13_prompt_20_decode(m135):
+    model, oracle = m135
+    prompt = synth.prompt_ids(13, V, 0)
+    ids = _check_run(model, oracle, prompt, 20)
+    # the graph-replay generation loop gives the same tokens
+    np.testing.assert_array_equal(model.generate(prompt, 20), ids)
+    assert model.cache_len() == 33
+
+
+def test_generation_203_prompt_128_decode(m135):
+    model, oracle = m135
+    prompt = synth.prompt_ids(203, V, 0)
+    ids = _check_run(model, oracle, prompt, 128)
+    for _ in range(2):  # fresh cache each repetition, same tokens
+        np.testing.assert_array_equal(model.generate(prompt, 128), ids)
+
+
+def test_kv_cache_after_rope_matches_oracle(m135):
+    model, oracle = m135
+    prompt = synth.prompt_ids(13, V, 5)
+    oracle.forward(prompt, 0)
+    model.forward(prompt, 0)
+    oracle.forward([7], 13)
+    model.forward([7], 13)
+    for layer in (0, 29):
+        k, v = model.read_kv(layer, 0, 14)
+        kc, vc = oracle.kv_cache[layer]
+        kr = np.transpose(kc, (1, 0, 2))
+        vr = np.transpose(vc, (1, 0, 2))
+        for got, ref in ((k, kr), (v, vr)):
+            err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+            assert err <= 1e-4 * float(np.max(np.abs(ref))), (layer, err)
+
+
+def test_index_pos_rules(m135):
+    model, _ = m135
+    B = binding()
+    prompt = synth.prompt_ids(13, V, 1)
+    full = model.forward(prompt, 0)
+    assert model.cache_len() == 13
+    # page transcript: a second chunk at the wrong index_pos is rejected ...
+    model.forward(prompt[:8], 0)
+    assert model.forward_status(prompt[8:], 5) == B.LQ8_ERR_POS
+    assert model.cache_len() == 8                      # state unchanged
+    # ... and at the right one it equals the single prefill
+    chunked = model.forward(prompt[8:], 8)
+    ok, err, bound = logits_close(chunked, full)
+    assert ok and int(np.argmax(chunked)) == int(np.argmax(full))
+    # decode with a wrong index_pos (silent on the pages) is an error here
+    assert model.forward_status([3], 20) == B.LQ8_ERR_POS
+    assert model.forward_status([3], 12) == B.LQ8_ERR_POS
+    # T == 0 and bad ids
+    assert model.forward_status(np.zeros(0, np.int32), 13) == B.LQ8_ERR_ARG
+    assert model.forward_status([V], 13) == B.LQ8_ERR_TOKEN
+    assert model.forward_status([-1], 13) == B.LQ8_ERR_TOKEN
+    assert model.cache_len() == 13
+    # reset: counter back to 0; continuing at the old position is an error
+    model.reset()
+    assert model.cache_len() == 0
+    assert model.forward_status(prompt, 33) == B.LQ8_ERR_POS
+    # index_pos 0 after use equals a fresh run, bit for bit
+    again = model.forward(prompt, 0)
+    np.testing.assert_array_equal(again, full)
+
+
+def test_context_limit(m135):
+    model, _ = m135
+    B = binding()
+    prompt = synth.prompt_ids(64, V, 2)
+    assert model.forward_status(np.zeros(4097, np.int32), 0) == B.LQ8_ERR_CTX
+    model.forward(prompt, 0)
+    assert model.forward_status([1], 4095) == B.LQ8_ERR_POS
+    assert model.cache_len() == 64
+    big = synth.prompt_ids(4032, V, 3)
+    model.forward(big, 64)                              # fills the cache to 4096
+    assert model.cache_len() == 4096
+    assert model.forward_status([1], 4096) == B.LQ8_ERR_CTX
+    assert model.cache_len() == 4096
+
+
+def test_prefill_and_decode_paths_agree(m135):
+    model, oracle = m135
+    seq = synth.prompt_ids(40, V, 4)
+    whole = model.forward(seq, 0)                       # matrix-matrix path
+    model.forward(seq[:39], 0)
+    last = model.forward(seq[39:], 39)                  # CUDA-graph decode step
+    ref = oracle.forward(seq, 0)
+    for got in (whole, last):
+        ok, err, bound = logits_close(got, ref)
+        assert ok, (err, bound)
+
+
+def test_device_resident_api(m135):
+    model, _ = m135
+    prompt = synth.prompt_ids(203, V, 0)
+    ref = model.generate(prompt, 16)
+    d_ids = torch.from_numpy(prompt).cuda()
+    d_next = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_out = torch.zeros(16, dtype=torch.int32, device="cuda")
+    model.prefill_async(d_ids, 203, 0, d_next)
+    model.decode_async(16, d_out)
+    model.sync()
+    got = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
+    np.testing.assert_array_equal(got, ref)
+    assert model.cache_len() == 203 + 16
+    assert model.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
