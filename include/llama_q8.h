@@ -247,6 +247,31 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
                                    float* out, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Allocation-free single-token attention. No counterpart on the pages: it is
+ * a service to callers that cannot allocate device memory — a host that
+ * hands all GPU memory to its own pool and accepts only the buffers it
+ * passes in, a real-time loop that cannot afford cudaMalloc's implicit
+ * device synchronisation, or a plugin that must not create allocations it
+ * cannot account for. Same computation as llama_q8_attention with T == 1
+ * (q[n_head][head_dim] against cache positions [0, kv_len), out
+ * [n_head][head_dim]), but the split-KV partial results and completion
+ * counters live in a fixed 2 MiB device array inside this library, which
+ * every GPU that loads the library holds until the process exits. The call
+ * makes no allocation of any kind; it clears the counters at the start of
+ * every call (the array keeps the previous call's contents). Shapes whose
+ * scratch need exceeds 2 MiB (n_head_kv * ceil(cache_stride/64) * group *
+ * (head_dim + 2) floats, plus counters) return LQ8_ERR_UNSUPPORTED, as do
+ * head_dim other than 64/128 and groups above 8; kv_len > cache_stride is
+ * LQ8_ERR_CTX. The first call on each device looks up the array's device
+ * address (and sets the kernel's shared-memory limit): make that first call
+ * before any stream capture. All calls share the one array, so calls that
+ * overlap on the GPU (other streams, other threads) race and give wrong
+ * results; serialise them. Enqueues on `stream` and returns. */
+llama_q8_status llama_q8_attention_decode_noalloc(const float* q, const float* k_cache,
+                                                  const float* v_cache, int32_t kv_len, int32_t n_head,
+                                                  int32_t n_head_kv, int32_t head_dim,
+                                                  int32_t cache_stride, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,7 +13,10 @@
 // 32-query tile), streaming 32-position K/V tiles through shared memory with
 // an online softmax; query t sees positions <= index_pos + t ("量化 llama 的一次
 // 前向", forward：mask 什么时候建 — the mask is a predicate here, never built).
+#include <mutex>
+
 #include "kernels.cuh"
+#include "llama_q8.h"
 
 namespace lq8 {
 
@@ -284,3 +287,67 @@ cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const floa
 }
 
 }  // namespace lq8
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode attention: the split-KV decode kernel above, with its
+// partial results and completion counters in a fixed device array of this
+// library instead of caller-provided or allocated memory.
+// ---------------------------------------------------------------------------
+namespace lq8 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 2u << 20;  // 2 MiB, held by every GPU that loads the library
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side name of the array is not a device address).
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        err = init_attention_attributes();
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace lq8
+
+extern "C" llama_q8_status llama_q8_attention_decode_noalloc(const float* q, const float* k_cache,
+                                                             const float* v_cache, int32_t kv_len, int32_t n_head,
+                                                             int32_t n_head_kv, int32_t head_dim,
+                                                             int32_t cache_stride, float* out, void* stream) {
+    using namespace lq8;
+    if (!q || !k_cache || !v_cache || !out || kv_len <= 0 || n_head <= 0 || n_head_kv <= 0 ||
+        n_head % n_head_kv || cache_stride <= 0)
+        return LQ8_ERR_ARG;
+    if (kv_len > cache_stride) return LQ8_ERR_CTX;
+    if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
+    if (n_head / n_head_kv > kMaxGroup) return LQ8_ERR_UNSUPPORTED;
+    if (attn_workspace_bytes(n_head, n_head_kv, head_dim, cache_stride) > kNoAllocScratchBytes)
+        return LQ8_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return LQ8_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The completion counters must start at zero; the array keeps whatever the
+    // previous call left, so clear them on every call.
+    const size_t counter_bytes = ((size_t)n_head_kv * 4 + 255) / 256 * 256;
+    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return LQ8_ERR_CUDA;
+    if (launch_attn_decode(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, kv_len, nullptr, out,
+                           scratch, s) != cudaSuccess)
+        return LQ8_ERR_CUDA;
+    return LQ8_OK;
+}
