@@ -52,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--only", choices=["gemv7b"], default=None,
+                   help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
 
 
@@ -357,6 +359,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        torch.cuda.nvtx.range_push("timed_region")
         for i in range(args.steps):
             ev[i][0].record(stream)
             model.prefill_async(d_prompt, PROMPT_LEN, 0, d_next)
@@ -364,6 +367,7 @@ def run_ours(args):
             model.decode_async(DECODE_STEPS, d_out)
             ev[i][2].record(stream)
         model.sync()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     barrier(world)
     gpu_launches = model.launch_count() - launches0
@@ -451,6 +455,14 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.only == "gemv7b":
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        print(json.dumps(gemv_7b_roofline(torch, B, synth, torch.device("cuda", 0), hbm_peak()[0])))
         return
     run_ours(args)
 

@@ -17,6 +17,7 @@
 
 #include "kernels.cuh"
 #include "llama_q8.h"
+#include "ptx.cuh"
 
 namespace lq8 {
 
@@ -57,14 +58,25 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(
     const int j0 = split * kChunk;
     const int n = min(kChunk, kv_len - j0);
 
-    for (int i = tid; i < G * HD; i += kDecThreads) Qs[i] = q[(int64_t)kh * G * HD + i];
+    // Rows cached by earlier steps are read before waiting on the preceding
+    // kernel; the newest row (position kv_len - 1) is written by that kernel
+    // (the QKV epilogue) and is read after the wait, together with q.
+    const int n_old = (st && j0 + n == kv_len) ? n - 1 : n;
     const float4* kb = reinterpret_cast<const float4*>(kc + ((int64_t)kh * cache_stride + j0) * HD);
     const float4* vb = reinterpret_cast<const float4*>(vc + ((int64_t)kh * cache_stride + j0) * HD);
-    for (int f = tid; f < n * (HD / 4); f += kDecThreads) {
+    for (int f = tid; f < n_old * (HD / 4); f += kDecThreads) {
         const int row = f / (HD / 4), c = f % (HD / 4);
         *reinterpret_cast<float4*>(Ks + row * (HD + 4) + c * 4) = kb[f];
         reinterpret_cast<float4*>(Vs)[f] = vb[f];
     }
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    for (int f = n_old * (HD / 4) + tid; f < n * (HD / 4); f += kDecThreads) {
+        const int row = f / (HD / 4), c = f % (HD / 4);
+        *reinterpret_cast<float4*>(Ks + row * (HD + 4) + c * 4) = kb[f];
+        reinterpret_cast<float4*>(Vs)[f] = vb[f];
+    }
+    for (int i = tid; i < G * HD; i += kDecThreads) Qs[i] = q[(int64_t)kh * G * HD + i];
     __syncthreads();
 
     if (tid < n) {
@@ -155,7 +167,7 @@ cudaError_t init_attention_attributes() {
 template <int HD>
 static cudaError_t attn_decode_launch(const float* q, const float* kc, const float* vc, int n_head,
                                       int n_kv, int cache_stride, int kv_len, const DevState* st,
-                                      float* out, void* ws, cudaStream_t s) {
+                                      float* out, void* ws, bool pdl, cudaStream_t s) {
     const int ms = max_splits_for(cache_stride);
     const int G = n_head / n_kv;
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
@@ -167,18 +179,19 @@ static cudaError_t attn_decode_launch(const float* q, const float* kc, const flo
     const size_t smem = decode_smem_bytes(HD);
     const int grid_y = st ? ms : (kv_len + kChunk - 1) / kChunk;
     const float scale = 1.0f / sqrtf((float)HD);
-    attn_decode_kernel<HD><<<dim3(n_kv, grid_y), kDecThreads, smem, s>>>(
-        q, kc, vc, n_head, n_kv, cache_stride, kv_len, st, scale, out, counters, part_ml, part_o, ms);
-    return cudaGetLastError();
+    return launch_ex(attn_decode_kernel<HD>, dim3(n_kv, grid_y), dim3(kDecThreads), smem, s, pdl, q, kc, vc,
+                     n_head, n_kv, cache_stride, kv_len, st, scale, out, counters, part_ml, part_o, ms);
 }
 
 cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                int n_head_kv, int head_dim, int cache_stride, int kv_len,
-                               const DevState* st, float* out, void* workspace, cudaStream_t s) {
+                               const DevState* st, float* out, void* workspace, bool pdl, cudaStream_t s) {
     if (head_dim == 64)
-        return attn_decode_launch<64>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, workspace, s);
+        return attn_decode_launch<64>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
+                                      workspace, pdl, s);
     if (head_dim == 128)
-        return attn_decode_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, workspace, s);
+        return attn_decode_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
+                                       workspace, pdl, s);
     return cudaErrorInvalidValue;
 }
 
@@ -196,6 +209,8 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const float* __restri
     constexpr int DS = HD / 4;  // dims per thread
     __shared__ __align__(16) float Ks[kKTile][HD + 4];
     __shared__ __align__(16) float Vs[kKTile][HD + 4];
+    pdl_wait();
+    pdl_launch_dependents();
     const int h = blockIdx.x, qt = blockIdx.y;
     const int G = n_head / n_kv, kh = h / G;
     const int tid = threadIdx.x, r = tid >> 2, c = tid & 3;
@@ -271,19 +286,16 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const float* __restri
 
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache, int T,
                                 int index_pos, int n_head, int n_head_kv, int head_dim, int cache_stride,
-                                float* out, cudaStream_t s) {
+                                float* out, bool pdl, cudaStream_t s) {
     dim3 grid(n_head, (T + kQTile - 1) / kQTile);
     const float scale = 1.0f / sqrtf((float)head_dim);
-    if (head_dim == 64) {
-        attn_prefill_kernel<64><<<grid, 128, 0, s>>>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv,
-                                                    cache_stride, scale, out);
-    } else if (head_dim == 128) {
-        attn_prefill_kernel<128><<<grid, 128, 0, s>>>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv,
-                                                     cache_stride, scale, out);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (head_dim == 64)
+        return launch_ex(attn_prefill_kernel<64>, grid, dim3(128), 0, s, pdl, q, k_cache, v_cache, T, index_pos,
+                         n_head, n_head_kv, cache_stride, scale, out);
+    if (head_dim == 128)
+        return launch_ex(attn_prefill_kernel<128>, grid, dim3(128), 0, s, pdl, q, k_cache, v_cache, T, index_pos,
+                         n_head, n_head_kv, cache_stride, scale, out);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace lq8
@@ -347,7 +359,7 @@ extern "C" llama_q8_status llama_q8_attention_decode_noalloc(const float* q, con
     const size_t counter_bytes = ((size_t)n_head_kv * 4 + 255) / 256 * 256;
     if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return LQ8_ERR_CUDA;
     if (launch_attn_decode(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, kv_len, nullptr, out,
-                           scratch, s) != cudaSuccess)
+                           scratch, false, s) != cudaSuccess)
         return LQ8_ERR_CUDA;
     return LQ8_OK;
 }

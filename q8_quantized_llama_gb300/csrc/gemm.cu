@@ -8,6 +8,7 @@
 // thread accumulates a 4 x 4 sub-tile in f32. The epilogues are the ones of
 // the matrix-vector kernel, applied per (token, row pair).
 #include "epilogue.cuh"
+#include "ptx.cuh"
 
 namespace lq8 {
 
@@ -21,6 +22,8 @@ __global__ void __launch_bounds__(kGemmThreads) q8_gemm_simt_kernel(PackedQ8 W, 
                                                                     int m, int ldx, EpiArgs e) {
     __shared__ __align__(16) float Xs[kBK][kBM + 4];
     __shared__ __align__(16) float Ws[kBK][kBN + 4];
+    pdl_wait();
+    pdl_launch_dependents();
     const int k = W.k, nb = k >> 5;
     const int n0 = blockIdx.x * kBN, t0 = blockIdx.y * kBM;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -103,16 +106,16 @@ __global__ void __launch_bounds__(kGemmThreads) q8_gemm_simt_kernel(PackedQ8 W, 
 }
 
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
-                        const EpiArgs& e, cudaStream_t s) {
+                        const EpiArgs& e, bool pdl, cudaStream_t s) {
     dim3 grid((W.rows_pad + kBN - 1) / kBN, (m + kBM - 1) / kBM);
+    dim3 block(kGemmThreads);
     switch (epi) {
-        case EPI_STORE: q8_gemm_simt_kernel<EPI_STORE><<<grid, kGemmThreads, 0, s>>>(W, X, m, ldx, e); break;
-        case EPI_RESIDUAL: q8_gemm_simt_kernel<EPI_RESIDUAL><<<grid, kGemmThreads, 0, s>>>(W, X, m, ldx, e); break;
-        case EPI_QKV: q8_gemm_simt_kernel<EPI_QKV><<<grid, kGemmThreads, 0, s>>>(W, X, m, ldx, e); break;
-        case EPI_SILU: q8_gemm_simt_kernel<EPI_SILU><<<grid, kGemmThreads, 0, s>>>(W, X, m, ldx, e); break;
+        case EPI_STORE: return launch_ex(q8_gemm_simt_kernel<EPI_STORE>, grid, block, 0, s, pdl, W, X, m, ldx, e);
+        case EPI_RESIDUAL: return launch_ex(q8_gemm_simt_kernel<EPI_RESIDUAL>, grid, block, 0, s, pdl, W, X, m, ldx, e);
+        case EPI_QKV: return launch_ex(q8_gemm_simt_kernel<EPI_QKV>, grid, block, 0, s, pdl, W, X, m, ldx, e);
+        case EPI_SILU: return launch_ex(q8_gemm_simt_kernel<EPI_SILU>, grid, block, 0, s, pdl, W, X, m, ldx, e);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace lq8

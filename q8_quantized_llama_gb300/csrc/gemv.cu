@@ -3,22 +3,45 @@
 // "生成一个 token" (prefill 和 decode：同一个 forward，不同的路), written for
 // sm_103a.
 //
-// One CTA (8 warps) per tile of 32 output rows. The activation vector is staged
-// once in shared memory (RMSNorm applied there when the step fuses it); each
-// warp takes a contiguous range of 32-weight blocks, lane l owns row
-// tile*32 + l and streams its codes with 128-bit loads: a warp instruction
-// reads 512 contiguous bytes of the packed layout. Codes become f32 exactly
-// (byte-permute into 2^23 + u, one packed subtraction per pair) and are
-// multiplied into f32x2 accumulators; each block's sum is scaled by its fp16
-// d. Warp partials are summed in shared memory in warp order (deterministic),
-// then warp 0 runs the epilogue on its 32 rows.
+// Work unit: one tile of 32 output rows x a contiguous range of 32-weight
+// blocks. In the packed layout that range is one contiguous run of codes
+// (1 KiB per block) and one of scales (64 B per block), so a producer warp
+// streams it into a ring of shared-memory stages with bulk async copies
+// (8 blocks per stage, completion counted on an mbarrier). Eight consumer
+// warps take one block each per stage: lane l owns row tile*32 + l and reads
+// its 2 x 16 codes with conflict-free 128-bit shared loads. Codes become f32
+// exactly (byte-permute into 2^23 + u, one packed subtraction per pair) and
+// are multiplied into f32x2 accumulators against the activation vector
+// staged in shared memory (normalised there when RMSNorm is fused). When the
+// tile count alone cannot fill the GPU, the block range is split over a
+// cluster of CTAs and the leader adds its peers' partial sums through
+// distributed shared memory, in rank order (deterministic).
+//
+// Programmatic dependent launch: the producer starts streaming weights (which
+// no kernel writes) before the grid waits on its predecessor, so the weight
+// reads of a decode step overlap the tail of the previous kernel.
 #include "epilogue.cuh"
+#include "ptx.cuh"
 
 namespace lq8 {
 
-constexpr int kGemvWarps = 8;
-constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kGemvUnroll = 4;
+constexpr int kCWarps = 8;                        // consumer warps
+constexpr int kGemvThreads = (kCWarps + 1) * 32;  // + one producer warp
+constexpr int kStageBlocks = kCWarps;             // blocks per stage, one per consumer warp
+constexpr int kStages = 6;
+constexpr int kStageCodeBytes = kStageBlocks * 1024;
+constexpr int kStageBytes = kStageCodeBytes + kStageBlocks * 64;
+constexpr int kGemvMaxSmem = 227 * 1024 - 4096;
+
+struct GemvArgs {
+    PackedQ8 W;
+    const float* x;
+    const float* g;  // RMSNorm weight when the norm is fused, else unused
+    float eps;
+    EpiArgs e;
+    int splits;      // CTAs (one cluster) per tile
+    int* err;        // set on a bounded-wait timeout
+};
 
 __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, const float* xs) {
     const float4* x4 = reinterpret_cast<const float4*>(xs);
@@ -34,84 +57,11 @@ __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, c
     return (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1));
 }
 
-template <int EPI, bool NORM>
-__global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(PackedQ8 W, const float* __restrict__ x,
-                                                               const float* __restrict__ g, float eps,
-                                                               EpiArgs e) {
-    extern __shared__ float4 smem4[];
-    float* sx = reinterpret_cast<float*>(smem4);
-    __shared__ float red[kGemvWarps][33];
-    __shared__ float s_rscale;
-
-    const int k = W.k, nb = k >> 5, tile = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // ---- prologue: stage x (and normalise it) ----------------------------
-    float ss = 0.0f;
-    for (int i = tid * 4; i < k; i += kGemvThreads * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(x + i);
-        *reinterpret_cast<float4*>(sx + i) = v;
-        if (NORM) {
-            ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
-            ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
-        }
-    }
-    if (NORM) {
-        ss = warp_sum(ss);
-        if (lane == 0) red[warp][0] = ss;
-        __syncthreads();
-        if (tid == 0) {
-            float t = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kGemvWarps; ++w) t += red[w][0];
-            s_rscale = 1.0f / sqrtf(t / (float)k + eps);
-        }
-        __syncthreads();
-        const float r = s_rscale;
-        for (int i = tid * 4; i < k; i += kGemvThreads * 4) {
-            float4 v = *reinterpret_cast<float4*>(sx + i);
-            const float4 gg = *reinterpret_cast<const float4*>(g + i);
-            v.x = v.x * r * gg.x; v.y = v.y * r * gg.y; v.z = v.z * r * gg.z; v.w = v.w * r * gg.w;
-            *reinterpret_cast<float4*>(sx + i) = v;
-        }
-    }
-    __syncthreads();
-
-    // ---- main loop -----------------------------------------------------------
-    const int b0 = (warp * nb) / kGemvWarps, b1 = ((warp + 1) * nb) / kGemvWarps;
-    const int8_t* qp = W.qs + (int64_t)tile * k * 32 + lane * 16;
-    const __half* dp = W.d + (int64_t)tile * nb * 32 + lane;
-    float acc = 0.0f;
-    int b = b0;
-    for (; b + kGemvUnroll <= b1; b += kGemvUnroll) {
-        uint4 q[2 * kGemvUnroll];
-        unsigned short dh[kGemvUnroll];
-#pragma unroll
-        for (int u = 0; u < kGemvUnroll; ++u) {
-            q[2 * u] = ld_stream_u4(qp + (int64_t)(2 * (b + u)) * 512);
-            q[2 * u + 1] = ld_stream_u4(qp + (int64_t)(2 * (b + u) + 1) * 512);
-            dh[u] = ld_stream_u16(dp + (b + u) * 32);
-        }
-#pragma unroll
-        for (int u = 0; u < kGemvUnroll; ++u)
-            acc = fmaf(__half2float(__ushort_as_half(dh[u])), block_dot32(q[2 * u], q[2 * u + 1], sx + 32 * (b + u)), acc);
-    }
-    for (; b < b1; ++b) {
-        const uint4 q0 = ld_stream_u4(qp + (int64_t)(2 * b) * 512);
-        const uint4 q1 = ld_stream_u4(qp + (int64_t)(2 * b + 1) * 512);
-        const unsigned short dh = ld_stream_u16(dp + b * 32);
-        acc = fmaf(__half2float(__ushort_as_half(dh)), block_dot32(q0, q1, sx + 32 * b), acc);
-    }
-    red[warp][lane] = acc;
-    __syncthreads();
-    if (warp != 0) return;
-
-    // ---- epilogue (warp 0, rows tile*32 + lane) -------------------------------
-    float v = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kGemvWarps; ++w) v += red[w][lane];
+// Epilogue on the 32 rows of a tile (warp-wide; lane = row within the tile).
+template <int EPI>
+__device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, int n_tiles) {
     const int r = tile * 32 + lane;
-    const bool valid = r < W.rows;
+    const bool valid = r < rows;
     if (EPI == EPI_STORE) {
         if (valid) e.y[r] = v;
     } else if (EPI == EPI_RESIDUAL) {
@@ -135,7 +85,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(PackedQ8 W, const
             atomicMax(e.best_key, key);
             __threadfence();
             const unsigned int ticket = atomicAdd(e.done_count, 1u);
-            if (ticket == gridDim.x - 1) {
+            if (ticket == (unsigned)(n_tiles - 1)) {
                 __threadfence();
                 const unsigned long long best = atomicExch(e.best_key, 0ull);
                 atomicExch(e.done_count, 0u);
@@ -151,14 +101,177 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(PackedQ8 W, const
 }
 
 template <int EPI, bool NORM>
-static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps,
-                                   const EpiArgs& e, cudaStream_t s) {
-    const size_t smem = (size_t)W.k * sizeof(float);
-    q8_gemv_kernel<EPI, NORM><<<W.rows_pad / 32, kGemvThreads, smem, s>>>(W, x, g, eps, e);
-    return cudaGetLastError();
+__global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    float* xs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ __align__(8) uint64_t empty[kStages];
+    __shared__ float red[kCWarps][33];
+    __shared__ float part[32];
+    __shared__ float s_rscale;
+
+    const PackedQ8& W = a.W;
+    const int k = W.k, nb = k >> 5;
+    const int S = a.splits;
+    const int tile = blockIdx.x / S, split = blockIdx.x % S;
+    const int b0 = (split * nb) / S, b1 = ((split + 1) * nb) / S;
+    const int nblk = b1 - b0;
+    const int n_stage = (nblk + kStageBlocks - 1) / kStageBlocks;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCWarps) {
+        // ---- producer: stream this unit's codes and scales -------------------
+        if (lane == 0) {
+            const uint8_t* gcodes = reinterpret_cast<const uint8_t*>(W.qs) + (size_t)tile * k * 32;
+            const uint8_t* gscales = reinterpret_cast<const uint8_t*>(W.d) + (size_t)tile * nb * 64;
+            for (int j = 0; j < n_stage; ++j) {
+                const int slot = j % kStages;
+                if (j >= kStages) mbar_wait_bounded(&empty[slot], ((j / kStages) - 1) & 1, a.err, 9);
+                const int bs = b0 + j * kStageBlocks;
+                const int nbs = min(kStageBlocks, b1 - bs);
+                uint8_t* dst = stages + slot * kStageBytes;
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbs * 1024 + nbs * 64));
+                bulk_g2s(dst, gcodes + (size_t)bs * 1024, nbs * 1024, &full[slot]);
+                bulk_g2s(dst + kStageCodeBytes, gscales + (size_t)bs * 64, nbs * 64, &full[slot]);
+            }
+        }
+    } else {
+        // ---- consumers --------------------------------------------------------
+        pdl_wait();  // x is written by the preceding kernel
+        if (tid == 0) pdl_launch_dependents();
+        constexpr int kCT = kCWarps * 32;
+        float r = 1.0f;
+        if (NORM) {
+            float ss = 0.0f;
+            for (int i = tid * 4; i < k; i += kCT * 4) {
+                const float4 v = *reinterpret_cast<const float4*>(a.x + i);
+                ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp][32] = ss;
+            named_bar_sync(1, kCT);
+            if (tid == 0) {
+                float t = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kCWarps; ++w) t += red[w][32];
+                s_rscale = 1.0f / sqrtf(t / (float)k + a.eps);
+            }
+            named_bar_sync(1, kCT);
+            r = s_rscale;
+        }
+        const int x0 = b0 * 32, xn = nblk * 32;
+        for (int i = tid * 4; i < xn; i += kCT * 4) {
+            float4 v = *reinterpret_cast<const float4*>(a.x + x0 + i);
+            if (NORM) {
+                const float4 gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
+                v.x = v.x * r * gg.x; v.y = v.y * r * gg.y; v.z = v.z * r * gg.z; v.w = v.w * r * gg.w;
+            }
+            *reinterpret_cast<float4*>(xs + i) = v;
+        }
+        named_bar_sync(1, kCT);
+
+        float acc = 0.0f;
+        for (int j = 0; j < n_stage; ++j) {
+            const int slot = j % kStages;
+            mbar_wait_bounded(&full[slot], (j / kStages) & 1, a.err, 10);
+            const int bs = j * kStageBlocks;  // relative to b0
+            const int nbs = min(kStageBlocks, nblk - bs);
+            if (warp < nbs) {
+                const uint8_t* st = stages + slot * kStageBytes;
+                const uint4 q0 = *reinterpret_cast<const uint4*>(st + warp * 1024 + lane * 16);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(st + warp * 1024 + 512 + lane * 16);
+                const float d = __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[warp * 32 + lane]);
+                acc = fmaf(d, block_dot32(q0, q1, xs + (bs + warp) * 32), acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        red[warp][lane] = acc;
+        named_bar_sync(1, kCT);
+        if (warp == 0) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCWarps; ++w) v += red[w][lane];
+            part[lane] = v;
+        }
+    }
+
+    // ---- cluster reduction and epilogue ---------------------------------------
+    __syncwarp();
+    if (S > 1) cluster_sync(); else __syncthreads();
+    if (split == 0 && warp == 0) {
+        float v = part[lane];
+        for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
+        gemv_epilogue<EPI>(a.e, W.rows, tile, lane, v, W.rows_pad / 32);
+    }
+    if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
 }
 
-constexpr int kGemvMaxSmem = 200 * 1024;  // activation vectors up to 51200 floats
+// Splits per tile: enough CTAs to cover the GPU in one wave, at least 16
+// blocks per split, at most 8 (a portable cluster).
+static int gemv_splits(int tiles, int nb, int sm_count) {
+    const int capacity = sm_count * 3;
+    int s = 1;
+    while (s < 8 && tiles * (s + 1) <= capacity && nb / (s + 1) >= 16) ++s;
+    return s;
+}
+
+static int g_sm_count[64] = {};
+
+static int sm_count_current() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 148;
+    }
+    return g_sm_count[dev];
+}
+
+template <int EPI, bool NORM>
+static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
+                                   bool pdl, int* err, cudaStream_t s) {
+    const int tiles = W.rows_pad / 32, nb = W.k / 32;
+    const int S = gemv_splits(tiles, nb, sm_count_current());
+    const int max_blk = (nb + S - 1) / S;
+    const size_t smem = (size_t)kStages * kStageBytes + (size_t)max_blk * 32 * sizeof(float);
+    if (smem > (size_t)kGemvMaxSmem) return cudaErrorInvalidValue;
+    GemvArgs a{W, x, g, eps, e, S, err};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int n = 0;
+    if (S > 1) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = S;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, q8_gemv_kernel<EPI, NORM>, a);
+}
 
 template <int EPI>
 static cudaError_t gemv_set_attr() {
@@ -172,6 +285,7 @@ static cudaError_t gemv_set_attr() {
 // Raise the dynamic shared-memory limit of every instantiation once per device
 // (before any stream capture).
 cudaError_t init_gemv_attributes() {
+    sm_count_current();
     cudaError_t err = gemv_set_attr<EPI_STORE>();
     if (err == cudaSuccess) err = gemv_set_attr<EPI_RESIDUAL>();
     if (err == cudaSuccess) err = gemv_set_attr<EPI_QKV>();
@@ -180,25 +294,30 @@ cudaError_t init_gemv_attributes() {
     return err;
 }
 
+size_t gemv_max_k() {
+    // stages + the x slice of an unsplit unit must fit in shared memory
+    return (size_t)(kGemvMaxSmem - kStages * kStageBytes) / sizeof(float) / 32 * 32;
+}
+
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, cudaStream_t s) {
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s) {
     const bool norm = norm_g != nullptr;
     switch (epi) {
         case EPI_STORE:
-            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, s)
-                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, s);
+            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, pdl, err, s)
+                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, pdl, err, s);
         case EPI_RESIDUAL:
-            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, s)
-                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, s);
+            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, pdl, err, s)
+                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, pdl, err, s);
         case EPI_QKV:
-            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, s)
-                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, s);
+            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, pdl, err, s)
+                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, pdl, err, s);
         case EPI_SILU:
-            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, s)
-                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, s);
+            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, pdl, err, s)
+                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, pdl, err, s);
         case EPI_ARGMAX:
-            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, s)
-                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, s);
+            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, pdl, err, s)
+                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, pdl, err, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "common.cuh"
 
@@ -50,32 +51,56 @@ struct EpiArgs {
     int pos_after = -1;  // >= 0: state->pos := pos_after; < 0: state->pos += 1
 };
 
+// Launch with an optional programmatic-dependent-launch attribute (the kernel
+// may start before its predecessor finishes and waits for it with
+// griddepcontrol.wait). Used inside the model's own launch sequences only;
+// device-level entry points launch plainly because a caller's preceding
+// kernel may have written any of their inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // quant.cu
 cudaError_t launch_quantize(const float* w, int64_t rows, int64_t k, uint8_t* out, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* q8, int64_t rows, int64_t k, uint8_t* packed_base,
                         int64_t dst_rows, int64_t row_offset, int64_t row_stride, cudaStream_t s);
 cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const DevState* st_token,
-                         DevState* st_err, float* x, int n_vocab, cudaStream_t s);
-cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y,
+                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
                            cudaStream_t s);
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
 
 // gemv.cu (m == 1)
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, cudaStream_t s);
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s);
+size_t gemv_max_k();
 // gemm.cu (m > 1)
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
-                        const EpiArgs& e, cudaStream_t s);
+                        const EpiArgs& e, bool pdl, cudaStream_t s);
 
 // attention.cu
 size_t attn_workspace_bytes(int n_head, int n_head_kv, int head_dim, int max_seq);
 cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float* v_cache,
                                int n_head, int n_head_kv, int head_dim, int cache_stride,
                                int kv_len, const DevState* st, float* out, void* workspace,
-                               cudaStream_t s);
+                               bool pdl, cudaStream_t s);
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache,
                                 int T, int index_pos, int n_head, int n_head_kv, int head_dim,
-                                int cache_stride, float* out, cudaStream_t s);
+                                int cache_stride, float* out, bool pdl, cudaStream_t s);
 
 PackedQ8 packed_view(const uint8_t* base, int64_t rows, int64_t k);
 

@@ -1,6 +1,7 @@
 // Q8_0 quantisation, repacking into the device layout, embedding gather and
 // the stand-alone RMSNorm used by the prefill path.
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace lq8 {
 
@@ -104,6 +105,8 @@ cudaError_t launch_pack(const uint8_t* q8, int64_t rows, int64_t k, uint8_t* pac
 // ---------------------------------------------------------------------------
 __global__ void embed_kernel(PackedQ8 E, const int32_t* __restrict__ ids, const DevState* st_token,
                              DevState* st_err, float* __restrict__ x, int n_vocab) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int t = blockIdx.x;
     int id = ids ? ids[t] : st_token->token;
     if (id < 0 || id >= n_vocab) {
@@ -129,9 +132,8 @@ __global__ void embed_kernel(PackedQ8 E, const int32_t* __restrict__ ids, const 
 }
 
 cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const DevState* st_token,
-                         DevState* st_err, float* x, int n_vocab, cudaStream_t s) {
-    embed_kernel<<<T, 128, 0, s>>>(E, ids, st_token, st_err, x, n_vocab);
-    return cudaGetLastError();
+                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s) {
+    return launch_ex(embed_kernel, dim3(T), dim3(128), 0, s, pdl, E, ids, st_token, st_err, x, n_vocab);
 }
 
 // ---------------------------------------------------------------------------
@@ -140,6 +142,8 @@ cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const Dev
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g, float eps,
                                int k, float* __restrict__ y) {
     __shared__ float red[32];
+    pdl_wait();
+    pdl_launch_dependents();
     const float* xr = x + (int64_t)blockIdx.x * k;
     float* yr = y + (int64_t)blockIdx.x * k;
     float ss = 0.0f;
@@ -166,10 +170,9 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
     }
 }
 
-cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y,
+cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
                            cudaStream_t s) {
-    rmsnorm_kernel<<<m, 256, 0, s>>>(x, g, eps, k, y);
-    return cudaGetLastError();
+    return launch_ex(rmsnorm_kernel, dim3(m), dim3(256), 0, s, pdl, x, g, eps, k, y);
 }
 
 __global__ void set_state_kernel(DevState* st, int pos, int token, int n_out) {

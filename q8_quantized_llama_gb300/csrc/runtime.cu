@@ -47,29 +47,31 @@ cudaError_t ensure_kernel_attributes() {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Event-pair timing of individual launches (llama_q8_profile_decode).
+// Event-pair timing of individual launches (llama_q8_profile_decode). The
+// events are recorded as external event nodes of a captured graph, so each
+// kernel's time is taken on the GPU's own clock, free of host launch gaps.
 struct Profiler {
     struct Rec {
         int family;
-        double bytes;
+        double bytes;  // algorithmic bytes of the launch (attention: per cached position)
         cudaEvent_t a, b;
     };
     std::vector<Rec> recs;
     cudaStream_t s = nullptr;
+    cudaEvent_t cur_a = nullptr;
     int cur = -1;
     double cur_bytes = 0;
-    cudaEvent_t cur_a = nullptr;
     cudaError_t begin(int family, double bytes) {
         cur = family;
         cur_bytes = bytes;
         cudaError_t e = cudaEventCreate(&cur_a);
-        if (e == cudaSuccess) e = cudaEventRecord(cur_a, s);
+        if (e == cudaSuccess) e = cudaEventRecordWithFlags(cur_a, s, cudaEventRecordExternal);
         return e;
     }
     cudaError_t end() {
         cudaEvent_t b = nullptr;
         cudaError_t e = cudaEventCreate(&b);
-        if (e == cudaSuccess) e = cudaEventRecord(b, s);
+        if (e == cudaSuccess) e = cudaEventRecordWithFlags(b, s, cudaEventRecordExternal);
         recs.push_back({cur, cur_bytes, cur_a, b});
         cur_a = nullptr;
         return e;
@@ -79,6 +81,7 @@ struct Profiler {
             cudaEventDestroy(r.a);
             cudaEventDestroy(r.b);
         }
+        if (cur_a) cudaEventDestroy(cur_a);
     }
 };
 
@@ -196,10 +199,13 @@ double q8_bytes(int64_t rows, int64_t k) { return (double)rows * (double)k * 34.
 // One decode step (T = 1): position and token come from the device state, so
 // the same launch sequence serves every position and can be captured once.
 // With a profiler, each launch is bracketed by events and tagged with its
-// algorithmic bytes; kv_len is then the host's view of the step's cache length.
-cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof = nullptr, int kv_len = 0) {
+// algorithmic bytes (attention bytes are per cached position, scaled by the
+// step's cache length when the times are read); launches are then plain, since
+// an event node between two kernels leaves nothing for PDL to overlap.
+cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof = nullptr) {
     const llama_q8_config& cfg = c->cfg;
     cudaStream_t s = c->stream;
+    const bool pdl = prof == nullptr;
     const int64_t h = cfg.n_embd, F = cfg.n_ff, qr = c->q_rows, kvr = c->kv_rows;
     int n = 0;
     cudaError_t err = cudaSuccess;
@@ -211,30 +217,30 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
         ++n;
     };
     run(F_EMBED, q8_bytes(1, h) + 4.0 * h,
-        [&] { return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, s); });
+        [&] { return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, pdl, s); });
     for (int l = 0; l < cfg.n_layer; ++l) {
         const LayerDev& L = c->layers[l];
         EpiArgs e = qkv_epi(c, l);
         e.state = c->d_state;
         run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr),
-            [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, s); });
-        run(F_ATTN, 8.0 * (double)cfg.n_head_kv * kv_len * cfg.head_dim + 8.0 * qr, [&] {
+            [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
+        run(F_ATTN, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
             return launch_attn_decode(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv, cfg.head_dim,
-                                      cfg.max_seq, 0, c->d_state, c->d_o, c->d_attn_ws, s);
+                                      cfg.max_seq, 0, c->d_state, c->d_o, c->d_attn_ws, pdl, s);
         });
         EpiArgs r;
         r.y = c->d_x;
         run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h,
-            [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, s); });
+            [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
         EpiArgs g;
         g.a_out = c->d_a;
         run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F,
-            [&] { return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, s); });
+            [&] { return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s); });
         run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h,
-            [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, s); });
+            [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
     }
     run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab,
-        [&] { return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), s); });
+        [&] { return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl, &c->d_state->err, s); });
     if (n_kernels) *n_kernels = n;
     return err;
 }
@@ -245,31 +251,42 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
     const llama_q8_config& cfg = c->cfg;
     cudaStream_t s = c->stream;
     const int h = cfg.n_embd;
-    cudaError_t err = launch_embed(c->embd, d_ids, T, nullptr, c->d_state, c->d_x, cfg.n_vocab, s);
+    cudaError_t err = launch_embed(c->embd, d_ids, T, nullptr, c->d_state, c->d_x, cfg.n_vocab, true, s);
     for (int l = 0; l < cfg.n_layer && err == cudaSuccess; ++l) {
         const LayerDev& L = c->layers[l];
-        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, s);
+        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
         EpiArgs e = qkv_epi(c, l);
         e.pos0 = index_pos;
-        if (err == cudaSuccess) err = launch_gemm(L.qkv, c->d_y, T, h, EPI_QKV, e, s);
+        if (err == cudaSuccess) err = launch_gemm(L.qkv, c->d_y, T, h, EPI_QKV, e, true, s);
         if (err == cudaSuccess)
             err = launch_attn_prefill(c->d_q, c->kcache(l), c->vcache(l), T, index_pos, cfg.n_head, cfg.n_head_kv,
-                                      cfg.head_dim, cfg.max_seq, c->d_o, s);
+                                      cfg.head_dim, cfg.max_seq, c->d_o, true, s);
         EpiArgs r;
         r.y = c->d_x;
         r.ldy = h;
-        if (err == cudaSuccess) err = launch_gemm(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, s);
-        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, s);
+        if (err == cudaSuccess) err = launch_gemm(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, s);
+        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
         EpiArgs g;
         g.a_out = c->d_a;
         g.lda = cfg.n_ff;
-        if (err == cudaSuccess) err = launch_gemm(L.gu, c->d_y, T, h, EPI_SILU, g, s);
-        if (err == cudaSuccess) err = launch_gemm(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, s);
+        if (err == cudaSuccess) err = launch_gemm(L.gu, c->d_y, T, h, EPI_SILU, g, true, s);
+        if (err == cudaSuccess) err = launch_gemm(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, s);
     }
     if (err == cudaSuccess)
         err = launch_gemv(c->head, c->d_x + (size_t)(T - 1) * h, c->out_norm, cfg.rms_eps, EPI_ARGMAX,
-                          head_epi(c, index_pos + T), s);
+                          head_epi(c, index_pos + T), true, &c->d_state->err, s);
     return err;
+}
+
+// Status raised on the device (read back into h_state): an out-of-range id in
+// device memory (LQ8_ERR_TOKEN, the context stays usable), or a bounded wait
+// that timed out inside a kernel (the context is marked failed).
+llama_q8_status device_status(llama_q8_ctx* c) {
+    const int e = c->h_state->err;
+    if (e == 0) return LQ8_OK;
+    if (e == LQ8_ERR_TOKEN) return LQ8_ERR_TOKEN;
+    c->failed = true;
+    return LQ8_ERR_CUDA;
 }
 
 int prefill_kernel_count(const llama_q8_ctx* c) { return 1 + 7 * c->cfg.n_layer + 1; }
@@ -541,8 +558,7 @@ llama_q8_status llama_q8_forward(llama_q8_ctx* ctx, const int32_t* ids, int32_t 
     LQ8_CK(ctx, cudaMemcpyAsync(ctx->h_state, ctx->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
     LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
     std::memcpy(logits, ctx->h_logits, sizeof(float) * ctx->cfg.n_vocab);
-    if (ctx->h_state->err) return (llama_q8_status)ctx->h_state->err;
-    return LQ8_OK;
+    return device_status(ctx);
 }
 
 llama_q8_status llama_q8_forward_argmax(llama_q8_ctx* ctx, const int32_t* ids, int32_t T, int32_t index_pos,
@@ -553,8 +569,7 @@ llama_q8_status llama_q8_forward_argmax(llama_q8_ctx* ctx, const int32_t* ids, i
     LQ8_CK(ctx, cudaMemcpyAsync(ctx->h_state, ctx->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
     LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
     *next = ctx->h_state->token;
-    if (ctx->h_state->err) return (llama_q8_status)ctx->h_state->err;
-    return LQ8_OK;
+    return device_status(ctx);
 }
 
 llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int32_t T, int32_t n_decode,
@@ -585,8 +600,7 @@ llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int3
     LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
     std::memcpy(out_ids, ctx->h_out, sizeof(int32_t) * (n_decode + 1));
     ctx->len = T + n_decode;
-    if (ctx->h_state->err) return (llama_q8_status)ctx->h_state->err;
-    return LQ8_OK;
+    return device_status(ctx);
 }
 
 llama_q8_status llama_q8_prefill_async(llama_q8_ctx* ctx, const int32_t* d_ids, int32_t T, int32_t index_pos,
@@ -640,15 +654,23 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
     LQ8_CK(ctx, cudaSetDevice(ctx->device));
     Profiler prof;
     prof.s = ctx->stream;
-    LQ8_CK(ctx, launch_set_state(ctx->d_state, -1, -1, 0, ctx->stream));
-    ctx->launches += 1;
-    for (int i = 0; i < n_steps; ++i) {
-        int n = 0;
-        // the step processes the token at position len + i: kv_len = len + i + 1
-        LQ8_CK(ctx, enqueue_decode_step(ctx, &n, &prof, ctx->len + i + 1));
-        ctx->launches += n;
+    int n = 0;
+    LQ8_CK(ctx, cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t lerr = enqueue_decode_step(ctx, &n, &prof);
+    cudaGraph_t g = nullptr;
+    cudaError_t cerr = cudaStreamEndCapture(ctx->stream, &g);
+    if (lerr != cudaSuccess || cerr != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        ctx->failed = true;
+        return LQ8_ERR_CUDA;
     }
-    LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
+    cudaGraphExec_t exec = nullptr;
+    cerr = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (cerr != cudaSuccess) {
+        ctx->failed = true;
+        return LQ8_ERR_CUDA;
+    }
     for (int f = 0; f < F_COUNT; ++f) {
         std::memset(stats[f].name, 0, sizeof(stats[f].name));
         std::strncpy(stats[f].name, kFamilyNames[f], sizeof(stats[f].name) - 1);
@@ -656,12 +678,25 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
         stats[f].ms = 0.0;
         stats[f].bytes = 0.0;
     }
-    for (const auto& r : prof.recs) {
-        float ms = 0.f;
-        LQ8_CK(ctx, cudaEventElapsedTime(&ms, r.a, r.b));
-        stats[r.family].launches += 1;
-        stats[r.family].ms += ms;
-        stats[r.family].bytes += r.bytes;
+    cudaError_t err = launch_set_state(ctx->d_state, -1, -1, 0, ctx->stream);
+    ctx->launches += 1;
+    for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
+        err = cudaGraphLaunch(exec, ctx->stream);
+        if (err == cudaSuccess) err = cudaStreamSynchronize(ctx->stream);
+        ctx->launches += n;
+        const double kv_len = (double)(ctx->len + i + 1);  // the step's token sits at len + i
+        for (const auto& r : prof.recs) {
+            float ms = 0.f;
+            if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, r.a, r.b);
+            stats[r.family].launches += 1;
+            stats[r.family].ms += ms;
+            stats[r.family].bytes += r.family == F_ATTN ? r.bytes * kv_len + 8.0 * ctx->q_rows : r.bytes;
+        }
+    }
+    cudaGraphExecDestroy(exec);
+    if (err != cudaSuccess) {
+        ctx->failed = true;
+        return LQ8_ERR_CUDA;
     }
     *n_stats = F_COUNT;
     ctx->len += n_steps;
@@ -675,11 +710,13 @@ llama_q8_status llama_q8_sync(llama_q8_ctx* ctx) {
     LQ8_CK(ctx, cudaMemcpyAsync(ctx->h_state, ctx->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, ctx->stream));
     LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
     if (ctx->h_state->err) {
-        const int e = ctx->h_state->err;
-        ctx->h_state->err = 0;
-        LQ8_CK(ctx, cudaMemsetAsync(&ctx->d_state->err, 0, sizeof(int32_t), ctx->stream));
-        LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
-        return (llama_q8_status)e;
+        llama_q8_status st = device_status(ctx);
+        if (st == LQ8_ERR_TOKEN) {
+            ctx->h_state->err = 0;
+            LQ8_CK(ctx, cudaMemsetAsync(&ctx->d_state->err, 0, sizeof(int32_t), ctx->stream));
+            LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
+        }
+        return st;
     }
     return LQ8_OK;
 }
@@ -766,10 +803,10 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
     e.ldy = (int)rows;
     cudaError_t err;
     if (m == 1) {
-        if (k > 51200) return LQ8_ERR_UNSUPPORTED;
-        err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, (cudaStream_t)stream);
+        if ((size_t)k > gemv_max_k()) return LQ8_ERR_UNSUPPORTED;
+        err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
     } else {
-        err = launch_gemm(W, x, (int)m, (int)k, EPI_STORE, e, (cudaStream_t)stream);
+        err = launch_gemm(W, x, (int)m, (int)k, EPI_STORE, e, false, (cudaStream_t)stream);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
@@ -796,10 +833,10 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
         if (!workspace || workspace_bytes < attn_workspace_bytes(n_head, n_head_kv, head_dim, cache_stride))
             return LQ8_ERR_ARG;
         err = launch_attn_decode(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, index_pos + 1,
-                                 nullptr, out, workspace, (cudaStream_t)stream);
+                                 nullptr, out, workspace, false, (cudaStream_t)stream);
     } else {
         err = launch_attn_prefill(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, head_dim, cache_stride, out,
-                                  (cudaStream_t)stream);
+                                  false, (cudaStream_t)stream);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
