@@ -222,9 +222,12 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
                               void* stream);
 
 /* QMatMul forward: y[m][rows] = x[m][k] . W[rows][k]^T with W the packed Q8_0
- * matrix, f32 x and y, f32 accumulation. m == 1 runs the matrix-vector kernel,
- * m > 1 the matrix-matrix kernel (the dispatch "生成一个 token" describes for
- * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32). */
+ * matrix, f32 x and y. m == 1 runs the matrix-vector kernel, m > 1 a
+ * matrix-matrix kernel (the dispatch "生成一个 token" describes for
+ * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32): up to 16 rows on the CUDA
+ * cores with f32 accumulation, more rows on the tcgen05 tensor cores in
+ * split-TF32 (three TF32 products per step, f32 accumulation in tensor memory,
+ * about 2^-22 relative error per product). */
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
                                 int64_t m, float* y, void* stream);
 

@@ -1,0 +1,285 @@
+// Q8_0 matrix-matrix product for prefill rows on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory): C[t][n] = X[t][:] . W[n][:]
+// for T > 16 tokens, the dense contraction of the prefill path ("生成一个
+// token", prefill 和 decode：同一个 forward，不同的路: many rows go to the
+// matrix-matrix kernel).
+//
+// Precision: split-TF32 ("3xTF32"). A dequantised weight d*q (f32, at most 18
+// significant bits) is exactly hi + lo with hi = tf32(w) and lo = w - hi (at
+// most 7 bits, exact in tf32). An activation x is hi + lo with hi = tf32(x)
+// and lo = x - hi (lo truncated to tf32 by the MMA: 22 significant bits kept).
+// Three MMAs per k-step, w_hi.x_hi + w_hi.x_lo + w_lo.x_hi, accumulate in f32
+// in TMEM; the dropped w_lo.x_lo term is below 2^-22 relative.
+//
+// CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-step 32 (one Q8_0
+// block = one 128-byte swizzle row of tf32). All 8 warps dequantise/split the
+// next k-block into a 3-slot shared-memory ring (128-byte swizzled K-major
+// layout the MMA reads through its descriptors) while the tensor core works on
+// the previous ones; one thread issues the MMAs and commits each slot to an
+// mbarrier that releases it. The epilogue reads TMEM with tcgen05.ld (warp w
+// reads lanes 32*(w%4).., column half w/4) and applies the shared epilogues.
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace lq8 {
+
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 128;
+constexpr int kTcSlots = 3;
+constexpr int kTcThreads = 256;
+constexpr int kTileBytes = 128 * 128;           // 128 rows x 128 bytes
+constexpr int kSlotBytes = 4 * kTileBytes;      // A_hi, A_lo, B_hi, B_lo
+constexpr int kTcSmem = kTcSlots * kSlotBytes + 1024;  // + alignment slack
+
+// ---- tcgen05 wrappers ---------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);         // start address
+    d |= (uint64_t)(16 >> 4) << 16;                   // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: D f32, A/B tf32, both K-major, M = 128, N = 128.
+constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTcBN >> 3) << 17) |
+                                ((uint32_t)(kTcBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdescTf32), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a 128-row x 128-byte
+// K-major tile with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Exact f32 values of 16 codes (4 words) times the block scale.
+__device__ __forceinline__ void dequant16(const uint4& q, float d, float (&w)[16]) {
+    const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = ws[i] ^ 0x80808080u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float biased = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 + j));
+            w[4 * i + j] = d * (biased - 8388736.0f);
+        }
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, const float* __restrict__ X, int m,
+                                                                    int ldx, EpiArgs e, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t mma_done[kTcSlots];
+    __shared__ uint32_t tmem_holder;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k = W.k, nb = k >> 5;
+    const int m0 = blockIdx.x * kTcBM;  // weight rows
+    const int t0 = blockIdx.y * kTcBN;  // tokens
+
+    if (tid == 0) {
+        for (int s = 0; s < kTcSlots; ++s) mbar_init(&mma_done[s], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_holder, kTcBN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_holder;
+
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+
+    // this thread's share of a k-block: one 16-code half-row of A, four 4-float chunks of B
+    const int a_row = tid >> 1, a_half = tid & 1;
+    const int a_n = m0 + a_row;
+    const bool a_ok = a_n < W.rows_pad;
+    const int64_t a_tile = a_n >> 5, a_lane = a_n & 31;
+    uint4 qa = make_uint4(0, 0, 0, 0);
+    float da = 0.0f;
+    float4 xb[4];
+
+    auto load_block = [&](int kb) {
+        if (a_ok) {
+            qa = *reinterpret_cast<const uint4*>(W.qs + ((a_tile * (k >> 4) + 2 * kb + a_half) * 512 + a_lane * 16));
+            da = __half2float(W.d[(a_tile * nb + kb) * 32 + a_lane]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int f = tid + i * kTcThreads;
+            const int row = f >> 3, c = f & 7;
+            const int t = t0 + row;
+            xb[i] = t < m ? *reinterpret_cast<const float4*>(X + (int64_t)t * ldx + kb * 32 + c * 4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+
+    load_block(0);
+    for (int kb = 0; kb < nb; ++kb) {
+        const int slot = kb % kTcSlots;
+        if (kb >= kTcSlots) mbar_wait_bounded(&mma_done[slot], ((kb / kTcSlots) - 1) & 1, err, 11);
+        uint8_t* sA_hi = smem + slot * kSlotBytes;
+        uint8_t* sA_lo = sA_hi + kTileBytes;
+        uint8_t* sB_hi = sA_lo + kTileBytes;
+        uint8_t* sB_lo = sB_hi + kTileBytes;
+        // A: dequantise, split, store 4 chunks of this half-row
+        {
+            float w[16];
+            dequant16(qa, da, w);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float4 hi, lo;
+                hi.x = tf32_rna(w[4 * c + 0]); lo.x = w[4 * c + 0] - hi.x;
+                hi.y = tf32_rna(w[4 * c + 1]); lo.y = w[4 * c + 1] - hi.y;
+                hi.z = tf32_rna(w[4 * c + 2]); lo.z = w[4 * c + 2] - hi.z;
+                hi.w = tf32_rna(w[4 * c + 3]); lo.w = w[4 * c + 3] - hi.w;
+                const uint32_t off = sw128_off(a_row, a_half * 4 + c);
+                *reinterpret_cast<float4*>(sA_hi + off) = hi;
+                *reinterpret_cast<float4*>(sA_lo + off) = lo;
+            }
+        }
+        // B: split the activations
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int f = tid + i * kTcThreads;
+            const int row = f >> 3, c = f & 7;
+            const float4 x = xb[i];
+            float4 hi, lo;
+            hi.x = tf32_rna(x.x); lo.x = x.x - hi.x;
+            hi.y = tf32_rna(x.y); lo.y = x.y - hi.y;
+            hi.z = tf32_rna(x.z); lo.z = x.z - hi.z;
+            hi.w = tf32_rna(x.w); lo.w = x.w - hi.w;
+            const uint32_t off = sw128_off(row, c);
+            *reinterpret_cast<float4*>(sB_hi + off) = hi;
+            *reinterpret_cast<float4*>(sB_lo + off) = lo;
+        }
+        if (kb + 1 < nb) load_block(kb + 1);  // global loads of the next block overlap the MMAs
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t a_hi = smem_u32(sA_hi), a_lo = smem_u32(sA_lo);
+            const uint32_t b_hi = smem_u32(sB_hi), b_lo = smem_u32(sB_lo);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t o = kk * 32;
+                mma_tf32(tmem, sw128_desc(a_hi + o), sw128_desc(b_hi + o), (kb | kk) != 0);
+                mma_tf32(tmem, sw128_desc(a_hi + o), sw128_desc(b_lo + o), 1u);
+                mma_tf32(tmem, sw128_desc(a_lo + o), sw128_desc(b_hi + o), 1u);
+            }
+            mma_commit(&mma_done[slot]);
+        }
+    }
+    // all MMAs are complete once the last slot's commit has arrived
+    mbar_wait_bounded(&mma_done[(nb - 1) % kTcSlots], ((nb - 1) / kTcSlots) & 1, err, 12);
+    tc_fence_after();
+
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. and token columns of half w/4
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = m0 + quarter * 32 + lane;
+    const bool row_ok = r < W.rows;
+    for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int t = t0 + c0 + j;
+            const float val = v[j];
+            if (EPI == EPI_QKV || EPI == EPI_SILU) {
+                const float other = __shfl_xor_sync(0xffffffffu, val, 1);
+                if (t < m && row_ok && !(lane & 1)) {
+                    if (EPI == EPI_QKV) epi_qkv_pair(e, t, e.pos0 + t, r, val, other);
+                    else e.a_out[(int64_t)t * e.lda + (r >> 1)] = silu_f32(val) * other;
+                }
+            } else if (t < m && row_ok) {
+                if (EPI == EPI_STORE) e.y[(int64_t)t * e.ldy + r] = val;
+                else if (EPI == EPI_RESIDUAL) e.y[(int64_t)t * e.ldy + r] += val;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTcBN);
+}
+
+template <int EPI>
+static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
+                               int* err, cudaStream_t s) {
+    dim3 grid((W.rows_pad + kTcBM - 1) / kTcBM, (m + kTcBN - 1) / kTcBN);
+    return launch_ex(q8_gemm_tc_kernel<EPI>, grid, dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W, X, m, ldx, e, err);
+}
+
+cudaError_t init_gemm_tc_attributes() {
+    cudaError_t err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kTcSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_RESIDUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kTcSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    return err;
+}
+
+cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
+                           int* err, cudaStream_t s) {
+    switch (epi) {
+        case EPI_STORE: return gemm_tc_one<EPI_STORE>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_RESIDUAL: return gemm_tc_one<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_QKV: return gemm_tc_one<EPI_QKV>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_SILU: return gemm_tc_one<EPI_SILU>(W, X, m, ldx, e, pdl, err, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace lq8

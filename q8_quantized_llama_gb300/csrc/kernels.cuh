@@ -88,9 +88,20 @@ cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaSt
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
                         const EpiArgs& e, bool pdl, int* err, cudaStream_t s);
 size_t gemv_max_k();
-// gemm.cu (m > 1)
+// gemm.cu (m > 1): CUDA-core kernel for a few rows
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
                         const EpiArgs& e, bool pdl, cudaStream_t s);
+// gemm_tc.cu: tcgen05 split-TF32 kernel for many rows
+cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
+                           int* err, cudaStream_t s);
+cudaError_t init_gemm_tc_attributes();
+// Rows above which the matrix-matrix product runs on the tensor cores.
+constexpr int kTensorCoreMinRows = 16;
+inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,
+                                      bool pdl, int* err, cudaStream_t s) {
+    return m > kTensorCoreMinRows ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s)
+                                  : launch_gemm(W, X, m, ldx, epi, e, pdl, s);
+}
 
 // attention.cu
 size_t attn_workspace_bytes(int n_head, int n_head_kv, int head_dim, int max_seq);

@@ -41,6 +41,7 @@ cudaError_t ensure_kernel_attributes() {
     if (g_init_done[dev]) return cudaSuccess;
     err = init_gemv_attributes();
     if (err == cudaSuccess) err = init_attention_attributes();
+    if (err == cudaSuccess) err = init_gemm_tc_attributes();
     if (err == cudaSuccess) g_init_done[dev] = true;
     return err;
 }
@@ -257,20 +258,20 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
         err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
         EpiArgs e = qkv_epi(c, l);
         e.pos0 = index_pos;
-        if (err == cudaSuccess) err = launch_gemm(L.qkv, c->d_y, T, h, EPI_QKV, e, true, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.qkv, c->d_y, T, h, EPI_QKV, e, true, &c->d_state->err, s);
         if (err == cudaSuccess)
             err = launch_attn_prefill(c->d_q, c->kcache(l), c->vcache(l), T, index_pos, cfg.n_head, cfg.n_head_kv,
                                       cfg.head_dim, cfg.max_seq, c->d_o, true, s);
         EpiArgs r;
         r.y = c->d_x;
         r.ldy = h;
-        if (err == cudaSuccess) err = launch_gemm(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, &c->d_state->err, s);
         if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
         EpiArgs g;
         g.a_out = c->d_a;
         g.lda = cfg.n_ff;
-        if (err == cudaSuccess) err = launch_gemm(L.gu, c->d_y, T, h, EPI_SILU, g, true, s);
-        if (err == cudaSuccess) err = launch_gemm(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.gu, c->d_y, T, h, EPI_SILU, g, true, &c->d_state->err, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, &c->d_state->err, s);
     }
     if (err == cudaSuccess)
         err = launch_gemv(c->head, c->d_x + (size_t)(T - 1) * h, c->out_norm, cfg.rms_eps, EPI_ARGMAX,
@@ -806,7 +807,7 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
         if ((size_t)k > gemv_max_k()) return LQ8_ERR_UNSUPPORTED;
         err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
     } else {
-        err = launch_gemm(W, x, (int)m, (int)k, EPI_STORE, e, false, (cudaStream_t)stream);
+        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
