@@ -349,7 +349,7 @@ def run_ours(args):
         model.prefill_async(d_prompt, PROMPT_LEN, 0, d_next)
         model.decode_async(DECODE_STEPS, d_out)
 
-    for _ in range(args.warmup):
+    for _ in range(max(1, args.warmup)):
         one_step()
     model.sync()
     ref_tokens = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])

@@ -27,7 +27,7 @@ namespace lq8 {
 
 constexpr int kCWarps = 8;                        // consumer warps
 constexpr int kGemvThreads = (kCWarps + 1) * 32;  // + one producer warp
-constexpr int kStageBlocks = kCWarps;             // blocks per stage, one per consumer warp
+constexpr int kStageBlocks = 8;                   // blocks per stage (a multiple of kCWarps)
 constexpr int kStages = 6;
 constexpr int kStageCodeBytes = kStageBlocks * 1024;
 constexpr int kStageBytes = kStageCodeBytes + kStageBlocks * 64;
@@ -187,12 +187,16 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             mbar_wait_bounded(&full[slot], (j / kStages) & 1, a.err, 10);
             const int bs = j * kStageBlocks;  // relative to b0
             const int nbs = min(kStageBlocks, nblk - bs);
-            if (warp < nbs) {
-                const uint8_t* st = stages + slot * kStageBytes;
-                const uint4 q0 = *reinterpret_cast<const uint4*>(st + warp * 1024 + lane * 16);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(st + warp * 1024 + 512 + lane * 16);
-                const float d = __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[warp * 32 + lane]);
-                acc = fmaf(d, block_dot32(q0, q1, xs + (bs + warp) * 32), acc);
+            const uint8_t* st = stages + slot * kStageBytes;
+#pragma unroll
+            for (int bi = warp; bi < kStageBlocks; bi += kCWarps) {
+                if (bi < nbs) {
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(st + bi * 1024 + lane * 16);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(st + bi * 1024 + 512 + lane * 16);
+                    const float d =
+                        __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[bi * 32 + lane]);
+                    acc = fmaf(d, block_dot32(q0, q1, xs + (bs + bi) * 32), acc);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
@@ -218,10 +222,12 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
 }
 
+constexpr int kGemvCtasPerSm = (227 * 1024) / (kStages * kStageBytes + 16 * 1024 + 2048);
+
 // Splits per tile: enough CTAs to cover the GPU in one wave, at least 16
 // blocks per split, at most 8 (a portable cluster).
 static int gemv_splits(int tiles, int nb, int sm_count) {
-    const int capacity = sm_count * 3;
+    const int capacity = sm_count * kGemvCtasPerSm;
     int s = 1;
     while (s < 8 && tiles * (s + 1) <= capacity && nb / (s + 1) >= 16) ++s;
     return s;
