@@ -52,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b"], default=None,
+    p.add_argument("--only", choices=["gemv7b", "attn"], default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
 
@@ -327,6 +327,41 @@ def gemv_7b_roofline(torch, B, synth, device, peak):
             "algorithmic_bytes": algo, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak}
 
 
+def attention_microbench(torch, B, synth, device, peak):
+    """GQA decode attention at the 135M shape (9/3 heads of 64) and the 7B
+    shape (32/8 heads of 128), kv_len 32..4096, the decode step's kernel
+    (llama_q8_attention_decode), each launch on its own cache copy so that the
+    K/V rows stream from HBM (one 4096-position cache is 6.3 / 33.6 MB)."""
+    out = []
+    s = torch.cuda.current_stream()
+    for nh, nkv, hd in ((9, 3, 64), (32, 8, 128)):
+        stride = 4096
+        ncopy = 8 if hd == 64 else 4
+        kc = [torch.randn(nkv * stride * hd, device=device) for _ in range(ncopy)]
+        vc = [torch.randn(nkv * stride * hd, device=device) for _ in range(ncopy)]
+        q = torch.randn(nh * hd, device=device)
+        o = torch.empty(nh * hd, device=device)
+        for kv in (32, 256, 1024, 4096):
+            for i in range(8):
+                B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
+                                            s.cuda_stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 200
+            e0.record(s)
+            for i in range(n):
+                B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
+                                            s.cuda_stream)
+            e1.record(s)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000 / n
+            algo = 2 * nkv * kv * hd * 4 + 2 * nh * hd * 4
+            out.append({"heads": f"{nh}/{nkv}x{hd}", "kv_len": kv, "us": us, "gbs": algo / (us * 1e-6) / 1e9,
+                        "frac": algo / (us * 1e-6) / 1e9 / peak})
+        del kc, vc
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -405,6 +440,7 @@ def run_ours(args):
     out = None
     if rank == 0:
         gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
+        attn = attention_microbench(torch, B, synth, device, peak)
         dec_tok_ms = [d / DECODE_STEPS for d in dec_ms]
         out = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -437,6 +473,7 @@ def run_ours(args):
             "kernels": {k: {"launches": v[0], "ms": v[1], "gbs": (v[2] / (v[1] * 1e-3) / 1e9) if v[1] else None,
                             "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items()},
             "gemv_7b": gemv7,
+            "attention_decode": attn,
         }
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)
@@ -455,6 +492,15 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.only == "attn":
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        print(json.dumps({"attention_decode": attention_microbench(torch, B, synth, torch.device("cuda", 0),
+                                                                    hbm_peak()[0])}))
         return
     if args.only == "gemv7b":
         import torch

@@ -250,6 +250,20 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
                                    float* out, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/* Single-token grouped-query attention as the decode step runs it: out =
+ * softmax(q k^T / sqrt(head_dim)) v over cache positions [0, kv_len), query
+ * head h reading KV head h / (n_head / n_head_kv) ("生成一个 token", prefill
+ * 和 decode: the fused single-token kernel, query heads of a group sharing their
+ * KV head). q[n_head][head_dim]; k_cache, v_cache [n_head_kv][cache_stride]
+ * [head_dim]; out[n_head][head_dim]. One cluster of 8 CTAs per KV head splits
+ * the positions and merges its partial results through distributed shared
+ * memory, so no scratch memory is needed. Errors as llama_q8_attention.
+ * Enqueues on `stream` and returns. */
+llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache,
+                                          int32_t kv_len, int32_t n_head, int32_t n_head_kv,
+                                          int32_t head_dim, int32_t cache_stride, float* out,
+                                          void* stream);
+
 /* Allocation-free single-token attention. No counterpart on the pages: it is
  * a service to callers that cannot allocate device memory — a host that
  * hands all GPU memory to its own pool and accepts only the buffers it

@@ -30,7 +30,7 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_decode_kernel_count", "llama_q8_status_str", "llama_q8_quantize",
            "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul",
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
-           "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc")
+           "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode")
 
 
 class Q8Error(RuntimeError):
@@ -95,6 +95,7 @@ def lib() -> C.CDLL:
         "llama_q8_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
         "llama_q8_launch_count": (i64, [vp]),
         "llama_q8_attention_decode_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
+        "llama_q8_attention_decode": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "llama_q8_profile_decode": (i32, [vp, i32, C.POINTER(llama_q8_kernel_stat), i32, C.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
@@ -264,6 +265,13 @@ def llama_q8_attention(q, k_cache, v_cache, T: int, index_pos: int, n_head: int,
     check(lib().llama_q8_attention(ptr(q), ptr(k_cache), ptr(v_cache), T, index_pos, n_head, n_head_kv, head_dim,
                                    cache_stride, ptr(out), ptr(workspace), workspace_bytes, stream or None),
           "llama_q8_attention")
+
+
+def llama_q8_attention_decode(q, k_cache, v_cache, kv_len: int, n_head: int, n_head_kv: int, head_dim: int,
+                              cache_stride: int, out, stream=0) -> None:
+    """Single-token attention with the decode step's cluster kernel."""
+    check(lib().llama_q8_attention_decode(ptr(q), ptr(k_cache), ptr(v_cache), kv_len, n_head, n_head_kv, head_dim,
+                                          cache_stride, ptr(out), stream or None), "llama_q8_attention_decode")
 
 
 def llama_q8_attention_decode_noalloc(q, k_cache, v_cache, kv_len: int, n_head: int, n_head_kv: int,

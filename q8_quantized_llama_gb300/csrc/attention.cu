@@ -156,13 +156,7 @@ static constexpr size_t decode_smem_bytes(int hd) {
     return (size_t)(kChunk * (hd + 4) + kChunk * hd + kMaxGroup * hd + kMaxGroup * kChunk) * 4;
 }
 
-cudaError_t init_attention_attributes() {
-    cudaError_t err = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)decode_smem_bytes(64));
-    if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)decode_smem_bytes(128));
-}
+
 
 template <int HD>
 static cudaError_t attn_decode_launch(const float* q, const float* kc, const float* vc, int n_head,
@@ -193,6 +187,223 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
         return attn_decode_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
                                        workspace, pdl, s);
     return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Decode, cluster form (the decode step's kernel): one cluster of kClusterCtas
+// CTAs per KV head; CTA r takes an equal share of the cached positions and
+// walks it in 64-position sub-chunks (K/V rows streamed by bulk async copies,
+// two buffers, online softmax across sub-chunks). The group's query heads are
+// handled together, so each K/V row is read once. The CTAs' (max, sum,
+// weighted values) are merged by the cluster's first CTA through distributed
+// shared memory: no global scratch, no atomics.
+// ---------------------------------------------------------------------------
+constexpr int kClusterCtas = 8;
+constexpr int kSub = 64;
+
+template <int HD>
+struct ClusterSmem {
+    float K[2][kSub * HD];
+    float V[2][kSub * HD];
+    float Q[kMaxGroup * HD];
+    float P[kMaxGroup * kSub];
+    float O[kMaxGroup * HD];  // this CTA's unnormalised output (exchanged through DSMEM)
+    float M[kMaxGroup];
+    float L[kMaxGroup];
+    uint64_t bar[2];
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
+    const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int n_head, int n_kv,
+    int cache_stride, int kv_len_host, const DevState* st, float scale, float* __restrict__ out, int* err) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    ClusterSmem<HD>& S = *reinterpret_cast<ClusterSmem<HD>*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kh = blockIdx.x / kClusterCtas, rank = blockIdx.x % kClusterCtas;
+    const int G = n_head / n_kv;
+    const int kv_len = st ? st->pos + 1 : kv_len_host;
+    const int per = (kv_len + kClusterCtas - 1) / kClusterCtas;
+    const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
+    const int n_rows = j_end - j_begin;
+    const int n_sub = (n_rows + kSub - 1) / kSub;
+    // The newest position is written by the preceding kernel (QKV epilogue):
+    // everything older may be read before the grid dependency wait.
+    const int j_new = st ? kv_len - 1 : kv_len;
+    const float* kb = kc + (int64_t)kh * cache_stride * HD;
+    const float* vb = vc + (int64_t)kh * cache_stride * HD;
+
+    if (tid == 0) {
+        mbar_init(&S.bar[0], 1);
+        mbar_init(&S.bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // rows of sub-chunk i that are safe to copy before the wait
+    auto issue_sub = [&](int i, bool pre_wait) {
+        const int a = j_begin + i * kSub;
+        const int b = min(j_end, a + kSub);
+        const int c = pre_wait ? min(b, j_new) : b;
+        if (c > a) {
+            const uint32_t bytes = (uint32_t)(c - a) * HD * 4;
+            mbar_arrive_expect_tx(&S.bar[i & 1], 2 * bytes);
+            bulk_g2s(S.K[i & 1], kb + (int64_t)a * HD, bytes, &S.bar[i & 1]);
+            bulk_g2s(S.V[i & 1], vb + (int64_t)a * HD, bytes, &S.bar[i & 1]);
+        } else {
+            mbar_arrive(&S.bar[i & 1]);
+        }
+        return c;  // first row not yet copied
+    };
+    int first_missing = j_begin;
+    if (tid == 0 && n_sub > 0) first_missing = issue_sub(0, true);
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    for (int i = tid; i < G * HD; i += kDecThreads) S.Q[i] = q[(int64_t)kh * G * HD + i];
+    if (tid < kMaxGroup) {
+        S.M[tid] = -INFINITY;
+        S.L[tid] = 0.0f;
+    }
+    for (int i = tid; i < G * HD; i += kDecThreads) S.O[i] = 0.0f;
+    // rows of sub-chunk 0 not covered by the pre-wait copy (the newest row)
+    __shared__ int s_first_missing;
+    if (tid == 0) s_first_missing = first_missing;
+    __syncthreads();
+    if (n_sub > 0) {
+        const int a = s_first_missing, b = min(j_end, j_begin + kSub);
+        for (int f = tid; f < (b - a) * (HD / 4); f += kDecThreads) {
+            const int row = (a - j_begin) + f / (HD / 4), c4 = f % (HD / 4);
+            reinterpret_cast<float4*>(S.K[0] + row * HD)[c4] = reinterpret_cast<const float4*>(kb + (int64_t)(j_begin + row) * HD)[c4];
+            reinterpret_cast<float4*>(S.V[0] + row * HD)[c4] = reinterpret_cast<const float4*>(vb + (int64_t)(j_begin + row) * HD)[c4];
+        }
+    }
+    if (tid == 0 && n_sub > 1) issue_sub(1, false);
+
+    for (int i = 0; i < n_sub; ++i) {
+        const int buf = i & 1;
+        const int n = min(kSub, n_rows - i * kSub);
+        mbar_wait_bounded(&S.bar[buf], (i >> 1) & 1, err, 14);
+        __syncthreads();  // plain-load rows of sub-chunk 0 are visible too
+        // scores: thread j < n, all heads of the group; rotated chunk order
+        // keeps the row-per-thread reads free of bank conflicts
+        if (tid < n) {
+            const float* kr = S.K[buf] + tid * HD;
+            for (int g = 0; g < G; ++g) {
+                const float* qg = S.Q + g * HD;
+                float acc = 0.0f;
+#pragma unroll 8
+                for (int c = 0; c < HD / 4; ++c) {
+                    const int cc = (c + tid) & (HD / 4 - 1);
+                    const float4 kk = reinterpret_cast<const float4*>(kr)[cc];
+                    const float4 qq = reinterpret_cast<const float4*>(qg)[cc];
+                    acc = fmaf(qq.x, kk.x, acc); acc = fmaf(qq.y, kk.y, acc);
+                    acc = fmaf(qq.z, kk.z, acc); acc = fmaf(qq.w, kk.w, acc);
+                }
+                S.P[g * kSub + tid] = acc * scale;
+            }
+        }
+        __syncthreads();
+        // online softmax statistics per head (one warp per head)
+        __shared__ float s_corr[kMaxGroup];
+        for (int g = warp; g < G; g += kDecThreads / 32) {
+            const float a = lane < n ? S.P[g * kSub + lane] : -INFINITY;
+            const float b = lane + 32 < n ? S.P[g * kSub + lane + 32] : -INFINITY;
+            const float m_old = S.M[g];
+            const float m_new = fmaxf(m_old, warp_max(fmaxf(a, b)));
+            const float ea = lane < n ? expf(a - m_new) : 0.0f;
+            const float eb = lane + 32 < n ? expf(b - m_new) : 0.0f;
+            S.P[g * kSub + lane] = ea;
+            S.P[g * kSub + lane + 32] = eb;
+            const float sum = warp_sum(ea + eb);
+            if (lane == 0) {
+                const float corr = expf(m_old - m_new);  // 0 on the first sub-chunk
+                s_corr[g] = corr;
+                S.L[g] = S.L[g] * corr + sum;
+                S.M[g] = m_new;
+            }
+        }
+        __syncthreads();
+        for (int o = tid; o < G * HD; o += kDecThreads) {
+            const int g = o / HD, d = o % HD;
+            const float* pg = S.P + g * kSub;
+            float acc = S.O[o] * s_corr[g];
+            for (int j = 0; j < n; ++j) acc = fmaf(pg[j], S.V[buf][j * HD + d], acc);
+            S.O[o] = acc;
+        }
+        __syncthreads();  // buffer buf is free again
+        if (tid == 0 && i + 2 < n_sub) issue_sub(i + 2, false);
+    }
+
+    // ---- merge the cluster's partial results on rank 0 ----------------------
+    cluster_sync();
+    if (rank == 0) {
+        for (int o = tid; o < G * HD; o += kDecThreads) {
+            const int g = o / HD;
+            float M = -INFINITY;
+            for (int r = 0; r < kClusterCtas; ++r) M = fmaxf(M, ld_dsmem_f32(&S.M[g], (uint32_t)r));
+            float Lsum = 0.0f, acc = 0.0f;
+            for (int r = 0; r < kClusterCtas; ++r) {
+                const float m_r = ld_dsmem_f32(&S.M[g], (uint32_t)r);
+                const float w = m_r == -INFINITY ? 0.0f : expf(m_r - M);
+                Lsum = fmaf(w, ld_dsmem_f32(&S.L[g], (uint32_t)r), Lsum);
+                acc = fmaf(w, ld_dsmem_f32(&S.O[o], (uint32_t)r), acc);
+            }
+            out[(int64_t)kh * G * HD + o] = acc / Lsum;
+        }
+    }
+    cluster_sync();  // peers keep their shared memory until rank 0 has read it
+}
+
+template <int HD>
+static cudaError_t attn_cluster_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv,
+                                       int cache_stride, int kv_len, const DevState* st, float* out, bool pdl,
+                                       int* err, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_kv * kClusterCtas);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = sizeof(ClusterSmem<HD>);
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = kClusterCtas;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    int n = 1;
+    if (pdl) {
+        attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[1].val.programmaticStreamSerializationAllowed = 1;
+        n = 2;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    const float scale = 1.0f / sqrtf((float)HD);
+    return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD>, q, kc, vc, n_head, n_kv, cache_stride, kv_len, st,
+                              scale, out, err);
+}
+
+cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
+                                       int n_head_kv, int head_dim, int cache_stride, int kv_len,
+                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
+    if (head_dim == 64)
+        return attn_cluster_launch<64>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+                                       err, s);
+    if (head_dim == 128)
+        return attn_cluster_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+                                        err, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t init_attention_attributes() {
+    cudaError_t err = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)decode_smem_bytes(64));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)decode_smem_bytes(128));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(attn_decode_cluster_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(ClusterSmem<64>));
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(attn_decode_cluster_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(ClusterSmem<128>));
 }
 
 // ---------------------------------------------------------------------------

@@ -27,8 +27,8 @@ namespace lq8 {
 
 constexpr int kCWarps = 8;                        // consumer warps
 constexpr int kGemvThreads = (kCWarps + 1) * 32;  // + one producer warp
-constexpr int kStageBlocks = 8;                   // blocks per stage (a multiple of kCWarps)
-constexpr int kStages = 6;
+constexpr int kStageBlocks = 16;                  // blocks per stage (a multiple of kCWarps)
+constexpr int kStages = 3;
 constexpr int kStageCodeBytes = kStageBlocks * 1024;
 constexpr int kStageBytes = kStageCodeBytes + kStageBlocks * 64;
 constexpr int kGemvMaxSmem = 227 * 1024 - 4096;
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     float* xs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ __align__(8) uint64_t empty[kStages];
+    __shared__ __align__(8) uint64_t xbar;
     __shared__ float red[kCWarps][33];
     __shared__ float part[32];
     __shared__ float s_rscale;
@@ -120,11 +121,19 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     const int n_stage = (nblk + kStageBlocks - 1) / kStageBlocks;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    // The activation vector goes to shared memory by one bulk copy issued after
+    // the grid dependency wait: the whole vector when the fused RMSNorm needs
+    // all of it on a split unit, else only this unit's slice.
+    const bool x_full = NORM && S > 1;
+    const int x0 = b0 * 32, xn = nblk * 32;
+    float* xslice = x_full ? xs + x0 : xs;
+
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCWarps);
         }
+        mbar_init(&xbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -134,7 +143,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         if (lane == 0) {
             const uint8_t* gcodes = reinterpret_cast<const uint8_t*>(W.qs) + (size_t)tile * k * 32;
             const uint8_t* gscales = reinterpret_cast<const uint8_t*>(W.d) + (size_t)tile * nb * 64;
-            for (int j = 0; j < n_stage; ++j) {
+            auto issue_stage = [&](int j) {
                 const int slot = j % kStages;
                 if (j >= kStages) mbar_wait_bounded(&empty[slot], ((j / kStages) - 1) & 1, a.err, 9);
                 const int bs = b0 + j * kStageBlocks;
@@ -143,18 +152,26 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbs * 1024 + nbs * 64));
                 bulk_g2s(dst, gcodes + (size_t)bs * 1024, nbs * 1024, &full[slot]);
                 bulk_g2s(dst + kStageCodeBytes, gscales + (size_t)bs * 64, nbs * 64, &full[slot]);
-            }
+            };
+            const int first = min(kStages, n_stage);
+            for (int j = 0; j < first; ++j) issue_stage(j);  // weights: no kernel writes them
+            pdl_wait();                                      // x: written by the preceding kernel
+            const int xoff = x_full ? 0 : x0, xcnt = x_full ? k : xn;
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(xcnt * 4));
+            bulk_g2s(xs, a.x + xoff, (uint32_t)(xcnt * 4), &xbar);
+            for (int j = first; j < n_stage; ++j) issue_stage(j);
         }
     } else {
         // ---- consumers --------------------------------------------------------
-        pdl_wait();  // x is written by the preceding kernel
+        pdl_wait();
         if (tid == 0) pdl_launch_dependents();
         constexpr int kCT = kCWarps * 32;
-        float r = 1.0f;
+        mbar_wait_bounded(&xbar, 0, a.err, 13);
         if (NORM) {
+            const int nx = x_full ? k : xn;  // == k when unsplit
             float ss = 0.0f;
-            for (int i = tid * 4; i < k; i += kCT * 4) {
-                const float4 v = *reinterpret_cast<const float4*>(a.x + i);
+            for (int i = tid * 4; i < nx; i += kCT * 4) {
+                const float4 v = *reinterpret_cast<const float4*>(xs + i);
                 ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
                 ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
             }
@@ -168,18 +185,15 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 s_rscale = 1.0f / sqrtf(t / (float)k + a.eps);
             }
             named_bar_sync(1, kCT);
-            r = s_rscale;
-        }
-        const int x0 = b0 * 32, xn = nblk * 32;
-        for (int i = tid * 4; i < xn; i += kCT * 4) {
-            float4 v = *reinterpret_cast<const float4*>(a.x + x0 + i);
-            if (NORM) {
+            const float r = s_rscale;
+            for (int i = tid * 4; i < xn; i += kCT * 4) {
+                float4 v = *reinterpret_cast<float4*>(xslice + i);
                 const float4 gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
                 v.x = v.x * r * gg.x; v.y = v.y * r * gg.y; v.z = v.z * r * gg.z; v.w = v.w * r * gg.w;
+                *reinterpret_cast<float4*>(xslice + i) = v;
             }
-            *reinterpret_cast<float4*>(xs + i) = v;
+            named_bar_sync(1, kCT);
         }
-        named_bar_sync(1, kCT);
 
         float acc = 0.0f;
         for (int j = 0; j < n_stage; ++j) {
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                     const uint4 q1 = *reinterpret_cast<const uint4*>(st + bi * 1024 + 512 + lane * 16);
                     const float d =
                         __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[bi * 32 + lane]);
-                    acc = fmaf(d, block_dot32(q0, q1, xs + (bs + bi) * 32), acc);
+                    acc = fmaf(d, block_dot32(q0, q1, xslice + (bs + bi) * 32), acc);
                 }
             }
             __syncwarp();
@@ -252,7 +266,8 @@ static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const floa
     const int tiles = W.rows_pad / 32, nb = W.k / 32;
     const int S = gemv_splits(tiles, nb, sm_count_current());
     const int max_blk = (nb + S - 1) / S;
-    const size_t smem = (size_t)kStages * kStageBytes + (size_t)max_blk * 32 * sizeof(float);
+    const size_t x_floats = (NORM && S > 1) ? (size_t)W.k : (size_t)max_blk * 32;
+    const size_t smem = (size_t)kStages * kStageBytes + x_floats * sizeof(float);
     if (smem > (size_t)kGemvMaxSmem) return cudaErrorInvalidValue;
     GemvArgs a{W, x, g, eps, e, S, err};
     cudaLaunchConfig_t cfg = {};

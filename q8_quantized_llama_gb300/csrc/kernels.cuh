@@ -109,6 +109,9 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
                                int n_head, int n_head_kv, int head_dim, int cache_stride,
                                int kv_len, const DevState* st, float* out, void* workspace,
                                bool pdl, cudaStream_t s);
+cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
+                                       int n_head_kv, int head_dim, int cache_stride, int kv_len,
+                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s);
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache,
                                 int T, int index_pos, int n_head, int n_head_kv, int head_dim,
                                 int cache_stride, float* out, bool pdl, cudaStream_t s);

@@ -226,8 +226,9 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
         run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr),
             [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
         run(F_ATTN, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
-            return launch_attn_decode(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv, cfg.head_dim,
-                                      cfg.max_seq, 0, c->d_state, c->d_o, c->d_attn_ws, pdl, s);
+            return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
+                                              cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
+                                              &c->d_state->err, s);
         });
         EpiArgs r;
         r.y = c->d_x;
@@ -809,6 +810,21 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
     } else {
         err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
     }
+    return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
+}
+
+llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache, int32_t kv_len,
+                                         int32_t n_head, int32_t n_head_kv, int32_t head_dim, int32_t cache_stride,
+                                         float* out, void* stream) {
+    if (!q || !k_cache || !v_cache || !out || kv_len <= 0 || n_head <= 0 || n_head_kv <= 0 ||
+        n_head % n_head_kv || cache_stride <= 0)
+        return LQ8_ERR_ARG;
+    if (kv_len > cache_stride) return LQ8_ERR_CTX;
+    if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
+    if (n_head / n_head_kv > 8) return LQ8_ERR_UNSUPPORTED;
+    if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
+    cudaError_t err = launch_attn_decode_cluster(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride,
+                                                 kv_len, nullptr, out, false, nullptr, (cudaStream_t)stream);
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
 

@@ -123,7 +123,7 @@ def test_matmul_tensor_core_7b_prefill_shapes(rows, k):
 
 # ------------------------------------------------------------------ attention
 
-def _attention_case(T, index_pos, nh, nkv, hd, stride, seed):
+def _attention_case(T, index_pos, nh, nkv, hd, stride, seed, entry="attention"):
     B = binding()
     kv_len = index_pos + T
     q = synth.normal_f32((T, nh, hd), seed, 1)
@@ -135,7 +135,10 @@ def _attention_case(T, index_pos, nh, nkv, hd, stride, seed):
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.full((T, nh, hd), float("nan"), dtype=torch.float32, device="cuda")
     dq, dk, dv = to_dev(q), to_dev(kc), to_dev(vc)
-    B.llama_q8_attention(dq, dk, dv, T, index_pos, nh, nkv, hd, stride, out, ws, ws_bytes)
+    if entry == "attention":
+        B.llama_q8_attention(dq, dk, dv, T, index_pos, nh, nkv, hd, stride, out, ws, ws_bytes)
+    else:
+        B.llama_q8_attention_decode(dq, dk, dv, kv_len, nh, nkv, hd, stride, out)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     k = np.transpose(kc[:, :kv_len], (1, 0, 2))
@@ -171,6 +174,16 @@ def test_attention_prefill_135m(T, index_pos):
 @pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8)])
 def test_attention_prefill_7b(T, index_pos):
     _attention_case(T, index_pos, 32, 8, 128, 4096, seed=T * 3 + index_pos)
+
+
+@pytest.mark.parametrize("kv_len", [1, 5, 8, 9, 63, 64, 65, 331, 513, 1024, 4096])
+def test_attention_decode_cluster_135m(kv_len):
+    _attention_case(1, kv_len - 1, 9, 3, 64, 4096, seed=kv_len + 7, entry="decode")
+
+
+@pytest.mark.parametrize("kv_len", [1, 32, 768, 1024, 4096])
+def test_attention_decode_cluster_7b(kv_len):
+    _attention_case(1, kv_len - 1, 32, 8, 128, 4096, seed=kv_len + 9, entry="decode")
 
 
 def test_attention_two_calls_reuse_workspace():
