@@ -52,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b", "attn"], default=None,
+    p.add_argument("--only", choices=["gemv7b", "attn", "gemm"], default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
 
@@ -327,6 +327,40 @@ def gemv_7b_roofline(torch, B, synth, device, peak):
             "algorithmic_bytes": algo, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak}
 
 
+def gemm_microbench(torch, B, synth, device):
+    """Q8_0 matrix-matrix products on the tensor cores: the pages' QMatMul
+    shape [203,1536]x[1536,576] ("速度", CPU GGUF), the 135M prefill shapes at
+    203 rows, and 7B prefill shapes at 512 rows. Algorithmic TFLOP/s =
+    2*m*rows*k / time (the split-TF32 path issues three MMAs per product)."""
+    out = []
+    s = torch.cuda.current_stream()
+    for m, rows, k in ((203, 576, 1536), (203, 960, 576), (203, 3072, 576), (512, 6144, 4096), (512, 28672, 4096),
+                       (512, 4096, 14336)):
+        w = synth.weight_matrix_f32(rows, k, 5, stream=rows + k)
+        dw = torch.from_numpy(w).to(device)
+        q = torch.empty((rows, k // 32 * 34), dtype=torch.uint8, device=device)
+        B.llama_q8_quantize(dw, rows, k, q)
+        packed = torch.empty(B.llama_q8_packed_bytes(rows, k), dtype=torch.uint8, device=device)
+        B.llama_q8_pack(q, rows, k, packed)
+        del dw, q
+        x = torch.from_numpy(synth.normal_f32((m, k), 5, 1)).to(device)
+        y = torch.empty((m, rows), dtype=torch.float32, device=device)
+        for _ in range(3):
+            B.llama_q8_matmul(packed, rows, k, x, m, y, s.cuda_stream)
+        n = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(n):
+            B.llama_q8_matmul(packed, rows, k, x, m, y, s.cuda_stream)
+        e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000 / n
+        out.append({"shape": f"[{m},{k}]x[{k},{rows}]", "us": us, "tflops": 2.0 * m * rows * k / (us * 1e-6) / 1e12})
+        del packed, x, y
+        torch.cuda.empty_cache()
+    return out
+
+
 def attention_microbench(torch, B, synth, device, peak):
     """GQA decode attention at the 135M shape (9/3 heads of 64) and the 7B
     shape (32/8 heads of 128), kv_len 32..4096, the decode step's kernel
@@ -441,6 +475,7 @@ def run_ours(args):
     if rank == 0:
         gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
         attn = attention_microbench(torch, B, synth, device, peak)
+        gemm = gemm_microbench(torch, B, synth, device)
         dec_tok_ms = [d / DECODE_STEPS for d in dec_ms]
         out = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -474,6 +509,7 @@ def run_ours(args):
                             "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items()},
             "gemv_7b": gemv7,
             "attention_decode": attn,
+            "gemm_prefill": gemm,
         }
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)
@@ -492,6 +528,14 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.only == "gemm":
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        print(json.dumps({"gemm": gemm_microbench(torch, B, synth, torch.device("cuda", 0))}))
         return
     if args.only == "attn":
         import torch

@@ -12,11 +12,12 @@
 // in TMEM; the dropped w_lo.x_lo term is below 2^-22 relative.
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-step 32 (one Q8_0
-// block = one 128-byte swizzle row of tf32). All 8 warps dequantise/split the
-// next k-block into a 3-slot shared-memory ring (128-byte swizzled K-major
-// layout the MMA reads through its descriptors) while the tensor core works on
-// the previous ones; one thread issues the MMAs and commits each slot to an
-// mbarrier that releases it. The epilogue reads TMEM with tcgen05.ld (warp w
+// block = one 128-byte swizzle row of tf32). Raw k-blocks (codes, scales,
+// activation rows) arrive by cp.async three blocks ahead; all 8 warps
+// dequantise/split the current block into one of two operand slots
+// (128-byte swizzled K-major layout the MMA reads through its descriptors)
+// while the tensor core works on the other; one thread issues the MMAs and
+// commits each slot to an mbarrier that releases it. The epilogue reads TMEM with tcgen05.ld (warp w
 // reads lanes 32*(w%4).., column half w/4) and applies the shared epilogues.
 #include "epilogue.cuh"
 #include "ptx.cuh"
@@ -25,11 +26,13 @@ namespace lq8 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
-constexpr int kTcSlots = 3;
+constexpr int kTcSlots = 2;                     // operand slots (ping-pong with the tensor core)
 constexpr int kTcThreads = 256;
 constexpr int kTileBytes = 128 * 128;           // 128 rows x 128 bytes
 constexpr int kSlotBytes = 4 * kTileBytes;      // A_hi, A_lo, B_hi, B_lo
-constexpr int kTcSmem = kTcSlots * kSlotBytes + 1024;  // + alignment slack
+constexpr int kRawStages = 4;                   // raw k-blocks in flight (cp.async)
+constexpr int kRawBytes = 4096 + 256 + 128 * 128;  // codes, scales, activations of one k-block
+constexpr int kTcSmem = kTcSlots * kSlotBytes + kRawStages * kRawBytes + 1024;  // + alignment slack
 
 // ---- tcgen05 wrappers ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
@@ -113,11 +116,25 @@ __device__ __forceinline__ void dequant16(const uint4& q, float d, float (&w)[16
     }
 }
 
+// ---- cp.async (16-byte global -> shared copies, zero-filled when src_bytes = 0)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, const float* __restrict__ X, int m,
                                                                     int ldx, EpiArgs e, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ops = smem;                                 // kTcSlots operand slots (A_hi, A_lo, B_hi, B_lo)
+    uint8_t* raw = smem + kTcSlots * kSlotBytes;         // kRawStages raw k-blocks
     __shared__ __align__(8) uint64_t mma_done[kTcSlots];
     __shared__ uint32_t tmem_holder;
 
@@ -125,6 +142,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     const int k = W.k, nb = k >> 5;
     const int m0 = blockIdx.x * kTcBM;  // weight rows
     const int t0 = blockIdx.y * kTcBN;  // tokens
+    const int tile0 = m0 >> 5;
+    const int n_tiles = W.rows_pad >> 5;
 
     if (tid == 0) {
         for (int s = 0; s < kTcSlots; ++s) mbar_init(&mma_done[s], 1);
@@ -139,40 +158,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     pdl_wait();
     if (tid == 0) pdl_launch_dependents();
 
-    // this thread's share of a k-block: one 16-code half-row of A, four 4-float chunks of B
-    const int a_row = tid >> 1, a_half = tid & 1;
-    const int a_n = m0 + a_row;
-    const bool a_ok = a_n < W.rows_pad;
-    const int64_t a_tile = a_n >> 5, a_lane = a_n & 31;
-    uint4 qa = make_uint4(0, 0, 0, 0);
-    float da = 0.0f;
-    float4 xb[4];
-
-    auto load_block = [&](int kb) {
-        if (a_ok) {
-            qa = *reinterpret_cast<const uint4*>(W.qs + ((a_tile * (k >> 4) + 2 * kb + a_half) * 512 + a_lane * 16));
-            da = __half2float(W.d[(a_tile * nb + kb) * 32 + a_lane]);
+    // Raw k-block: codes of the CTA's 4 row tiles (1 KiB each, contiguous in
+    // the packed layout), their scales (64 B each) and the 128 token rows of
+    // activations (128 B each). Thread tid copies 16 B of codes, threads < 16
+    // 16 B of scales, and 4 x 16 B of activations.
+    auto issue_raw = [&](int kb) {
+        uint8_t* r = raw + (kb % kRawStages) * kRawBytes;
+        {
+            const int t = tid >> 6, within = (tid & 63) * 16;
+            const bool ok = tile0 + t < n_tiles;
+            const int8_t* src = W.qs + ((int64_t)(ok ? tile0 + t : 0) * k * 32 + (int64_t)kb * 1024 + within);
+            cp_async16(r + t * 1024 + within, src, ok ? 16u : 0u);
+        }
+        if (tid < 16) {
+            const int t = tid >> 2, within = (tid & 3) * 16;
+            const bool ok = tile0 + t < n_tiles;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(W.d) +
+                                 ((int64_t)(ok ? tile0 + t : 0) * nb + kb) * 64 + within;
+            cp_async16(r + 4096 + t * 64 + within, src, ok ? 16u : 0u);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int f = tid + i * kTcThreads;
             const int row = f >> 3, c = f & 7;
-            const int t = t0 + row;
-            xb[i] = t < m ? *reinterpret_cast<const float4*>(X + (int64_t)t * ldx + kb * 32 + c * 4)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            const bool ok = t0 + row < m;
+            const float* src = X + (int64_t)(ok ? t0 + row : 0) * ldx + kb * 32 + c * 4;
+            cp_async16(r + 4096 + 256 + row * 128 + c * 16, src, ok ? 16u : 0u);
         }
+        cp_async_commit();
     };
 
-    load_block(0);
+    for (int j = 0; j < kRawStages - 1; ++j) {
+        if (j < nb) issue_raw(j);
+        else cp_async_commit();  // keep the group count uniform
+    }
+
+    const int a_row = tid >> 1, a_half = tid & 1;
     for (int kb = 0; kb < nb; ++kb) {
+        cp_async_wait<kRawStages - 2>();
+        __syncthreads();  // raw block kb complete for every thread; raw slot (kb-1) fully converted
+        if (kb + kRawStages - 1 < nb) issue_raw(kb + kRawStages - 1);
+        else cp_async_commit();
         const int slot = kb % kTcSlots;
         if (kb >= kTcSlots) mbar_wait_bounded(&mma_done[slot], ((kb / kTcSlots) - 1) & 1, err, 11);
-        uint8_t* sA_hi = smem + slot * kSlotBytes;
+        const uint8_t* r = raw + (kb % kRawStages) * kRawBytes;
+        uint8_t* sA_hi = ops + slot * kSlotBytes;
         uint8_t* sA_lo = sA_hi + kTileBytes;
         uint8_t* sB_hi = sA_lo + kTileBytes;
         uint8_t* sB_lo = sB_hi + kTileBytes;
-        // A: dequantise, split, store 4 chunks of this half-row
         {
+            const int t = a_row >> 5, ln = a_row & 31;
+            const uint4 qa = *reinterpret_cast<const uint4*>(r + t * 1024 + a_half * 512 + ln * 16);
+            const float da = __half2float(reinterpret_cast<const __half*>(r + 4096)[t * 32 + ln]);
             float w[16];
             dequant16(qa, da, w);
 #pragma unroll
@@ -187,12 +224,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
                 *reinterpret_cast<float4*>(sA_lo + off) = lo;
             }
         }
-        // B: split the activations
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int f = tid + i * kTcThreads;
             const int row = f >> 3, c = f & 7;
-            const float4 x = xb[i];
+            const float4 x = *reinterpret_cast<const float4*>(r + 4096 + 256 + row * 128 + c * 16);
             float4 hi, lo;
             hi.x = tf32_rna(x.x); lo.x = x.x - hi.x;
             hi.y = tf32_rna(x.y); lo.y = x.y - hi.y;
@@ -202,7 +238,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
             *reinterpret_cast<float4*>(sB_hi + off) = hi;
             *reinterpret_cast<float4*>(sB_lo + off) = lo;
         }
-        if (kb + 1 < nb) load_block(kb + 1);  // global loads of the next block overlap the MMAs
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -219,6 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
             mma_commit(&mma_done[slot]);
         }
     }
+    cp_async_wait<0>();
     // all MMAs are complete once the last slot's commit has arrived
     mbar_wait_bounded(&mma_done[(nb - 1) % kTcSlots], ((nb - 1) / kTcSlots) & 1, err, 12);
     tc_fence_after();
