@@ -192,11 +192,12 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
 // ---------------------------------------------------------------------------
 // Decode, cluster form (the decode step's kernel): one cluster of kClusterCtas
 // CTAs per KV head; CTA r takes an equal share of the cached positions and
-// walks it in 64-position sub-chunks (K/V rows streamed by bulk async copies,
-// two buffers, online softmax across sub-chunks). The group's query heads are
-// handled together, so each K/V row is read once. The CTAs' (max, sum,
-// weighted values) are merged by the cluster's first CTA through distributed
-// shared memory: no global scratch, no atomics.
+// walks it in 64-position sub-chunks (K/V rows by cp.async, two buffers,
+// online softmax across sub-chunks). The group's query heads are handled
+// together, so each K/V row is read once. Each CTA stores its (max, sum,
+// weighted values) straight into the first CTA's shared memory through the
+// cluster's distributed shared memory; one cluster barrier later the first
+// CTA merges them: no global scratch, no atomics.
 // ---------------------------------------------------------------------------
 constexpr int kClusterCtas = 8;
 constexpr int kSub = 64;
@@ -207,11 +208,25 @@ struct ClusterSmem {
     float V[2][kSub * HD];
     float Q[kMaxGroup * HD];
     float P[kMaxGroup * kSub];
-    float O[kMaxGroup * HD];  // this CTA's unnormalised output (exchanged through DSMEM)
+    float O[kMaxGroup * HD];                   // this CTA's running unnormalised output
     float M[kMaxGroup];
     float L[kMaxGroup];
-    uint64_t bar[2];
+    float corr[kMaxGroup];
+    float PO[kClusterCtas][kMaxGroup * HD];    // rank 0: the cluster's partial outputs
+    float PM[kClusterCtas][kMaxGroup];
+    float PL[kClusterCtas][kMaxGroup];
 };
+
+__device__ __forceinline__ void cp_async16_attn(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_attn() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void st_dsmem_f32(float* local_ptr, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
@@ -232,78 +247,98 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
     const int j_new = st ? kv_len - 1 : kv_len;
     const float* kb = kc + (int64_t)kh * cache_stride * HD;
     const float* vb = vc + (int64_t)kh * cache_stride * HD;
+    constexpr int C4 = HD / 4;  // float4 chunks per row
 
-    if (tid == 0) {
-        mbar_init(&S.bar[0], 1);
-        mbar_init(&S.bar[1], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    // rows of sub-chunk i that are safe to copy before the wait
-    auto issue_sub = [&](int i, bool pre_wait) {
-        const int a = j_begin + i * kSub;
-        const int b = min(j_end, a + kSub);
-        const int c = pre_wait ? min(b, j_new) : b;
-        if (c > a) {
-            const uint32_t bytes = (uint32_t)(c - a) * HD * 4;
-            mbar_arrive_expect_tx(&S.bar[i & 1], 2 * bytes);
-            bulk_g2s(S.K[i & 1], kb + (int64_t)a * HD, bytes, &S.bar[i & 1]);
-            bulk_g2s(S.V[i & 1], vb + (int64_t)a * HD, bytes, &S.bar[i & 1]);
-        } else {
-            mbar_arrive(&S.bar[i & 1]);
+    // copy rows [a, b) of sub-chunk i into buffer i&1 (one commit group)
+    auto copy_rows = [&](int i, int a, int b) {
+        const int base = j_begin + i * kSub;
+        for (int f = tid; f < (b - a) * C4; f += kDecThreads) {
+            const int row = a - base + f / C4, c = f % C4;
+            cp_async16_attn(S.K[i & 1] + row * HD + c * 4, kb + (int64_t)(base + row) * HD + c * 4);
+            cp_async16_attn(S.V[i & 1] + row * HD + c * 4, vb + (int64_t)(base + row) * HD + c * 4);
         }
-        return c;  // first row not yet copied
     };
-    int first_missing = j_begin;
-    if (tid == 0 && n_sub > 0) first_missing = issue_sub(0, true);
+    int split0 = j_begin;
+    if (n_sub > 0) {
+        const int b = min(j_end, j_begin + kSub);
+        split0 = min(b, j_new);
+        if (split0 < j_begin) split0 = j_begin;
+        copy_rows(0, j_begin, split0);  // cached rows, before the wait
+    }
     pdl_wait();
     if (tid == 0) pdl_launch_dependents();
-    for (int i = tid; i < G * HD; i += kDecThreads) S.Q[i] = q[(int64_t)kh * G * HD + i];
+    if (n_sub > 0) copy_rows(0, split0, min(j_end, j_begin + kSub));  // the newest row, if it is here
+    cp_async_commit_attn();
+    if (n_sub > 1) copy_rows(1, j_begin + kSub, min(j_end, j_begin + 2 * kSub));
+    cp_async_commit_attn();
+    for (int i = tid; i < G * HD; i += kDecThreads) {
+        S.Q[i] = q[(int64_t)kh * G * HD + i];
+        S.O[i] = 0.0f;
+    }
     if (tid < kMaxGroup) {
         S.M[tid] = -INFINITY;
         S.L[tid] = 0.0f;
     }
-    for (int i = tid; i < G * HD; i += kDecThreads) S.O[i] = 0.0f;
-    // rows of sub-chunk 0 not covered by the pre-wait copy (the newest row)
-    __shared__ int s_first_missing;
-    if (tid == 0) s_first_missing = first_missing;
-    __syncthreads();
-    if (n_sub > 0) {
-        const int a = s_first_missing, b = min(j_end, j_begin + kSub);
-        for (int f = tid; f < (b - a) * (HD / 4); f += kDecThreads) {
-            const int row = (a - j_begin) + f / (HD / 4), c4 = f % (HD / 4);
-            reinterpret_cast<float4*>(S.K[0] + row * HD)[c4] = reinterpret_cast<const float4*>(kb + (int64_t)(j_begin + row) * HD)[c4];
-            reinterpret_cast<float4*>(S.V[0] + row * HD)[c4] = reinterpret_cast<const float4*>(vb + (int64_t)(j_begin + row) * HD)[c4];
-        }
-    }
-    if (tid == 0 && n_sub > 1) issue_sub(1, false);
 
     for (int i = 0; i < n_sub; ++i) {
         const int buf = i & 1;
         const int n = min(kSub, n_rows - i * kSub);
-        mbar_wait_bounded(&S.bar[buf], (i >> 1) & 1, err, 14);
-        __syncthreads();  // plain-load rows of sub-chunk 0 are visible too
-        // scores: thread j < n, all heads of the group; rotated chunk order
-        // keeps the row-per-thread reads free of bank conflicts
-        if (tid < n) {
-            const float* kr = S.K[buf] + tid * HD;
+        cp_async_wait_all_but_one();
+        __syncthreads();
+        // scores: 4 threads per position, each a quarter of the head dimension
+        {
+            const int row = tid >> 2, part = tid & 3;
+            const float* kr = S.K[buf] + row * HD + part * (HD / 4);
             for (int g = 0; g < G; ++g) {
-                const float* qg = S.Q + g * HD;
-                float acc = 0.0f;
-#pragma unroll 8
-                for (int c = 0; c < HD / 4; ++c) {
-                    const int cc = (c + tid) & (HD / 4 - 1);
-                    const float4 kk = reinterpret_cast<const float4*>(kr)[cc];
-                    const float4 qq = reinterpret_cast<const float4*>(qg)[cc];
-                    acc = fmaf(qq.x, kk.x, acc); acc = fmaf(qq.y, kk.y, acc);
-                    acc = fmaf(qq.z, kk.z, acc); acc = fmaf(qq.w, kk.w, acc);
+                const float* qg = S.Q + g * HD + part * (HD / 4);
+                float a0 = 0.0f, a1 = 0.0f;
+                if (row < n) {
+#pragma unroll
+                    for (int d = 0; d < HD / 4; d += 8) {
+                        const float4 k0 = *reinterpret_cast<const float4*>(kr + d);
+                        const float4 k1 = *reinterpret_cast<const float4*>(kr + d + 4);
+                        const float4 q0 = *reinterpret_cast<const float4*>(qg + d);
+                        const float4 q1 = *reinterpret_cast<const float4*>(qg + d + 4);
+                        a0 = fmaf(q0.x, k0.x, a0); a0 = fmaf(q0.y, k0.y, a0);
+                        a0 = fmaf(q0.z, k0.z, a0); a0 = fmaf(q0.w, k0.w, a0);
+                        a1 = fmaf(q1.x, k1.x, a1); a1 = fmaf(q1.y, k1.y, a1);
+                        a1 = fmaf(q1.z, k1.z, a1); a1 = fmaf(q1.w, k1.w, a1);
+                    }
                 }
-                S.P[g * kSub + tid] = acc * scale;
+                float sc = a0 + a1;
+                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+                if (part == 0 && row < kSub) S.P[g * kSub + row] = sc * scale;
+            }
+            // rows 32..63 of the sub-chunk
+            if (kSub > kDecThreads / 4) {
+                const int row2 = row + kDecThreads / 4;
+                const float* kr2 = S.K[buf] + row2 * HD + part * (HD / 4);
+                for (int g = 0; g < G; ++g) {
+                    const float* qg = S.Q + g * HD + part * (HD / 4);
+                    float a0 = 0.0f, a1 = 0.0f;
+                    if (row2 < n) {
+#pragma unroll
+                        for (int d = 0; d < HD / 4; d += 8) {
+                            const float4 k0 = *reinterpret_cast<const float4*>(kr2 + d);
+                            const float4 k1 = *reinterpret_cast<const float4*>(kr2 + d + 4);
+                            const float4 q0 = *reinterpret_cast<const float4*>(qg + d);
+                            const float4 q1 = *reinterpret_cast<const float4*>(qg + d + 4);
+                            a0 = fmaf(q0.x, k0.x, a0); a0 = fmaf(q0.y, k0.y, a0);
+                            a0 = fmaf(q0.z, k0.z, a0); a0 = fmaf(q0.w, k0.w, a0);
+                            a1 = fmaf(q1.x, k1.x, a1); a1 = fmaf(q1.y, k1.y, a1);
+                            a1 = fmaf(q1.z, k1.z, a1); a1 = fmaf(q1.w, k1.w, a1);
+                        }
+                    }
+                    float sc = a0 + a1;
+                    sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                    sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+                    if (part == 0 && row2 < kSub) S.P[g * kSub + row2] = sc * scale;
+                }
             }
         }
         __syncthreads();
         // online softmax statistics per head (one warp per head)
-        __shared__ float s_corr[kMaxGroup];
         for (int g = warp; g < G; g += kDecThreads / 32) {
             const float a = lane < n ? S.P[g * kSub + lane] : -INFINITY;
             const float b = lane + 32 < n ? S.P[g * kSub + lane + 32] : -INFINITY;
@@ -316,7 +351,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
             const float sum = warp_sum(ea + eb);
             if (lane == 0) {
                 const float corr = expf(m_old - m_new);  // 0 on the first sub-chunk
-                s_corr[g] = corr;
+                S.corr[g] = corr;
                 S.L[g] = S.L[g] * corr + sum;
                 S.M[g] = m_new;
             }
@@ -325,32 +360,54 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
         for (int o = tid; o < G * HD; o += kDecThreads) {
             const int g = o / HD, d = o % HD;
             const float* pg = S.P + g * kSub;
-            float acc = S.O[o] * s_corr[g];
-            for (int j = 0; j < n; ++j) acc = fmaf(pg[j], S.V[buf][j * HD + d], acc);
-            S.O[o] = acc;
+            const float* vcol = S.V[buf] + d;
+            float a0 = 0.0f, a1 = 0.0f;
+            int j = 0;
+            for (; j + 1 < n; j += 2) {
+                a0 = fmaf(pg[j], vcol[j * HD], a0);
+                a1 = fmaf(pg[j + 1], vcol[(j + 1) * HD], a1);
+            }
+            if (j < n) a0 = fmaf(pg[j], vcol[j * HD], a0);
+            S.O[o] = fmaf(S.O[o], S.corr[g], a0 + a1);
         }
         __syncthreads();  // buffer buf is free again
-        if (tid == 0 && i + 2 < n_sub) issue_sub(i + 2, false);
+        if (i + 2 < n_sub) copy_rows(i + 2, j_begin + (i + 2) * kSub, min(j_end, j_begin + (i + 3) * kSub));
+        cp_async_commit_attn();
     }
 
-    // ---- merge the cluster's partial results on rank 0 ----------------------
+    // ---- push this CTA's partial result into rank 0, then merge there --------
+    if (rank == 0) {
+        for (int o = tid; o < G * HD; o += kDecThreads) S.PO[0][o] = S.O[o];
+        if (tid < G) {
+            S.PM[0][tid] = S.M[tid];
+            S.PL[0][tid] = S.L[tid];
+        }
+    } else {
+        for (int o = tid; o < G * HD; o += kDecThreads) st_dsmem_f32(&S.PO[rank][o], 0, S.O[o]);
+        if (tid < G) {
+            st_dsmem_f32(&S.PM[rank][tid], 0, S.M[tid]);
+            st_dsmem_f32(&S.PL[rank][tid], 0, S.L[tid]);
+        }
+    }
     cluster_sync();
     if (rank == 0) {
         for (int o = tid; o < G * HD; o += kDecThreads) {
             const int g = o / HD;
             float M = -INFINITY;
-            for (int r = 0; r < kClusterCtas; ++r) M = fmaxf(M, ld_dsmem_f32(&S.M[g], (uint32_t)r));
+#pragma unroll
+            for (int r = 0; r < kClusterCtas; ++r) M = fmaxf(M, S.PM[r][g]);
             float Lsum = 0.0f, acc = 0.0f;
+#pragma unroll
             for (int r = 0; r < kClusterCtas; ++r) {
-                const float m_r = ld_dsmem_f32(&S.M[g], (uint32_t)r);
+                const float m_r = S.PM[r][g];
                 const float w = m_r == -INFINITY ? 0.0f : expf(m_r - M);
-                Lsum = fmaf(w, ld_dsmem_f32(&S.L[g], (uint32_t)r), Lsum);
-                acc = fmaf(w, ld_dsmem_f32(&S.O[o], (uint32_t)r), acc);
+                Lsum = fmaf(w, S.PL[r][g], Lsum);
+                acc = fmaf(w, S.PO[r][o], acc);
             }
             out[(int64_t)kh * G * HD + o] = acc / Lsum;
         }
     }
-    cluster_sync();  // peers keep their shared memory until rank 0 has read it
+    (void)err;
 }
 
 template <int HD>
