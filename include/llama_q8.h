@@ -73,6 +73,9 @@ typedef struct llama_q8_config {
     float rms_eps;        /* 1e-5 */
     float rope_theta;     /* 10000 */
     int32_t tied_output;  /* 1: the head is token_embd (no output.weight) */
+    int32_t decode_kernel; /* decode step: 0 = automatic (embedding and all layers as ONE
+                              cluster kernel whenever the model's activations fit in shared
+                              memory, else per-layer kernels), 1 = per-layer kernels */
 } llama_q8_config;
 
 typedef struct llama_q8_layer_weights {
@@ -170,7 +173,9 @@ llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0,
  * the _async calls. */
 void* llama_q8_stream(llama_q8_ctx* ctx);
 
-/* Number of kernel launches one decode step makes (the CUDA-graph nodes). */
+/* Number of kernel launches one decode step makes (the CUDA-graph nodes):
+ * 2 with the one-cluster layer kernel (layers, then lm_head + argmax),
+ * n_layer * 5 + 2 with per-layer kernels. */
 int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx);
 
 /* Cumulative number of kernel launches this context has issued; a CUDA-graph

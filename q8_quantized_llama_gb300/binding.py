@@ -47,7 +47,7 @@ class llama_q8_config(C.Structure):
     _fields_ = [("n_layer", C.c_int32), ("n_embd", C.c_int32), ("n_head", C.c_int32),
                 ("n_head_kv", C.c_int32), ("head_dim", C.c_int32), ("n_ff", C.c_int32),
                 ("n_vocab", C.c_int32), ("max_seq", C.c_int32), ("rms_eps", C.c_float),
-                ("rope_theta", C.c_float), ("tied_output", C.c_int32)]
+                ("rope_theta", C.c_float), ("tied_output", C.c_int32), ("decode_kernel", C.c_int32)]
 
 
 class llama_q8_layer_weights(C.Structure):
@@ -129,7 +129,8 @@ def check(status: int, where: str) -> None:
 def make_config(cfg: dict) -> llama_q8_config:
     return llama_q8_config(cfg["n_layer"], cfg["n_embd"], cfg["n_head"], cfg["n_head_kv"], cfg["head_dim"],
                            cfg["n_ff"], cfg["n_vocab"], cfg.get("max_seq", 4096), cfg.get("rms_eps", 1e-5),
-                           cfg.get("rope_theta", 10000.0), int(cfg.get("tied_output", 1)))
+                           cfg.get("rope_theta", 10000.0), int(cfg.get("tied_output", 1)),
+                           int(cfg.get("decode_kernel", 0)))
 
 
 _LAYER_KEYS = ("attn_norm", "ffn_norm", "attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up",

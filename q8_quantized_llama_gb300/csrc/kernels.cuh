@@ -116,6 +116,29 @@ cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const floa
                                 int T, int index_pos, int n_head, int n_head_kv, int head_dim,
                                 int cache_stride, float* out, bool pdl, cudaStream_t s);
 
+// decode_cluster.cu: the per-layer part of a decode step as one cluster
+struct LayerPtrs {
+    PackedQ8 qkv, o, gu, down;
+    const float* attn_norm;
+    const float* ffn_norm;
+    float* kc;  // [n_kv][max_seq][hd]
+    float* vc;
+};
+struct ClusterStepArgs {
+    const LayerPtrs* layers;
+    int n_layer;
+    PackedQ8 embd;
+    int n_vocab, h, n_head, n_kv, hd, ff, max_seq;
+    float eps, scale;
+    const float* rope_cos;
+    const float* rope_sin;
+    DevState* st;
+    float* x_out;  // final residual stream for the lm_head kernel
+    int* err;
+};
+int decode_cluster_size(int h, int n_head, int n_kv, int hd, int ff);
+cudaError_t launch_decode_cluster(int cl, const ClusterStepArgs& args, cudaStream_t s);
+
 PackedQ8 packed_view(const uint8_t* base, int64_t rows, int64_t k);
 
 }  // namespace lq8

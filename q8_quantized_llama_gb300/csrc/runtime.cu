@@ -54,17 +54,19 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 struct Profiler {
     struct Rec {
         int family;
-        double bytes;  // algorithmic bytes of the launch (attention: per cached position)
+        double bytes;       // algorithmic bytes of the launch, fixed part
+        double kv_per_pos;  // plus this many bytes per cached position (K/V reads)
         cudaEvent_t a, b;
     };
     std::vector<Rec> recs;
     cudaStream_t s = nullptr;
     cudaEvent_t cur_a = nullptr;
     int cur = -1;
-    double cur_bytes = 0;
-    cudaError_t begin(int family, double bytes) {
+    double cur_bytes = 0, cur_kv = 0;
+    cudaError_t begin(int family, double bytes, double kv_per_pos) {
         cur = family;
         cur_bytes = bytes;
+        cur_kv = kv_per_pos;
         cudaError_t e = cudaEventCreate(&cur_a);
         if (e == cudaSuccess) e = cudaEventRecordWithFlags(cur_a, s, cudaEventRecordExternal);
         return e;
@@ -73,7 +75,7 @@ struct Profiler {
         cudaEvent_t b = nullptr;
         cudaError_t e = cudaEventCreate(&b);
         if (e == cudaSuccess) e = cudaEventRecordWithFlags(b, s, cudaEventRecordExternal);
-        recs.push_back({cur, cur_bytes, cur_a, b});
+        recs.push_back({cur, cur_bytes, cur_kv, cur_a, b});
         cur_a = nullptr;
         return e;
     }
@@ -86,9 +88,10 @@ struct Profiler {
     }
 };
 
-enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_COUNT };
+enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_COUNT };
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
-                                     "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax"};
+                                     "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
+                                     "decode_cluster_layers"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -135,6 +138,8 @@ struct llama_q8_ctx {
 
     int len = 0;
     int64_t launches = 0;
+    int cluster = 0;                     // > 0: decode layers run as one cluster of this many CTAs
+    LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
     int decode_kernels = 0;
@@ -160,7 +165,7 @@ void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
                    c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_logits, c->d_ids, c->d_out_ids,
-                   c->d_state, c->d_best, c->d_done, c->d_attn_ws};
+                   c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_layer_ptrs};
     for (void* p : dev)
         if (p) cudaFree(p);
     void* host[] = {c->h_ids, c->h_out, c->h_logits, c->h_state};
@@ -210,38 +215,70 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
     const int64_t h = cfg.n_embd, F = cfg.n_ff, qr = c->q_rows, kvr = c->kv_rows;
     int n = 0;
     cudaError_t err = cudaSuccess;
-    auto run = [&](int fam, double bytes, auto&& launch) {
+    auto run = [&](int fam, double bytes, double kv_per_pos, auto&& launch) {
         if (err != cudaSuccess) return;
-        if (prof) err = prof->begin(fam, bytes);
+        if (prof) err = prof->begin(fam, bytes, kv_per_pos);
         if (err == cudaSuccess) err = launch();
         if (err == cudaSuccess && prof) err = prof->end();
         ++n;
     };
-    run(F_EMBED, q8_bytes(1, h) + 4.0 * h,
+    if (c->cluster > 0) {
+        // embedding + all layers in one cluster kernel, then the lm_head on the whole GPU
+        double wbytes = 0.0;
+        for (int l = 0; l < cfg.n_layer; ++l)
+            wbytes += q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + q8_bytes(2 * F, h) + q8_bytes(h, F) + 8.0 * h;
+        ClusterStepArgs a{};
+        a.layers = c->d_layer_ptrs;
+        a.n_layer = cfg.n_layer;
+        a.embd = c->embd;
+        a.n_vocab = cfg.n_vocab;
+        a.h = cfg.n_embd;
+        a.n_head = cfg.n_head;
+        a.n_kv = cfg.n_head_kv;
+        a.hd = cfg.head_dim;
+        a.ff = cfg.n_ff;
+        a.max_seq = cfg.max_seq;
+        a.eps = cfg.rms_eps;
+        a.scale = 1.0f / sqrtf((float)cfg.head_dim);
+        a.rope_cos = c->d_rope_cos;
+        a.rope_sin = c->d_rope_sin;
+        a.st = c->d_state;
+        a.x_out = c->d_x;
+        a.err = &c->d_state->err;
+        run(F_CLUSTER, wbytes + q8_bytes(1, h) + 4.0 * h, 8.0 * (double)cfg.n_head_kv * cfg.head_dim * cfg.n_layer,
+            [&] { return launch_decode_cluster(c->cluster, a, s); });
+        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
+            return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
+                               &c->d_state->err, s);
+        });
+        if (n_kernels) *n_kernels = n;
+        return err;
+    }
+    run(F_EMBED, q8_bytes(1, h) + 4.0 * h, 0.0,
         [&] { return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, pdl, s); });
     for (int l = 0; l < cfg.n_layer; ++l) {
         const LayerDev& L = c->layers[l];
         EpiArgs e = qkv_epi(c, l);
         e.state = c->d_state;
-        run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr),
+        run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0,
             [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
-        run(F_ATTN, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
+        run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
             return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
                                               cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
                                               &c->d_state->err, s);
         });
         EpiArgs r;
         r.y = c->d_x;
-        run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h,
+        run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h, 0.0,
             [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
         EpiArgs g;
         g.a_out = c->d_a;
-        run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F,
+        run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F, 0.0,
             [&] { return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s); });
-        run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h,
+        run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
             [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
     }
-    run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab,
+    run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0,
         [&] { return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl, &c->d_state->err, s); });
     if (n_kernels) *n_kernels = n;
     return err;
@@ -378,6 +415,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         C.n_vocab <= 0 || C.max_seq <= 0 || C.head_dim <= 0 || !(C.rms_eps >= 0.f) || !(C.rope_theta > 0.f))
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
+    if (C.decode_kernel < 0 || C.decode_kernel > 1) return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -543,6 +581,26 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_logits, sizeof(float) * V));
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
+    // decode path: the whole layer stack as one cluster when it fits
+    if (C.decode_kernel == 0) {
+        c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);
+        cudaGetLastError();
+    }
+    if (c->cluster > 0) {
+        std::vector<LayerPtrs> lp(L);
+        for (int l = 0; l < L; ++l) {
+            lp[l].qkv = c->layers[l].qkv;
+            lp[l].o = c->layers[l].o;
+            lp[l].gu = c->layers[l].gu;
+            lp[l].down = c->layers[l].down;
+            lp[l].attn_norm = c->layers[l].attn_norm;
+            lp[l].ffn_norm = c->layers[l].ffn_norm;
+            lp[l].kc = c->kcache(l);
+            lp[l].vc = c->vcache(l);
+        }
+        LOAD_CK(cudaMalloc(&c->d_layer_ptrs, sizeof(LayerPtrs) * L));
+        LOAD_CK(cudaMemcpy(c->d_layer_ptrs, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice));
+    }
     LOAD_CK(ensure_decode_graph(c));
 #undef LOAD_CK
     c->len = 0;
@@ -692,7 +750,7 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
             if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, r.a, r.b);
             stats[r.family].launches += 1;
             stats[r.family].ms += ms;
-            stats[r.family].bytes += r.family == F_ATTN ? r.bytes * kv_len + 8.0 * ctx->q_rows : r.bytes;
+            stats[r.family].bytes += r.bytes + r.kv_per_pos * kv_len;
         }
     }
     cudaGraphExecDestroy(exec);

@@ -25,12 +25,20 @@ def m135():
     for name, t in dev_t.items():     # the GPU quantiser matches the oracle's bytes
         if ora_t[name].dtype == np.uint8:
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
-    model = B.Model(CFG, dev_t, on_device=True)
+    model = B.Model(CFG, dev_t, on_device=True)                              # one-cluster decode step
+    layered = B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True)      # per-layer decode kernels
     del dev_t
     torch.cuda.empty_cache()
     oracle = O.ModelWeights(CFG, ora_t, weight_cache="f64")
-    yield model, oracle
+    yield model, oracle, layered
     model.close()
+    layered.close()
+
+
+@pytest.fixture(params=["cluster", "layered"])
+def either(request, m135):
+    model, oracle, layered = m135
+    return (model if request.param == "cluster" else layered), oracle
 
 
 def _check_run(model, oracle, prompt, n_decode):
@@ -51,8 +59,8 @@ def _check_run(model, oracle, prompt, n_decode):
     return ora_ids
 
 
-def test_generation_13_prompt_20_decode(m135):
-    model, oracle = m135
+def test_generation_13_prompt_20_decode(either):
+    model, oracle = either
     prompt = synth.prompt_ids(13, V, 0)
     ids = _check_run(model, oracle, prompt, 20)
     # the graph-replay generation loop gives the same tokens
@@ -60,16 +68,16 @@ def test_generation_13_prompt_20_decode(m135):
     assert model.cache_len() == 33
 
 
-def test_generation_203_prompt_128_decode(m135):
-    model, oracle = m135
+def test_generation_203_prompt_128_decode(either):
+    model, oracle = either
     prompt = synth.prompt_ids(203, V, 0)
     ids = _check_run(model, oracle, prompt, 128)
     for _ in range(2):  # fresh cache each repetition, same tokens
         np.testing.assert_array_equal(model.generate(prompt, 128), ids)
 
 
-def test_kv_cache_after_rope_matches_oracle(m135):
-    model, oracle = m135
+def test_kv_cache_after_rope_matches_oracle(either):
+    model, oracle = either
     prompt = synth.prompt_ids(13, V, 5)
     oracle.forward(prompt, 0)
     model.forward(prompt, 0)
@@ -86,7 +94,7 @@ def test_kv_cache_after_rope_matches_oracle(m135):
 
 
 def test_index_pos_rules(m135):
-    model, _ = m135
+    model, _, _ = m135
     B = binding()
     prompt = synth.prompt_ids(13, V, 1)
     full = model.forward(prompt, 0)
@@ -117,7 +125,7 @@ def test_index_pos_rules(m135):
 
 
 def test_context_limit(m135):
-    model, _ = m135
+    model, _, _ = m135
     B = binding()
     prompt = synth.prompt_ids(64, V, 2)
     assert model.forward_status(np.zeros(4097, np.int32), 0) == B.LQ8_ERR_CTX
@@ -131,8 +139,8 @@ def test_context_limit(m135):
     assert model.cache_len() == 4096
 
 
-def test_prefill_and_decode_paths_agree(m135):
-    model, oracle = m135
+def test_prefill_and_decode_paths_agree(either):
+    model, oracle = either
     seq = synth.prompt_ids(40, V, 4)
     whole = model.forward(seq, 0)                       # matrix-matrix path
     model.forward(seq[:39], 0)
@@ -144,7 +152,7 @@ def test_prefill_and_decode_paths_agree(m135):
 
 
 def test_device_resident_api(m135):
-    model, _ = m135
+    model, _, layered = m135
     prompt = synth.prompt_ids(203, V, 0)
     ref = model.generate(prompt, 16)
     d_ids = torch.from_numpy(prompt).cuda()
@@ -156,4 +164,5 @@ def test_device_resident_api(m135):
     got = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
     np.testing.assert_array_equal(got, ref)
     assert model.cache_len() == 203 + 16
-    assert model.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
+    assert model.decode_kernel_count() == 2                    # layers in one cluster + lm_head
+    assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
