@@ -293,8 +293,11 @@ def gpu_model(torch, B, synth, device):
 
 def gemv_7b_roofline(torch, B, synth, device, peak):
     """The Q8_0 GEMV at the 7B shape [1,4096]x[4096,14336], timed with CUDA
-    events over back-to-back launches that rotate through 8 weight copies
-    (8 x 62.4 MB > L2), so every launch streams its matrix from HBM."""
+    events over 400 back-to-back launches that rotate through 8 weight copies
+    (8 x 62.4 MB > L2), so every launch streams its matrix from HBM. Two forms:
+    "chained" lets each launch start its weight stream while the previous one
+    finishes (the way the decode step chains its projections), "serial" waits
+    for the previous launch to end before the next one starts."""
     rows, k = 14336, 4096
     w = synth.weight_matrix_f32(rows, k, 1)
     dw = torch.from_numpy(w).to(device)
@@ -308,23 +311,28 @@ def gemv_7b_roofline(torch, B, synth, device, peak):
     x = torch.from_numpy(synth.normal_f32((1, k), 1, 7)).to(device)
     y = torch.empty((1, rows), dtype=torch.float32, device=device)
     s = torch.cuda.current_stream()
-    for i in range(16):
-        B.llama_q8_matmul(copies[i % 8], rows, k, x, 1, y, s.cuda_stream)
-    n = 400
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(s)
-    for i in range(n):
-        B.llama_q8_matmul(copies[i % 8], rows, k, x, 1, y, s.cuda_stream)
-    e1.record(s)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1000 / n
     algo = rows * k * 34 / 32 + 4 * k + 4 * rows
-    gbs = algo / (us * 1e-6) / 1e9
+    res = {}
+    for form, flags in (("serial", 0), ("chained", B.LQ8_MATMUL_EARLY_WEIGHTS)):
+        for i in range(16):
+            B.llama_q8_matmul_ex(copies[i % 8], rows, k, x, 1, y, flags, s.cuda_stream)
+        n = 400
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for i in range(n):
+            B.llama_q8_matmul_ex(copies[i % 8], rows, k, x, 1, y, flags, s.cuda_stream)
+        e1.record(s)
+        torch.cuda.synchronize()
+        res[form] = e0.elapsed_time(e1) * 1000 / n
     del copies
     torch.cuda.empty_cache()
+    us = res["chained"]
+    gbs = algo / (us * 1e-6) / 1e9
     return {"kernel": "q8_gemv_kernel<EPI_STORE>", "shape": "[1,4096]x[4096,14336]", "us": us,
-            "algorithmic_bytes": algo, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak}
+            "form": "chained launches (weight stream starts before the previous launch ends)",
+            "algorithmic_bytes": algo, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+            "serial_us": res["serial"], "serial_frac": algo / (res["serial"] * 1e-6) / 1e9 / peak}
 
 
 def gemm_microbench(torch, B, synth, device):

@@ -73,9 +73,10 @@ typedef struct llama_q8_config {
     float rms_eps;        /* 1e-5 */
     float rope_theta;     /* 10000 */
     int32_t tied_output;  /* 1: the head is token_embd (no output.weight) */
-    int32_t decode_kernel; /* decode step: 0 = automatic (embedding and all layers as ONE
-                              cluster kernel whenever the model's activations fit in shared
-                              memory, else per-layer kernels), 1 = per-layer kernels */
+    int32_t decode_kernel; /* decode step: 0 = automatic (per-layer kernels, the faster form
+                              on the models measured), 1 = per-layer kernels, 2 = embedding
+                              and all layers as ONE cluster kernel (LQ8_ERR_UNSUPPORTED at
+                              load when the activations do not fit in shared memory) */
 } llama_q8_config;
 
 typedef struct llama_q8_layer_weights {
@@ -174,8 +175,8 @@ llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0,
 void* llama_q8_stream(llama_q8_ctx* ctx);
 
 /* Number of kernel launches one decode step makes (the CUDA-graph nodes):
- * 2 with the one-cluster layer kernel (layers, then lm_head + argmax),
- * n_layer * 5 + 2 with per-layer kernels. */
+ * n_layer * 5 + 2 with per-layer kernels, 2 with the one-cluster layer kernel
+ * (layers, then lm_head + argmax). */
 int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx);
 
 /* Cumulative number of kernel launches this context has issued; a CUDA-graph
@@ -235,6 +236,16 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
  * about 2^-22 relative error per product). */
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
                                 int64_t m, float* y, void* stream);
+
+/* llama_q8_matmul with flags. LQ8_MATMUL_EARLY_WEIGHTS: the kernel may start
+ * streaming W before the kernel enqueued just before it on `stream` has
+ * finished (programmatic dependent launch; x is still read, and y written,
+ * only after that kernel has completed). Set it only when no kernel in flight
+ * on the stream writes W; it is how the decode step chains its projections.
+ * Unknown flag bits -> LQ8_ERR_ARG. */
+#define LQ8_MATMUL_EARLY_WEIGHTS 1
+llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, const float* x,
+                                   int64_t m, float* y, int32_t flags, void* stream);
 
 /* Grouped-query attention over a KV cache: for each of T queries at
  * positions index_pos + t, out = softmax(q k^T / sqrt(head_dim) + mask) v,

@@ -28,7 +28,7 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_prefill_async", "llama_q8_decode_async", "llama_q8_sync", "llama_q8_reset",
            "llama_q8_free", "llama_q8_cache_len", "llama_q8_read_kv", "llama_q8_stream",
            "llama_q8_decode_kernel_count", "llama_q8_status_str", "llama_q8_quantize",
-           "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul",
+           "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul", "llama_q8_matmul_ex",
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
            "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode")
 
@@ -91,6 +91,7 @@ def lib() -> C.CDLL:
         "llama_q8_packed_bytes": (sz, [i64, i64]),
         "llama_q8_pack": (i32, [vp, i64, i64, vp, vp]),
         "llama_q8_matmul": (i32, [vp, i64, i64, vp, i64, vp, vp]),
+        "llama_q8_matmul_ex": (i32, [vp, i64, i64, vp, i64, vp, i32, vp]),
         "llama_q8_attention_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "llama_q8_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
         "llama_q8_launch_count": (i64, [vp]),
@@ -255,6 +256,14 @@ def llama_q8_pack(q8, rows: int, k: int, packed, stream=0) -> None:
 
 def llama_q8_matmul(packed, rows: int, k: int, x, m: int, y, stream=0) -> None:
     check(lib().llama_q8_matmul(ptr(packed), rows, k, ptr(x), m, ptr(y), stream or None), "llama_q8_matmul")
+
+
+LQ8_MATMUL_EARLY_WEIGHTS = 1
+
+
+def llama_q8_matmul_ex(packed, rows: int, k: int, x, m: int, y, flags: int, stream=0) -> None:
+    check(lib().llama_q8_matmul_ex(ptr(packed), rows, k, ptr(x), m, ptr(y), flags, stream or None),
+          "llama_q8_matmul_ex")
 
 
 def llama_q8_attention_workspace_bytes(n_head: int, n_head_kv: int, head_dim: int, cache_stride: int) -> int:

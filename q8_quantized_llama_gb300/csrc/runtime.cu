@@ -415,7 +415,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         C.n_vocab <= 0 || C.max_seq <= 0 || C.head_dim <= 0 || !(C.rms_eps >= 0.f) || !(C.rope_theta > 0.f))
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
-    if (C.decode_kernel < 0 || C.decode_kernel > 1) return LQ8_ERR_ARG;
+    if (C.decode_kernel < 0 || C.decode_kernel > 2) return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -581,10 +581,15 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_logits, sizeof(float) * V));
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
-    // decode path: the whole layer stack as one cluster when it fits
-    if (C.decode_kernel == 0) {
+    // decode path: the whole layer stack as one cluster when asked for and it fits
+    if (C.decode_kernel == 2) {
         c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);
         cudaGetLastError();
+        if (c->cluster <= 0) {
+            free_ctx_memory(c);
+            delete c;
+            return LQ8_ERR_UNSUPPORTED;
+        }
     }
     if (c->cluster > 0) {
         std::vector<LayerPtrs> lp(L);
@@ -854,7 +859,14 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
 
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x, int64_t m, float* y,
                                 void* stream) {
+    return llama_q8_matmul_ex(packed, rows, k, x, m, y, 0, stream);
+}
+
+llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, const float* x, int64_t m, float* y,
+                                   int32_t flags, void* stream) {
     if (!packed || !x || !y || rows <= 0 || k <= 0 || k % 32 || m <= 0) return LQ8_ERR_ARG;
+    if (flags & ~LQ8_MATMUL_EARLY_WEIGHTS) return LQ8_ERR_ARG;
+    const bool early = (flags & LQ8_MATMUL_EARLY_WEIGHTS) != 0;
     if (rows > (1 << 30) || m > (1 << 30)) return LQ8_ERR_UNSUPPORTED;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
     PackedQ8 W = packed_view(reinterpret_cast<const uint8_t*>(packed), rows, k);
@@ -864,9 +876,9 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
     cudaError_t err;
     if (m == 1) {
         if ((size_t)k > gemv_max_k()) return LQ8_ERR_UNSUPPORTED;
-        err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
+        err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
     } else {
-        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, false, nullptr, (cudaStream_t)stream);
+        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }

@@ -51,6 +51,7 @@ def test_null_arguments_rejected_without_a_gpu(B):
     assert L.llama_q8_free(None) == B.LQ8_OK
     assert L.llama_q8_quantize(None, 1, 32, None, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_matmul(None, 1, 32, None, 1, None, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_matmul_ex(None, 1, 32, None, 1, None, 0, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_attention(None, None, None, 1, 0, 9, 3, 64, 4096, None, None, 0, None) == B.LQ8_ERR_ARG
 
 
@@ -62,7 +63,8 @@ def test_config_validation_without_a_gpu(B):
     t = {n: dummy for n, _, _ in synth.model_tensor_specs(cfg)}
     for bad, status in [(dict(head_dim=96), B.LQ8_ERR_UNSUPPORTED), (dict(n_embd=500), B.LQ8_ERR_UNSUPPORTED),
                         (dict(n_head_kv=4), B.LQ8_ERR_ARG), (dict(n_layer=0), B.LQ8_ERR_ARG),
-                        (dict(tied_output=0), B.LQ8_ERR_ARG)]:
+                        (dict(tied_output=0), B.LQ8_ERR_ARG), (dict(decode_kernel=3), B.LQ8_ERR_ARG),
+                        (dict(decode_kernel=-1), B.LQ8_ERR_ARG)]:
         c = B.make_config(dict(cfg, **bad))
         w, keep = B.make_weights(cfg, t, on_device=False)
         out = C.c_void_p()

@@ -116,6 +116,35 @@ def test_matmul_ragged_edges(rows, k, m):
     _matmul_case(rows, k, m, seed=4)
 
 
+def test_matmul_early_weights_chain_equals_serial_calls():
+    """A chain of matrix-vector calls whose weight streams start before the
+    previous call ends (each call reading the previous call's output) gives
+    the same bytes as the same calls made one at a time."""
+    B = binding()
+    rows = k = 1024
+    mats = []
+    for i in range(3):
+        w = synth.weight_matrix_f32(rows, k, 6, stream=i)
+        mats.append(_packed(gpu_quantize(w), rows, k))
+    x0 = to_dev(synth.normal_f32((1, k), 6, 9))
+    ys = [torch.empty((1, rows), dtype=torch.float32, device="cuda") for _ in range(6)]
+
+    def run(flags):
+        src = x0
+        for i in range(6):
+            B.llama_q8_matmul_ex(mats[i % 3], rows, k, src, 1, ys[i], flags)
+            src = ys[i]
+        torch.cuda.synchronize()
+        return [y.cpu().numpy().copy() for y in ys]
+
+    serial = run(0)
+    chained = run(B.LQ8_MATMUL_EARLY_WEIGHTS)
+    for a, b in zip(serial, chained):
+        np.testing.assert_array_equal(a, b)
+    with pytest.raises(B.Q8Error):
+        B.llama_q8_matmul_ex(mats[0], rows, k, x0, 1, ys[0], 2)
+
+
 @pytest.mark.parametrize("rows,k", [(4096, 4096), (6144, 4096), (4096, 14336)])
 def test_matmul_tensor_core_7b_prefill_shapes(rows, k):
     _matmul_case(rows, k, 512, seed=5)

@@ -25,8 +25,8 @@ def m135():
     for name, t in dev_t.items():     # the GPU quantiser matches the oracle's bytes
         if ora_t[name].dtype == np.uint8:
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
-    model = B.Model(CFG, dev_t, on_device=True)                              # one-cluster decode step
-    layered = B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True)      # per-layer decode kernels
+    model = B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True)      # one-cluster decode step
+    layered = B.Model(CFG, dev_t, on_device=True)                            # automatic: per-layer kernels
     del dev_t
     torch.cuda.empty_cache()
     oracle = O.ModelWeights(CFG, ora_t, weight_cache="f64")
