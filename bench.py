@@ -372,10 +372,11 @@ def gemm_microbench(torch, B, synth, device):
 def attention_microbench(torch, B, synth, device, peak):
     """GQA decode attention at the 135M shape (9/3 heads of 64) and the 7B
     shape (32/8 heads of 128), kv_len 32..4096, the decode step's kernel
-    (llama_q8_attention_decode), each launch on its own cache copy so that the
-    K/V rows stream from HBM (one 4096-position cache is 6.3 / 33.6 MB)."""
+    (llama_q8_attention_decode). 100 launches, each on its own cache copy so
+    that the K/V rows stream from HBM (one 4096-position cache is 6.3 / 33.6
+    MB), are captured in a CUDA graph and replayed: the per-launch time is the
+    kernel plus the graph's launch-to-launch gap, without host overhead."""
     out = []
-    s = torch.cuda.current_stream()
     for nh, nkv, hd in ((9, 3, 64), (32, 8, 128)):
         stride = 4096
         ncopy = 8 if hd == 64 else 4
@@ -384,17 +385,27 @@ def attention_microbench(torch, B, synth, device, peak):
         q = torch.randn(nh * hd, device=device)
         o = torch.empty(nh * hd, device=device)
         for kv in (32, 256, 1024, 4096):
+            s = torch.cuda.current_stream()
             for i in range(8):
                 B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
                                             s.cuda_stream)
+            torch.cuda.synchronize()
+            n = 100
+            g = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            with torch.cuda.graph(g, stream=cs):
+                for i in range(n):
+                    B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
+                                                cs.cuda_stream)
+            g.replay()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = 200
+            s = torch.cuda.current_stream()
             e0.record(s)
-            for i in range(n):
-                B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
-                                            s.cuda_stream)
+            g.replay()
             e1.record(s)
             torch.cuda.synchronize()
+            del g
             us = e0.elapsed_time(e1) * 1000 / n
             algo = 2 * nkv * kv * hd * 4 + 2 * nh * hd * 4
             out.append({"heads": f"{nh}/{nkv}x{hd}", "kv_len": kv, "us": us, "gbs": algo / (us * 1e-6) / 1e9,

@@ -271,10 +271,12 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
  * head h reading KV head h / (n_head / n_head_kv) ("生成一个 token", prefill
  * 和 decode: the fused single-token kernel, query heads of a group sharing their
  * KV head). q[n_head][head_dim]; k_cache, v_cache [n_head_kv][cache_stride]
- * [head_dim]; out[n_head][head_dim]. One cluster of 8 CTAs per KV head splits
- * the positions and merges its partial results through distributed shared
- * memory, so no scratch memory is needed. Errors as llama_q8_attention.
- * Enqueues on `stream` and returns. */
+ * [head_dim]; out[n_head][head_dim]. One cluster of 16 CTAs per KV head (8
+ * when the clusters of all KV heads cannot be resident together) splits the
+ * positions, streams K/V rows with bulk async copies and merges its partial
+ * results through distributed shared memory, so no scratch memory is needed. k_cache and v_cache must be
+ * 16-byte aligned (LQ8_ERR_ARG otherwise); other errors as
+ * llama_q8_attention. Enqueues on `stream` and returns. */
 llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache,
                                           int32_t kv_len, int32_t n_head, int32_t n_head_kv,
                                           int32_t head_dim, int32_t cache_stride, float* out,

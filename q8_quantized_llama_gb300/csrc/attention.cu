@@ -190,238 +190,312 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
 }
 
 // ---------------------------------------------------------------------------
-// Decode, cluster form (the decode step's kernel): one cluster of kClusterCtas
-// CTAs per KV head; CTA r takes an equal share of the cached positions and
-// walks it in 64-position sub-chunks (K/V rows by cp.async, two buffers,
-// online softmax across sub-chunks). The group's query heads are handled
-// together, so each K/V row is read once. Each CTA stores its (max, sum,
-// weighted values) straight into the first CTA's shared memory through the
-// cluster's distributed shared memory; one cluster barrier later the first
-// CTA merges them: no global scratch, no atomics.
+// Decode, cluster form (the decode step's kernel): one cluster of CL CTAs per
+// KV head (CL = 16 when all the heads' clusters can be resident at once, else
+// 8); CTA r takes an equal share of the positions. The share is walked in
+// windows of up to 256 positions, each in two passes over 64-position stages
+// that a producer warp streams (one bulk copy per stage) through a 4-deep
+// ring of shared-memory stages:
+//   K pass  lane c of a warp holds float4 chunk c of every query head of the
+//           group in registers and multiplies it into chunk c of the warp's
+//           rows (one conflict-free 128-bit load per row); a butterfly
+//           reduce-scatter over the lanes of a row then leaves one finished
+//           (row, head) score in each lane;
+//   softmax warp g updates head g's running max and sum over the window and
+//           turns its scores into weights in place;
+//   V pass  thread (d4, slice) accumulates the float4 of output dims d4 for
+//           every head over its slice of positions (the group's weights of a
+//           position in one broadcast load).
+// The V rows of a window are requested as soon as a stage is free, so they
+// overlap the K pass and the softmax. K/V rows cached by earlier steps are
+// requested before the grid dependency wait, the newest row after it. The
+// slices are summed in shared memory and every CTA stores its (max, sum,
+// weighted values) into the first CTA's shared memory through distributed
+// shared memory; one cluster barrier later the first CTA merges them. All the
+// group's query heads share each K/V row read ("生成一个 token": the KV heads
+// are shared inside the kernel, no repeat_kv copy). GP is the group size
+// rounded up to 4 or 8; the padding heads have q = 0 and are never stored.
 // ---------------------------------------------------------------------------
-constexpr int kClusterCtas = 8;
-constexpr int kSub = 64;
+constexpr int kCaRows = 64;                // positions per stage
+constexpr int kCaStages = 4;
+constexpr int kCaWin = 256;                // positions per window
+constexpr int kCaWarps = 8;                // consumer warps
+constexpr int kCaCT = kCaWarps * 32;
+constexpr int kCaThreads = kCaCT + 32;     // + producer warp
+constexpr int kCaRowsPerWarp = kCaRows / kCaWarps;
 
 template <int HD>
-struct ClusterSmem {
-    float K[2][kSub * HD];
-    float V[2][kSub * HD];
-    float Q[kMaxGroup * HD];
-    float P[kMaxGroup * kSub];
-    float O[kMaxGroup * HD];                   // this CTA's running unnormalised output
-    float M[kMaxGroup];
-    float L[kMaxGroup];
-    float corr[kMaxGroup];
-    float PO[kClusterCtas][kMaxGroup * HD];    // rank 0: the cluster's partial outputs
-    float PM[kClusterCtas][kMaxGroup];
-    float PL[kClusterCtas][kMaxGroup];
+struct CaGeom {
+    static constexpr int kSlot = kCaRows * HD;             // ring slot (floats)
+    static constexpr int kRing = kCaStages * kSlot;
+    static constexpr int kSlices = kCaCT / (HD / 4);       // position slices in the V pass
+    static_assert(kSlices * kMaxGroup * HD <= kRing, "slice sums reuse the ring");
 };
-
-__device__ __forceinline__ void cp_async16_attn(void* smem_dst, const void* gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+struct CaPlan {
+    int s, q, corr, po, pm, pl, floats;
+};
+template <int HD>
+__host__ __device__ inline CaPlan ca_plan(int G, int GP, int cl) {
+    CaPlan p;
+    p.s = CaGeom<HD>::kRing;        // [kCaWin][GP] scores, then weights
+    p.q = p.s + kCaWin * GP;        // [GP][HD]
+    p.corr = p.q + GP * HD;         // [kMaxGroup]
+    p.po = p.corr + kMaxGroup;      // [cl][G][HD]
+    p.pm = p.po + cl * G * HD;      // [cl][G]
+    p.pl = p.pm + cl * G;
+    p.floats = p.pl + cl * G;
+    return p;
 }
-__device__ __forceinline__ void cp_async_commit_attn() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+inline int ca_group_pad(int G) { return G <= 4 ? 4 : 8; }
+template <int HD>
+inline size_t ca_smem_bytes(int G, int cl) { return (size_t)ca_plan<HD>(G, ca_group_pad(G), cl).floats * 4; }
+
 __device__ __forceinline__ void st_dsmem_f32(float* local_ptr, uint32_t rank, float v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-template <int HD>
-__global__ void __launch_bounds__(kDecThreads) attn_decode_cluster_kernel(
+// Butterfly reduce-scatter over groups of LPR lanes: on entry every lane
+// holds NV partial values; on exit v[k] (k < NV / LPR) holds the sum over the
+// group of value index (NV / LPR) * (lane % LPR) + k.
+template <int NV, int LPR>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int o = LPR / 2; o >= 1; o >>= 1) {
+        const int half = n >> 1;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < NV / 2; ++k) {
+            if (k < half) {
+                const float send = upper ? v[k] : v[k + half];
+                const float keep = upper ? v[k + half] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        n = half;
+    }
+}
+
+template <int HD, int CL, int GP>
+__global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
     const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int n_head, int n_kv,
     int cache_stride, int kv_len_host, const DevState* st, float scale, float* __restrict__ out, int* err) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    ClusterSmem<HD>& S = *reinterpret_cast<ClusterSmem<HD>*>(smem_raw);
+    using Geo = CaGeom<HD>;
+    constexpr int D4 = HD / 4;
+    constexpr int LPR = D4;                          // lanes per K row in the K pass
+    constexpr int RPI = 32 / LPR;                    // rows per warp-wide load
+    constexpr int RS = kCaRowsPerWarp / RPI;         // row slots per lane
+    constexpr int NV = RS * GP;                      // partial scores per lane
+    constexpr int R = NV / LPR;                      // finished scores per lane
+    static_assert(R >= 1 && NV % LPR == 0, "K pass shape");
+    extern __shared__ __align__(128) float smf[];
+    __shared__ __align__(8) uint64_t full[kCaStages];
+    __shared__ __align__(8) uint64_t empty[kCaStages];
+
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kh = blockIdx.x / kClusterCtas, rank = blockIdx.x % kClusterCtas;
+    const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
     const int G = n_head / n_kv;
+    const CaPlan pl = ca_plan<HD>(G, GP, CL);
+    float* S = smf + pl.s;
+    float* Q = smf + pl.q;
+    float* CORR = smf + pl.corr;
+    float* PO = smf + pl.po;
+    float* PM = smf + pl.pm;
+    float* PLs = smf + pl.pl;
+
     const int kv_len = st ? st->pos + 1 : kv_len_host;
-    const int per = (kv_len + kClusterCtas - 1) / kClusterCtas;
+    const int per = (kv_len + CL - 1) / CL;
     const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
     const int n_rows = j_end - j_begin;
-    const int n_sub = (n_rows + kSub - 1) / kSub;
-    // The newest position is written by the preceding kernel (QKV epilogue):
-    // everything older may be read before the grid dependency wait.
+    const int n_win = (n_rows + kCaWin - 1) / kCaWin;
+    // The newest position is written by the preceding kernel (the QKV
+    // epilogue) in the decode step; every older row may be read before the
+    // grid dependency wait.
     const int j_new = st ? kv_len - 1 : kv_len;
     const float* kb = kc + (int64_t)kh * cache_stride * HD;
     const float* vb = vc + (int64_t)kh * cache_stride * HD;
-    constexpr int C4 = HD / 4;  // float4 chunks per row
 
-    // copy rows [a, b) of sub-chunk i into buffer i&1 (one commit group)
-    auto copy_rows = [&](int i, int a, int b) {
-        const int base = j_begin + i * kSub;
-        for (int f = tid; f < (b - a) * C4; f += kDecThreads) {
-            const int row = a - base + f / C4, c = f % C4;
-            cp_async16_attn(S.K[i & 1] + row * HD + c * 4, kb + (int64_t)(base + row) * HD + c * 4);
-            cp_async16_attn(S.V[i & 1] + row * HD + c * 4, vb + (int64_t)(base + row) * HD + c * 4);
+    if (tid == 0) {
+        for (int s = 0; s < kCaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCaWarps);
         }
-    };
-    int split0 = j_begin;
-    if (n_sub > 0) {
-        const int b = min(j_end, j_begin + kSub);
-        split0 = min(b, j_new);
-        if (split0 < j_begin) split0 = j_begin;
-        copy_rows(0, j_begin, split0);  // cached rows, before the wait
+        fence_mbar_init();
     }
+    __syncthreads();
+
+    if (warp == kCaWarps) {
+        // ---- producer: per window, the K stages then the V stages -------------------
+        if (lane == 0) {
+            bool waited = false;
+            int j = 0;  // stage counter
+            for (int w = 0; w < n_win; ++w) {
+                const int wa = j_begin + w * kCaWin, wn = min(kCaWin, j_end - wa);
+                for (int pass = 0; pass < 2; ++pass) {
+                    for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
+                        const int a = wa + r0, n = min(kCaRows, wn - r0);
+                        const int slot = j % kCaStages;
+                        if (!waited && a + n > j_new) {
+                            pdl_wait();
+                            waited = true;
+                        }
+                        if (j >= kCaStages) mbar_wait_bounded(&empty[slot], ((j / kCaStages) - 1) & 1, err, 21);
+                        mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * HD * 4));
+                        bulk_g2s(smf + slot * Geo::kSlot, (pass == 0 ? kb : vb) + (int64_t)a * HD,
+                                 (uint32_t)(n * HD * 4), &full[slot]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync();  // pairs with the consumers' cluster barrier below
+        return;
+    }
+
+    // ---- consumers ---------------------------------------------------------------------
     pdl_wait();
     if (tid == 0) pdl_launch_dependents();
-    if (n_sub > 0) copy_rows(0, split0, min(j_end, j_begin + kSub));  // the newest row, if it is here
-    cp_async_commit_attn();
-    if (n_sub > 1) copy_rows(1, j_begin + kSub, min(j_end, j_begin + 2 * kSub));
-    cp_async_commit_attn();
-    for (int i = tid; i < G * HD; i += kDecThreads) {
-        S.Q[i] = q[(int64_t)kh * G * HD + i];
-        S.O[i] = 0.0f;
-    }
-    if (tid < kMaxGroup) {
-        S.M[tid] = -INFINITY;
-        S.L[tid] = 0.0f;
-    }
+    for (int i = tid; i < GP * HD; i += kCaCT) Q[i] = i < G * HD ? q[(int64_t)kh * G * HD + i] : 0.0f;
+    named_bar_sync(1, kCaCT);
 
-    for (int i = 0; i < n_sub; ++i) {
-        const int buf = i & 1;
-        const int n = min(kSub, n_rows - i * kSub);
-        cp_async_wait_all_but_one();
-        __syncthreads();
-        // scores: 4 threads per position, each a quarter of the head dimension
-        {
-            const int row = tid >> 2, part = tid & 3;
-            const float* kr = S.K[buf] + row * HD + part * (HD / 4);
-            for (int g = 0; g < G; ++g) {
-                const float* qg = S.Q + g * HD + part * (HD / 4);
-                float a0 = 0.0f, a1 = 0.0f;
-                if (row < n) {
+    const int kc4 = lane % LPR, khalf = lane / LPR;   // K pass: chunk, row within a load
+    float4 qr[GP];
 #pragma unroll
-                    for (int d = 0; d < HD / 4; d += 8) {
-                        const float4 k0 = *reinterpret_cast<const float4*>(kr + d);
-                        const float4 k1 = *reinterpret_cast<const float4*>(kr + d + 4);
-                        const float4 q0 = *reinterpret_cast<const float4*>(qg + d);
-                        const float4 q1 = *reinterpret_cast<const float4*>(qg + d + 4);
-                        a0 = fmaf(q0.x, k0.x, a0); a0 = fmaf(q0.y, k0.y, a0);
-                        a0 = fmaf(q0.z, k0.z, a0); a0 = fmaf(q0.w, k0.w, a0);
-                        a1 = fmaf(q1.x, k1.x, a1); a1 = fmaf(q1.y, k1.y, a1);
-                        a1 = fmaf(q1.z, k1.z, a1); a1 = fmaf(q1.w, k1.w, a1);
-                    }
-                }
-                float sc = a0 + a1;
-                sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-                sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-                if (part == 0 && row < kSub) S.P[g * kSub + row] = sc * scale;
-            }
-            // rows 32..63 of the sub-chunk
-            if (kSub > kDecThreads / 4) {
-                const int row2 = row + kDecThreads / 4;
-                const float* kr2 = S.K[buf] + row2 * HD + part * (HD / 4);
-                for (int g = 0; g < G; ++g) {
-                    const float* qg = S.Q + g * HD + part * (HD / 4);
-                    float a0 = 0.0f, a1 = 0.0f;
-                    if (row2 < n) {
+    for (int g = 0; g < GP; ++g) qr[g] = *reinterpret_cast<const float4*>(Q + g * HD + kc4 * 4);
+    const int d4 = tid % D4, slice = tid / D4;        // V pass
+    float4 o[GP];
 #pragma unroll
-                        for (int d = 0; d < HD / 4; d += 8) {
-                            const float4 k0 = *reinterpret_cast<const float4*>(kr2 + d);
-                            const float4 k1 = *reinterpret_cast<const float4*>(kr2 + d + 4);
-                            const float4 q0 = *reinterpret_cast<const float4*>(qg + d);
-                            const float4 q1 = *reinterpret_cast<const float4*>(qg + d + 4);
-                            a0 = fmaf(q0.x, k0.x, a0); a0 = fmaf(q0.y, k0.y, a0);
-                            a0 = fmaf(q0.z, k0.z, a0); a0 = fmaf(q0.w, k0.w, a0);
-                            a1 = fmaf(q1.x, k1.x, a1); a1 = fmaf(q1.y, k1.y, a1);
-                            a1 = fmaf(q1.z, k1.z, a1); a1 = fmaf(q1.w, k1.w, a1);
-                        }
-                    }
-                    float sc = a0 + a1;
-                    sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-                    sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-                    if (part == 0 && row2 < kSub) S.P[g * kSub + row2] = sc * scale;
+    for (int g = 0; g < GP; ++g) o[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float m_run = -INFINITY, l_run = 0.0f;  // warp g < G: head g
+    int j = 0;
+
+    for (int w = 0; w < n_win; ++w) {
+        const int wa = j_begin + w * kCaWin, wn = min(kCaWin, j_end - wa);
+        if (w > 0) named_bar_sync(1, kCaCT);  // every thread is done with the previous weights
+        // ---- K pass: scores of every head of the group --------------------------------
+        for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
+            const int slot = j % kCaStages, n = min(kCaRows, wn - r0);
+            mbar_wait_bounded(&full[slot], (j / kCaStages) & 1, err, 22);
+            const float* Ks = smf + slot * Geo::kSlot;
+            float v[NV];
+#pragma unroll
+            for (int rs = 0; rs < RS; ++rs) {
+                const int row = warp * kCaRowsPerWarp + rs * RPI + khalf;
+                const float4 kv = row < n ? *reinterpret_cast<const float4*>(Ks + row * HD + kc4 * 4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    float a = qr[g].x * kv.x;
+                    a = fmaf(qr[g].y, kv.y, a);
+                    a = fmaf(qr[g].z, kv.z, a);
+                    v[rs * GP + g] = fmaf(qr[g].w, kv.w, a);
                 }
             }
-        }
-        __syncthreads();
-        // online softmax statistics per head (one warp per head)
-        for (int g = warp; g < G; g += kDecThreads / 32) {
-            const float a = lane < n ? S.P[g * kSub + lane] : -INFINITY;
-            const float b = lane + 32 < n ? S.P[g * kSub + lane + 32] : -INFINITY;
-            const float m_old = S.M[g];
-            const float m_new = fmaxf(m_old, warp_max(fmaxf(a, b)));
-            const float ea = lane < n ? expf(a - m_new) : 0.0f;
-            const float eb = lane + 32 < n ? expf(b - m_new) : 0.0f;
-            S.P[g * kSub + lane] = ea;
-            S.P[g * kSub + lane + 32] = eb;
-            const float sum = warp_sum(ea + eb);
-            if (lane == 0) {
-                const float corr = expf(m_old - m_new);  // 0 on the first sub-chunk
-                S.corr[g] = corr;
-                S.L[g] = S.L[g] * corr + sum;
-                S.M[g] = m_new;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            reduce_scatter<NV, LPR>(v, lane);
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const int idx = R * kc4 + k, rs = idx / GP, g = idx % GP;
+                const int row = warp * kCaRowsPerWarp + rs * RPI + khalf;
+                if (row < n) S[(r0 + row) * GP + g] = v[k] * scale;
             }
         }
-        __syncthreads();
-        for (int o = tid; o < G * HD; o += kDecThreads) {
-            const int g = o / HD, d = o % HD;
-            const float* pg = S.P + g * kSub;
-            const float* vcol = S.V[buf] + d;
-            float a0 = 0.0f, a1 = 0.0f;
-            int j = 0;
-            for (; j + 1 < n; j += 2) {
-                a0 = fmaf(pg[j], vcol[j * HD], a0);
-                a1 = fmaf(pg[j + 1], vcol[(j + 1) * HD], a1);
+        named_bar_sync(1, kCaCT);
+        // ---- softmax statistics over the window, weights in place ---------------------
+        if (warp < G) {
+            float mw = -INFINITY;
+            for (int p = lane; p < wn; p += 32) mw = fmaxf(mw, S[p * GP + warp]);
+            const float m_new = fmaxf(m_run, warp_max(mw));
+            float sum = 0.0f;
+            for (int p = lane; p < wn; p += 32) {
+                const float e = expf(S[p * GP + warp] - m_new);
+                S[p * GP + warp] = e;
+                sum += e;
             }
-            if (j < n) a0 = fmaf(pg[j], vcol[j * HD], a0);
-            S.O[o] = fmaf(S.O[o], S.corr[g], a0 + a1);
+            const float corr = expf(m_run - m_new);  // 0 on the first window
+            l_run = l_run * corr + warp_sum(sum);
+            m_run = m_new;
+            if (lane == 0) CORR[warp] = corr;
         }
-        __syncthreads();  // buffer buf is free again
-        if (i + 2 < n_sub) copy_rows(i + 2, j_begin + (i + 2) * kSub, min(j_end, j_begin + (i + 3) * kSub));
-        cp_async_commit_attn();
+        named_bar_sync(1, kCaCT);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            const float c = g < G ? CORR[g] : 0.0f;
+            o[g].x *= c; o[g].y *= c; o[g].z *= c; o[g].w *= c;
+        }
+        // ---- V pass: weighted sum of the value rows -------------------------------------
+        for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
+            const int slot = j % kCaStages, n = min(kCaRows, wn - r0);
+            mbar_wait_bounded(&full[slot], (j / kCaStages) & 1, err, 23);
+            const float* Vs = smf + slot * Geo::kSlot;
+            for (int jj = slice; jj < n; jj += Geo::kSlices) {
+                const float4 vv = *reinterpret_cast<const float4*>(Vs + jj * HD + d4 * 4);
+                const float* pw = S + (r0 + jj) * GP;
+#pragma unroll
+                for (int g4 = 0; g4 < GP; g4 += 4) {
+                    const float4 p4 = *reinterpret_cast<const float4*>(pw + g4);
+                    const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float4& acc = o[g4 + u];
+                        acc.x = fmaf(pp[u], vv.x, acc.x); acc.y = fmaf(pp[u], vv.y, acc.y);
+                        acc.z = fmaf(pp[u], vv.z, acc.z); acc.w = fmaf(pp[u], vv.w, acc.w);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
     }
 
-    // ---- push this CTA's partial result into rank 0, then merge there --------
-    if (rank == 0) {
-        for (int o = tid; o < G * HD; o += kDecThreads) S.PO[0][o] = S.O[o];
-        if (tid < G) {
-            S.PM[0][tid] = S.M[tid];
-            S.PL[0][tid] = S.L[tid];
-        }
-    } else {
-        for (int o = tid; o < G * HD; o += kDecThreads) st_dsmem_f32(&S.PO[rank][o], 0, S.O[o]);
-        if (tid < G) {
-            st_dsmem_f32(&S.PM[rank][tid], 0, S.M[tid]);
-            st_dsmem_f32(&S.PL[rank][tid], 0, S.L[tid]);
-        }
+    // ---- sum the position slices, push the CTA's partial result to rank 0 ----------------
+    named_bar_sync(1, kCaCT);  // the ring is free: reuse it for the slice sums
+    float* RED = smf;          // [kSlices][G][HD]
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+        if (g < G) *reinterpret_cast<float4*>(RED + (slice * G + g) * HD + d4 * 4) = o[g];
+    named_bar_sync(1, kCaCT);
+    for (int e = tid; e < G * HD; e += kCaCT) {
+        float acc = 0.0f;
+        for (int s = 0; s < Geo::kSlices; ++s) acc += RED[s * G * HD + e];
+        st_dsmem_f32(&PO[rank * G * HD + e], 0, acc);
+    }
+    if (warp < G && lane == 0) {
+        st_dsmem_f32(&PM[rank * G + warp], 0, m_run);
+        st_dsmem_f32(&PLs[rank * G + warp], 0, l_run);
     }
     cluster_sync();
     if (rank == 0) {
-        for (int o = tid; o < G * HD; o += kDecThreads) {
-            const int g = o / HD;
+        for (int e = tid; e < G * HD; e += kCaCT) {
+            const int g = e / HD;
             float M = -INFINITY;
 #pragma unroll
-            for (int r = 0; r < kClusterCtas; ++r) M = fmaxf(M, S.PM[r][g]);
+            for (int r = 0; r < CL; ++r) M = fmaxf(M, PM[r * G + g]);
             float Lsum = 0.0f, acc = 0.0f;
 #pragma unroll
-            for (int r = 0; r < kClusterCtas; ++r) {
-                const float m_r = S.PM[r][g];
-                const float w = m_r == -INFINITY ? 0.0f : expf(m_r - M);
-                Lsum = fmaf(w, S.PL[r][g], Lsum);
-                acc = fmaf(w, S.PO[r][o], acc);
+            for (int r = 0; r < CL; ++r) {
+                const float m_r = PM[r * G + g];
+                const float wgt = m_r == -INFINITY ? 0.0f : expf(m_r - M);
+                Lsum = fmaf(wgt, PLs[r * G + g], Lsum);
+                acc = fmaf(wgt, PO[r * G * HD + e], acc);
             }
-            out[(int64_t)kh * G * HD + o] = acc / Lsum;
+            out[(int64_t)kh * G * HD + e] = acc / Lsum;
         }
     }
-    (void)err;
 }
 
-template <int HD>
-static cudaError_t attn_cluster_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv,
-                                       int cache_stride, int kv_len, const DevState* st, float* out, bool pdl,
-                                       int* err, cudaStream_t s) {
+template <int HD, int CL, int GP>
+static cudaLaunchConfig_t ca_config(int n_kv, int G, cudaStream_t s, cudaLaunchAttribute* attrs, bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_kv * kClusterCtas);
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = sizeof(ClusterSmem<HD>);
+    cfg.gridDim = dim3(n_kv * CL);
+    cfg.blockDim = dim3(kCaThreads);
+    cfg.dynamicSmemBytes = (size_t)ca_plan<HD>(G, GP, CL).floats * 4;
     cfg.stream = s;
-    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = kClusterCtas;
+    attrs[0].val.clusterDim.x = CL;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     int n = 1;
@@ -432,19 +506,76 @@ static cudaError_t attn_cluster_launch(const float* q, const float* kc, const fl
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
+    return cfg;
+}
+
+template <int HD, int CL, int GP>
+static cudaError_t ca_set_attrs() {
+    const int gmax = GP;  // the largest group this instantiation serves
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((size_t)ca_plan<HD>(gmax, GP, CL).floats * 4));
+    if (e == cudaSuccess && CL > 8)
+        e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+// How many 16-CTA clusters of this kernel can be resident at once, per head
+// dimension and group size (0: unknown yet, -1: none). A launch uses 16-CTA
+// clusters only when every KV head's cluster fits at the same time.
+static int g_ca_max16[2][kMaxGroup + 1] = {};
+static bool g_ca16_ok[2] = {false, false};
+
+template <int HD, int GP>
+static int ca_cluster_size(int n_kv, int G) {
+    const int hi = HD == 64 ? 0 : 1;
+    if (!g_ca16_ok[hi]) return 8;
+    int& m = g_ca_max16[hi][G];
+    if (m == 0) {
+        cudaLaunchAttribute attrs[2];
+        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP>(1, G, 0, attrs, false);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_decode_cluster_kernel<HD, 16, GP>, &cfg) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = -1;
+        }
+        m = n;
+    }
+    return m >= n_kv ? 16 : 8;
+}
+
+template <int HD, int GP>
+static cudaError_t ca_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv, int cache_stride,
+                             int kv_len, const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
+    const int G = n_head / n_kv;
     const float scale = 1.0f / sqrtf((float)HD);
-    return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD>, q, kc, vc, n_head, n_kv, cache_stride, kv_len, st,
-                              scale, out, err);
+    cudaLaunchAttribute attrs[2];
+    if (ca_cluster_size<HD, GP>(n_kv, G) == 16) {
+        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP>(n_kv, G, s, attrs, pdl);
+        return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 16, GP>, q, kc, vc, n_head, n_kv,
+                                  cache_stride, kv_len, st, scale, out, err);
+    }
+    cudaLaunchConfig_t cfg = ca_config<HD, 8, GP>(n_kv, G, s, attrs, pdl);
+    return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 8, GP>, q, kc, vc, n_head, n_kv, cache_stride,
+                              kv_len, st, scale, out, err);
 }
 
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
                                        const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
+    if (n_head_kv <= 0 || n_head % n_head_kv || n_head / n_head_kv > kMaxGroup) return cudaErrorInvalidValue;
+    const bool wide = n_head / n_head_kv > 4;
     if (head_dim == 64)
-        return attn_cluster_launch<64>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+        return wide ? ca_launch<64, 8>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+                                       err, s)
+                    : ca_launch<64, 4>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
                                        err, s);
     if (head_dim == 128)
-        return attn_cluster_launch<128>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+        return wide ? ca_launch<128, 8>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
+                                        err, s)
+                    : ca_launch<128, 4>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
                                         err, s);
     return cudaErrorInvalidValue;
 }
@@ -456,11 +587,15 @@ cudaError_t init_attention_attributes() {
     err = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)decode_smem_bytes(128));
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(attn_decode_cluster_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sizeof(ClusterSmem<64>));
-    if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(attn_decode_cluster_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)sizeof(ClusterSmem<128>));
+    if ((err = ca_set_attrs<64, 8, 4>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<64, 8, 8>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 4>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 8>()) != cudaSuccess) return err;
+    g_ca16_ok[0] = ca_set_attrs<64, 16, 4>() == cudaSuccess && ca_set_attrs<64, 16, 8>() == cudaSuccess;
+    cudaGetLastError();
+    g_ca16_ok[1] = ca_set_attrs<128, 16, 4>() == cudaSuccess && ca_set_attrs<128, 16, 8>() == cudaSuccess;
+    cudaGetLastError();
+    return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------

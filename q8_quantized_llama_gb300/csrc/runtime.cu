@@ -892,6 +892,8 @@ llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, 
     if (kv_len > cache_stride) return LQ8_ERR_CTX;
     if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
     if (n_head / n_head_kv > 8) return LQ8_ERR_UNSUPPORTED;
+    // K/V rows are fetched by bulk async copies: 16-byte aligned caches only
+    if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return LQ8_ERR_ARG;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
     cudaError_t err = launch_attn_decode_cluster(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride,
                                                  kv_len, nullptr, out, false, nullptr, (cudaStream_t)stream);

@@ -215,6 +215,24 @@ def test_attention_decode_cluster_7b(kv_len):
     _attention_case(1, kv_len - 1, 32, 8, 128, 4096, seed=kv_len + 9, entry="decode")
 
 
+@pytest.mark.parametrize("nh,nkv,hd,kv_len", [(4, 4, 64, 100), (8, 1, 128, 777), (16, 2, 64, 4095),
+                                             (6, 3, 128, 17), (8, 8, 128, 2048), (9, 3, 64, 512)])
+def test_attention_decode_cluster_group_sizes(nh, nkv, hd, kv_len):
+    """Groups of 1, 2 and 8 query heads per KV head, position counts on and off
+    the 16-CTA x 32-position grid."""
+    _attention_case(1, kv_len - 1, nh, nkv, hd, 4096, seed=nh * 7 + kv_len, entry="decode")
+
+
+def test_attention_decode_rejects_unaligned_cache():
+    B = binding()
+    q = torch.zeros(9 * 64, dtype=torch.float32, device="cuda")
+    kv = torch.zeros(3 * 64 * 64 + 1, dtype=torch.float32, device="cuda")
+    out = torch.zeros(9 * 64, dtype=torch.float32, device="cuda")
+    with pytest.raises(B.Q8Error) as e:
+        B.llama_q8_attention_decode(q, kv[1:], kv[1:], 10, 9, 3, 64, 64, out)
+    assert e.value.status == B.LQ8_ERR_ARG
+
+
 def test_attention_two_calls_reuse_workspace():
     for kv in (700, 130):
         _attention_case(1, kv - 1, 9, 3, 64, 1024, seed=kv)
