@@ -232,23 +232,44 @@ struct CaGeom {
     static_assert(kSlices * kMaxGroup * HD <= kRing, "slice sums reuse the ring");
 };
 struct CaPlan {
-    int s, q, corr, po, pm, pl, floats;
+    int s, q, corr, po, pm, pl, om, red2, wo, floats;
 };
+__host__ __device__ inline int ca_round(int n) { return (n + 31) / 32 * 32; }
+// wo_bytes: the W_o slice one CTA holds when the kernel also applies the O
+// projection (0 otherwise).
 template <int HD>
-__host__ __device__ inline CaPlan ca_plan(int G, int GP, int cl) {
+__host__ __device__ inline CaPlan ca_plan(int G, int GP, int cl, int wo_bytes) {
     CaPlan p;
-    p.s = CaGeom<HD>::kRing;        // [kCaWin][GP] scores, then weights
-    p.q = p.s + kCaWin * GP;        // [GP][HD]
-    p.corr = p.q + GP * HD;         // [kMaxGroup]
-    p.po = p.corr + kMaxGroup;      // [cl][G][HD]
-    p.pm = p.po + cl * G * HD;      // [cl][G]
-    p.pl = p.pm + cl * G;
-    p.floats = p.pl + cl * G;
+    int o = CaGeom<HD>::kRing;
+    auto take = [&](int n) { const int r = o; o += ca_round(n); return r; };
+    p.s = take(kCaWin * GP);        // [kCaWin][GP] scores, then weights
+    p.q = take(GP * HD);            // [GP][HD]
+    p.corr = take(kMaxGroup);
+    p.po = take(cl * G * HD);       // [cl][G][HD]
+    p.pm = take(cl * G);            // [cl][G]
+    p.pl = take(cl * G);
+    p.om = take(wo_bytes ? G * HD : 0);          // merged output of the group (O projection input)
+    p.red2 = take(wo_bytes ? kCaWarps * 33 : 0);
+    p.wo = take(wo_bytes / 4);                   // W_o tiles: per tile, codes then scales
+    p.floats = o;
     return p;
 }
 inline int ca_group_pad(int G) { return G <= 4 ? 4 : 8; }
-template <int HD>
-inline size_t ca_smem_bytes(int G, int cl) { return (size_t)ca_plan<HD>(G, ca_group_pad(G), cl).floats * 4; }
+
+// The O projection applied inside the decode attention kernel: cluster kh
+// multiplies its query heads' output o (G * head_dim values) by the matching
+// column blocks of W_o and writes the partial product part[kh][0..rows); the
+// n_kv partials sum to W_o o.
+struct AttnOproj {
+    PackedQ8 wo;
+    float* part;
+    int part_stride;
+};
+constexpr int kFoMaxWoBytes = 32 * 1024;  // W_o bytes one CTA may hold
+__host__ __device__ inline int fo_tiles_per_cta(int rows_pad, int cl) { return (rows_pad / 32 + cl - 1) / cl; }
+__host__ __device__ inline int fo_wo_bytes(int rows_pad, int G, int hd, int cl) {
+    return fo_tiles_per_cta(rows_pad, cl) * (G * hd / 32) * 1088;
+}
 
 __device__ __forceinline__ void st_dsmem_f32(float* local_ptr, uint32_t rank, float v) {
     uint32_t remote;
@@ -278,10 +299,42 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
     }
 }
 
-template <int HD, int CL, int GP>
-__global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
-    const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int n_head, int n_kv,
-    int cache_stride, int kv_len_host, const DevState* st, float scale, float* __restrict__ out, int* err) {
+// Producer side of one KV head's share [ja, jb): per window, the K stages then
+// the V stages, one bulk copy each, through the ring. Rows at or after j_new
+// (written by the preceding kernel) are requested only after the grid
+// dependency wait. Run by one thread.
+template <int HD>
+__device__ __forceinline__ void ca_produce_head(float* smf, uint64_t* full, uint64_t* empty, const float* kb,
+                                                const float* vb, int ja, int jb, int j_new, bool& waited, int& j,
+                                                int* err) {
+    for (int wa = ja; wa < jb; wa += kCaWin) {
+        const int wn = min(kCaWin, jb - wa);
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
+                const int a = wa + r0, n = min(kCaRows, wn - r0);
+                const int slot = j % kCaStages;
+                if (!waited && a + n > j_new) {
+                    pdl_wait();
+                    waited = true;
+                }
+                if (j >= kCaStages) mbar_wait_bounded(&empty[slot], ((j / kCaStages) - 1) & 1, err, 21);
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * HD * 4));
+                bulk_g2s(smf + slot * CaGeom<HD>::kSlot, (pass == 0 ? kb : vb) + (int64_t)a * HD,
+                         (uint32_t)(n * HD * 4), &full[slot]);
+            }
+        }
+    }
+}
+
+// Consumer side of one KV head's share [ja, jb) (all consumer threads): the
+// K pass, softmax and V pass of every window. qr: this lane's q chunk of every
+// head of the group; o, m_run, l_run: running state (m/l valid in warp g < G
+// for head g). `first`: no earlier window used S in this kernel.
+template <int HD, int GP>
+__device__ __forceinline__ void ca_consume_head(const float* smf, uint64_t* full, uint64_t* empty, float* S,
+                                                float* CORR, const float4 (&qr)[GP], int G, int ja, int jb,
+                                                float scale, int& j, bool& first, float4 (&o)[GP], float& m_run,
+                                                float& l_run, int* err) {
     using Geo = CaGeom<HD>;
     constexpr int D4 = HD / 4;
     constexpr int LPR = D4;                          // lanes per K row in the K pass
@@ -290,90 +343,14 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
     constexpr int NV = RS * GP;                      // partial scores per lane
     constexpr int R = NV / LPR;                      // finished scores per lane
     static_assert(R >= 1 && NV % LPR == 0, "K pass shape");
-    extern __shared__ __align__(128) float smf[];
-    __shared__ __align__(8) uint64_t full[kCaStages];
-    __shared__ __align__(8) uint64_t empty[kCaStages];
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
-    const int G = n_head / n_kv;
-    const CaPlan pl = ca_plan<HD>(G, GP, CL);
-    float* S = smf + pl.s;
-    float* Q = smf + pl.q;
-    float* CORR = smf + pl.corr;
-    float* PO = smf + pl.po;
-    float* PM = smf + pl.pm;
-    float* PLs = smf + pl.pl;
-
-    const int kv_len = st ? st->pos + 1 : kv_len_host;
-    const int per = (kv_len + CL - 1) / CL;
-    const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
-    const int n_rows = j_end - j_begin;
-    const int n_win = (n_rows + kCaWin - 1) / kCaWin;
-    // The newest position is written by the preceding kernel (the QKV
-    // epilogue) in the decode step; every older row may be read before the
-    // grid dependency wait.
-    const int j_new = st ? kv_len - 1 : kv_len;
-    const float* kb = kc + (int64_t)kh * cache_stride * HD;
-    const float* vb = vc + (int64_t)kh * cache_stride * HD;
-
-    if (tid == 0) {
-        for (int s = 0; s < kCaStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCaWarps);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == kCaWarps) {
-        // ---- producer: per window, the K stages then the V stages -------------------
-        if (lane == 0) {
-            bool waited = false;
-            int j = 0;  // stage counter
-            for (int w = 0; w < n_win; ++w) {
-                const int wa = j_begin + w * kCaWin, wn = min(kCaWin, j_end - wa);
-                for (int pass = 0; pass < 2; ++pass) {
-                    for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
-                        const int a = wa + r0, n = min(kCaRows, wn - r0);
-                        const int slot = j % kCaStages;
-                        if (!waited && a + n > j_new) {
-                            pdl_wait();
-                            waited = true;
-                        }
-                        if (j >= kCaStages) mbar_wait_bounded(&empty[slot], ((j / kCaStages) - 1) & 1, err, 21);
-                        mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * HD * 4));
-                        bulk_g2s(smf + slot * Geo::kSlot, (pass == 0 ? kb : vb) + (int64_t)a * HD,
-                                 (uint32_t)(n * HD * 4), &full[slot]);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        cluster_sync();  // pairs with the consumers' cluster barrier below
-        return;
-    }
-
-    // ---- consumers ---------------------------------------------------------------------
-    pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
-    for (int i = tid; i < GP * HD; i += kCaCT) Q[i] = i < G * HD ? q[(int64_t)kh * G * HD + i] : 0.0f;
-    named_bar_sync(1, kCaCT);
-
     const int kc4 = lane % LPR, khalf = lane / LPR;   // K pass: chunk, row within a load
-    float4 qr[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) qr[g] = *reinterpret_cast<const float4*>(Q + g * HD + kc4 * 4);
     const int d4 = tid % D4, slice = tid / D4;        // V pass
-    float4 o[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) o[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float m_run = -INFINITY, l_run = 0.0f;  // warp g < G: head g
-    int j = 0;
 
-    for (int w = 0; w < n_win; ++w) {
-        const int wa = j_begin + w * kCaWin, wn = min(kCaWin, j_end - wa);
-        if (w > 0) named_bar_sync(1, kCaCT);  // every thread is done with the previous weights
+    for (int wa = ja; wa < jb; wa += kCaWin) {
+        const int wn = min(kCaWin, jb - wa);
+        if (!first) named_bar_sync(1, kCaCT);  // every thread is done with the previous weights in S
+        first = false;
         // ---- K pass: scores of every head of the group --------------------------------
         for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
             const int slot = j % kCaStages, n = min(kCaRows, wn - r0);
@@ -450,8 +427,102 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
     }
+}
+
+template <int HD, int CL, int GP, bool FO>
+__global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
+    const float* __restrict__ q, const float* __restrict__ kc, const float* __restrict__ vc, int n_head, int n_kv,
+    int cache_stride, int kv_len_host, const DevState* st, float scale, float* __restrict__ out, AttnOproj fo,
+    int* err) {
+    using Geo = CaGeom<HD>;
+    constexpr int D4 = HD / 4;
+    extern __shared__ __align__(128) float smf[];
+    __shared__ __align__(8) uint64_t full[kCaStages];
+    __shared__ __align__(8) uint64_t empty[kCaStages];
+    __shared__ __align__(8) uint64_t wo_bar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
+    const int G = n_head / n_kv;
+    const int nbk = G * HD / 32;                       // W_o column blocks of this group
+    const int tiles = FO ? fo.wo.rows_pad >> 5 : 0;
+    const CaPlan pl = ca_plan<HD>(G, GP, CL, FO ? fo_wo_bytes(fo.wo.rows_pad, G, HD, CL) : 0);
+    float* S = smf + pl.s;
+    float* Q = smf + pl.q;
+    float* CORR = smf + pl.corr;
+    float* PO = smf + pl.po;
+    float* PM = smf + pl.pm;
+    float* PLs = smf + pl.pl;
+    float* OM = smf + pl.om;
+    float* RED2 = smf + pl.red2;
+    uint8_t* WO = reinterpret_cast<uint8_t*>(smf + pl.wo);
+
+    const int kv_len = st ? st->pos + 1 : kv_len_host;
+    const int per = (kv_len + CL - 1) / CL;
+    const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
+    // The newest position is written by the preceding kernel (the QKV
+    // epilogue) in the decode step; every older row may be read before the
+    // grid dependency wait.
+    const int j_new = st ? kv_len - 1 : kv_len;
+    const float* kb = kc + (int64_t)kh * cache_stride * HD;
+    const float* vb = vc + (int64_t)kh * cache_stride * HD;
+
+    if (tid == 0) {
+        for (int s = 0; s < kCaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCaWarps);
+        }
+        mbar_init(&wo_bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCaWarps) {
+        if (lane == 0) {
+            if (FO) {
+                // this CTA's W_o tiles, the group's column blocks: constant weights, requested first
+                int n_t = 0;
+                for (int t = rank; t < tiles; t += CL) ++n_t;
+                mbar_arrive_expect_tx(&wo_bar, (uint32_t)(n_t * nbk * 1088));
+                const int nb = fo.wo.k >> 5, b0 = kh * nbk;
+                int i = 0;
+                for (int t = rank; t < tiles; t += CL, ++i) {
+                    uint8_t* dst = WO + (size_t)i * nbk * 1088;
+                    bulk_g2s(dst, reinterpret_cast<const uint8_t*>(fo.wo.qs) + (size_t)t * fo.wo.k * 32 + b0 * 1024,
+                             (uint32_t)(nbk * 1024), &wo_bar);
+                    bulk_g2s(dst + nbk * 1024,
+                             reinterpret_cast<const uint8_t*>(fo.wo.d) + ((size_t)t * nb + b0) * 64,
+                             (uint32_t)(nbk * 64), &wo_bar);
+                }
+            }
+            bool waited = false;
+            int j = 0;
+            ca_produce_head<HD>(smf, full, empty, kb, vb, j_begin, j_end, j_new, waited, j, err);
+        }
+        __syncwarp();
+        cluster_sync();  // pairs with the consumers' cluster barriers below
+        if (FO) cluster_sync();
+        return;
+    }
+
+    // ---- consumers ---------------------------------------------------------------------
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    for (int i = tid; i < GP * HD; i += kCaCT) Q[i] = i < G * HD ? q[(int64_t)kh * G * HD + i] : 0.0f;
+    named_bar_sync(1, kCaCT);
+    float4 qr[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) qr[g] = *reinterpret_cast<const float4*>(Q + g * HD + (lane % D4) * 4);
+    float4 o[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) o[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float m_run = -INFINITY, l_run = 0.0f;
+    int j = 0;
+    bool first = true;
+    ca_consume_head<HD, GP>(smf, full, empty, S, CORR, qr, G, j_begin, j_end, scale, j, first, o, m_run, l_run, err);
 
     // ---- sum the position slices, push the CTA's partial result to rank 0 ----------------
+    const int d4 = tid % D4, slice = tid / D4;
     named_bar_sync(1, kCaCT);  // the ring is free: reuse it for the slice sums
     float* RED = smf;          // [kSlices][G][HD]
 #pragma unroll
@@ -482,17 +553,56 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
                 Lsum = fmaf(wgt, PLs[r * G + g], Lsum);
                 acc = fmaf(wgt, PO[r * G * HD + e], acc);
             }
-            out[(int64_t)kh * G * HD + e] = acc / Lsum;
+            const float val = acc / Lsum;
+            if (FO) {
+#pragma unroll
+                for (int r = 0; r < CL; ++r) st_dsmem_f32(&OM[e], (uint32_t)r, val);
+            } else {
+                out[(int64_t)kh * G * HD + e] = val;
+            }
         }
+    }
+    if (!FO) return;
+
+    // ---- O projection of the group: part[kh] = W_o[:, group columns] o ---------------------
+    cluster_sync();  // the merged output is in every CTA
+    mbar_wait_bounded(&wo_bar, 0, err, 24);
+    int i = 0;
+    for (int t = rank; t < tiles; t += CL, ++i) {
+        const uint8_t* tw = WO + (size_t)i * nbk * 1088;
+        float acc = 0.0f;
+        for (int b = warp; b < nbk; b += kCaWarps) {
+            const uint4 q0 = *reinterpret_cast<const uint4*>(tw + b * 1024 + lane * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(tw + b * 1024 + 512 + lane * 16);
+            const float d = __half2float(reinterpret_cast<const __half*>(tw + nbk * 1024)[b * 32 + lane]);
+            const float4* x4 = reinterpret_cast<const float4*>(OM + b * 32);
+            uint64_t a0 = 0, a1 = 0;
+            a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
+            a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
+            a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
+            a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
+            acc = fmaf(d, (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)), acc);
+        }
+        RED2[warp * 33 + lane] = acc;
+        named_bar_sync(1, kCaCT);
+        if (warp == 0) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
+            const int r = t * 32 + lane;
+            if (r < fo.wo.rows) fo.part[(int64_t)kh * fo.part_stride + r] = v;
+        }
+        named_bar_sync(1, kCaCT);
     }
 }
 
-template <int HD, int CL, int GP>
-static cudaLaunchConfig_t ca_config(int n_kv, int G, cudaStream_t s, cudaLaunchAttribute* attrs, bool pdl) {
+template <int HD, int CL, int GP, bool FO>
+static cudaLaunchConfig_t ca_config(int n_kv, int G, int wo_bytes, cudaStream_t s, cudaLaunchAttribute* attrs,
+                                    bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_kv * CL);
     cfg.blockDim = dim3(kCaThreads);
-    cfg.dynamicSmemBytes = (size_t)ca_plan<HD>(G, GP, CL).floats * 4;
+    cfg.dynamicSmemBytes = (size_t)ca_plan<HD>(G, GP, CL, wo_bytes).floats * 4;
     cfg.stream = s;
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = CL;
@@ -509,75 +619,125 @@ static cudaLaunchConfig_t ca_config(int n_kv, int G, cudaStream_t s, cudaLaunchA
     return cfg;
 }
 
-template <int HD, int CL, int GP>
+static constexpr int kCaSmemLimit = 227 * 1024 - 1024;
+
+template <int HD, int CL, int GP, bool FO>
 static cudaError_t ca_set_attrs() {
-    const int gmax = GP;  // the largest group this instantiation serves
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((size_t)ca_plan<HD>(gmax, GP, CL).floats * 4));
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP, FO>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCaSmemLimit);
     if (e == cudaSuccess && CL > 8)
-        e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP>,
+        e = cudaFuncSetAttribute(attn_decode_cluster_kernel<HD, CL, GP, FO>,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
-// How many 16-CTA clusters of this kernel can be resident at once, per head
-// dimension and group size (0: unknown yet, -1: none). A launch uses 16-CTA
-// clusters only when every KV head's cluster fits at the same time.
-static int g_ca_max16[2][kMaxGroup + 1] = {};
-static bool g_ca16_ok[2] = {false, false};
+// How many 16-CTA clusters of a configuration can be resident at once, cached
+// per (head dim, group, O-projection bytes). A launch uses 16-CTA clusters
+// only when every KV head's cluster fits at the same time.
+struct CaOcc {
+    int hd, G, wo_bytes, max16;
+};
+static CaOcc g_ca_occ[32];
+static int g_ca_n_occ = 0;
+static std::mutex g_ca_mu;
+static bool g_ca16_ok = false;
 
-template <int HD, int GP>
-static int ca_cluster_size(int n_kv, int G) {
-    const int hi = HD == 64 ? 0 : 1;
-    if (!g_ca16_ok[hi]) return 8;
-    int& m = g_ca_max16[hi][G];
-    if (m == 0) {
+template <int HD, int GP, bool FO>
+static int ca_max16(int G, int wo_bytes) {
+    std::lock_guard<std::mutex> lock(g_ca_mu);
+    for (int i = 0; i < g_ca_n_occ; ++i)
+        if (g_ca_occ[i].hd == HD && g_ca_occ[i].G == G && g_ca_occ[i].wo_bytes == wo_bytes) return g_ca_occ[i].max16;
+    int n = -1;
+    if (g_ca16_ok && (size_t)ca_plan<HD>(G, GP, 16, wo_bytes).floats * 4 <= (size_t)kCaSmemLimit) {
         cudaLaunchAttribute attrs[2];
-        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP>(1, G, 0, attrs, false);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_decode_cluster_kernel<HD, 16, GP>, &cfg) != cudaSuccess ||
+        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP, FO>(1, G, wo_bytes, 0, attrs, false);
+        if (cudaOccupancyMaxActiveClusters(&n, attn_decode_cluster_kernel<HD, 16, GP, FO>, &cfg) != cudaSuccess ||
             n < 1) {
             cudaGetLastError();
             n = -1;
         }
-        m = n;
     }
-    return m >= n_kv ? 16 : 8;
+    if (g_ca_n_occ < 32) g_ca_occ[g_ca_n_occ++] = CaOcc{HD, G, wo_bytes, n};
+    return n;
 }
 
-template <int HD, int GP>
+template <int HD, int GP, bool FO>
+static int ca_cluster_size(int n_kv, int G, const AttnOproj* fo) {
+    const int wo16 = FO ? fo_wo_bytes(fo->wo.rows_pad, G, HD, 16) : 0;
+    return ca_max16<HD, GP, FO>(G, wo16) >= n_kv ? 16 : 8;
+}
+
+template <int HD, int GP, bool FO>
 static cudaError_t ca_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv, int cache_stride,
-                             int kv_len, const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
+                             int kv_len, const DevState* st, float* out, const AttnOproj* fo, bool pdl, int* err,
+                             cudaStream_t s) {
     const int G = n_head / n_kv;
     const float scale = 1.0f / sqrtf((float)HD);
+    const AttnOproj none{};
+    const AttnOproj& f = FO ? *fo : none;
     cudaLaunchAttribute attrs[2];
-    if (ca_cluster_size<HD, GP>(n_kv, G) == 16) {
-        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP>(n_kv, G, s, attrs, pdl);
-        return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 16, GP>, q, kc, vc, n_head, n_kv,
-                                  cache_stride, kv_len, st, scale, out, err);
+    if (ca_cluster_size<HD, GP, FO>(n_kv, G, fo) == 16) {
+        const int wo = FO ? fo_wo_bytes(f.wo.rows_pad, G, HD, 16) : 0;
+        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP, FO>(n_kv, G, wo, s, attrs, pdl);
+        return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 16, GP, FO>, q, kc, vc, n_head, n_kv,
+                                  cache_stride, kv_len, st, scale, out, f, err);
     }
-    cudaLaunchConfig_t cfg = ca_config<HD, 8, GP>(n_kv, G, s, attrs, pdl);
-    return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 8, GP>, q, kc, vc, n_head, n_kv, cache_stride,
-                              kv_len, st, scale, out, err);
+    const int wo = FO ? fo_wo_bytes(f.wo.rows_pad, G, HD, 8) : 0;
+    cudaLaunchConfig_t cfg = ca_config<HD, 8, GP, FO>(n_kv, G, wo, s, attrs, pdl);
+    return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 8, GP, FO>, q, kc, vc, n_head, n_kv, cache_stride,
+                              kv_len, st, scale, out, f, err);
+}
+
+template <bool FO>
+static cudaError_t ca_dispatch(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
+                               int head_dim, int cache_stride, int kv_len, const DevState* st, float* out,
+                               const AttnOproj* fo, bool pdl, int* err, cudaStream_t s) {
+    if (n_head_kv <= 0 || n_head % n_head_kv || n_head / n_head_kv > kMaxGroup) return cudaErrorInvalidValue;
+    const bool wide = n_head / n_head_kv > 4;
+    if (head_dim == 64)
+        return wide ? ca_launch<64, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
+                                           pdl, err, s)
+                    : ca_launch<64, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
+                                           pdl, err, s);
+    if (head_dim == 128)
+        return wide ? ca_launch<128, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
+                                            fo, pdl, err, s)
+                    : ca_launch<128, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
+                                            fo, pdl, err, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
                                        const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
-    if (n_head_kv <= 0 || n_head % n_head_kv || n_head / n_head_kv > kMaxGroup) return cudaErrorInvalidValue;
-    const bool wide = n_head / n_head_kv > 4;
-    if (head_dim == 64)
-        return wide ? ca_launch<64, 8>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
-                                       err, s)
-                    : ca_launch<64, 4>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
-                                       err, s);
-    if (head_dim == 128)
-        return wide ? ca_launch<128, 8>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
-                                        err, s)
-                    : ca_launch<128, 4>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, pdl,
-                                        err, s);
-    return cudaErrorInvalidValue;
+    return ca_dispatch<false>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, kv_len, st, out,
+                              nullptr, pdl, err, s);
+}
+
+// The O projection fits the decode attention kernel when every CTA's W_o
+// slice (its 32-row tiles x the group's column blocks) is at most 32 KB and
+// the shared-memory plan fits.
+bool attn_oproj_fused_supported(int n_head, int n_kv, int head_dim, const PackedQ8& Wo) {
+    if (n_kv <= 0 || n_head % n_kv || n_head / n_kv > kMaxGroup) return false;
+    if (head_dim != 64 && head_dim != 128) return false;
+    if (Wo.k != n_head * head_dim) return false;
+    const int G = n_head / n_kv, GP = ca_group_pad(G);
+    for (int cl : {16, 8}) {
+        const int wo = fo_wo_bytes(Wo.rows_pad, G, head_dim, cl);
+        if (wo > kFoMaxWoBytes) return false;
+        const int floats = head_dim == 64 ? ca_plan<64>(G, GP, cl, wo).floats : ca_plan<128>(G, GP, cl, wo).floats;
+        if ((size_t)floats * 4 > (size_t)kCaSmemLimit) return false;
+    }
+    return true;
+}
+
+cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
+                              int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
+                              int part_stride, bool pdl, int* err, cudaStream_t s) {
+    if (!st) return cudaErrorInvalidValue;
+    const AttnOproj fo{Wo, part, part_stride};
+    return ca_dispatch<true>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, 0, st, nullptr, &fo,
+                             pdl, err, s);
 }
 
 cudaError_t init_attention_attributes() {
@@ -587,13 +747,18 @@ cudaError_t init_attention_attributes() {
     err = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)decode_smem_bytes(128));
     if (err != cudaSuccess) return err;
-    if ((err = ca_set_attrs<64, 8, 4>()) != cudaSuccess) return err;
-    if ((err = ca_set_attrs<64, 8, 8>()) != cudaSuccess) return err;
-    if ((err = ca_set_attrs<128, 8, 4>()) != cudaSuccess) return err;
-    if ((err = ca_set_attrs<128, 8, 8>()) != cudaSuccess) return err;
-    g_ca16_ok[0] = ca_set_attrs<64, 16, 4>() == cudaSuccess && ca_set_attrs<64, 16, 8>() == cudaSuccess;
-    cudaGetLastError();
-    g_ca16_ok[1] = ca_set_attrs<128, 16, 4>() == cudaSuccess && ca_set_attrs<128, 16, 8>() == cudaSuccess;
+    if ((err = ca_set_attrs<64, 8, 4, false>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<64, 8, 8, false>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 4, false>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 8, false>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<64, 8, 4, true>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<64, 8, 8, true>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 4, true>()) != cudaSuccess) return err;
+    if ((err = ca_set_attrs<128, 8, 8, true>()) != cudaSuccess) return err;
+    g_ca16_ok = ca_set_attrs<64, 16, 4, false>() == cudaSuccess && ca_set_attrs<64, 16, 8, false>() == cudaSuccess &&
+                ca_set_attrs<128, 16, 4, false>() == cudaSuccess && ca_set_attrs<128, 16, 8, false>() == cudaSuccess &&
+                ca_set_attrs<64, 16, 4, true>() == cudaSuccess && ca_set_attrs<64, 16, 8, true>() == cudaSuccess &&
+                ca_set_attrs<128, 16, 4, true>() == cudaSuccess && ca_set_attrs<128, 16, 8, true>() == cudaSuccess;
     cudaGetLastError();
     return cudaSuccess;
 }

@@ -41,6 +41,7 @@ struct GemvArgs {
     EpiArgs e;
     int splits;      // CTAs (one cluster) per tile
     int* err;        // set on a bounded-wait timeout
+    GemvPreSum pre;  // fused norm only: partials added to x first
 };
 
 __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, const float* xs) {
@@ -65,7 +66,7 @@ __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int ti
     if (EPI == EPI_STORE) {
         if (valid) e.y[r] = v;
     } else if (EPI == EPI_RESIDUAL) {
-        if (valid) e.y[r] += v;
+        if (valid) e.y[r] = (e.res ? e.res[r] : e.y[r]) + v;
     } else if (EPI == EPI_QKV) {
         const float other = __shfl_xor_sync(0xffffffffu, v, 1);
         const int pos = e.state ? e.state->pos : e.pos0;
@@ -157,8 +158,12 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             for (int j = 0; j < first; ++j) issue_stage(j);  // weights: no kernel writes them
             pdl_wait();                                      // x: written by the preceding kernel
             const int xoff = x_full ? 0 : x0, xcnt = x_full ? k : xn;
-            mbar_arrive_expect_tx(&xbar, (uint32_t)(xcnt * 4));
+            const int np = NORM ? a.pre.n_part : 0;  // with the norm, xcnt == k
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(xcnt * 4 * (1 + np)));
             bulk_g2s(xs, a.x + xoff, (uint32_t)(xcnt * 4), &xbar);
+            for (int p = 0; p < np; ++p)
+                bulk_g2s(xs + (size_t)(p + 1) * k, a.pre.part + (size_t)p * a.pre.part_stride, (uint32_t)(k * 4),
+                         &xbar);
             for (int j = first; j < n_stage; ++j) issue_stage(j);
         }
     } else {
@@ -169,6 +174,19 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         mbar_wait_bounded(&xbar, 0, a.err, 13);
         if (NORM) {
             const int nx = x_full ? k : xn;  // == k when unsplit
+            if (a.pre.n_part > 0) {
+                // x + part[0] + part[1] + ..., in that order; the first CTA keeps the sum
+                const bool keep = blockIdx.x == 0 && a.pre.x_sum_out != nullptr;
+                for (int i = tid * 4; i < nx; i += kCT * 4) {
+                    float4 v = *reinterpret_cast<const float4*>(xs + i);
+                    for (int p = 0; p < a.pre.n_part; ++p) {
+                        const float4 w = *reinterpret_cast<const float4*>(xs + (size_t)(p + 1) * k + i);
+                        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+                    }
+                    *reinterpret_cast<float4*>(xs + i) = v;
+                    if (keep) *reinterpret_cast<float4*>(a.pre.x_sum_out + i) = v;
+                }
+            }
             float ss = 0.0f;
             for (int i = tid * 4; i < nx; i += kCT * 4) {
                 const float4 v = *reinterpret_cast<const float4*>(xs + i);
@@ -262,14 +280,16 @@ static int sm_count_current() {
 
 template <int EPI, bool NORM>
 static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
-                                   bool pdl, int* err, cudaStream_t s) {
+                                   bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
     const int tiles = W.rows_pad / 32, nb = W.k / 32;
     const int S = gemv_splits(tiles, nb, sm_count_current());
     const int max_blk = (nb + S - 1) / S;
-    const size_t x_floats = (NORM && S > 1) ? (size_t)W.k : (size_t)max_blk * 32;
+    const int n_part = (NORM && pre) ? pre->n_part : 0;
+    const size_t x_floats = (NORM && S > 1) ? (size_t)W.k * (1 + n_part)
+                                            : (size_t)max_blk * 32 + (size_t)n_part * W.k;
     const size_t smem = (size_t)kStages * kStageBytes + x_floats * sizeof(float);
     if (smem > (size_t)kGemvMaxSmem) return cudaErrorInvalidValue;
-    GemvArgs a{W, x, g, eps, e, S, err};
+    GemvArgs a{W, x, g, eps, e, S, err, (NORM && pre) ? *pre : GemvPreSum{}};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles * S);
     cfg.blockDim = dim3(kGemvThreads);
@@ -321,24 +341,24 @@ size_t gemv_max_k() {
 }
 
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s) {
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
     const bool norm = norm_g != nullptr;
     switch (epi) {
         case EPI_STORE:
-            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, pdl, err, s)
-                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, pdl, err, s);
+            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
+                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
         case EPI_RESIDUAL:
-            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, pdl, err, s)
-                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, pdl, err, s);
+            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
+                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
         case EPI_QKV:
-            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, pdl, err, s)
-                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, pdl, err, s);
+            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
+                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
         case EPI_SILU:
-            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, pdl, err, s)
-                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, pdl, err, s);
+            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
+                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
         case EPI_ARGMAX:
-            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, pdl, err, s)
-                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, pdl, err, s);
+            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
+                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
     }
     return cudaErrorInvalidValue;
 }

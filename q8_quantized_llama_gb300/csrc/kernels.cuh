@@ -30,6 +30,7 @@ enum Epi : int {
 struct EpiArgs {
     float* y = nullptr;  // STORE / RESIDUAL output, row stride ldy
     int ldy = 0;
+    const float* res = nullptr;  // RESIDUAL (matrix-vector only): y = res + acc instead of y += acc
     // QKV
     float* q_out = nullptr;  // [m][q_rows]
     float* k_cache = nullptr;  // layer base, [n_head_kv][max_seq][head_dim]
@@ -85,8 +86,18 @@ cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
 
 // gemv.cu (m == 1)
+// With the fused RMSNorm, the input may first be the sum x + part[0] + ... +
+// part[n_part - 1] (partials of the preceding kernel, each k floats, stride
+// part_stride), taken in that order; the first CTA stores that sum to
+// x_sum_out for the residual of a later kernel.
+struct GemvPreSum {
+    const float* part = nullptr;
+    int n_part = 0;
+    int part_stride = 0;
+    float* x_sum_out = nullptr;
+};
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s);
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre = nullptr);
 size_t gemv_max_k();
 // gemm.cu (m > 1): CUDA-core kernel for a few rows
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
@@ -112,6 +123,14 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
                                        const DevState* st, float* out, bool pdl, int* err, cudaStream_t s);
+// Decode attention whose clusters also apply the O projection: cluster kh
+// writes part[kh][0..rows) = W_o[:, columns of its query heads] o, the n_kv
+// partials summing to W_o o (added to the residual by the next kernel).
+// supported() is false when the model's W_o does not fit the kernel.
+bool attn_oproj_fused_supported(int n_head, int n_kv, int head_dim, const PackedQ8& Wo);
+cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
+                              int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
+                              int part_stride, bool pdl, int* err, cudaStream_t s);
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache,
                                 int T, int index_pos, int n_head, int n_head_kv, int head_dim,
                                 int cache_stride, float* out, bool pdl, cudaStream_t s);

@@ -88,10 +88,10 @@ struct Profiler {
     }
 };
 
-enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_COUNT };
+enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_COUNT };
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
                                      "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
-                                     "decode_cluster_layers"};
+                                     "decode_cluster_layers", "attn_oproj_residual"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -119,6 +119,8 @@ struct llama_q8_ctx {
     float* d_q = nullptr;
     float* d_o = nullptr;
     float* d_a = nullptr;
+    float* d_part = nullptr;  // decode: per-KV-head partials of W_o o
+    float* d_xsum = nullptr;  // decode: x + W_o o, the residual of the down projection
     float* d_logits = nullptr;
     int32_t* d_ids = nullptr;
     int32_t* d_out_ids = nullptr;
@@ -139,6 +141,7 @@ struct llama_q8_ctx {
     int len = 0;
     int64_t launches = 0;
     int cluster = 0;                     // > 0: decode layers run as one cluster of this many CTAs
+    bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
     LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
@@ -164,7 +167,8 @@ void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
-                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_logits, c->d_ids, c->d_out_ids,
+                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_logits, c->d_ids,
+                   c->d_out_ids,
                    c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_layer_ptrs};
     for (void* p : dev)
         if (p) cudaFree(p);
@@ -262,21 +266,49 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
         e.state = c->d_state;
         run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0,
             [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
-        run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
-            return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
-                                              cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
-                                              &c->d_state->err, s);
-        });
         EpiArgs r;
         r.y = c->d_x;
-        run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h, 0.0,
-            [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
-        EpiArgs g;
-        g.a_out = c->d_a;
-        run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F, 0.0,
-            [&] { return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s); });
-        run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
-            [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
+        if (c->fuse_o) {
+            // attention + W_o per KV head (partials), the sum folded into the gate/up kernel's norm,
+            // and the down projection's residual taken from that sum
+            run(F_ATTN_O, 4.0 * qr + q8_bytes(h, qr) + 4.0 * h * cfg.n_head_kv, 8.0 * (double)cfg.n_head_kv * cfg.head_dim,
+                [&] {
+                    return launch_attn_oproj(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
+                                             cfg.head_dim, cfg.max_seq, c->d_state, L.o, c->d_part, (int)h, pdl,
+                                             &c->d_state->err, s);
+                });
+            EpiArgs g;
+            g.a_out = c->d_a;
+            GemvPreSum pre;
+            pre.part = c->d_part;
+            pre.n_part = cfg.n_head_kv;
+            pre.part_stride = (int)h;
+            pre.x_sum_out = c->d_xsum;
+            run(F_GATEUP, q8_bytes(2 * F, h) + 4.0 * h * (2 + cfg.n_head_kv) + 4.0 * F, 0.0, [&] {
+                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s,
+                                   &pre);
+            });
+            EpiArgs rd;
+            rd.y = c->d_x;
+            rd.res = c->d_xsum;
+            run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
+                [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, rd, pdl, &c->d_state->err, s); });
+        } else {
+            run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
+                return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
+                                                  cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
+                                                  &c->d_state->err, s);
+            });
+            run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h, 0.0,
+                [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
+            EpiArgs g;
+            g.a_out = c->d_a;
+            run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F, 0.0, [&] {
+                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s);
+            });
+            run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
+                [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
+        }
     }
     run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0,
         [&] { return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl, &c->d_state->err, s); });
@@ -564,6 +596,8 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_q, sizeof(float) * T * c->q_rows));
     LOAD_CK(cudaMalloc(&c->d_o, sizeof(float) * T * c->q_rows));
     LOAD_CK(cudaMalloc(&c->d_a, sizeof(float) * T * F));
+    LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
+    LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_logits, sizeof(float) * V));
     LOAD_CK(cudaMalloc(&c->d_ids, sizeof(int32_t) * T));
     LOAD_CK(cudaMalloc(&c->d_out_ids, sizeof(int32_t) * (T + 1)));
@@ -582,6 +616,8 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
     // decode path: the whole layer stack as one cluster when asked for and it fits
+    if (C.decode_kernel == 0) c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
+    cudaGetLastError();
     if (C.decode_kernel == 2) {
         c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);
         cudaGetLastError();

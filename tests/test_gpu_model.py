@@ -25,20 +25,22 @@ def m135():
     for name, t in dev_t.items():     # the GPU quantiser matches the oracle's bytes
         if ora_t[name].dtype == np.uint8:
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
-    model = B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True)      # one-cluster decode step
-    layered = B.Model(CFG, dev_t, on_device=True)                            # automatic: per-layer kernels
+    model = B.Model(CFG, dev_t, on_device=True)                              # automatic: attention + W_o fused
+    layered = B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True)      # five kernels per layer
+    cluster = B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True)      # one-cluster decode step
     del dev_t
     torch.cuda.empty_cache()
     oracle = O.ModelWeights(CFG, ora_t, weight_cache="f64")
-    yield model, oracle, layered
+    yield model, oracle, layered, cluster
     model.close()
     layered.close()
+    cluster.close()
 
 
-@pytest.fixture(params=["cluster", "layered"])
+@pytest.fixture(params=["fused", "layered", "cluster"])
 def either(request, m135):
-    model, oracle, layered = m135
-    return (model if request.param == "cluster" else layered), oracle
+    model, oracle, layered, cluster = m135
+    return {"fused": model, "layered": layered, "cluster": cluster}[request.param], oracle
 
 
 def _check_run(model, oracle, prompt, n_decode):
@@ -94,7 +96,7 @@ def test_kv_cache_after_rope_matches_oracle(either):
 
 
 def test_index_pos_rules(m135):
-    model, _, _ = m135
+    model, _, _, _ = m135
     B = binding()
     prompt = synth.prompt_ids(13, V, 1)
     full = model.forward(prompt, 0)
@@ -125,7 +127,7 @@ def test_index_pos_rules(m135):
 
 
 def test_context_limit(m135):
-    model, _, _ = m135
+    model, _, _, _ = m135
     B = binding()
     prompt = synth.prompt_ids(64, V, 2)
     assert model.forward_status(np.zeros(4097, np.int32), 0) == B.LQ8_ERR_CTX
@@ -152,7 +154,7 @@ def test_prefill_and_decode_paths_agree(either):
 
 
 def test_device_resident_api(m135):
-    model, _, layered = m135
+    model, _, layered, cluster = m135
     prompt = synth.prompt_ids(203, V, 0)
     ref = model.generate(prompt, 16)
     d_ids = torch.from_numpy(prompt).cuda()
@@ -164,5 +166,27 @@ def test_device_resident_api(m135):
     got = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
     np.testing.assert_array_equal(got, ref)
     assert model.cache_len() == 203 + 16
-    assert model.decode_kernel_count() == 2                    # layers in one cluster + lm_head
+    assert model.decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1   # attention kernel applies W_o
     assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
+    assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
+
+
+def test_fused_attention_oproj_at_long_context(m135):
+    """Decode steps at positions near the 4096 limit: the attention kernel that
+    also applies W_o gives the logits and tokens of the five-kernel layer."""
+    model, _, layered, _ = m135
+    prompt = synth.prompt_ids(3900, V, 6)
+    a = model.forward(prompt, 0)
+    b = layered.forward(prompt, 0)
+    ok, err, bound = logits_close(a, b)
+    assert ok, (err, bound)
+    tok = int(np.argmax(a))
+    pos = len(prompt)
+    for _ in range(4):
+        a = model.forward([tok], pos)
+        b = layered.forward([tok], pos)
+        ok, err, bound = logits_close(a, b)
+        assert ok, (pos, err, bound)
+        assert int(np.argmax(a)) == int(np.argmax(b))
+        tok = int(np.argmax(a))
+        pos += 1
