@@ -52,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b", "attn", "gemm"], default=None,
+    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode"], default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
 
@@ -291,6 +291,78 @@ def gpu_model(torch, B, synth, device):
     return cfg, model
 
 
+def q8_bytes(rows: int, k: int) -> float:
+    return rows * k * 34 / 32
+
+
+def decode_bytes(cfg: dict, kv_len: float) -> tuple[float, float]:
+    """Algorithmic bytes of one decode step: (Q8_0 weights of every projection
+    and the lm_head + f32 norms, f32 K and V rows read by the attention)."""
+    h, hd, F = cfg["n_embd"], cfg["head_dim"], cfg["n_ff"]
+    qd, kvd = cfg["n_head"] * hd, cfg["n_head_kv"] * hd
+    per_layer = q8_bytes(qd + 2 * kvd, h) + q8_bytes(h, qd) + q8_bytes(2 * F, h) + q8_bytes(h, F) + 8 * h
+    weights = cfg["n_layer"] * per_layer + q8_bytes(cfg["n_vocab"], h) + 4 * h + q8_bytes(1, h)
+    kv = 2 * cfg["n_layer"] * kvd * 4 * kv_len
+    return weights, kv
+
+
+def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3):
+    """Greedy decode of the Llama-7B-shaped Q8_0 model (32 x 4096, 32/8 heads of
+    128, FFN 14336, vocab 32000, untied head) after a 512-token prefill: the
+    decode step streams 7.55 GB of weights, so this is where the matrix-vector
+    kernel's bandwidth shows in a whole model. Weights N(0, 0.02) drawn on the
+    GPU (seeded) and quantised there; ms/token timed with CUDA events on the
+    library stream over the CUDA-graph decode steps."""
+    cfg = dict(synth.MODEL_7B)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1)
+    t = {}
+    s = torch.cuda.current_stream()
+    for name, shape, kind in synth.model_tensor_specs(cfg):
+        if kind == "matrix":
+            rows, k = shape
+            w = torch.randn(shape, generator=gen, device=device) * synth.WEIGHT_STD
+            q = torch.empty((rows, k // 32 * 34), dtype=torch.uint8, device=device)
+            B.llama_q8_quantize(w, rows, k, q, s.cuda_stream)
+            del w
+            t[name] = q
+        else:
+            t[name] = 1.0 + synth.WEIGHT_STD * torch.randn(shape, generator=gen, device=device)
+    torch.cuda.synchronize()
+    model = B.Model(cfg, t, device=device.index, on_device=True)
+    del t
+    torch.cuda.empty_cache()
+    prompt = synth.prompt_ids(prompt_len, cfg["n_vocab"], 1)
+    d_prompt = torch.from_numpy(prompt).to(device)
+    d_next = torch.zeros(1, dtype=torch.int32, device=device)
+    d_out = torch.zeros(n_decode, dtype=torch.int32, device=device)
+    stream = torch.cuda.ExternalStream(model.stream(), device=device)
+    model.prefill_async(d_prompt, prompt_len, 0, d_next)
+    model.decode_async(8, d_out)
+    model.sync()
+    pre, dec = [], []
+    for _ in range(reps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        model.prefill_async(d_prompt, prompt_len, 0, d_next)
+        e[1].record(stream)
+        model.decode_async(n_decode, d_out)
+        e[2].record(stream)
+        model.sync()
+        torch.cuda.synchronize()
+        pre.append(e[0].elapsed_time(e[1]))
+        dec.append(e[1].elapsed_time(e[2]) / n_decode)
+    model.close()
+    torch.cuda.empty_cache()
+    ms = statistics.median(dec)
+    w, kv = decode_bytes(cfg, prompt_len + (n_decode + 1) / 2)
+    roof_ms = (w + kv) / (peak * 1e9) * 1e3
+    return {"workload": f"7B-shaped Q8_0 Llama, {prompt_len}-token prefill + {n_decode} greedy decode steps",
+            "decode_ms_per_token": ms, "decode_tok_s": 1000.0 / ms, "prefill_ms": statistics.median(pre),
+            "prefill_tok_s": prompt_len / (statistics.median(pre) / 1000),
+            "weights_bytes": w, "kv_bytes_mean": kv, "roofline_ms": roof_ms, "frac": roof_ms / ms}
+
+
 def gemv_7b_roofline(torch, B, synth, device, peak):
     """The Q8_0 GEMV at the 7B shape [1,4096]x[4096,14336], timed with CUDA
     events over 400 back-to-back launches that rotate through 8 weight copies
@@ -466,6 +538,12 @@ def run_ours(args):
     assert np.array_equal(tokens, ref_tokens), "decode tokens changed between repetitions"
     value, t_max = aggregate_throughput(DECODE_STEPS * args.steps, sum(dec_ms) / 1000, world, device)
     clk = clocks.summary()
+    if args.only == "decode":  # the timed region alone (launch-list captures)
+        if rank == 0:
+            print(json.dumps({"decode_ms_per_token": sum(dec_ms) / (DECODE_STEPS * args.steps),
+                              "prefill_ms": statistics.median(pre_ms), "gpu_launches": gpu_launches}))
+        model.close()
+        return
 
     # end to end through the host API: the pages' loop, one synchronous call per token
     e2e_dec = []
@@ -487,14 +565,14 @@ def run_ours(args):
     dom_name = max(prof, key=lambda k: prof[k][1])
     dl, dms, dbytes = prof[dom_name]
     dom_gbs = (dbytes / dl) / (dms / dl * 1e-3) / 1e9
-    weights_bytes = sum(v[2] for k, v in prof.items() if k != "attn_decode") / DECODE_STEPS
-    kv_bytes = prof["attn_decode"][2] / DECODE_STEPS
+    weights_bytes, kv_bytes = decode_bytes(cfg, PROMPT_LEN + (DECODE_STEPS + 1) / 2)
 
     out = None
     if rank == 0:
         gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
         attn = attention_microbench(torch, B, synth, device, peak)
         gemm = gemm_microbench(torch, B, synth, device)
+        model7 = decode_7b(torch, B, synth, device, peak)
         dec_tok_ms = [d / DECODE_STEPS for d in dec_ms]
         out = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -525,10 +603,11 @@ def run_ours(args):
                                      "frac": ((weights_bytes + kv_bytes) / (peak * 1e9) * 1e6)
                                      / (1000 * statistics.median(dec_tok_ms))},
             "kernels": {k: {"launches": v[0], "ms": v[1], "gbs": (v[2] / (v[1] * 1e-3) / 1e9) if v[1] else None,
-                            "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items()},
+                            "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items() if v[0] > 0},
             "gemv_7b": gemv7,
             "attention_decode": attn,
             "gemm_prefill": gemm,
+            "decode_7b": model7,
         }
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)

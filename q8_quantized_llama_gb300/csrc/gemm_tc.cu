@@ -128,7 +128,29 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Epilogue of one output element pair/element (row r of W, token t).
 template <int EPI>
+__device__ __forceinline__ void tc_epilogue_one(const EpiArgs& e, int m, int rows, int t, int r, float val,
+                                                float other) {
+    if (EPI == EPI_QKV || EPI == EPI_SILU) {
+        if (t < m && r < rows && !(r & 1)) {
+            if (EPI == EPI_QKV) epi_qkv_pair(e, t, e.pos0 + t, r, val, other);
+            else e.a_out[(int64_t)t * e.lda + (r >> 1)] = silu_f32(val) * other;
+        }
+    } else if (t < m && r < rows) {
+        if (EPI == EPI_STORE) e.y[(int64_t)t * e.ldy + r] = val;
+        else if (EPI == EPI_RESIDUAL) e.y[(int64_t)t * e.ldy + r] += val;
+    }
+}
+
+constexpr int kPartStride = kTcBN + 4;  // floats per row of a partial tile in shared memory
+
+// SPLIT: the CTAs of a cluster (blockIdx.z = cluster rank) take equal shares
+// of the k-blocks; each stores its partial tile in its shared memory and,
+// after a cluster barrier, rank z sums rows [z * 128 / S, (z + 1) * 128 / S)
+// over the S partials (in rank order, through distributed shared memory) and
+// applies the epilogue to them.
+template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, const float* __restrict__ X, int m,
                                                                     int ldx, EpiArgs e, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -139,7 +161,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     __shared__ uint32_t tmem_holder;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k = W.k, nb = k >> 5;
+    const int k = W.k, nb_all = k >> 5;
+    const int S = SPLIT ? (int)gridDim.z : 1, z = SPLIT ? (int)blockIdx.z : 0;
+    const int kb0 = (z * nb_all) / S, nb = ((z + 1) * nb_all) / S - kb0;  // this CTA's k-blocks
     const int m0 = blockIdx.x * kTcBM;  // weight rows
     const int t0 = blockIdx.y * kTcBN;  // tokens
     const int tile0 = m0 >> 5;
@@ -162,8 +186,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     // the packed layout), their scales (64 B each) and the 128 token rows of
     // activations (128 B each). Thread tid copies 16 B of codes, threads < 16
     // 16 B of scales, and 4 x 16 B of activations.
-    auto issue_raw = [&](int kb) {
-        uint8_t* r = raw + (kb % kRawStages) * kRawBytes;
+    auto issue_raw = [&](int kbr) {
+        uint8_t* r = raw + (kbr % kRawStages) * kRawBytes;
+        const int kb = kb0 + kbr;
         {
             const int t = tid >> 6, within = (tid & 63) * 16;
             const bool ok = tile0 + t < n_tiles;
@@ -174,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
             const int t = tid >> 2, within = (tid & 3) * 16;
             const bool ok = tile0 + t < n_tiles;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(W.d) +
-                                 ((int64_t)(ok ? tile0 + t : 0) * nb + kb) * 64 + within;
+                                 ((int64_t)(ok ? tile0 + t : 0) * nb_all + kb) * 64 + within;
             cp_async16(r + 4096 + t * 64 + within, src, ok ? 16u : 0u);
         }
 #pragma unroll
@@ -262,48 +287,118 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. and token columns of half w/4
     const int quarter = warp & 3, half = warp >> 2;
     const int r = m0 + quarter * 32 + lane;
-    const bool row_ok = r < W.rows;
-    for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+    if (!SPLIT) {
+        for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = t0 + c0 + j;
-            const float val = v[j];
-            if (EPI == EPI_QKV || EPI == EPI_SILU) {
-                const float other = __shfl_xor_sync(0xffffffffu, val, 1);
-                if (t < m && row_ok && !(lane & 1)) {
-                    if (EPI == EPI_QKV) epi_qkv_pair(e, t, e.pos0 + t, r, val, other);
-                    else e.a_out[(int64_t)t * e.lda + (r >> 1)] = silu_f32(val) * other;
-                }
-            } else if (t < m && row_ok) {
-                if (EPI == EPI_STORE) e.y[(int64_t)t * e.ldy + r] = val;
-                else if (EPI == EPI_RESIDUAL) e.y[(int64_t)t * e.ldy + r] += val;
+            for (int j = 0; j < 16; ++j) {
+                const float other = (EPI == EPI_QKV || EPI == EPI_SILU) ? __shfl_xor_sync(0xffffffffu, v[j], 1) : 0.f;
+                tc_epilogue_one<EPI>(e, m, W.rows, t0 + c0 + j, r, v[j], other);
             }
         }
+    } else {
+        // partial tile -> own shared memory (the operand slots are free now)
+        float* part = reinterpret_cast<float*>(ops);  // [128 rows][kPartStride]
+        const int row = quarter * 32 + lane;
+        for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4*>(part + row * kPartStride + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+        cluster_sync();
+        // rank z sums its rows over the S partials; thread -> (row pair, 4 tokens)
+        const int rows_per = kTcBM / S;
+        const int ra = z * rows_per;
+        for (int f = tid; f < (rows_per / 2) * (kTcBN / 4); f += kTcThreads) {
+            const int rp = f % (rows_per / 2), t = (f / (rows_per / 2)) * 4;
+            const int lr = ra + 2 * rp;
+            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+            for (int zz = 0; zz < S; ++zz) {
+                const float4 a = ld_dsmem_f32x4(part + lr * kPartStride + t, (uint32_t)zz);
+                const float4 b = ld_dsmem_f32x4(part + (lr + 1) * kPartStride + t, (uint32_t)zz);
+                v0.x += a.x; v0.y += a.y; v0.z += a.z; v0.w += a.w;
+                v1.x += b.x; v1.y += b.y; v1.z += b.z; v1.w += b.w;
+            }
+            const float e0[4] = {v0.x, v0.y, v0.z, v0.w}, e1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (EPI == EPI_QKV || EPI == EPI_SILU) {
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr, e0[j], e1[j]);
+                } else {
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr, e0[j], 0.f);
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr + 1, e1[j], 0.f);
+                }
+            }
+        }
+        cluster_sync();  // peers keep their shared memory until every rank has read it
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTcBN);
 }
 
+static int g_tc_sms = 0;
+
+// k-splits per output tile: enough CTAs to cover the GPU once, at most 8 (a
+// portable cluster), at least two k-blocks per CTA.
+static int gemm_tc_splits(int tiles, int nb) {
+    if (g_tc_sms <= 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_tc_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_tc_sms <= 0) g_tc_sms = 148;
+    }
+    int S = 1;
+    while (S < 8 && tiles * S * 2 <= g_tc_sms && nb / (S * 2) >= 2) S *= 2;
+    return S;
+}
+
 template <int EPI>
 static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
                                int* err, cudaStream_t s) {
-    dim3 grid((W.rows_pad + kTcBM - 1) / kTcBM, (m + kTcBN - 1) / kTcBN);
-    return launch_ex(q8_gemm_tc_kernel<EPI>, grid, dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W, X, m, ldx, e, err);
+    const int gx = (W.rows_pad + kTcBM - 1) / kTcBM, gy = (m + kTcBN - 1) / kTcBN;
+    const int S = gemm_tc_splits(gx * gy, W.k / 32);
+    if (S == 1)
+        return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gx, gy), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
+                         X, m, ldx, e, err);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, gy, S);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = (size_t)kTcSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 1;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = S;
+    int n = 1;
+    if (pdl) {
+        attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[1].val.programmaticStreamSerializationAllowed = 1;
+        n = 2;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, X, m, ldx, e, err);
+}
+
+template <int EPI>
+static cudaError_t gemm_tc_attr() {
+    cudaError_t err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kTcSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    return err;
 }
 
 cudaError_t init_gemm_tc_attributes() {
-    cudaError_t err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kTcSmem);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_RESIDUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kTcSmem);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    cudaError_t err = gemm_tc_attr<EPI_STORE>();
+    if (err == cudaSuccess) err = gemm_tc_attr<EPI_RESIDUAL>();
+    if (err == cudaSuccess) err = gemm_tc_attr<EPI_QKV>();
+    if (err == cudaSuccess) err = gemm_tc_attr<EPI_SILU>();
     return err;
 }
 
