@@ -302,25 +302,29 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
 // Producer side of one KV head's share [ja, jb): per window, the K stages then
 // the V stages, one bulk copy each, through the ring. Rows at or after j_new
 // (written by the preceding kernel) are requested only after the grid
-// dependency wait. Run by one thread.
+// dependency wait; with skip_new the row j_new is not requested at all (the
+// consumers take it from shared memory). Run by one thread.
 template <int HD>
 __device__ __forceinline__ void ca_produce_head(float* smf, uint64_t* full, uint64_t* empty, const float* kb,
-                                                const float* vb, int ja, int jb, int j_new, bool& waited, int& j,
-                                                int* err) {
+                                                const float* vb, int ja, int jb, int j_new, bool skip_new,
+                                                bool& waited, int& j, int* err) {
     for (int wa = ja; wa < jb; wa += kCaWin) {
         const int wn = min(kCaWin, jb - wa);
         for (int pass = 0; pass < 2; ++pass) {
             for (int r0 = 0; r0 < wn; r0 += kCaRows, ++j) {
-                const int a = wa + r0, n = min(kCaRows, wn - r0);
+                const int a = wa + r0;
+                int n = min(kCaRows, wn - r0);
                 const int slot = j % kCaStages;
-                if (!waited && a + n > j_new) {
+                if (skip_new && a + n > j_new) n = j_new - a;  // rows before the newest one
+                else if (!waited && a + n > j_new) {
                     pdl_wait();
                     waited = true;
                 }
                 if (j >= kCaStages) mbar_wait_bounded(&empty[slot], ((j / kCaStages) - 1) & 1, err, 21);
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * HD * 4));
-                bulk_g2s(smf + slot * CaGeom<HD>::kSlot, (pass == 0 ? kb : vb) + (int64_t)a * HD,
-                         (uint32_t)(n * HD * 4), &full[slot]);
+                if (n > 0)
+                    bulk_g2s(smf + slot * CaGeom<HD>::kSlot, (pass == 0 ? kb : vb) + (int64_t)a * HD,
+                             (uint32_t)(n * HD * 4), &full[slot]);
             }
         }
     }
@@ -334,7 +338,8 @@ template <int HD, int GP>
 __device__ __forceinline__ void ca_consume_head(const float* smf, uint64_t* full, uint64_t* empty, float* S,
                                                 float* CORR, const float4 (&qr)[GP], int G, int ja, int jb,
                                                 float scale, int& j, bool& first, float4 (&o)[GP], float& m_run,
-                                                float& l_run, int* err) {
+                                                float& l_run, int* err, int j_new = -1,
+                                                const float* knew = nullptr, const float* vnew = nullptr) {
     using Geo = CaGeom<HD>;
     constexpr int D4 = HD / 4;
     constexpr int LPR = D4;                          // lanes per K row in the K pass
@@ -360,7 +365,8 @@ __device__ __forceinline__ void ca_consume_head(const float* smf, uint64_t* full
 #pragma unroll
             for (int rs = 0; rs < RS; ++rs) {
                 const int row = warp * kCaRowsPerWarp + rs * RPI + khalf;
-                const float4 kv = row < n ? *reinterpret_cast<const float4*>(Ks + row * HD + kc4 * 4)
+                const float* kr = (knew && wa + r0 + row == j_new) ? knew : Ks + row * HD;
+                const float4 kv = row < n ? *reinterpret_cast<const float4*>(kr + kc4 * 4)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int g = 0; g < GP; ++g) {
@@ -409,7 +415,8 @@ __device__ __forceinline__ void ca_consume_head(const float* smf, uint64_t* full
             mbar_wait_bounded(&full[slot], (j / kCaStages) & 1, err, 23);
             const float* Vs = smf + slot * Geo::kSlot;
             for (int jj = slice; jj < n; jj += Geo::kSlices) {
-                const float4 vv = *reinterpret_cast<const float4*>(Vs + jj * HD + d4 * 4);
+                const float* vr = (vnew && wa + r0 + jj == j_new) ? vnew : Vs + jj * HD;
+                const float4 vv = *reinterpret_cast<const float4*>(vr + d4 * 4);
                 const float* pw = S + (r0 + jj) * GP;
 #pragma unroll
                 for (int g4 = 0; g4 < GP; g4 += 4) {
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
             }
             bool waited = false;
             int j = 0;
-            ca_produce_head<HD>(smf, full, empty, kb, vb, j_begin, j_end, j_new, waited, j, err);
+            ca_produce_head<HD>(smf, full, empty, kb, vb, j_begin, j_end, j_new, false, waited, j, err);
         }
         __syncwarp();
         cluster_sync();  // pairs with the consumers' cluster barriers below
@@ -591,6 +598,336 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
             for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
             const int r = t * 32 + lane;
             if (r < fo.wo.rows) fo.part[(int64_t)kh * fo.part_stride + r] = v;
+        }
+        named_bar_sync(1, kCaCT);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Front half of a decode layer for models whose per-KV-head projections are
+// small: ONE kernel per layer does RMSNorm -> the Q/K/V rows of KV head kh ->
+// rope_i -> KV append -> attention -> the group's W_o column slice, in one
+// cluster of CL CTAs per KV head ("量化 llama 的一次前向", forward: the same
+// steps as the separate kernels, fused). Cluster kh owns the q rows of its G
+// query heads and the k and v rows of head kh (G*hd/32 + 2*hd/32 tiles of
+// [Wq;Wk;Wv]); CTA r computes tiles r, r + CL, ... of that list against the
+// normalised x and broadcasts the finished (rotated) rows into every CTA of
+// the cluster through distributed shared memory, writing k and v to the
+// cache as well. After a cluster barrier each CTA runs the attention passes
+// over its position share with the newest K/V row taken from shared memory,
+// then the merge and the W_o slice as the attention kernel does. The
+// exchanges between CTAs are asynchronous stores (st.async) that complete
+// transaction counts on the receiving CTA's mbarriers, so no cluster-wide
+// barrier waits on the producer warp while it waits for free ring stages.
+// Weights (both projections' tiles) and the cached K/V rows are requested
+// before the grid dependency wait; only x waits for the preceding kernel.
+// ---------------------------------------------------------------------------
+
+__host__ __device__ inline int front_qkv_tiles(int G, int hd) { return (G * hd + 2 * hd) / 32; }
+__host__ __device__ inline int front_wq_bytes(int G, int hd, int h, int cl) {
+    return (front_qkv_tiles(G, hd) + cl - 1) / cl * (h / 32) * 1088;
+}
+struct FrontPlan {
+    CaPlan ca;
+    int wq, xn, knew, vnew, floats;
+};
+template <int HD>
+__host__ __device__ inline FrontPlan front_plan(int G, int GP, int cl, int h, int wo_bytes) {
+    FrontPlan p;
+    p.ca = ca_plan<HD>(G, GP, cl, wo_bytes);
+    int o = p.ca.floats;
+    auto take = [&](int n) { const int r = o; o += ca_round(n); return r; };
+    p.wq = take(front_wq_bytes(G, HD, h, cl) / 4);
+    p.xn = take(h);
+    p.knew = take(HD);
+    p.vnew = take(HD);
+    p.floats = o;
+    return p;
+}
+
+template <int HD, int CL, int GP>
+__global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(FrontArgs fa) {
+    constexpr int D4 = HD / 4;
+    extern __shared__ __align__(128) float smf[];
+    __shared__ __align__(8) uint64_t full[kCaStages];
+    __shared__ __align__(8) uint64_t empty[kCaStages];
+    __shared__ __align__(8) uint64_t wo_bar, wq_bar;
+    __shared__ __align__(8) uint64_t rows_bar, part_bar;  // completed by st.async bytes
+    __shared__ float s_rscale;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
+    const int n_head = fa.n_head, n_kv = fa.n_kv, G = n_head / n_kv;
+    const int h = fa.wqkv.k, nbx = h >> 5;
+    const int qd = n_head * HD, kvd = n_kv * HD;
+    const int nbk = G * HD / 32;                        // W_o column blocks of this group
+    const int o_tiles = fa.wo.rows_pad >> 5;
+    const int nq = G * HD / 32, nkt = HD / 32, n_qkv = nq + 2 * nkt;
+    const FrontPlan pl = front_plan<HD>(G, GP, CL, h, fo_wo_bytes(fa.wo.rows_pad, G, HD, CL));
+    float* S = smf + pl.ca.s;
+    float* Q = smf + pl.ca.q;
+    float* CORR = smf + pl.ca.corr;
+    float* PO = smf + pl.ca.po;
+    float* PM = smf + pl.ca.pm;
+    float* PLs = smf + pl.ca.pl;
+    float* OM = smf + pl.ca.om;
+    float* RED2 = smf + pl.ca.red2;
+    uint8_t* WO = reinterpret_cast<uint8_t*>(smf + pl.ca.wo);
+    uint8_t* WQ = reinterpret_cast<uint8_t*>(smf + pl.wq);
+    float* XN = smf + pl.xn;
+    float* KNEW = smf + pl.knew;
+    float* VNEW = smf + pl.vnew;
+
+    const int pos = fa.st->pos;  // written two or more launches back
+    const int kv_len = pos + 1;
+    const int per = (kv_len + CL - 1) / CL;
+    const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
+    const int j_new = kv_len - 1;
+    const float* kb = fa.kc + (int64_t)kh * fa.stride * HD;
+    const float* vb = fa.vc + (int64_t)kh * fa.stride * HD;
+
+    // first row (in [Wq;Wk;Wv]) of entry i of this cluster's tile list
+    auto qkv_tile_row0 = [&](int i) -> int {
+        if (i < nq) return kh * G * HD + i * 32;
+        if (i < nq + nkt) return qd + kh * HD + (i - nq) * 32;
+        return qd + kvd + kh * HD + (i - nq - nkt) * 32;
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kCaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCaWarps);
+        }
+        mbar_init(&wo_bar, 1);
+        mbar_init(&wq_bar, 1);
+        mbar_init(&rows_bar, 1);
+        mbar_init(&part_bar, 1);
+        fence_mbar_init();
+        // the bytes each exchange brings into this CTA
+        mbar_arrive_expect_tx(&rows_bar, (uint32_t)((G + 2) * HD * 4));
+        mbar_arrive_expect_tx(&part_bar, (uint32_t)(CL * (G * HD + 2 * G) * 4));
+    }
+    __syncthreads();
+    // Every CTA's barriers exist (and expect their bytes) before any peer
+    // stores into it. This is the only cluster-wide barrier: the exchanges
+    // below are asynchronous stores that complete transaction counts on the
+    // receiver's mbarriers, so the producer warp never has to join a barrier
+    // while it waits for free ring stages.
+    cluster_sync();
+
+    if (warp == kCaWarps) {
+        if (lane == 0) {
+            // projection tiles: constant weights, requested first
+            int n_t = 0;
+            for (int i = rank; i < n_qkv; i += CL) ++n_t;
+            mbar_arrive_expect_tx(&wq_bar, (uint32_t)(n_t * nbx * 1088));
+            int u = 0;
+            for (int i = rank; i < n_qkv; i += CL, ++u) {
+                const int t = qkv_tile_row0(i) >> 5;
+                uint8_t* dst = WQ + (size_t)u * nbx * 1088;
+                bulk_g2s(dst, reinterpret_cast<const uint8_t*>(fa.wqkv.qs) + (size_t)t * h * 32,
+                         (uint32_t)(nbx * 1024), &wq_bar);
+                bulk_g2s(dst + nbx * 1024, reinterpret_cast<const uint8_t*>(fa.wqkv.d) + (size_t)t * nbx * 64,
+                         (uint32_t)(nbx * 64), &wq_bar);
+            }
+            n_t = 0;
+            for (int t = rank; t < o_tiles; t += CL) ++n_t;
+            mbar_arrive_expect_tx(&wo_bar, (uint32_t)(n_t * nbk * 1088));
+            const int nbo = fa.wo.k >> 5, b0 = kh * nbk;
+            u = 0;
+            for (int t = rank; t < o_tiles; t += CL, ++u) {
+                uint8_t* dst = WO + (size_t)u * nbk * 1088;
+                bulk_g2s(dst, reinterpret_cast<const uint8_t*>(fa.wo.qs) + (size_t)t * fa.wo.k * 32 + b0 * 1024,
+                         (uint32_t)(nbk * 1024), &wo_bar);
+                bulk_g2s(dst + nbk * 1024, reinterpret_cast<const uint8_t*>(fa.wo.d) + ((size_t)t * nbo + b0) * 64,
+                         (uint32_t)(nbk * 64), &wo_bar);
+            }
+            // cached K/V rows of this CTA's share; the newest row comes from the projection
+            bool waited = false;
+            int j = 0;
+            ca_produce_head<HD>(smf, full, empty, kb, vb, j_begin, j_end, j_new, true, waited, j, fa.err);
+        }
+        return;
+    }
+
+    // ---- consumers: RMSNorm of x ----------------------------------------------------------
+    // the norm weight is constant: loaded before the dependency wait (h <= 1024)
+    constexpr int kGPre = 4;
+    float gpre[kGPre];
+#pragma unroll
+    for (int u = 0; u < kGPre; ++u) {
+        const int i = tid + u * kCaCT;
+        gpre[u] = i < h ? fa.g[i] : 0.0f;
+    }
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    {
+        float ss = 0.0f;
+        for (int i = tid; i < h; i += kCaCT) {
+            const float v = fa.x[i];
+            XN[i] = v;
+            ss = fmaf(v, v, ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) RED2[warp * 33 + 32] = ss;
+        for (int i = tid; i < GP * HD; i += kCaCT)
+            if (i >= G * HD) Q[i] = 0.0f;  // padding heads
+        named_bar_sync(1, kCaCT);
+        if (tid == 0) {
+            float t = 0.0f;
+            for (int w = 0; w < kCaWarps; ++w) t += RED2[w * 33 + 32];
+            s_rscale = 1.0f / sqrtf(t / (float)h + fa.eps);
+        }
+        named_bar_sync(1, kCaCT);
+        const float r = s_rscale;
+        for (int i = tid, u = 0; i < h; i += kCaCT, ++u) {
+            float gg = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGPre; ++w)
+                if (w == u) gg = gpre[w];
+            if (u >= kGPre) gg = fa.g[i];
+            XN[i] = XN[i] * r * gg;
+        }
+        named_bar_sync(1, kCaCT);
+    }
+
+    // ---- this CTA's projection tiles; rotated rows to every CTA of the cluster ----------
+    mbar_wait_bounded(&wq_bar, 0, fa.err, 25);
+    {
+        const int half = HD >> 1;
+        const float* cosr = fa.rope_cos + (int64_t)pos * half;
+        const float* sinr = fa.rope_sin + (int64_t)pos * half;
+        int u = 0;
+        for (int i = rank; i < n_qkv; i += CL, ++u) {
+            const uint8_t* tw = WQ + (size_t)u * nbx * 1088;
+            float acc = 0.0f;
+            for (int b = warp; b < nbx; b += kCaWarps) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(tw + b * 1024 + lane * 16);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(tw + b * 1024 + 512 + lane * 16);
+                const float d = __half2float(reinterpret_cast<const __half*>(tw + nbx * 1024)[b * 32 + lane]);
+                const float4* x4 = reinterpret_cast<const float4*>(XN + b * 32);
+                uint64_t a0 = 0, a1 = 0;
+                a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
+                a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
+                a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
+                a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
+                acc = fmaf(d, (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)), acc);
+            }
+            RED2[warp * 33 + lane] = acc;
+            named_bar_sync(1, kCaCT);
+            if (warp == 0) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
+                const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+                const int row = qkv_tile_row0(i) + lane;  // row of [Wq;Wk;Wv]
+                if (i < nq + nkt) {
+                    // q or k row: rotate the pair (2m, 2m+1) of its head
+                    const int d = row % HD;
+                    const float cs = cosr[d >> 1], sn = sinr[d >> 1];
+                    const float rot = (lane & 1) ? other * sn + v * cs : v * cs - other * sn;
+                    if (i < nq) {
+                        float* dst = &Q[row - kh * G * HD];
+#pragma unroll 4
+                        for (int r = 0; r < CL; ++r) st_async_f32(dst, (uint32_t)r, rot, &rows_bar);
+                    } else {
+                        fa.kc[((int64_t)kh * fa.stride + pos) * HD + d] = rot;
+#pragma unroll 4
+                        for (int r = 0; r < CL; ++r) st_async_f32(&KNEW[d], (uint32_t)r, rot, &rows_bar);
+                    }
+                } else {
+                    const int d = row % HD;
+                    fa.vc[((int64_t)kh * fa.stride + pos) * HD + d] = v;
+#pragma unroll 4
+                    for (int r = 0; r < CL; ++r) st_async_f32(&VNEW[d], (uint32_t)r, v, &rows_bar);
+                }
+            }
+            named_bar_sync(1, kCaCT);
+        }
+    }
+    mbar_wait_bounded(&rows_bar, 0, fa.err, 26);  // q, k and v of the new position are here
+
+    // ---- attention over this CTA's positions, newest row from shared memory -------------
+    float4 qr[GP], o[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+        qr[g] = *reinterpret_cast<const float4*>(Q + g * HD + (lane % D4) * 4);
+        o[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m_run = -INFINITY, l_run = 0.0f;
+    int j = 0;
+    bool first = true;
+    ca_consume_head<HD, GP>(smf, full, empty, S, CORR, qr, G, j_begin, j_end, fa.scale, j, first, o, m_run, l_run,
+                            fa.err, j_new, KNEW, VNEW);
+    const int d4 = tid % D4, slice = tid / D4;
+    named_bar_sync(1, kCaCT);  // the ring is free: reuse it for the slice sums
+    float* RED = smf;          // [kSlices][G][HD]
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+        if (g < G) *reinterpret_cast<float4*>(RED + (slice * G + g) * HD + d4 * 4) = o[g];
+    named_bar_sync(1, kCaCT);
+    // every CTA gets every CTA's partial result and merges all of them itself
+    for (int e4 = tid; e4 < G * HD / 4; e4 += kCaCT) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < CaGeom<HD>::kSlices; ++s2) {
+            const float4 v = *reinterpret_cast<const float4*>(RED + s2 * G * HD + e4 * 4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+#pragma unroll 4
+        for (int r = 0; r < CL; ++r) st_async_f32x4(&PO[rank * G * HD + e4 * 4], (uint32_t)r, acc, &part_bar);
+    }
+    if (warp < G && lane < CL) {
+        st_async_f32(&PM[rank * G + warp], (uint32_t)lane, m_run, &part_bar);
+        st_async_f32(&PLs[rank * G + warp], (uint32_t)lane, l_run, &part_bar);
+    }
+    // every CTA's partial result is here; these are the last stores any peer
+    // makes into this CTA, so after this wait the CTA may run to its end
+    mbar_wait_bounded(&part_bar, 0, fa.err, 27);
+    {
+        for (int e = tid; e < G * HD; e += kCaCT) {
+            const int gg = e / HD;
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < CL; ++r) M = fmaxf(M, PM[r * G + gg]);
+            float Lsum = 0.0f, acc = 0.0f;
+#pragma unroll
+            for (int r = 0; r < CL; ++r) {
+                const float m_r = PM[r * G + gg];
+                const float wgt = m_r == -INFINITY ? 0.0f : expf(m_r - M);
+                Lsum = fmaf(wgt, PLs[r * G + gg], Lsum);
+                acc = fmaf(wgt, PO[r * G * HD + e], acc);
+            }
+            OM[e] = acc / Lsum;
+        }
+    }
+    named_bar_sync(1, kCaCT);
+
+    // ---- W_o column slice of the group: part[kh] ------------------------------------------
+    mbar_wait_bounded(&wo_bar, 0, fa.err, 24);
+    int u = 0;
+    for (int t = rank; t < o_tiles; t += CL, ++u) {
+        const uint8_t* tw = WO + (size_t)u * nbk * 1088;
+        float acc = 0.0f;
+        for (int b = warp; b < nbk; b += kCaWarps) {
+            const uint4 q0 = *reinterpret_cast<const uint4*>(tw + b * 1024 + lane * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(tw + b * 1024 + 512 + lane * 16);
+            const float d = __half2float(reinterpret_cast<const __half*>(tw + nbk * 1024)[b * 32 + lane]);
+            const float4* x4 = reinterpret_cast<const float4*>(OM + b * 32);
+            uint64_t a0 = 0, a1 = 0;
+            a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
+            a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
+            a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
+            a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
+            acc = fmaf(d, (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)), acc);
+        }
+        RED2[warp * 33 + lane] = acc;
+        named_bar_sync(1, kCaCT);
+        if (warp == 0) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
+            const int r = t * 32 + lane;
+            if (r < fa.wo.rows) fa.part[(int64_t)kh * fa.part_stride + r] = v;
         }
         named_bar_sync(1, kCaCT);
     }
@@ -740,6 +1077,101 @@ cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float*
                              pdl, err, s);
 }
 
+// ---- fused layer front: host side --------------------------------------------------------
+template <int HD, int CL, int GP>
+static cudaLaunchConfig_t front_config(const FrontArgs& fa, cudaStream_t s, cudaLaunchAttribute* attrs, bool pdl) {
+    const int G = fa.n_head / fa.n_kv;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(fa.n_kv * CL);
+    cfg.blockDim = dim3(kCaThreads);
+    cfg.dynamicSmemBytes =
+        (size_t)front_plan<HD>(G, GP, CL, fa.wqkv.k, fo_wo_bytes(fa.wo.rows_pad, G, HD, CL)).floats * 4;
+    cfg.stream = s;
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = CL;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    int n = 1;
+    if (pdl) {
+        attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[1].val.programmaticStreamSerializationAllowed = 1;
+        n = 2;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cfg;
+}
+
+template <int HD, int CL, int GP>
+static cudaError_t front_set_attrs() {
+    cudaError_t e = cudaFuncSetAttribute(layer_front_cluster_kernel<HD, CL, GP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCaSmemLimit);
+    if (e == cudaSuccess && CL > 8)
+        e = cudaFuncSetAttribute(layer_front_cluster_kernel<HD, CL, GP>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+static bool g_front_ok = false;
+
+// Cluster size for the fused front (16 when all KV heads' clusters fit at
+// once), or 0 when the model does not fit the kernel.
+template <int HD, int GP>
+static int front_cluster_t(const FrontArgs& fa) {
+    if (!g_front_ok) return 0;
+    const int G = fa.n_head / fa.n_kv, h = fa.wqkv.k;
+    for (int cl : {16, 8}) {
+        if (cl == 16 && !g_ca16_ok) continue;
+        if (front_wq_bytes(G, HD, h, cl) > 48 * 1024 || fo_wo_bytes(fa.wo.rows_pad, G, HD, cl) > kFoMaxWoBytes)
+            continue;
+        const size_t smem = (size_t)front_plan<HD>(G, GP, cl, h, fo_wo_bytes(fa.wo.rows_pad, G, HD, cl)).floats * 4;
+        if (smem > (size_t)kCaSmemLimit) continue;
+        cudaLaunchAttribute attrs[2];
+        int n = 0;
+        cudaError_t e;
+        if (cl == 16) {
+            cudaLaunchConfig_t cfg = front_config<HD, 16, GP>(fa, 0, attrs, false);
+            e = cudaOccupancyMaxActiveClusters(&n, layer_front_cluster_kernel<HD, 16, GP>, &cfg);
+        } else {
+            cudaLaunchConfig_t cfg = front_config<HD, 8, GP>(fa, 0, attrs, false);
+            e = cudaOccupancyMaxActiveClusters(&n, layer_front_cluster_kernel<HD, 8, GP>, &cfg);
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (n >= fa.n_kv) return cl;
+    }
+    return 0;
+}
+
+int layer_front_cluster_size(const FrontArgs& fa, int head_dim) {
+    if (fa.n_kv <= 0 || fa.n_head % fa.n_kv || fa.n_head / fa.n_kv > kMaxGroup) return 0;
+    if (fa.wo.k != fa.n_head * head_dim || (fa.n_head / fa.n_kv) * head_dim % 32) return 0;
+    const bool wide = fa.n_head / fa.n_kv > 4;
+    if (head_dim == 64) return wide ? front_cluster_t<64, 8>(fa) : front_cluster_t<64, 4>(fa);
+    if (head_dim == 128) return wide ? front_cluster_t<128, 8>(fa) : front_cluster_t<128, 4>(fa);
+    return 0;
+}
+
+template <int HD, int GP>
+static cudaError_t front_launch_t(const FrontArgs& fa, int cl, bool pdl, cudaStream_t s) {
+    cudaLaunchAttribute attrs[2];
+    if (cl == 16) {
+        cudaLaunchConfig_t cfg = front_config<HD, 16, GP>(fa, s, attrs, pdl);
+        return cudaLaunchKernelEx(&cfg, layer_front_cluster_kernel<HD, 16, GP>, fa);
+    }
+    cudaLaunchConfig_t cfg = front_config<HD, 8, GP>(fa, s, attrs, pdl);
+    return cudaLaunchKernelEx(&cfg, layer_front_cluster_kernel<HD, 8, GP>, fa);
+}
+
+cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool pdl, cudaStream_t s) {
+    if (!fa.st || (cl != 16 && cl != 8)) return cudaErrorInvalidValue;
+    const bool wide = fa.n_head / fa.n_kv > 4;
+    if (head_dim == 64) return wide ? front_launch_t<64, 8>(fa, cl, pdl, s) : front_launch_t<64, 4>(fa, cl, pdl, s);
+    if (head_dim == 128) return wide ? front_launch_t<128, 8>(fa, cl, pdl, s) : front_launch_t<128, 4>(fa, cl, pdl, s);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t init_attention_attributes() {
     cudaError_t err = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)decode_smem_bytes(64));
@@ -759,6 +1191,11 @@ cudaError_t init_attention_attributes() {
                 ca_set_attrs<128, 16, 4, false>() == cudaSuccess && ca_set_attrs<128, 16, 8, false>() == cudaSuccess &&
                 ca_set_attrs<64, 16, 4, true>() == cudaSuccess && ca_set_attrs<64, 16, 8, true>() == cudaSuccess &&
                 ca_set_attrs<128, 16, 4, true>() == cudaSuccess && ca_set_attrs<128, 16, 8, true>() == cudaSuccess;
+    cudaGetLastError();
+    g_front_ok = front_set_attrs<64, 8, 4>() == cudaSuccess && front_set_attrs<64, 8, 8>() == cudaSuccess &&
+                 front_set_attrs<128, 8, 4>() == cudaSuccess && front_set_attrs<128, 8, 8>() == cudaSuccess &&
+                 front_set_attrs<64, 16, 4>() == cudaSuccess && front_set_attrs<64, 16, 8>() == cudaSuccess &&
+                 front_set_attrs<128, 16, 4>() == cudaSuccess && front_set_attrs<128, 16, 8>() == cudaSuccess;
     cudaGetLastError();
     return cudaSuccess;
 }

@@ -59,14 +59,17 @@ __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, c
 }
 
 // Epilogue on the 32 rows of a tile (warp-wide; lane = row within the tile).
+// pre: for EPI_RESIDUAL, the residual value of this lane's row, read right
+// after the grid dependency wait so that its latency overlaps the products.
 template <int EPI>
-__device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, int n_tiles) {
+__device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, int n_tiles,
+                                              float pre) {
     const int r = tile * 32 + lane;
     const bool valid = r < rows;
     if (EPI == EPI_STORE) {
         if (valid) e.y[r] = v;
     } else if (EPI == EPI_RESIDUAL) {
-        if (valid) e.y[r] = (e.res ? e.res[r] : e.y[r]) + v;
+        if (valid) e.y[r] = pre + v;
     } else if (EPI == EPI_QKV) {
         const float other = __shfl_xor_sync(0xffffffffu, v, 1);
         const int pos = e.state ? e.state->pos : e.pos0;
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     const bool x_full = NORM && S > 1;
     const int x0 = b0 * 32, xn = nblk * 32;
     float* xslice = x_full ? xs + x0 : xs;
+    const int np = NORM ? a.pre.n_part : 0;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -138,6 +142,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
+    float res_pre = 0.0f;  // EPI_RESIDUAL: residual of the row this lane finishes (warp 0 of split 0)
 
     if (warp == kCWarps) {
         // ---- producer: stream this unit's codes and scales -------------------
@@ -158,7 +163,6 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             for (int j = 0; j < first; ++j) issue_stage(j);  // weights: no kernel writes them
             pdl_wait();                                      // x: written by the preceding kernel
             const int xoff = x_full ? 0 : x0, xcnt = x_full ? k : xn;
-            const int np = NORM ? a.pre.n_part : 0;  // with the norm, xcnt == k
             mbar_arrive_expect_tx(&xbar, (uint32_t)(xcnt * 4 * (1 + np)));
             bulk_g2s(xs, a.x + xoff, (uint32_t)(xcnt * 4), &xbar);
             for (int p = 0; p < np; ++p)
@@ -168,9 +172,24 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         }
     } else {
         // ---- consumers --------------------------------------------------------
+        // The norm weight is constant: each thread loads its float4s of the
+        // slice before the dependency wait (up to 4 per thread; k <= 4096).
+        constexpr int kGPre = 4;
+        float4 gpre[kGPre];
+        if (NORM) {
+#pragma unroll
+            for (int u = 0; u < kGPre; ++u) {
+                const int i = threadIdx.x * 4 + u * kCWarps * 32 * 4;
+                gpre[u] = i < xn ? *reinterpret_cast<const float4*>(a.g + x0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         pdl_wait();
         if (tid == 0) pdl_launch_dependents();
         constexpr int kCT = kCWarps * 32;
+        if (EPI == EPI_RESIDUAL && split == 0 && warp == 0) {
+            const int r = tile * 32 + lane;
+            if (r < W.rows) res_pre = a.e.res ? a.e.res[r] : a.e.y[r];
+        }
         mbar_wait_bounded(&xbar, 0, a.err, 13);
         if (NORM) {
             const int nx = x_full ? k : xn;  // == k when unsplit
@@ -204,9 +223,13 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             }
             named_bar_sync(1, kCT);
             const float r = s_rscale;
-            for (int i = tid * 4; i < xn; i += kCT * 4) {
+            for (int i = tid * 4, u = 0; i < xn; i += kCT * 4, ++u) {
                 float4 v = *reinterpret_cast<float4*>(xslice + i);
-                const float4 gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
+                float4 gg;
+#pragma unroll
+                for (int w = 0; w < kGPre; ++w)
+                    if (w == u) gg = gpre[w];
+                if (u >= kGPre) gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
                 v.x = v.x * r * gg.x; v.y = v.y * r * gg.y; v.z = v.z * r * gg.z; v.w = v.w * r * gg.w;
                 *reinterpret_cast<float4*>(xslice + i) = v;
             }
@@ -249,7 +272,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     if (split == 0 && warp == 0) {
         float v = part[lane];
         for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
-        gemv_epilogue<EPI>(a.e, W.rows, tile, lane, v, W.rows_pad / 32);
+        gemv_epilogue<EPI>(a.e, W.rows, tile, lane, v, W.rows_pad / 32, res_pre);
     }
     if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
 }
@@ -285,8 +308,8 @@ static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const floa
     const int S = gemv_splits(tiles, nb, sm_count_current());
     const int max_blk = (nb + S - 1) / S;
     const int n_part = (NORM && pre) ? pre->n_part : 0;
-    const size_t x_floats = (NORM && S > 1) ? (size_t)W.k * (1 + n_part)
-                                            : (size_t)max_blk * 32 + (size_t)n_part * W.k;
+    // x (its slice, or all of it for the norm) and the added partials
+    const size_t x_floats = NORM ? (size_t)W.k * (1 + n_part) : (size_t)max_blk * 32;
     const size_t smem = (size_t)kStages * kStageBytes + x_floats * sizeof(float);
     if (smem > (size_t)kGemvMaxSmem) return cudaErrorInvalidValue;
     GemvArgs a{W, x, g, eps, e, S, err, (NORM && pre) ? *pre : GemvPreSum{}};

@@ -128,6 +128,28 @@ cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, con
 // partials summing to W_o o (added to the residual by the next kernel).
 // supported() is false when the model's W_o does not fit the kernel.
 bool attn_oproj_fused_supported(int n_head, int n_kv, int head_dim, const PackedQ8& Wo);
+// The front half of a decode layer (RMSNorm, the Q/K/V rows of each KV head,
+// rope_i, KV append, attention, W_o column slice -> part) as one kernel with a
+// cluster per KV head, for models whose per-head projections are small.
+struct FrontArgs {
+    const float* x;        // [h] residual stream (written by the preceding kernel)
+    const float* g;        // [h] attention RMSNorm weight
+    float eps;
+    PackedQ8 wqkv;         // [Wq;Wk;Wv]
+    PackedQ8 wo;
+    float* kc;             // layer K cache [n_kv][stride][hd]
+    float* vc;
+    const float* rope_cos; // [stride][hd/2]
+    const float* rope_sin;
+    int n_head, n_kv, stride;
+    const DevState* st;
+    float scale;
+    float* part;           // [n_kv][part_stride] partials of W_o o
+    int part_stride;
+    int* err;
+};
+int layer_front_cluster_size(const FrontArgs& fa, int head_dim);  // 0: not supported
+cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool pdl, cudaStream_t s);
 cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                               int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
                               int part_stride, bool pdl, int* err, cudaStream_t s);

@@ -103,6 +103,27 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local_ptr, uint32_
     return v;
 }
 
+// Asynchronous store of one f32 into CTA `rank`'s shared memory (the same
+// offset as local_ptr there) that signals that CTA's mbarrier (the same offset
+// as local_bar) with 4 bytes of transaction count when it lands.
+__device__ __forceinline__ void st_async_f32(float* local_ptr, uint32_t rank, float v, uint64_t* local_bar) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(ra), "f"(v),
+                 "r"(rb)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32x4(float* local_ptr, uint32_t rank, float4 v, uint64_t* local_bar) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local_ptr)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+                 : "memory");
+}
+
 // ---- named barrier for a subset of the CTA's warps ------------------------------
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -88,10 +88,10 @@ struct Profiler {
     }
 };
 
-enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_COUNT };
+enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_COUNT };
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
                                      "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
-                                     "decode_cluster_layers", "attn_oproj_residual"};
+                                     "decode_cluster_layers", "attn_oproj_residual", "layer_front_qkv_attn_o"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -142,6 +142,7 @@ struct llama_q8_ctx {
     int64_t launches = 0;
     int cluster = 0;                     // > 0: decode layers run as one cluster of this many CTAs
     bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
+    int front_cl = 0;                    // > 0: norm + QKV + attention + W_o as one kernel (this cluster size)
     LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
@@ -212,6 +213,30 @@ double q8_bytes(int64_t rows, int64_t k) { return (double)rows * (double)k * 34.
 // algorithmic bytes (attention bytes are per cached position, scaled by the
 // step's cache length when the times are read); launches are then plain, since
 // an event node between two kernels leaves nothing for PDL to overlap.
+FrontArgs front_args(llama_q8_ctx* c, int l) {
+    const llama_q8_config& cfg = c->cfg;
+    const LayerDev& L = c->layers[l];
+    FrontArgs fa{};
+    fa.x = c->d_x;
+    fa.g = L.attn_norm;
+    fa.eps = cfg.rms_eps;
+    fa.wqkv = L.qkv;
+    fa.wo = L.o;
+    fa.kc = c->kcache(l);
+    fa.vc = c->vcache(l);
+    fa.rope_cos = c->d_rope_cos;
+    fa.rope_sin = c->d_rope_sin;
+    fa.n_head = cfg.n_head;
+    fa.n_kv = cfg.n_head_kv;
+    fa.stride = cfg.max_seq;
+    fa.st = c->d_state;
+    fa.scale = 1.0f / sqrtf((float)cfg.head_dim);
+    fa.part = c->d_part;
+    fa.part_stride = cfg.n_embd;
+    fa.err = &c->d_state->err;
+    return fa;
+}
+
 cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof = nullptr) {
     const llama_q8_config& cfg = c->cfg;
     cudaStream_t s = c->stream;
@@ -264,19 +289,27 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
         const LayerDev& L = c->layers[l];
         EpiArgs e = qkv_epi(c, l);
         e.state = c->d_state;
-        run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0,
-            [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
         EpiArgs r;
         r.y = c->d_x;
-        if (c->fuse_o) {
+        if (c->front_cl > 0 || c->fuse_o) {
             // attention + W_o per KV head (partials), the sum folded into the gate/up kernel's norm,
             // and the down projection's residual taken from that sum
-            run(F_ATTN_O, 4.0 * qr + q8_bytes(h, qr) + 4.0 * h * cfg.n_head_kv, 8.0 * (double)cfg.n_head_kv * cfg.head_dim,
-                [&] {
-                    return launch_attn_oproj(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
-                                             cfg.head_dim, cfg.max_seq, c->d_state, L.o, c->d_part, (int)h, pdl,
-                                             &c->d_state->err, s);
+            if (c->front_cl > 0) {
+                const FrontArgs fa = front_args(c, l);
+                run(F_FRONT, q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + 8.0 * h + 4.0 * h * cfg.n_head_kv,
+                    8.0 * (double)cfg.n_head_kv * cfg.head_dim,
+                    [&] { return launch_layer_front(fa, cfg.head_dim, c->front_cl, pdl, s); });
+            } else {
+                run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0, [&] {
+                    return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s);
                 });
+                run(F_ATTN_O, 4.0 * qr + q8_bytes(h, qr) + 4.0 * h * cfg.n_head_kv,
+                    8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
+                        return launch_attn_oproj(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
+                                                 cfg.head_dim, cfg.max_seq, c->d_state, L.o, c->d_part, (int)h, pdl,
+                                                 &c->d_state->err, s);
+                    });
+            }
             EpiArgs g;
             g.a_out = c->d_a;
             GemvPreSum pre;
@@ -294,6 +327,8 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
             run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
                 [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, rd, pdl, &c->d_state->err, s); });
         } else {
+            run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0,
+                [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
             run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
                 return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
                                                   cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
@@ -447,7 +482,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         C.n_vocab <= 0 || C.max_seq <= 0 || C.head_dim <= 0 || !(C.rms_eps >= 0.f) || !(C.rope_theta > 0.f))
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
-    if (C.decode_kernel < 0 || C.decode_kernel > 2) return LQ8_ERR_ARG;
+    if (C.decode_kernel < 0 || C.decode_kernel > 3) return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -616,7 +651,16 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
     // decode path: the whole layer stack as one cluster when asked for and it fits
-    if (C.decode_kernel == 0) c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
+    if (C.decode_kernel == 0 || C.decode_kernel == 3) {
+        c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
+        cudaGetLastError();
+        if (C.decode_kernel == 3 && !c->fuse_o) {
+            free_ctx_memory(c);
+            delete c;
+            return LQ8_ERR_UNSUPPORTED;
+        }
+    }
+    if (C.decode_kernel == 0 && c->fuse_o) c->front_cl = layer_front_cluster_size(front_args(c, 0), hd);
     cudaGetLastError();
     if (C.decode_kernel == 2) {
         c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);

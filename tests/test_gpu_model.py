@@ -25,22 +25,24 @@ def m135():
     for name, t in dev_t.items():     # the GPU quantiser matches the oracle's bytes
         if ora_t[name].dtype == np.uint8:
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
-    model = B.Model(CFG, dev_t, on_device=True)                              # automatic: attention + W_o fused
-    layered = B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True)      # five kernels per layer
-    cluster = B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True)      # one-cluster decode step
+    models = {
+        "front": B.Model(CFG, dev_t, on_device=True),                          # automatic: three kernels per layer
+        "four": B.Model(dict(CFG, decode_kernel=3), dev_t, on_device=True),    # attention applies W_o
+        "layered": B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True), # five kernels per layer
+        "cluster": B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True), # one-cluster decode step
+    }
     del dev_t
     torch.cuda.empty_cache()
-    oracle = O.ModelWeights(CFG, ora_t, weight_cache="f64")
-    yield model, oracle, layered, cluster
-    model.close()
-    layered.close()
-    cluster.close()
+    models["oracle"] = O.ModelWeights(CFG, ora_t, weight_cache="f64")
+    yield models
+    for name, m in models.items():
+        if name != "oracle":
+            m.close()
 
 
-@pytest.fixture(params=["fused", "layered", "cluster"])
+@pytest.fixture(params=["front", "four", "layered", "cluster"])
 def either(request, m135):
-    model, oracle, layered, cluster = m135
-    return {"fused": model, "layered": layered, "cluster": cluster}[request.param], oracle
+    return m135[request.param], m135["oracle"]
 
 
 def _check_run(model, oracle, prompt, n_decode):
@@ -96,7 +98,7 @@ def test_kv_cache_after_rope_matches_oracle(either):
 
 
 def test_index_pos_rules(m135):
-    model, _, _, _ = m135
+    model = m135["front"]
     B = binding()
     prompt = synth.prompt_ids(13, V, 1)
     full = model.forward(prompt, 0)
@@ -127,7 +129,7 @@ def test_index_pos_rules(m135):
 
 
 def test_context_limit(m135):
-    model, _, _, _ = m135
+    model = m135["front"]
     B = binding()
     prompt = synth.prompt_ids(64, V, 2)
     assert model.forward_status(np.zeros(4097, np.int32), 0) == B.LQ8_ERR_CTX
@@ -154,7 +156,7 @@ def test_prefill_and_decode_paths_agree(either):
 
 
 def test_device_resident_api(m135):
-    model, _, layered, cluster = m135
+    model, layered, cluster = m135["front"], m135["layered"], m135["cluster"]
     prompt = synth.prompt_ids(203, V, 0)
     ref = model.generate(prompt, 16)
     d_ids = torch.from_numpy(prompt).cuda()
@@ -166,15 +168,17 @@ def test_device_resident_api(m135):
     got = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
     np.testing.assert_array_equal(got, ref)
     assert model.cache_len() == 203 + 16
-    assert model.decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1   # attention kernel applies W_o
+    assert model.decode_kernel_count() == 1 + 3 * CFG["n_layer"] + 1   # norm+QKV+attention+W_o fused
+    assert m135["four"].decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1
     assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
     assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
 
 
-def test_fused_attention_oproj_at_long_context(m135):
-    """Decode steps at positions near the 4096 limit: the attention kernel that
-    also applies W_o gives the logits and tokens of the five-kernel layer."""
-    model, _, layered, _ = m135
+def test_fused_layer_front_at_long_context(m135):
+    """Decode steps at positions near the 4096 limit: the fused layer front
+    (norm, Q/K/V, attention, W_o in one kernel) gives the logits and tokens of
+    the five-kernel layer."""
+    model, layered = m135["front"], m135["layered"]
     prompt = synth.prompt_ids(3900, V, 6)
     a = model.forward(prompt, 0)
     b = layered.forward(prompt, 0)
