@@ -27,10 +27,19 @@ namespace lq8 {
 
 constexpr int kCWarps = 8;                        // consumer warps
 constexpr int kGemvThreads = (kCWarps + 1) * 32;  // + one producer warp
-constexpr int kStageBlocks = 16;                  // blocks per stage (a multiple of kCWarps)
-constexpr int kStages = 3;
-constexpr int kStageCodeBytes = kStageBlocks * 1024;
-constexpr int kStageBytes = kStageCodeBytes + kStageBlocks * 64;
+// Ring shape: stages x blocks per stage (a multiple of kCWarps). Matrices
+// with many row tiles stream best through 3 stages of 16 blocks (three CTAs
+// per SM); those split over clusters (few tiles) through 2 stages of 32.
+template <int STAGES, int SBLK>
+struct Ring {
+    static constexpr int kStages = STAGES;
+    static constexpr int kStageBlocks = SBLK;
+    static constexpr int kStageCodeBytes = SBLK * 1024;
+    static constexpr int kStageBytes = kStageCodeBytes + SBLK * 64;
+    static constexpr int kCtasPerSm = (227 * 1024) / (STAGES * kStageBytes + 16 * 1024 + 2048);
+};
+using RingWide = Ring<3, 16>;
+using RingDeep = Ring<2, 32>;
 constexpr int kGemvMaxSmem = 227 * 1024 - 4096;
 
 struct GemvArgs {
@@ -104,8 +113,10 @@ __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int ti
     }
 }
 
-template <int EPI, bool NORM>
+template <int EPI, bool NORM, typename RG>
 __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
+    constexpr int kStages = RG::kStages, kStageBlocks = RG::kStageBlocks;
+    constexpr int kStageCodeBytes = RG::kStageCodeBytes, kStageBytes = RG::kStageBytes;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     float* xs = reinterpret_cast<float*>(smem + kStages * kStageBytes);
@@ -277,12 +288,10 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
 }
 
-constexpr int kGemvCtasPerSm = (227 * 1024) / (kStages * kStageBytes + 16 * 1024 + 2048);
-
 // Splits per tile: enough CTAs to cover the GPU in one wave, at least 16
 // blocks per split, at most 8 (a portable cluster).
-static int gemv_splits(int tiles, int nb, int sm_count) {
-    const int capacity = sm_count * kGemvCtasPerSm;
+static int gemv_splits(int tiles, int nb, int sm_count, int ctas_per_sm) {
+    const int capacity = sm_count * ctas_per_sm;
     int s = 1;
     while (s < 8 && tiles * (s + 1) <= capacity && nb / (s + 1) >= 16) ++s;
     return s;
@@ -301,11 +310,12 @@ static int sm_count_current() {
     return g_sm_count[dev];
 }
 
-template <int EPI, bool NORM>
-static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
-                                   bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+template <int EPI, bool NORM, typename RG>
+static cudaError_t gemv_launch_ring(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
+                                    bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+    constexpr int kStages = RG::kStages, kStageBytes = RG::kStageBytes;
     const int tiles = W.rows_pad / 32, nb = W.k / 32;
-    const int S = gemv_splits(tiles, nb, sm_count_current());
+    const int S = gemv_splits(tiles, nb, sm_count_current(), RG::kCtasPerSm);
     const int max_blk = (nb + S - 1) / S;
     const int n_part = (NORM && pre) ? pre->n_part : 0;
     // x (its slice, or all of it for the norm) and the added partials
@@ -334,16 +344,29 @@ static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const floa
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, q8_gemv_kernel<EPI, NORM>, a);
+    return cudaLaunchKernelEx(&cfg, q8_gemv_kernel<EPI, NORM, RG>, a);
+}
+
+template <int EPI, bool NORM>
+static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
+                                   bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+    const int tiles = W.rows_pad / 32;
+    if (tiles >= 2 * sm_count_current())
+        return gemv_launch_ring<EPI, NORM, RingWide>(W, x, g, eps, e, pdl, err, s, pre);
+    return gemv_launch_ring<EPI, NORM, RingDeep>(W, x, g, eps, e, pdl, err, s, pre);
 }
 
 template <int EPI>
 static cudaError_t gemv_set_attr() {
-    cudaError_t err = cudaFuncSetAttribute(q8_gemv_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kGemvMaxSmem);
-    if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(q8_gemv_kernel<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kGemvMaxSmem);
+    cudaError_t err = cudaSuccess;
+    auto one = [&](auto kernel) {
+        if (err == cudaSuccess) err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+    };
+    one(q8_gemv_kernel<EPI, true, RingWide>);
+    one(q8_gemv_kernel<EPI, false, RingWide>);
+    one(q8_gemv_kernel<EPI, true, RingDeep>);
+    one(q8_gemv_kernel<EPI, false, RingDeep>);
+    return err;
 }
 
 // Raise the dynamic shared-memory limit of every instantiation once per device
@@ -360,7 +383,10 @@ cudaError_t init_gemv_attributes() {
 
 size_t gemv_max_k() {
     // stages + the x slice of an unsplit unit must fit in shared memory
-    return (size_t)(kGemvMaxSmem - kStages * kStageBytes) / sizeof(float) / 32 * 32;
+    constexpr int ring = RingWide::kStages * RingWide::kStageBytes > RingDeep::kStages * RingDeep::kStageBytes
+                             ? RingWide::kStages * RingWide::kStageBytes
+                             : RingDeep::kStages * RingDeep::kStageBytes;
+    return (size_t)(kGemvMaxSmem - ring) / sizeof(float) / 32 * 32;
 }
 
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
