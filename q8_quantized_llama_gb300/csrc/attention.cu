@@ -884,20 +884,22 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     // makes into this CTA, so after this wait the CTA may run to its end
     mbar_wait_bounded(&part_bar, 0, fa.err, 27);
     {
+        // merge weights once per (head, source CTA): w = exp(m_r - M) / sum_r' exp(m_r' - M) l_r'
+        float* WGT = RED2;  // [G][CL], G * CL <= 8 * 16 of the 8 x 33 floats
+        if (warp < G) {
+            const float m_r = lane < CL ? PM[lane * G + warp] : -INFINITY;
+            const float M = warp_max(m_r);
+            const float w = (lane < CL && m_r != -INFINITY) ? expf(m_r - M) : 0.0f;
+            const float L = warp_sum(lane < CL ? w * PLs[lane * G + warp] : 0.0f);
+            if (lane < CL) WGT[warp * CL + lane] = w / L;
+        }
+        named_bar_sync(1, kCaCT);
         for (int e = tid; e < G * HD; e += kCaCT) {
-            const int gg = e / HD;
-            float M = -INFINITY;
+            const float* wg = WGT + (e / HD) * CL;
+            float acc = 0.0f;
 #pragma unroll
-            for (int r = 0; r < CL; ++r) M = fmaxf(M, PM[r * G + gg]);
-            float Lsum = 0.0f, acc = 0.0f;
-#pragma unroll
-            for (int r = 0; r < CL; ++r) {
-                const float m_r = PM[r * G + gg];
-                const float wgt = m_r == -INFINITY ? 0.0f : expf(m_r - M);
-                Lsum = fmaf(wgt, PLs[r * G + gg], Lsum);
-                acc = fmaf(wgt, PO[r * G * HD + e], acc);
-            }
-            OM[e] = acc / Lsum;
+            for (int r = 0; r < CL; ++r) acc = fmaf(wg[r], PO[r * G * HD + e], acc);
+            OM[e] = acc;
         }
     }
     named_bar_sync(1, kCaCT);
