@@ -149,6 +149,26 @@ struct FrontArgs {
     int* err;
 };
 int layer_front_cluster_size(const FrontArgs& fa, int head_dim);  // 0: not supported
+
+// decode_layer.cu: a whole decode layer as one 16-CTA cluster kernel (small models).
+struct LayerKArgs {
+    const float* x_in;   // [h] residual stream in (written by the preceding kernel)
+    float* x_out;        // [h] residual stream out (a different buffer)
+    const float* g_attn; // [h] RMSNorm weights
+    const float* g_ffn;
+    float eps;
+    PackedQ8 wqkv, wo, wgu, wdown;  // [Wq;Wk;Wv], W_o, row-interleaved [Wg;Wu], W_down
+    float* kc;           // layer K cache [n_kv][stride][hd]
+    float* vc;
+    const float* rope_cos;  // [stride][hd/2]
+    const float* rope_sin;
+    int n_head, n_kv, stride;
+    const DevState* st;
+    float scale;
+    int* err;
+};
+bool decode_layer_supported(const LayerKArgs& la, int head_dim);
+cudaError_t launch_decode_layer(const LayerKArgs& la, int head_dim, bool pdl, cudaStream_t s);
 cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool pdl, cudaStream_t s);
 cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                               int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,

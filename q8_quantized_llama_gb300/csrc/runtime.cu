@@ -88,10 +88,13 @@ struct Profiler {
     }
 };
 
-enum Family { F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_COUNT };
+enum Family {
+    F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_LAYER, F_COUNT
+};
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
                                      "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
-                                     "decode_cluster_layers", "attn_oproj_residual", "layer_front_qkv_attn_o"};
+                                     "decode_cluster_layers", "attn_oproj_residual", "layer_front_qkv_attn_o",
+                                     "decode_layer_cluster"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -121,6 +124,7 @@ struct llama_q8_ctx {
     float* d_a = nullptr;
     float* d_part = nullptr;  // decode: per-KV-head partials of W_o o
     float* d_xsum = nullptr;  // decode: x + W_o o, the residual of the down projection
+    float* d_x2 = nullptr;    // decode with the layer kernel: odd layers' residual stream
     float* d_logits = nullptr;
     int32_t* d_ids = nullptr;
     int32_t* d_out_ids = nullptr;
@@ -143,6 +147,7 @@ struct llama_q8_ctx {
     int cluster = 0;                     // > 0: decode layers run as one cluster of this many CTAs
     bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
     int front_cl = 0;                    // > 0: norm + QKV + attention + W_o as one kernel (this cluster size)
+    bool layer_kernel = false;           // each decode layer as one 16-CTA cluster kernel
     LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
@@ -168,7 +173,7 @@ void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
-                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_logits, c->d_ids,
+                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_x2, c->d_logits, c->d_ids,
                    c->d_out_ids,
                    c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_layer_ptrs};
     for (void* p : dev)
@@ -237,6 +242,32 @@ FrontArgs front_args(llama_q8_ctx* c, int l) {
     return fa;
 }
 
+LayerKArgs layer_args(llama_q8_ctx* c, int l) {
+    const llama_q8_config& cfg = c->cfg;
+    const LayerDev& L = c->layers[l];
+    LayerKArgs la{};
+    la.x_in = (l & 1) ? c->d_x2 : c->d_x;
+    la.x_out = (l & 1) ? c->d_x : c->d_x2;
+    la.g_attn = L.attn_norm;
+    la.g_ffn = L.ffn_norm;
+    la.eps = cfg.rms_eps;
+    la.wqkv = L.qkv;
+    la.wo = L.o;
+    la.wgu = L.gu;
+    la.wdown = L.down;
+    la.kc = c->kcache(l);
+    la.vc = c->vcache(l);
+    la.rope_cos = c->d_rope_cos;
+    la.rope_sin = c->d_rope_sin;
+    la.n_head = cfg.n_head;
+    la.n_kv = cfg.n_head_kv;
+    la.stride = cfg.max_seq;
+    la.st = c->d_state;
+    la.scale = 1.0f / sqrtf((float)cfg.head_dim);
+    la.err = &c->d_state->err;
+    return la;
+}
+
 cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof = nullptr) {
     const llama_q8_config& cfg = c->cfg;
     cudaStream_t s = c->stream;
@@ -285,6 +316,23 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
     }
     run(F_EMBED, q8_bytes(1, h) + 4.0 * h, 0.0,
         [&] { return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, pdl, s); });
+    if (c->layer_kernel) {
+        // every layer as one cluster kernel; the residual stream alternates between two buffers
+        const double lbytes = q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + q8_bytes(2 * F, h) + q8_bytes(h, F) +
+                              16.0 * h;
+        for (int l = 0; l < cfg.n_layer; ++l) {
+            const LayerKArgs la = layer_args(c, l);
+            run(F_LAYER, lbytes, 8.0 * (double)cfg.n_head_kv * cfg.head_dim,
+                [&] { return launch_decode_layer(la, cfg.head_dim, pdl, s); });
+        }
+        float* xf = (cfg.n_layer & 1) ? c->d_x2 : c->d_x;
+        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
+            return launch_gemv(c->head, xf, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
+                               &c->d_state->err, s);
+        });
+        if (n_kernels) *n_kernels = n;
+        return err;
+    }
     for (int l = 0; l < cfg.n_layer; ++l) {
         const LayerDev& L = c->layers[l];
         EpiArgs e = qkv_epi(c, l);
@@ -482,7 +530,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         C.n_vocab <= 0 || C.max_seq <= 0 || C.head_dim <= 0 || !(C.rms_eps >= 0.f) || !(C.rope_theta > 0.f))
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
-    if (C.decode_kernel < 0 || C.decode_kernel > 3) return LQ8_ERR_ARG;
+    if (C.decode_kernel < 0 || C.decode_kernel > 5) return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -633,6 +681,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_a, sizeof(float) * T * F));
     LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
     LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
+    LOAD_CK(cudaMalloc(&c->d_x2, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_logits, sizeof(float) * V));
     LOAD_CK(cudaMalloc(&c->d_ids, sizeof(int32_t) * T));
     LOAD_CK(cudaMalloc(&c->d_out_ids, sizeof(int32_t) * (T + 1)));
@@ -651,17 +700,27 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
     // decode path: the whole layer stack as one cluster when asked for and it fits
-    if (C.decode_kernel == 0 || C.decode_kernel == 3) {
+    // decode_kernel: 0 automatic (three per layer when the model fits, else four, else five), 1 five
+    // per layer, 2 one cluster kernel for the whole step, 3 four per layer, 4 three per layer, 5 one
+    // cluster kernel per layer (measured slower than three per layer on the models here)
+    bool unsupported = false;
+    if (C.decode_kernel == 5) {
+        c->layer_kernel = decode_layer_supported(layer_args(c, 0), hd);
+        cudaGetLastError();
+        unsupported = !c->layer_kernel;
+    }
+    if (C.decode_kernel == 0 || C.decode_kernel == 3 || C.decode_kernel == 4) {
         c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
         cudaGetLastError();
-        if (C.decode_kernel == 3 && !c->fuse_o) {
-            free_ctx_memory(c);
-            delete c;
-            return LQ8_ERR_UNSUPPORTED;
-        }
+        if (C.decode_kernel != 3 && c->fuse_o) c->front_cl = layer_front_cluster_size(front_args(c, 0), hd);
+        cudaGetLastError();
+        unsupported = (C.decode_kernel == 3 && !c->fuse_o) || (C.decode_kernel == 4 && c->front_cl == 0);
     }
-    if (C.decode_kernel == 0 && c->fuse_o) c->front_cl = layer_front_cluster_size(front_args(c, 0), hd);
-    cudaGetLastError();
+    if (unsupported) {
+        free_ctx_memory(c);
+        delete c;
+        return LQ8_ERR_UNSUPPORTED;
+    }
     if (C.decode_kernel == 2) {
         c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);
         cudaGetLastError();

@@ -63,7 +63,7 @@ def test_config_validation_without_a_gpu(B):
     t = {n: dummy for n, _, _ in synth.model_tensor_specs(cfg)}
     for bad, status in [(dict(head_dim=96), B.LQ8_ERR_UNSUPPORTED), (dict(n_embd=500), B.LQ8_ERR_UNSUPPORTED),
                         (dict(n_head_kv=4), B.LQ8_ERR_ARG), (dict(n_layer=0), B.LQ8_ERR_ARG),
-                        (dict(tied_output=0), B.LQ8_ERR_ARG), (dict(decode_kernel=4), B.LQ8_ERR_ARG),
+                        (dict(tied_output=0), B.LQ8_ERR_ARG), (dict(decode_kernel=6), B.LQ8_ERR_ARG),
                         (dict(decode_kernel=-1), B.LQ8_ERR_ARG)]:
         c = B.make_config(dict(cfg, **bad))
         w, keep = B.make_weights(cfg, t, on_device=False)

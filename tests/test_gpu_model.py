@@ -27,6 +27,7 @@ def m135():
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
     models = {
         "front": B.Model(CFG, dev_t, on_device=True),                          # automatic: three kernels per layer
+        "layer": B.Model(dict(CFG, decode_kernel=5), dev_t, on_device=True),   # one cluster kernel per layer
         "four": B.Model(dict(CFG, decode_kernel=3), dev_t, on_device=True),    # attention applies W_o
         "layered": B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True), # five kernels per layer
         "cluster": B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True), # one-cluster decode step
@@ -40,7 +41,7 @@ def m135():
             m.close()
 
 
-@pytest.fixture(params=["front", "four", "layered", "cluster"])
+@pytest.fixture(params=["layer", "front", "four", "layered", "cluster"])
 def either(request, m135):
     return m135[request.param], m135["oracle"]
 
@@ -169,16 +170,18 @@ def test_device_resident_api(m135):
     np.testing.assert_array_equal(got, ref)
     assert model.cache_len() == 203 + 16
     assert model.decode_kernel_count() == 1 + 3 * CFG["n_layer"] + 1   # norm+QKV+attention+W_o fused
+    assert m135["layer"].decode_kernel_count() == 1 + CFG["n_layer"] + 1
     assert m135["four"].decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1
     assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
     assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
 
 
-def test_fused_layer_front_at_long_context(m135):
-    """Decode steps at positions near the 4096 limit: the fused layer front
-    (norm, Q/K/V, attention, W_o in one kernel) gives the logits and tokens of
-    the five-kernel layer."""
-    model, layered = m135["front"], m135["layered"]
+@pytest.mark.parametrize("variant", ["layer", "front"])
+def test_fused_decode_kernels_at_long_context(m135, variant):
+    """Decode steps at positions near the 4096 limit: the one-kernel layer and
+    the fused layer front give the logits and tokens of the five-kernel
+    layer."""
+    model, layered = m135[variant], m135["layered"]
     prompt = synth.prompt_ids(3900, V, 6)
     a = model.forward(prompt, 0)
     b = layered.forward(prompt, 0)
