@@ -208,6 +208,14 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
 
 const char* llama_q8_status_str(llama_q8_status s);
 
+/* Self-test of the kernels' bounded waits: launches one CTA that waits on a
+ * shared-memory barrier nothing completes, with the same ~1 s limit every
+ * kernel of the library uses; the kernel gives up, records the wait's code
+ * in device memory and returns. On return *code holds that code (the library
+ * uses nonzero codes only for such timeouts) and the device is still usable.
+ * Synchronous; about one second. LQ8_ERR_ARG for a NULL code. */
+llama_q8_status llama_q8_selftest_wait_timeout(int32_t* code);
+
 /* ---------------------------------------------------------------------------
  * Device-level entry points (kernel workloads). All data pointers are device
  * memory; `stream` is a cudaStream_t (NULL = legacy default stream). They

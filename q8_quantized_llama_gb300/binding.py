@@ -30,7 +30,8 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_decode_kernel_count", "llama_q8_status_str", "llama_q8_quantize",
            "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul", "llama_q8_matmul_ex",
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
-           "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode")
+           "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode",
+           "llama_q8_selftest_wait_timeout")
 
 
 class Q8Error(RuntimeError):
@@ -98,6 +99,7 @@ def lib() -> C.CDLL:
         "llama_q8_attention_decode_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "llama_q8_attention_decode": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "llama_q8_profile_decode": (i32, [vp, i32, C.POINTER(llama_q8_kernel_stat), i32, C.POINTER(i32)]),
+        "llama_q8_selftest_wait_timeout": (i32, [C.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -259,6 +261,13 @@ def llama_q8_matmul(packed, rows: int, k: int, x, m: int, y, stream=0) -> None:
 
 
 LQ8_MATMUL_EARLY_WEIGHTS = 1
+
+
+def llama_q8_selftest_wait_timeout() -> int:
+    """Code recorded by a kernel whose bounded wait ran out (see the header)."""
+    code = C.c_int32(0)
+    check(lib().llama_q8_selftest_wait_timeout(C.byref(code)), "llama_q8_selftest_wait_timeout")
+    return int(code.value)
 
 
 def llama_q8_matmul_ex(packed, rows: int, k: int, x, m: int, y, flags: int, stream=0) -> None:

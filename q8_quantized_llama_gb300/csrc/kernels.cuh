@@ -84,6 +84,7 @@ cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const Dev
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
                            cudaStream_t s);
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
+cudaError_t launch_wait_timeout(int* err, int code, cudaStream_t s);  // bounded-wait self-test
 
 // gemv.cu (m == 1)
 // With the fused RMSNorm, the input may first be the sum x + part[0] + ... +

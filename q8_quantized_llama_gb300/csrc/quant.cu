@@ -186,4 +186,21 @@ cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaSt
     return cudaGetLastError();
 }
 
+// A barrier that nothing completes: the bounded wait gives up after ~1 s and
+// records `code` (the failure path every kernel takes on a lost wait).
+__global__ void wait_timeout_kernel(int* err, int code) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait_bounded(&bar, 0, err, code);
+}
+
+cudaError_t launch_wait_timeout(int* err, int code, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(err, code);
+    return cudaGetLastError();
+}
+
 }  // namespace lq8

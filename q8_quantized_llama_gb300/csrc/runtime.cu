@@ -506,6 +506,21 @@ llama_q8_status run_forward(llama_q8_ctx* c, const int32_t* ids, int T, int inde
 
 extern "C" {
 
+llama_q8_status llama_q8_selftest_wait_timeout(int32_t* code) {
+    if (!code) return LQ8_ERR_ARG;
+    int* d = nullptr;
+    if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) return LQ8_ERR_OOM;
+    cudaError_t e = cudaMemset(d, 0, sizeof(int));
+    if (e == cudaSuccess) e = launch_wait_timeout(d, 41, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, d, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return LQ8_ERR_CUDA;
+    *code = h;
+    return LQ8_OK;
+}
+
 const char* llama_q8_status_str(llama_q8_status s) {
     switch (s) {
         case LQ8_OK: return "ok";

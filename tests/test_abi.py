@@ -52,6 +52,7 @@ def test_null_arguments_rejected_without_a_gpu(B):
     assert L.llama_q8_quantize(None, 1, 32, None, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_matmul(None, 1, 32, None, 1, None, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_matmul_ex(None, 1, 32, None, 1, None, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_selftest_wait_timeout(None) == B.LQ8_ERR_ARG
     assert L.llama_q8_attention(None, None, None, 1, 0, 9, 3, 64, 4096, None, None, 0, None) == B.LQ8_ERR_ARG
 
 

@@ -236,3 +236,20 @@ def test_attention_decode_rejects_unaligned_cache():
 def test_attention_two_calls_reuse_workspace():
     for kv in (700, 130):
         _attention_case(1, kv - 1, 9, 3, 64, 1024, seed=kv)
+
+
+# ------------------------------------------------------------------ failure path
+
+def test_bounded_wait_times_out_and_device_stays_usable():
+    """A kernel waiting on a barrier that nothing completes gives up after the
+    library's ~1 s limit, records its code, and the context keeps working."""
+    B = binding()
+    import time
+    t0 = time.perf_counter()
+    code = B.llama_q8_selftest_wait_timeout()
+    elapsed = time.perf_counter() - t0
+    assert code == 41
+    assert 0.5 < elapsed < 30.0
+    # the device still computes correctly afterwards
+    _matmul_case(64, 64, 1, seed=8)
+    torch.cuda.synchronize()
