@@ -433,7 +433,6 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     __shared__ __align__(8) uint64_t empty[kCaStages];
     __shared__ __align__(8) uint64_t wo_bar, wq_bar;
     __shared__ __align__(8) uint64_t rows_bar, part_bar;  // completed by st.async bytes
-    __shared__ float s_rscale;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
@@ -541,34 +540,30 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     }
     pdl_wait();
     if (tid == 0) pdl_launch_dependents();
+    // x * g into XN and the sum of squares; the scale 1/rms multiplies the finished
+    // projection rows, so no barrier waits on the reduction before the products.
+    float r_norm;
     {
         float ss = 0.0f;
-        for (int i = tid; i < h; i += kCaCT) {
+        for (int i = tid, u = 0; i < h; i += kCaCT, ++u) {
             const float v = fa.x[i];
-            XN[i] = v;
             ss = fmaf(v, v, ss);
+            float gg = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGPre; ++w)
+                if (w == u) gg = gpre[w];
+            if (u >= kGPre) gg = fa.g[i];
+            XN[i] = v * gg;
         }
         ss = warp_sum(ss);
         if (lane == 0) RED2[warp * 33 + 32] = ss;
         for (int i = tid; i < GP * HD; i += kCaCT)
             if (i >= G * HD) Q[i] = 0.0f;  // padding heads
         named_bar_sync(1, kCaCT);
-        if (tid == 0) {
-            float t = 0.0f;
-            for (int w = 0; w < kCaWarps; ++w) t += RED2[w * 33 + 32];
-            s_rscale = 1.0f / sqrtf(t / (float)h + fa.eps);
-        }
-        named_bar_sync(1, kCaCT);
-        const float r = s_rscale;
-        for (int i = tid, u = 0; i < h; i += kCaCT, ++u) {
-            float gg = 0.0f;
+        float t = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kGPre; ++w)
-                if (w == u) gg = gpre[w];
-            if (u >= kGPre) gg = fa.g[i];
-            XN[i] = XN[i] * r * gg;
-        }
-        named_bar_sync(1, kCaCT);
+        for (int w = 0; w < kCaWarps; ++w) t += RED2[w * 33 + 32];
+        r_norm = 1.0f / sqrtf(t / (float)h + fa.eps);
     }
 
     // ---- this CTA's projection tiles; rotated rows to every CTA of the cluster ----------
@@ -599,6 +594,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
                 float v = 0.0f;
 #pragma unroll
                 for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
+                v *= r_norm;
                 const float other = __shfl_xor_sync(0xffffffffu, v, 1);
                 const int row = qkv_tile_row0(i) + lane;  // row of [Wq;Wk;Wv]
                 if (i < nq + nkt) {

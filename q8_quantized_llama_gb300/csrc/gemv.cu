@@ -125,7 +125,6 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     __shared__ __align__(8) uint64_t xbar;
     __shared__ float red[kCWarps][33];
     __shared__ float part[32];
-    __shared__ float s_rscale;
 
     const PackedQ8& W = a.W;
     const int k = W.k, nb = k >> 5;
@@ -203,48 +202,47 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         }
         mbar_wait_bounded(&xbar, 0, a.err, 13);
         if (NORM) {
+            // x (+ the partials, in order) -> sum of squares for the scale, and x * g in
+            // place; the scale 1/rms multiplies the finished dot products in the epilogue,
+            // so no barrier waits on the reduction before the products start.
             const int nx = x_full ? k : xn;  // == k when unsplit
-            if (a.pre.n_part > 0) {
-                // x + part[0] + part[1] + ..., in that order; the first CTA keeps the sum
-                const bool keep = blockIdx.x == 0 && a.pre.x_sum_out != nullptr;
-                for (int i = tid * 4; i < nx; i += kCT * 4) {
-                    float4 v = *reinterpret_cast<const float4*>(xs + i);
-                    for (int p = 0; p < a.pre.n_part; ++p) {
-                        const float4 w = *reinterpret_cast<const float4*>(xs + (size_t)(p + 1) * k + i);
-                        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
-                    }
-                    *reinterpret_cast<float4*>(xs + i) = v;
-                    if (keep) *reinterpret_cast<float4*>(a.pre.x_sum_out + i) = v;
-                }
-            }
+            const bool keep = blockIdx.x == 0 && a.pre.x_sum_out != nullptr;
             float ss = 0.0f;
-            for (int i = tid * 4; i < nx; i += kCT * 4) {
-                const float4 v = *reinterpret_cast<const float4*>(xs + i);
+            for (int i = tid * 4, u = 0; i < nx; i += kCT * 4, ++u) {
+                float4 v = *reinterpret_cast<const float4*>(xs + i);
+                for (int p = 0; p < np; ++p) {
+                    const float4 w = *reinterpret_cast<const float4*>(xs + (size_t)(p + 1) * k + i);
+                    v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+                }
+                if (keep) *reinterpret_cast<float4*>(a.pre.x_sum_out + i) = v;
                 ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
                 ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+                if (!x_full) {  // unsplit: this thread's elements are the ones it scales
+                    float4 gg;
+#pragma unroll
+                    for (int w = 0; w < kGPre; ++w)
+                        if (w == u) gg = gpre[w];
+                    if (u >= kGPre) gg = *reinterpret_cast<const float4*>(a.g + i);
+                    v.x *= gg.x; v.y *= gg.y; v.z *= gg.z; v.w *= gg.w;
+                }
+                *reinterpret_cast<float4*>(xs + i) = v;
             }
             ss = warp_sum(ss);
             if (lane == 0) red[warp][32] = ss;
             named_bar_sync(1, kCT);
-            if (tid == 0) {
-                float t = 0.0f;
+            if (x_full) {  // split unit: scale this unit's slice after every sum has landed
+                for (int i = tid * 4, u = 0; i < xn; i += kCT * 4, ++u) {
+                    float4 v = *reinterpret_cast<float4*>(xslice + i);
+                    float4 gg;
 #pragma unroll
-                for (int w = 0; w < kCWarps; ++w) t += red[w][32];
-                s_rscale = 1.0f / sqrtf(t / (float)k + a.eps);
+                    for (int w = 0; w < kGPre; ++w)
+                        if (w == u) gg = gpre[w];
+                    if (u >= kGPre) gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
+                    v.x *= gg.x; v.y *= gg.y; v.z *= gg.z; v.w *= gg.w;
+                    *reinterpret_cast<float4*>(xslice + i) = v;
+                }
+                named_bar_sync(1, kCT);
             }
-            named_bar_sync(1, kCT);
-            const float r = s_rscale;
-            for (int i = tid * 4, u = 0; i < xn; i += kCT * 4, ++u) {
-                float4 v = *reinterpret_cast<float4*>(xslice + i);
-                float4 gg;
-#pragma unroll
-                for (int w = 0; w < kGPre; ++w)
-                    if (w == u) gg = gpre[w];
-                if (u >= kGPre) gg = *reinterpret_cast<const float4*>(a.g + x0 + i);
-                v.x = v.x * r * gg.x; v.y = v.y * r * gg.y; v.z = v.z * r * gg.z; v.w = v.w * r * gg.w;
-                *reinterpret_cast<float4*>(xslice + i) = v;
-            }
-            named_bar_sync(1, kCT);
         }
 
         float acc = 0.0f;
@@ -283,6 +281,12 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     if (split == 0 && warp == 0) {
         float v = part[lane];
         for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
+        if (NORM) {  // 1 / rms of the (full) input, from this CTA's warp sums
+            float t = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kCWarps; ++w) t += red[w][32];
+            v *= 1.0f / sqrtf(t / (float)k + a.eps);
+        }
         gemv_epilogue<EPI>(a.e, W.rows, tile, lane, v, W.rows_pad / 32, res_pre);
     }
     if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
