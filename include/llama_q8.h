@@ -73,14 +73,14 @@ typedef struct llama_q8_config {
     float rms_eps;        /* 1e-5 */
     float rope_theta;     /* 10000 */
     int32_t tied_output;  /* 1: the head is token_embd (no output.weight) */
-    int32_t decode_kernel; /* decode step: 0 = automatic (three kernels per layer when each KV
-                              head's Q/K/V rows and W_o slice fit a cluster, else four when
-                              the W_o slice does, else five), 1 = five per-layer kernels,
-                              2 = embedding and all layers as ONE cluster kernel, 3 = four
-                              per layer (attention applying W_o), 4 = three per layer (norm,
-                              Q/K/V, attention and W_o fused), 5 = one 16-CTA cluster kernel
-                              per layer; 2-5 give LQ8_ERR_UNSUPPORTED at load when the model
-                              does not fit */
+    int32_t decode_kernel; /* decode step: 0 = automatic (two kernels per layer when each KV
+                              head's Q/K/V rows and W_o slice fit a cluster and the MLP fits
+                              8-CTA clusters, else three, four or five), 1 = five per-layer
+                              kernels, 2 = embedding and all layers as ONE cluster kernel,
+                              3 = four per layer (attention applying W_o), 4 = three per
+                              layer (norm, Q/K/V, attention and W_o fused; gate/up; down),
+                              5 = one 16-CTA cluster kernel per layer; 2-5 give
+                              LQ8_ERR_UNSUPPORTED at load when the model does not fit */
 } llama_q8_config;
 
 typedef struct llama_q8_layer_weights {
@@ -179,7 +179,7 @@ llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0,
 void* llama_q8_stream(llama_q8_ctx* ctx);
 
 /* Number of kernel launches one decode step makes (the CUDA-graph nodes):
- * n_layer * {5, 4, 3, 1} + 2 with per-layer kernels (see decode_kernel), 2
+ * n_layer * {5, 4, 3, 2, 1} + 2 with per-layer kernels (see decode_kernel), 2
  * with the one-cluster whole-step kernel (layers, then lm_head + argmax). */
 int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx);
 

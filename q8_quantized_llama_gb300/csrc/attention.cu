@@ -545,8 +545,11 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     float r_norm;
     {
         float ss = 0.0f;
+        const bool keep = fa.x_store && kh == 0 && rank == 0;
         for (int i = tid, u = 0; i < h; i += kCaCT, ++u) {
-            const float v = fa.x[i];
+            float v = fa.x[i];
+            for (int p = 0; p < fa.n_xparts; ++p) v += fa.xparts[(size_t)p * h + i];
+            if (keep) fa.x_store[i] = v;
             ss = fmaf(v, v, ss);
             float gg = 0.0f;
 #pragma unroll

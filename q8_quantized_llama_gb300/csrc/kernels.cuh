@@ -133,7 +133,10 @@ bool attn_oproj_fused_supported(int n_head, int n_kv, int head_dim, const Packed
 // rope_i, KV append, attention, W_o column slice -> part) as one kernel with a
 // cluster per KV head, for models whose per-head projections are small.
 struct FrontArgs {
-    const float* x;        // [h] residual stream (written by the preceding kernel)
+    const float* x;        // [h] residual stream base (written by the preceding kernel)
+    const float* xparts;   // [n_xparts][h] partials added to x in order (the MLP's clusters), or null
+    int n_xparts;
+    float* x_store;        // [h] where the first CTA keeps x + partials (the MLP's input), or null
     const float* g;        // [h] attention RMSNorm weight
     float eps;
     PackedQ8 wqkv;         // [Wq;Wk;Wv]
@@ -169,6 +172,22 @@ struct LayerKArgs {
     int* err;
 };
 bool decode_layer_supported(const LayerKArgs& la, int head_dim);
+
+// mlp.cu: the MLP half of a decode layer as one kernel (clusters of 8 CTAs).
+struct MlpArgs {
+    const float* x;          // [h] residual stream before the attention output is added
+    const float* attn_part;  // [n_attn_part][h] partials of W_o o (added in order)
+    int n_attn_part;
+    const float* g;          // [h] FFN RMSNorm weight
+    float eps;
+    PackedQ8 wgu;            // row-interleaved [W_g;W_u]
+    PackedQ8 wdown;
+    float* xr_out;           // [h] x + W_o o (written by the first CTA): the next residual base
+    float* mlp_part;         // [clusters][h] partials of W_down a, one per cluster
+    int* err;
+};
+int decode_mlp_clusters(int h, int ff, int gu_rows);  // 0: not supported
+cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s);
 cudaError_t launch_decode_layer(const LayerKArgs& la, int head_dim, bool pdl, cudaStream_t s);
 cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool pdl, cudaStream_t s);
 cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,

@@ -1,0 +1,236 @@
+// The MLP half of a decode layer (T = 1) as ONE kernel: RMSNorm -> gate/up +
+// SiLU -> down projection ("量化 llama 的一次前向", forward, mlp: the same
+// steps as the gate/up and down kernels, one launch). CTA c owns 32 entries
+// of the SiLU product a = silu(W_g y) * (W_u y) (the gate/up row tiles 2c and
+// 2c + 1 of the row-interleaved [W_g;W_u]) and multiplies them into block
+// column c of W_down: a partial of W_down a over all h rows. The CTAs form
+// clusters of 8; each partial row goes (st.async, completing the receiver's
+// mbarrier) to the CTA of its cluster that owns the row, which adds the 8 in
+// rank order and writes the cluster's partial. The next kernel adds the
+// clusters' partials to the residual in a fixed order, so the result is
+// deterministic. Weights and the norm weight are requested before the grid
+// dependency wait; the input x + attention partials are read after it.
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace lq8 {
+
+constexpr int kMlpCl = 8;       // CTAs per cluster
+constexpr int kMlpWarps = 8;    // consumer warps
+constexpr int kMlpCT = kMlpWarps * 32;
+constexpr int kMlpThreads = kMlpCT + 32;
+
+struct MlpPlan {
+    int gu, wd, wds, xs, a, part, red_in, red, floats;  // offsets in floats
+};
+__host__ __device__ inline int mlp_round(int n) { return (n + 31) / 32 * 32; }
+__host__ __device__ inline int mlp_rows_per_owner(int h) { return (h / kMlpCl + 3) / 4 * 4; }
+__host__ __device__ inline MlpPlan mlp_plan(int h) {
+    MlpPlan p;
+    const int nbx = h / 32, tiles_h = h / 32;
+    int o = 0;
+    auto take = [&](int n) { const int r = o; o += mlp_round(n); return r; };
+    p.gu = take(2 * nbx * 1088 / 4);    // two gate/up tiles: codes then scales per tile
+    p.wd = take(tiles_h * 1024 / 4);    // block column c of W_down: codes of each row tile
+    p.wds = take(tiles_h * 64 / 4);     // and their scales
+    p.xs = take(h);                     // x * g
+    p.a = take(32);                     // this CTA's 32 SiLU products
+    p.part = take(h);                   // this CTA's partial of W_down a
+    p.red_in = take(kMlpCl * mlp_rows_per_owner(h));  // partials of the rows this CTA owns
+    p.red = take(kMlpWarps * 33);
+    p.floats = o;
+    return p;
+}
+
+__global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) {
+    extern __shared__ __align__(128) float smf[];
+    __shared__ __align__(8) uint64_t w_bar, red_bar;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;                 // block column of W_down = a entries [32c, 32c + 32)
+    const int q = (int)cluster_rank();        // rank in the cluster
+    const int cl_id = c / kMlpCl;
+    const int h = ma.wgu.k, nbx = h >> 5, tiles_h = h >> 5;
+    const int nbf = ma.wdown.k >> 5;
+    const int rpo = mlp_rows_per_owner(h);
+    const MlpPlan pl = mlp_plan(h);
+    uint8_t* GU = reinterpret_cast<uint8_t*>(smf + pl.gu);
+    uint8_t* WD = reinterpret_cast<uint8_t*>(smf + pl.wd);
+    uint8_t* WDS = reinterpret_cast<uint8_t*>(smf + pl.wds);
+    float* XS = smf + pl.xs;
+    float* A = smf + pl.a;
+    float* PART = smf + pl.part;
+    float* RIN = smf + pl.red_in;
+    float* RED = smf + pl.red;
+    const int own0 = q * rpo, own1 = min(h, own0 + rpo);  // rows this CTA reduces
+
+    if (tid == 0) {
+        mbar_init(&w_bar, 1);
+        mbar_init(&red_bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&red_bar, (uint32_t)(kMlpCl * max(0, own1 - own0) * 4));
+    }
+    __syncthreads();
+    cluster_sync();  // every CTA's barrier exists and expects its bytes before any peer stores
+
+    if (warp == kMlpWarps) {
+        if (lane == 0) {  // constant weights, before the dependency wait
+            mbar_arrive_expect_tx(&w_bar, (uint32_t)(2 * nbx * 1088 + tiles_h * 1088));
+            for (int u = 0; u < 2; ++u) {
+                const int t = 2 * c + u;
+                uint8_t* dst = GU + (size_t)u * nbx * 1088;
+                bulk_g2s(dst, reinterpret_cast<const uint8_t*>(ma.wgu.qs) + (size_t)t * h * 32,
+                         (uint32_t)(nbx * 1024), &w_bar);
+                bulk_g2s(dst + nbx * 1024, reinterpret_cast<const uint8_t*>(ma.wgu.d) + (size_t)t * nbx * 64,
+                         (uint32_t)(nbx * 64), &w_bar);
+            }
+            for (int t = 0; t < tiles_h; ++t) {
+                bulk_g2s(WD + (size_t)t * 1024,
+                         reinterpret_cast<const uint8_t*>(ma.wdown.qs) + (size_t)t * ma.wdown.k * 32 + (size_t)c * 1024,
+                         1024u, &w_bar);
+                bulk_g2s(WDS + (size_t)t * 64,
+                         reinterpret_cast<const uint8_t*>(ma.wdown.d) + ((size_t)t * nbf + c) * 64, 64u, &w_bar);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers: x' = x + attention partials (in order), RMSNorm ---------------------
+    constexpr int kGPre = 2;  // h <= 2048 floats: float4s per thread
+    float4 gpre[kGPre];
+#pragma unroll
+    for (int u = 0; u < kGPre; ++u) {
+        const int i = tid * 4 + u * kMlpCT * 4;
+        gpre[u] = i < h ? *reinterpret_cast<const float4*>(ma.g + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    float ss = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kGPre; ++u) {
+        const int i = tid * 4 + u * kMlpCT * 4;
+        if (i < h) {
+            float4 v = *reinterpret_cast<const float4*>(ma.x + i);
+            for (int p = 0; p < ma.n_attn_part; ++p) {
+                const float4 w = *reinterpret_cast<const float4*>(ma.attn_part + (size_t)p * h + i);
+                v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+            }
+            if (c == 0) *reinterpret_cast<float4*>(ma.xr_out + i) = v;
+            ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            const float4 gg = gpre[u];
+            *reinterpret_cast<float4*>(XS + i) = make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w);
+        }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) RED[warp * 33 + 32] = ss;
+    named_bar_sync(1, kMlpCT);
+    float t_ss = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kMlpWarps; ++w) t_ss += RED[w * 33 + 32];
+    const float r_norm = 1.0f / sqrtf(t_ss / (float)h + ma.eps);
+    mbar_wait_bounded(&w_bar, 0, ma.err, 51);
+
+    // ---- gate/up: warps 0-3 tile 2c, warps 4-7 tile 2c + 1; lane = row ---------------
+    {
+        const int u = warp >> 2, wq = warp & 3;
+        const uint8_t* tw = GU + (size_t)u * nbx * 1088;
+        float acc = 0.0f;
+        for (int b = wq; b < nbx; b += 4) {
+            const uint4 q0 = *reinterpret_cast<const uint4*>(tw + b * 1024 + lane * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(tw + b * 1024 + 512 + lane * 16);
+            const float d = __half2float(reinterpret_cast<const __half*>(tw + nbx * 1024)[b * 32 + lane]);
+            const float4* x4 = reinterpret_cast<const float4*>(XS + b * 32);
+            uint64_t a0 = 0, a1 = 0;
+            a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
+            a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
+            a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
+            a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
+            acc = fmaf(d, (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)), acc);
+        }
+        RED[warp * 33 + lane] = acc;
+        named_bar_sync(1, kMlpCT);
+        if (wq == 0) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) v += RED[(u * 4 + w) * 33 + lane];
+            v *= r_norm;
+            const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+            if (!(lane & 1)) A[u * 16 + (lane >> 1)] = silu_f32(v) * up;
+        }
+        named_bar_sync(1, kMlpCT);
+    }
+
+    // ---- down: block column c of W_down times a, every row tile; lane = row -----------
+    for (int t = warp; t < tiles_h; t += kMlpWarps) {
+        const uint4 q0 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 1024 + lane * 16);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 1024 + 512 + lane * 16);
+        const float d = __half2float(reinterpret_cast<const __half*>(WDS + (size_t)t * 64)[lane]);
+        const float4* a4 = reinterpret_cast<const float4*>(A);
+        uint64_t a0 = 0, a1 = 0;
+        a0 = dot4_acc(q0.x, a4[0], a0); a1 = dot4_acc(q1.x, a4[4], a1);
+        a0 = dot4_acc(q0.y, a4[1], a0); a1 = dot4_acc(q1.y, a4[5], a1);
+        a0 = dot4_acc(q0.z, a4[2], a0); a1 = dot4_acc(q1.z, a4[6], a1);
+        a0 = dot4_acc(q0.w, a4[3], a0); a1 = dot4_acc(q1.w, a4[7], a1);
+        PART[t * 32 + lane] = d * ((f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)));
+    }
+    named_bar_sync(1, kMlpCT);
+    // rows r go to the cluster CTA owning them: RIN[source rank][r - owner's first row]
+    for (int f = tid; f < h / 4; f += kMlpCT) {
+        const int r = f * 4, owner = r / rpo;
+        const float4 v = *reinterpret_cast<const float4*>(PART + r);
+        st_async_f32x4(&RIN[q * rpo + (r - owner * rpo)], (uint32_t)owner, v, &red_bar);
+    }
+    mbar_wait_bounded(&red_bar, 0, ma.err, 52);  // the 8 partials of the rows this CTA owns
+    for (int r = own0 + tid; r < own1; r += kMlpCT) {
+        float v = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMlpCl; ++s) v += RIN[s * rpo + (r - own0)];
+        ma.mlp_part[(size_t)cl_id * h + r] = v;
+    }
+}
+
+static constexpr int kMlpSmemLimit = 227 * 1024 - 1024;
+static bool g_mlp_attr = false;
+
+// The kernel serves the model when F / 32 is a multiple of 8 (whole
+// clusters), h <= 2048 with h / 8 rows per owner a multiple of 4, and the
+// shared-memory plan fits.
+int decode_mlp_clusters(int h, int ff, int gu_rows) {
+    if (h % 32 || ff % 32 || gu_rows != 2 * ff || h > 2048 || (h / kMlpCl) % 4) return 0;
+    if ((ff / 32) % kMlpCl) return 0;
+    const size_t smem = (size_t)mlp_plan(h).floats * 4;
+    if (smem > (size_t)kMlpSmemLimit) return 0;
+    if (!g_mlp_attr) {
+        if (cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlpSmemLimit) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_mlp_attr = true;
+    }
+    return (ff / 32) / kMlpCl;
+}
+
+cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s) {
+    const int h = ma.wgu.k, ff = ma.wdown.k;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ff / 32);
+    cfg.blockDim = dim3(kMlpThreads);
+    cfg.dynamicSmemBytes = (size_t)mlp_plan(h).floats * 4;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = kMlpCl;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    int n = 1;
+    if (pdl) {
+        attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[1].val.programmaticStreamSerializationAllowed = 1;
+        n = 2;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, decode_mlp_kernel, ma);
+}
+
+}  // namespace lq8

@@ -89,12 +89,13 @@ struct Profiler {
 };
 
 enum Family {
-    F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_LAYER, F_COUNT
+    F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_LAYER, F_MLP,
+    F_COUNT
 };
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
                                      "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
                                      "decode_cluster_layers", "attn_oproj_residual", "layer_front_qkv_attn_o",
-                                     "decode_layer_cluster"};
+                                     "decode_layer_cluster", "decode_mlp"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -125,6 +126,8 @@ struct llama_q8_ctx {
     float* d_part = nullptr;  // decode: per-KV-head partials of W_o o
     float* d_xsum = nullptr;  // decode: x + W_o o, the residual of the down projection
     float* d_x2 = nullptr;    // decode with the layer kernel: odd layers' residual stream
+    float* d_xr = nullptr;    // decode with the MLP kernel: x + W_o o of the last layer
+    float* d_mlp = nullptr;   // decode with the MLP kernel: per-cluster partials of W_down a
     float* d_logits = nullptr;
     int32_t* d_ids = nullptr;
     int32_t* d_out_ids = nullptr;
@@ -148,6 +151,7 @@ struct llama_q8_ctx {
     bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
     int front_cl = 0;                    // > 0: norm + QKV + attention + W_o as one kernel (this cluster size)
     bool layer_kernel = false;           // each decode layer as one 16-CTA cluster kernel
+    int mlp_clusters = 0;                // > 0: gate/up + down as one kernel with this many 8-CTA clusters
     LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
@@ -173,7 +177,7 @@ void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
-                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_x2, c->d_logits, c->d_ids,
+                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_x2, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
                    c->d_out_ids,
                    c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_layer_ptrs};
     for (void* p : dev)
@@ -223,6 +227,12 @@ FrontArgs front_args(llama_q8_ctx* c, int l) {
     const LayerDev& L = c->layers[l];
     FrontArgs fa{};
     fa.x = c->d_x;
+    if (c->mlp_clusters > 0 && l > 0) {  // x = the MLP's residual base + its cluster partials
+        fa.x = c->d_xr;
+        fa.xparts = c->d_mlp;
+        fa.n_xparts = c->mlp_clusters;
+        fa.x_store = c->d_x;
+    }
     fa.g = L.attn_norm;
     fa.eps = cfg.rms_eps;
     fa.wqkv = L.qkv;
@@ -358,6 +368,22 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
                                                  &c->d_state->err, s);
                     });
             }
+            if (c->mlp_clusters > 0) {
+                MlpArgs ma{};
+                ma.x = c->d_x;
+                ma.attn_part = c->d_part;
+                ma.n_attn_part = cfg.n_head_kv;
+                ma.g = L.ffn_norm;
+                ma.eps = cfg.rms_eps;
+                ma.wgu = L.gu;
+                ma.wdown = L.down;
+                ma.xr_out = c->d_xr;
+                ma.mlp_part = c->d_mlp;
+                ma.err = &c->d_state->err;
+                run(F_MLP, q8_bytes(2 * F, h) + q8_bytes(h, F) + 4.0 * h * (3 + cfg.n_head_kv + c->mlp_clusters), 0.0,
+                    [&] { return launch_decode_mlp(ma, pdl, s); });
+                continue;
+            }
             EpiArgs g;
             g.a_out = c->d_a;
             GemvPreSum pre;
@@ -393,8 +419,21 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
                 [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
         }
     }
-    run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0,
-        [&] { return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl, &c->d_state->err, s); });
+    if (c->mlp_clusters > 0) {  // the last layer's residual = its base + the MLP's cluster partials
+        GemvPreSum pre;
+        pre.part = c->d_mlp;
+        pre.n_part = c->mlp_clusters;
+        pre.part_stride = (int)h;
+        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * h * c->mlp_clusters + 4.0 * cfg.n_vocab, 0.0, [&] {
+            return launch_gemv(c->head, c->d_xr, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
+                               &c->d_state->err, s, &pre);
+        });
+    } else {
+        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
+            return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
+                               &c->d_state->err, s);
+        });
+    }
     if (n_kernels) *n_kernels = n;
     return err;
 }
@@ -697,6 +736,8 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
     LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_x2, sizeof(float) * h));
+    LOAD_CK(cudaMalloc(&c->d_xr, sizeof(float) * h));
+    LOAD_CK(cudaMalloc(&c->d_mlp, sizeof(float) * h * (F / 32 / 8 + 1)));
     LOAD_CK(cudaMalloc(&c->d_logits, sizeof(float) * V));
     LOAD_CK(cudaMalloc(&c->d_ids, sizeof(int32_t) * T));
     LOAD_CK(cudaMalloc(&c->d_out_ids, sizeof(int32_t) * (T + 1)));
@@ -728,6 +769,8 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
         cudaGetLastError();
         if (C.decode_kernel != 3 && c->fuse_o) c->front_cl = layer_front_cluster_size(front_args(c, 0), hd);
+        cudaGetLastError();
+        if (C.decode_kernel == 0 && c->front_cl > 0) c->mlp_clusters = decode_mlp_clusters(h, F, c->layers[0].gu.rows);
         cudaGetLastError();
         unsupported = (C.decode_kernel == 3 && !c->fuse_o) || (C.decode_kernel == 4 && c->front_cl == 0);
     }

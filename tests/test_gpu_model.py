@@ -26,7 +26,8 @@ def m135():
         if ora_t[name].dtype == np.uint8:
             np.testing.assert_array_equal(t.cpu().numpy(), ora_t[name], err_msg=name)
     models = {
-        "front": B.Model(CFG, dev_t, on_device=True),                          # automatic: three kernels per layer
+        "front": B.Model(CFG, dev_t, on_device=True),                          # automatic: two kernels per layer
+        "three": B.Model(dict(CFG, decode_kernel=4), dev_t, on_device=True),   # front, gate/up, down
         "layer": B.Model(dict(CFG, decode_kernel=5), dev_t, on_device=True),   # one cluster kernel per layer
         "four": B.Model(dict(CFG, decode_kernel=3), dev_t, on_device=True),    # attention applies W_o
         "layered": B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True), # five kernels per layer
@@ -41,7 +42,7 @@ def m135():
             m.close()
 
 
-@pytest.fixture(params=["layer", "front", "four", "layered", "cluster"])
+@pytest.fixture(params=["front", "three", "four", "layered", "layer", "cluster"])
 def either(request, m135):
     return m135[request.param], m135["oracle"]
 
@@ -169,14 +170,15 @@ def test_device_resident_api(m135):
     got = np.concatenate([d_next.cpu().numpy(), d_out.cpu().numpy()])
     np.testing.assert_array_equal(got, ref)
     assert model.cache_len() == 203 + 16
-    assert model.decode_kernel_count() == 1 + 3 * CFG["n_layer"] + 1   # norm+QKV+attention+W_o fused
+    assert model.decode_kernel_count() == 1 + 2 * CFG["n_layer"] + 1   # layer front + MLP
+    assert m135["three"].decode_kernel_count() == 1 + 3 * CFG["n_layer"] + 1
     assert m135["layer"].decode_kernel_count() == 1 + CFG["n_layer"] + 1
     assert m135["four"].decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1
     assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
     assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
 
 
-@pytest.mark.parametrize("variant", ["layer", "front"])
+@pytest.mark.parametrize("variant", ["front", "three", "layer"])
 def test_fused_decode_kernels_at_long_context(m135, variant):
     """Decode steps at positions near the 4096 limit: the one-kernel layer and
     the fused layer front give the logits and tokens of the five-kernel
