@@ -40,6 +40,14 @@ SEED = 0
 # M2 Max CPU ("速度", CPU GGUF：decode 快，prefill 慢). Context, not the target.
 PAGES_DECODE_MS = 7.40
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# decode step's kernels, from the ncu captures summarised under profiles/ (the
+# kernel sources they were taken on are the committed ones). The layer front's
+# figure is at kv_len 205; its K/V part grows by 1536 bytes per position.
+NCU_TRAFFIC = {
+    "layer_front_qkv_attn_o": {"bytes": 1322752, "kv_len": 205, "profile": "profiles/layer_front_135m_decode.md"},
+    "decode_mlp": {"bytes": 2865920, "kv_len": None, "profile": "profiles/decode_mlp_135m.md"},
+}
 L2_BYTES = 126 * 2 ** 20
 
 
@@ -595,8 +603,11 @@ def run_ours(args):
             "gpu_launches": gpu_launches,
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
                          "frac": dom_gbs / peak, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "traffic": None,
-                         "note": "algorithmic bytes per launch / mean event-timed launch duration, eager decode"},
+                         "traffic": NCU_TRAFFIC.get(dom_name, {}).get("bytes"),
+                         "traffic_source": NCU_TRAFFIC.get(dom_name),
+                         "algorithmic_bytes_per_launch": dbytes / dl,
+                         "note": "algorithmic bytes per launch / mean event-timed launch duration, eager decode; "
+                                 "the kernel is latency-bound (a chain of dependent steps), see profiles/"},
             "decode_step_roofline": {"weights_bytes": weights_bytes, "kv_bytes_mean": kv_bytes,
                                      "roofline_us": (weights_bytes + kv_bytes) / (peak * 1e9) * 1e6,
                                      "graph_step_us": 1000 * statistics.median(dec_tok_ms),
