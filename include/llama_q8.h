@@ -245,7 +245,8 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
  * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32): up to 16 rows on the CUDA
  * cores with f32 accumulation, more rows on the tcgen05 tensor cores in
  * split-TF32 (three TF32 products per step, f32 accumulation in tensor memory,
- * about 2^-22 relative error per product). */
+ * less than 2^-19 relative error per product). packed and x must be 16-byte
+ * aligned (LQ8_ERR_ARG otherwise). */
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
                                 int64_t m, float* y, void* stream);
 

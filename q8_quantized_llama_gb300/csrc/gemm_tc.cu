@@ -5,20 +5,32 @@
 // matrix-matrix kernel).
 //
 // Precision: split-TF32 ("3xTF32"). A dequantised weight d*q (f32, at most 18
-// significant bits) is exactly hi + lo with hi = tf32(w) and lo = w - hi (at
-// most 7 bits, exact in tf32). An activation x is hi + lo with hi = tf32(x)
-// and lo = x - hi (lo truncated to tf32 by the MMA: 22 significant bits kept).
-// Three MMAs per k-step, w_hi.x_hi + w_hi.x_lo + w_lo.x_hi, accumulate in f32
-// in TMEM; the dropped w_lo.x_lo term is below 2^-22 relative.
+// significant bits) is exactly hi + lo with hi = w rounded to tf32 and
+// lo = w - hi (at most 8 bits, exact in tf32). An activation x is read by the
+// MMA as tf32 (its low 13 mantissa bits ignored: x_hi = x truncated) and
+// x_lo = x - x_hi is exact in f32 (below 2^-10 |x|; the MMA keeps its top 11
+// bits). Three MMAs per k-step, w_hi.x_hi + w_hi.x_lo + w_lo.x_hi, accumulate
+// in f32 in TMEM; the truncated x_lo and the dropped w_lo.x_lo leave each
+// product off by less than 2^-19 relative.
 //
-// CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-step 32 (one Q8_0
-// block = one 128-byte swizzle row of tf32). Raw k-blocks (codes, scales,
-// activation rows) arrive by cp.async three blocks ahead; all 8 warps
-// dequantise/split the current block into one of two operand slots
-// (128-byte swizzled K-major layout the MMA reads through its descriptors)
-// while the tensor core works on the other; one thread issues the MMAs and
-// commits each slot to an mbarrier that releases it. The epilogue reads TMEM with tcgen05.ld (warp w
-// reads lanes 32*(w%4).., column half w/4) and applies the shared epilogues.
+// CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
+// Q8_0 block; one 128-byte swizzle row of f32). Warp roles:
+//  - warp 8 (producer): per k-block one 2-D tensor copy of the activation tile
+//    (128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B layout)
+//    and bulk copies of the codes (1 KiB per 32-row tile) and scales;
+//  - warps 0-7 (converters): dequantise the weights, split them into hi/lo and
+//    write them into tensor memory (tcgen05.st; A operand, row r in lane r),
+//    and write x_lo next to the activation tile in shared memory;
+//  - warp 9 (MMA): one thread issues the 12 MMAs of a k-block with A read from
+//    tensor memory and commits them to the stage's "done" barrier, which frees
+//    the stage for the producer.
+// Stages are handed on with mbarriers (no CTA-wide barrier in the k loop), so
+// copies, conversion and MMAs of different k-blocks overlap. The epilogue
+// reads TMEM with tcgen05.ld (warp w reads lanes 32*(w%4).., column half w/4)
+// and applies the shared epilogues.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "epilogue.cuh"
 #include "ptx.cuh"
 
@@ -26,13 +38,19 @@ namespace lq8 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
-constexpr int kTcSlots = 2;                     // operand slots (ping-pong with the tensor core)
-constexpr int kTcThreads = 256;
-constexpr int kTileBytes = 128 * 128;           // 128 rows x 128 bytes
-constexpr int kSlotBytes = 4 * kTileBytes;      // A_hi, A_lo, B_hi, B_lo
-constexpr int kRawStages = 4;                   // raw k-blocks in flight (cp.async)
-constexpr int kRawBytes = 4096 + 256 + 128 * 128;  // codes, scales, activations of one k-block
-constexpr int kTcSmem = kTcSlots * kSlotBytes + kRawStages * kRawBytes + 1024;  // + alignment slack
+constexpr int kTcStages = 4;
+constexpr int kTcConvWarps = 8;
+constexpr int kTcThreads = (kTcConvWarps + 2) * 32;  // converters, producer, MMA issuer
+constexpr int kTcProducerWarp = kTcConvWarps, kTcMmaWarp = kTcConvWarps + 1;
+constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
+// one stage: x tile (hi as loaded), x_lo tile, codes of 4 row tiles, their scales
+constexpr int kStXlo = kTileBytes, kStCodes = 2 * kTileBytes, kStScales = kStCodes + 4096;
+constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
+constexpr int kTcSmem = kTcStages * kStageBytes + 1024;  // + alignment slack
+// tensor memory: accumulator columns [0, 128), then per stage A_hi (32) and A_lo (32)
+constexpr int kTmemCols = 512;
+constexpr int kTmemA = kTcBN;
+static_assert(kTmemA + kTcStages * 64 <= kTmemCols, "tensor memory columns");
 
 // ---- tcgen05 wrappers ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
@@ -66,12 +84,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTcBN >> 3) << 17) |
                                 ((uint32_t)(kTcBM >> 4) << 24);
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+// D (tensor memory) += A (tensor memory, row i in lane i, k along columns) * B (shared memory)
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdescTf32), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(kIdescTf32), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -89,17 +108,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+// 16 consecutive columns of this thread's lane (the warp's 32 lanes at taddr).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a 128-row x 128-byte
-// K-major tile with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+// 2-D tensor copy global -> shared, completing on an mbarrier; coordinates in
+// elements (x innermost).
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Exact f32 values of 16 codes (4 words) times the block scale.
@@ -116,17 +143,14 @@ __device__ __forceinline__ void dequant16(const uint4& q, float d, float (&w)[16
     }
 }
 
-// ---- cp.async (16-byte global -> shared copies, zero-filled when src_bytes = 0)
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
-                 "r"(src_bytes)
-                 : "memory");
+// w rounded to the nearest tf32 value (low 13 mantissa bits zero).
+__device__ __forceinline__ uint32_t tf32_rna_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent and the 10 mantissa bits of tf32
 
 // Epilogue of one output element pair/element (row r of W, token t).
 template <int EPI>
@@ -144,6 +168,7 @@ __device__ __forceinline__ void tc_epilogue_one(const EpiArgs& e, int m, int row
 }
 
 constexpr int kPartStride = kTcBN + 4;  // floats per row of a partial tile in shared memory
+static_assert(kTcBM * kPartStride * 4 <= kTcStages * kStageBytes, "partial tile fits the stages");
 
 // SPLIT: the CTAs of a cluster (blockIdx.z = cluster rank) take equal shares
 // of the k-blocks; each stores its partial tile in its shared memory and,
@@ -151,13 +176,13 @@ constexpr int kPartStride = kTcBN + 4;  // floats per row of a partial tile in s
 // over the S partials (in rank order, through distributed shared memory) and
 // applies the epilogue to them.
 template <int EPI, bool SPLIT>
-__global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, const float* __restrict__ X, int m,
-                                                                    int ldx, EpiArgs e, int* err) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    q8_gemm_tc_kernel(PackedQ8 W, const __grid_constant__ CUtensorMap xmap, int m, EpiArgs e, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ops = smem;                                 // kTcSlots operand slots (A_hi, A_lo, B_hi, B_lo)
-    uint8_t* raw = smem + kTcSlots * kSlotBytes;         // kRawStages raw k-blocks
-    __shared__ __align__(8) uint64_t mma_done[kTcSlots];
+    __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
+    __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and x_lo
+    __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
     __shared__ uint32_t tmem_holder;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -168,145 +193,167 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     const int t0 = blockIdx.y * kTcBN;  // tokens
     const int tile0 = m0 >> 5;
     const int n_tiles = W.rows_pad >> 5;
+    const int valid_tiles = min(4, n_tiles - tile0);
 
     if (tid == 0) {
-        for (int s = 0; s < kTcSlots; ++s) mbar_init(&mma_done[s], 1);
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&conv_bar[s], kTcConvWarps);
+            mbar_init(&done_bar[s], 1);
+        }
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_holder, kTcBN);
+    if (warp == kTcMmaWarp) tmem_alloc(&tmem_holder, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_holder;
+    bool alive = true;  // cleared by a wait that ran out; later waits are skipped
 
-    pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
-
-    // Raw k-block: codes of the CTA's 4 row tiles (1 KiB each, contiguous in
-    // the packed layout), their scales (64 B each) and the 128 token rows of
-    // activations (128 B each). Thread tid copies 16 B of codes, threads < 16
-    // 16 B of scales, and 4 x 16 B of activations.
-    auto issue_raw = [&](int kbr) {
-        uint8_t* r = raw + (kbr % kRawStages) * kRawBytes;
-        const int kb = kb0 + kbr;
-        {
-            const int t = tid >> 6, within = (tid & 63) * 16;
-            const bool ok = tile0 + t < n_tiles;
-            const int8_t* src = W.qs + ((int64_t)(ok ? tile0 + t : 0) * k * 32 + (int64_t)kb * 1024 + within);
-            cp_async16(r + t * 1024 + within, src, ok ? 16u : 0u);
+    if (warp == kTcProducerWarp) {
+        if (lane == 0) {
+            const uint32_t stage_tx = (uint32_t)kTileBytes + (uint32_t)valid_tiles * (1024u + 64u);
+            auto issue_weights = [&](int kb) {
+                uint8_t* st = smem + (kb % kTcStages) * kStageBytes;
+                uint64_t* bar = &full_bar[kb % kTcStages];
+                mbar_arrive_expect_tx(bar, stage_tx);
+                const int kbg = kb0 + kb;
+                for (int t = 0; t < valid_tiles; ++t) {
+                    bulk_g2s(st + kStCodes + t * 1024, W.qs + ((int64_t)(tile0 + t) * k * 32 + (int64_t)kbg * 1024),
+                             1024u, bar);
+                    bulk_g2s(st + kStScales + t * 64,
+                             reinterpret_cast<const uint8_t*>(W.d) + ((int64_t)(tile0 + t) * nb_all + kbg) * 64, 64u,
+                             bar);
+                }
+            };
+            auto issue_x = [&](int kb) {
+                tma_load_2d(smem + (kb % kTcStages) * kStageBytes, &xmap, (kb0 + kb) * 32, t0,
+                            &full_bar[kb % kTcStages]);
+            };
+            // the first stages' weights stream before the dependency on the previous kernel
+            const int pre = min(kTcStages, nb);
+            for (int kb = 0; kb < pre; ++kb) issue_weights(kb);
+            pdl_wait();
+            for (int kb = 0; kb < pre; ++kb) issue_x(kb);
+            for (int kb = pre; kb < nb; ++kb) {
+                const int s = kb % kTcStages;
+                if (alive) alive = mbar_wait_bounded(&done_bar[s], ((kb / kTcStages) - 1) & 1, err, 13);
+                issue_weights(kb);
+                issue_x(kb);
+            }
+            // every copy has landed before the CTA may exit
+            for (int kb = max(0, nb - kTcStages); kb < nb; ++kb)
+                if (alive) alive = mbar_wait_bounded(&full_bar[kb % kTcStages], (kb / kTcStages) & 1, err, 14);
+        } else {
+            pdl_wait();
         }
-        if (tid < 16) {
-            const int t = tid >> 2, within = (tid & 3) * 16;
-            const bool ok = tile0 + t < n_tiles;
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(W.d) +
-                                 ((int64_t)(ok ? tile0 + t : 0) * nb_all + kb) * 64 + within;
-            cp_async16(r + 4096 + t * 64 + within, src, ok ? 16u : 0u);
-        }
+        __syncwarp();
+    } else if (warp == kTcMmaWarp) {
+        pdl_wait();
+        if (lane == 0) {
+            for (int kb = 0; kb < nb; ++kb) {
+                const int s = kb % kTcStages;
+                if (alive) alive = mbar_wait_bounded(&conv_bar[s], (kb / kTcStages) & 1, err, 15);
+                tc_fence_after();
+                const uint32_t xs = smem_u32(smem + s * kStageBytes);
+                const uint32_t a = tmem + (uint32_t)(kTmemA + s * 64);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int f = tid + i * kTcThreads;
-            const int row = f >> 3, c = f & 7;
-            const bool ok = t0 + row < m;
-            const float* src = X + (int64_t)(ok ? t0 + row : 0) * ldx + kb * 32 + c * 4;
-            cp_async16(r + 4096 + 256 + row * 128 + c * 16, src, ok ? 16u : 0u);
-        }
-        cp_async_commit();
-    };
-
-    for (int j = 0; j < kRawStages - 1; ++j) {
-        if (j < nb) issue_raw(j);
-        else cp_async_commit();  // keep the group count uniform
-    }
-
-    const int a_row = tid >> 1, a_half = tid & 1;
-    for (int kb = 0; kb < nb; ++kb) {
-        cp_async_wait<kRawStages - 2>();
-        __syncthreads();  // raw block kb complete for every thread; raw slot (kb-1) fully converted
-        if (kb + kRawStages - 1 < nb) issue_raw(kb + kRawStages - 1);
-        else cp_async_commit();
-        const int slot = kb % kTcSlots;
-        if (kb >= kTcSlots) mbar_wait_bounded(&mma_done[slot], ((kb / kTcSlots) - 1) & 1, err, 11);
-        const uint8_t* r = raw + (kb % kRawStages) * kRawBytes;
-        uint8_t* sA_hi = ops + slot * kSlotBytes;
-        uint8_t* sA_lo = sA_hi + kTileBytes;
-        uint8_t* sB_hi = sA_lo + kTileBytes;
-        uint8_t* sB_lo = sB_hi + kTileBytes;
-        {
-            const int t = a_row >> 5, ln = a_row & 31;
-            const uint4 qa = *reinterpret_cast<const uint4*>(r + t * 1024 + a_half * 512 + ln * 16);
-            const float da = __half2float(reinterpret_cast<const __half*>(r + 4096)[t * 32 + ln]);
-            float w[16];
-            dequant16(qa, da, w);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float4 hi, lo;
-                hi.x = tf32_rna(w[4 * c + 0]); lo.x = w[4 * c + 0] - hi.x;
-                hi.y = tf32_rna(w[4 * c + 1]); lo.y = w[4 * c + 1] - hi.y;
-                hi.z = tf32_rna(w[4 * c + 2]); lo.z = w[4 * c + 2] - hi.z;
-                hi.w = tf32_rna(w[4 * c + 3]); lo.w = w[4 * c + 3] - hi.w;
-                const uint32_t off = sw128_off(a_row, a_half * 4 + c);
-                *reinterpret_cast<float4*>(sA_hi + off) = hi;
-                *reinterpret_cast<float4*>(sA_lo + off) = lo;
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t b_hi = sw128_desc(xs + kk * 32), b_lo = sw128_desc(xs + kStXlo + kk * 32);
+                    mma_tf32_ts(tmem, a + kk * 8, b_hi, (kb | kk) != 0);
+                    mma_tf32_ts(tmem, a + kk * 8, b_lo, 1u);
+                    mma_tf32_ts(tmem, a + 32 + kk * 8, b_hi, 1u);
+                }
+                mma_commit(&done_bar[s]);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int f = tid + i * kTcThreads;
-            const int row = f >> 3, c = f & 7;
-            const float4 x = *reinterpret_cast<const float4*>(r + 4096 + 256 + row * 128 + c * 16);
-            float4 hi, lo;
-            hi.x = tf32_rna(x.x); lo.x = x.x - hi.x;
-            hi.y = tf32_rna(x.y); lo.y = x.y - hi.y;
-            hi.z = tf32_rna(x.z); lo.z = x.z - hi.z;
-            hi.w = tf32_rna(x.w); lo.w = x.w - hi.w;
-            const uint32_t off = sw128_off(row, c);
-            *reinterpret_cast<float4*>(sB_hi + off) = hi;
-            *reinterpret_cast<float4*>(sB_lo + off) = lo;
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        __syncwarp();
+    } else {
+        pdl_wait();
+        if (tid == 0) pdl_launch_dependents();
+        // converter: row r = 32 * (warp % 4) + lane of the CTA's 128 weight rows, k half warp / 4
+        const int quarter = warp & 3, khalf = warp >> 2;
+        const bool row_ok = quarter < valid_tiles;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        for (int kb = 0; kb < nb; ++kb) {
+            const int s = kb % kTcStages;
+            if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 11);
             tc_fence_after();
-            const uint32_t a_hi = smem_u32(sA_hi), a_lo = smem_u32(sA_lo);
-            const uint32_t b_hi = smem_u32(sB_hi), b_lo = smem_u32(sB_lo);
+            uint8_t* st = smem + s * kStageBytes;
+            uint32_t hi[16], lo[16];
+            {
+                uint4 qa = make_uint4(0u, 0u, 0u, 0u);
+                float da = 0.f;
+                if (row_ok) {
+                    qa = *reinterpret_cast<const uint4*>(st + kStCodes + quarter * 1024 + khalf * 512 + lane * 16);
+                    da = __half2float(reinterpret_cast<const __half*>(st + kStScales)[quarter * 32 + lane]);
+                }
+                float w[16];
+                dequant16(qa, da, w);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t o = kk * 32;
-                mma_tf32(tmem, sw128_desc(a_hi + o), sw128_desc(b_hi + o), (kb | kk) != 0);
-                mma_tf32(tmem, sw128_desc(a_hi + o), sw128_desc(b_lo + o), 1u);
-                mma_tf32(tmem, sw128_desc(a_lo + o), sw128_desc(b_hi + o), 1u);
+                for (int i = 0; i < 16; ++i) {
+                    hi[i] = tf32_rna_bits(w[i]);
+                    lo[i] = __float_as_uint(w[i] - __uint_as_float(hi[i]));
+                }
             }
-            mma_commit(&mma_done[slot]);
+            const uint32_t a = tmem + lane_base + (uint32_t)(kTmemA + s * 64 + khalf * 16);
+            tmem_st16(a, hi);
+            tmem_st16(a + 32, lo);
+            // x_lo: elementwise, so the swizzled positions of the x tile carry over
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int off = (tid + i * kTcConvWarps * 32) * 16;
+                const float4 x = *reinterpret_cast<const float4*>(st + off);
+                float4 xl;
+                xl.x = x.x - __uint_as_float(__float_as_uint(x.x) & kTf32Mask);
+                xl.y = x.y - __uint_as_float(__float_as_uint(x.y) & kTf32Mask);
+                xl.z = x.z - __uint_as_float(__float_as_uint(x.z) & kTf32Mask);
+                xl.w = x.w - __uint_as_float(__float_as_uint(x.w) & kTf32Mask);
+                *reinterpret_cast<float4*>(st + kStXlo + off) = xl;
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv_bar[s]);
         }
+        // all MMAs are complete once the last stage's commit has arrived
+        if (nb > 0 && alive)
+            alive = mbar_wait_bounded(&done_bar[(nb - 1) % kTcStages], ((nb - 1) / kTcStages) & 1, err, 12);
+        tc_fence_after();
     }
-    cp_async_wait<0>();
-    // all MMAs are complete once the last slot's commit has arrived
-    mbar_wait_bounded(&mma_done[(nb - 1) % kTcSlots], ((nb - 1) / kTcSlots) & 1, err, 12);
-    tc_fence_after();
 
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. and token columns of half w/4
+    // ---- epilogue: converter warp w reads TMEM lanes 32*(w%4).. and token columns of half w/4
     const int quarter = warp & 3, half = warp >> 2;
+    const bool reader = warp < kTcConvWarps;
     const int r = m0 + quarter * 32 + lane;
     if (!SPLIT) {
-        for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        if (reader) {
+            for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float other = (EPI == EPI_QKV || EPI == EPI_SILU) ? __shfl_xor_sync(0xffffffffu, v[j], 1) : 0.f;
-                tc_epilogue_one<EPI>(e, m, W.rows, t0 + c0 + j, r, v[j], other);
+                for (int j = 0; j < 16; ++j) {
+                    const float other =
+                        (EPI == EPI_QKV || EPI == EPI_SILU) ? __shfl_xor_sync(0xffffffffu, v[j], 1) : 0.f;
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + c0 + j, r, v[j], other);
+                }
             }
         }
     } else {
-        // partial tile -> own shared memory (the operand slots are free now)
-        float* part = reinterpret_cast<float*>(ops);  // [128 rows][kPartStride]
-        const int row = quarter * 32 + lane;
-        for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        // partial tile -> own shared memory (the stages are free now)
+        float* part = reinterpret_cast<float*>(smem);  // [128 rows][kPartStride]
+        __syncthreads();                              // every converter has left the stages
+        if (reader) {
+            const int row = quarter * 32 + lane;
+            for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4*>(part + row * kPartStride + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(part + row * kPartStride + c0 + j) =
+                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
         }
         cluster_sync();
         // rank z sums its rows over the S partials; thread -> (row pair, 4 tokens)
@@ -337,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) q8_gemm_tc_kernel(PackedQ8 W, c
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTcBN);
+    if (warp == kTcMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 static int g_tc_sms = 0;
@@ -356,14 +403,44 @@ static int gemm_tc_splits(int tiles, int nb) {
     return S;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+// Tensor map of the activations X[m][ldx] (f32, k columns used): boxes of 32
+// columns x 128 rows with the 128-byte swizzle; rows past m read as zeros.
+static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, int ldx) {
+    if (((uintptr_t)X & 15) || (ldx & 3) || ldx < k) return cudaErrorInvalidValue;
+    if (!g_encode_tiled) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return cudaErrorNotSupported;
+        g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
+    const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kTcBN};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides,
+                                      box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int EPI>
 static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
                                int* err, cudaStream_t s) {
+    CUtensorMap xmap;
+    cudaError_t merr = make_x_map(&xmap, X, m, W.k, ldx);
+    if (merr != cudaSuccess) return merr;
     const int gx = (W.rows_pad + kTcBM - 1) / kTcBM, gy = (m + kTcBN - 1) / kTcBN;
     const int S = gemm_tc_splits(gx * gy, W.k / 32);
     if (S == 1)
         return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gx, gy), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
-                         X, m, ldx, e, err);
+                         xmap, m, e, err);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, gy, S);
     cfg.blockDim = dim3(kTcThreads);
@@ -382,7 +459,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, X, m, ldx, e, err);
+    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, m, e, err);
 }
 
 template <int EPI>

@@ -1063,6 +1063,8 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
                                    int32_t flags, void* stream) {
     if (!packed || !x || !y || rows <= 0 || k <= 0 || k % 32 || m <= 0) return LQ8_ERR_ARG;
     if (flags & ~LQ8_MATMUL_EARLY_WEIGHTS) return LQ8_ERR_ARG;
+    // W and x are fetched by bulk and tensor copies: 16-byte aligned only
+    if (((uintptr_t)packed | (uintptr_t)x) & 15) return LQ8_ERR_ARG;
     const bool early = (flags & LQ8_MATMUL_EARLY_WEIGHTS) != 0;
     if (rows > (1 << 30) || m > (1 << 30)) return LQ8_ERR_UNSUPPORTED;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
