@@ -15,19 +15,23 @@
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
 // Q8_0 block; one 128-byte swizzle row of f32). Warp roles:
-//  - warp 8 (producer): per k-block one 2-D tensor copy of the activation tile
+//  - producer warp: per k-block one 2-D tensor copy of the activation tile
 //    (128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B layout)
 //    and bulk copies of the codes (1 KiB per 32-row tile) and scales;
-//  - warps 0-7 (converters): dequantise the weights, split them into hi/lo and
-//    write them into tensor memory (tcgen05.st; A operand, row r in lane r),
-//    and write x_lo next to the activation tile in shared memory;
-//  - warp 9 (MMA): one thread issues the 12 MMAs of a k-block with A read from
+//  - two groups of 8 converter warps, taking k-blocks in turn: dequantise the
+//    weights, split them into hi/lo and write them into tensor memory
+//    (tcgen05.st; A operand, row r in lane r), and write x_lo next to the
+//    activation tile in shared memory. A group's chain per k-block (loads,
+//    tensor-memory stores and their completion, proxy fence) is latency
+//    bound; two groups keep two k-blocks in conversion at once;
+//  - MMA warp: one thread issues the 12 MMAs of a k-block with A read from
 //    tensor memory and commits them to the stage's "done" barrier, which frees
 //    the stage for the producer.
 // Stages are handed on with mbarriers (no CTA-wide barrier in the k loop), so
-// copies, conversion and MMAs of different k-blocks overlap. The epilogue
-// reads TMEM with tcgen05.ld (warp w reads lanes 32*(w%4).., column half w/4)
-// and applies the shared epilogues.
+// copies, conversion and MMAs of different k-blocks overlap. Token tiles vary
+// fastest in the grid: the CTAs that share a weight tile run at the same time
+// and read it from DRAM once. The epilogue reads TMEM with tcgen05.ld (warp w
+// reads lanes 32*(w%4)) and applies the shared epilogues.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,8 +43,11 @@ namespace lq8 {
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
 constexpr int kTcStages = 4;
-constexpr int kTcConvWarps = 8;
+constexpr int kTcConvGroups = 2;                      // converter groups, taking k-blocks in turn
+constexpr int kTcGroupWarps = 8;                      // warps of one group (one k-block)
+constexpr int kTcConvWarps = kTcConvGroups * kTcGroupWarps;
 constexpr int kTcThreads = (kTcConvWarps + 2) * 32;  // converters, producer, MMA issuer
+static_assert(kTcStages % kTcConvGroups == 0, "each stage is converted by one group");
 constexpr int kTcProducerWarp = kTcConvWarps, kTcMmaWarp = kTcConvWarps + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
 // one stage: x tile (hi as loaded), x_lo tile, codes of 4 row tiles, their scales
@@ -189,8 +196,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int k = W.k, nb_all = k >> 5;
     const int S = SPLIT ? (int)gridDim.z : 1, z = SPLIT ? (int)blockIdx.z : 0;
     const int kb0 = (z * nb_all) / S, nb = ((z + 1) * nb_all) / S - kb0;  // this CTA's k-blocks
-    const int m0 = blockIdx.x * kTcBM;  // weight rows
-    const int t0 = blockIdx.y * kTcBN;  // tokens
+    // token tiles vary fastest, so the CTAs sharing a weight tile run together
+    const int m0 = blockIdx.y * kTcBM;  // weight rows
+    const int t0 = blockIdx.x * kTcBN;  // tokens
     const int tile0 = m0 >> 5;
     const int n_tiles = W.rows_pad >> 5;
     const int valid_tiles = min(4, n_tiles - tile0);
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&conv_bar[s], kTcConvWarps);
+            mbar_init(&conv_bar[s], kTcGroupWarps);
             mbar_init(&done_bar[s], 1);
         }
         fence_mbar_init();
@@ -271,11 +279,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
         pdl_wait();
         if (tid == 0) pdl_launch_dependents();
-        // converter: row r = 32 * (warp % 4) + lane of the CTA's 128 weight rows, k half warp / 4
-        const int quarter = warp & 3, khalf = warp >> 2;
+        // converter group g takes k-blocks g, g + G, ...; within it warp w
+        // converts row r = 32 * (w % 4) + lane of the CTA's 128 weight rows,
+        // k half (w / 4) % 2
+        const int group = warp / kTcGroupWarps, gtid = tid - group * kTcGroupWarps * 32;
+        const int quarter = warp & 3, khalf = (warp >> 2) & 1;
         const bool row_ok = quarter < valid_tiles;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        for (int kb = 0; kb < nb; ++kb) {
+        for (int kb = group; kb < nb; kb += kTcConvGroups) {
             const int s = kb % kTcStages;
             if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 11);
             tc_fence_after();
@@ -302,7 +313,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // x_lo: elementwise, so the swizzled positions of the x tile carry over
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int off = (tid + i * kTcConvWarps * 32) * 16;
+                const int off = (gtid + i * kTcGroupWarps * 32) * 16;
                 const float4 x = *reinterpret_cast<const float4*>(st + off);
                 float4 xl;
                 xl.x = x.x - __uint_as_float(__float_as_uint(x.x) & kTf32Mask);
@@ -323,13 +334,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
     }
 
-    // ---- epilogue: converter warp w reads TMEM lanes 32*(w%4).. and token columns of half w/4
+    // ---- epilogue: converter warp w reads TMEM lanes 32*(w%4).. and token
+    // columns [w/4 * 128/P, (w/4 + 1) * 128/P) of P = kTcConvWarps / 4 parts
+    constexpr int kColsPer = kTcBN / (kTcConvWarps / 4);
+    static_assert(kColsPer % 16 == 0, "epilogue column part");
     const int quarter = warp & 3, half = warp >> 2;
     const bool reader = warp < kTcConvWarps;
     const int r = m0 + quarter * 32 + lane;
     if (!SPLIT) {
         if (reader) {
-            for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+            for (int c0 = half * kColsPer; c0 < (half + 1) * kColsPer; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -346,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncthreads();                              // every converter has left the stages
         if (reader) {
             const int row = quarter * 32 + lane;
-            for (int c0 = half * (kTcBN / 2); c0 < (half + 1) * (kTcBN / 2); c0 += 16) {
+            for (int c0 = half * kColsPer; c0 < (half + 1) * kColsPer; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
@@ -439,10 +453,10 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     const int gx = (W.rows_pad + kTcBM - 1) / kTcBM, gy = (m + kTcBN - 1) / kTcBN;
     const int S = gemm_tc_splits(gx * gy, W.k / 32);
     if (S == 1)
-        return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gx, gy), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
+        return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gy, gx), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
                          xmap, m, e, err);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(gx, gy, S);
+    cfg.gridDim = dim3(gy, gx, S);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = (size_t)kTcSmem;
     cfg.stream = s;
