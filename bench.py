@@ -60,7 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode"], default=None,
+    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode", "decode7b", "prefill", "prefill7b"],
+                   default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
 
@@ -314,13 +315,9 @@ def decode_bytes(cfg: dict, kv_len: float) -> tuple[float, float]:
     return weights, kv
 
 
-def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3):
-    """Greedy decode of the Llama-7B-shaped Q8_0 model (32 x 4096, 32/8 heads of
-    128, FFN 14336, vocab 32000, untied head) after a 512-token prefill: the
-    decode step streams 7.55 GB of weights, so this is where the matrix-vector
-    kernel's bandwidth shows in a whole model. Weights N(0, 0.02) drawn on the
-    GPU (seeded) and quantised there; ms/token timed with CUDA events on the
-    library stream over the CUDA-graph decode steps."""
+def gpu_model_7b(torch, B, synth, device):
+    """The Llama-7B-shaped Q8_0 model: weights N(0, 0.02) drawn on the GPU
+    (seed 1) and quantised there, norm weights 1 + N(0, 0.02)."""
     cfg = dict(synth.MODEL_7B)
     gen = torch.Generator(device=device)
     gen.manual_seed(1)
@@ -340,6 +337,48 @@ def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3
     model = B.Model(cfg, t, device=device.index, on_device=True)
     del t
     torch.cuda.empty_cache()
+    return cfg, model
+
+
+def prefill_only(torch, B, synth, device, args, big: bool):
+    """Prefill alone (the 203-token prompt on the 135M model, or 512 tokens on
+    the 7B model), W warm-up and K timed calls on the library stream: the
+    command behind the prefill launch lists."""
+    cfg, model = gpu_model_7b(torch, B, synth, device) if big else gpu_model(torch, B, synth, device)
+    n = 512 if big else PROMPT_LEN
+    prompt = synth.prompt_ids(n, cfg["n_vocab"], 1 if big else SEED)
+    d_prompt = torch.from_numpy(prompt).to(device)
+    d_next = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.ExternalStream(model.stream(), device=device)
+    for _ in range(max(1, args.warmup)):
+        model.prefill_async(d_prompt, n, 0, d_next)
+    model.sync()
+    l0 = model.launch_count()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    torch.cuda.nvtx.range_push("timed_region")
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        model.prefill_async(d_prompt, n, 0, d_next)
+        ev[i][1].record(stream)
+    model.sync()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    out = {"workload": f"{'7B' if big else '135M'}-shaped Q8_0 Llama, {n}-token prefill",
+           "prefill_ms": statistics.median(ms), "prefill_tok_s": n / (statistics.median(ms) / 1000),
+           "launches_per_prefill": (model.launch_count() - l0) / args.steps}
+    model.close()
+    return out
+
+
+def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3):
+    """Greedy decode of the Llama-7B-shaped Q8_0 model (32 x 4096, 32/8 heads of
+    128, FFN 14336, vocab 32000, untied head) after a 512-token prefill: the
+    decode step streams 7.55 GB of weights, so this is where the matrix-vector
+    kernel's bandwidth shows in a whole model. Weights N(0, 0.02) drawn on the
+    GPU (seeded) and quantised there; ms/token timed with CUDA events on the
+    library stream over the CUDA-graph decode steps."""
+    cfg, model = gpu_model_7b(torch, B, synth, device)
     prompt = synth.prompt_ids(prompt_len, cfg["n_vocab"], 1)
     d_prompt = torch.from_numpy(prompt).to(device)
     d_next = torch.zeros(1, dtype=torch.int32, device=device)
@@ -349,12 +388,16 @@ def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3
     model.decode_async(8, d_out)
     model.sync()
     pre, dec = [], []
-    for _ in range(reps):
+    for rep in range(reps):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record(stream)
         model.prefill_async(d_prompt, prompt_len, 0, d_next)
         e[1].record(stream)
+        if rep == 0:
+            torch.cuda.nvtx.range_push("timed_region")  # the decode steps (launch-list captures)
         model.decode_async(n_decode, d_out)
+        if rep == 0:
+            torch.cuda.nvtx.range_pop()
         e[2].record(stream)
         model.sync()
         torch.cuda.synchronize()
@@ -637,6 +680,22 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.only == "decode7b":
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        print(json.dumps(decode_7b(torch, B, synth, torch.device("cuda", 0), hbm_peak()[0])))
+        return
+    if args.only in ("prefill", "prefill7b"):
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        print(json.dumps(prefill_only(torch, B, synth, torch.device("cuda", 0), args, args.only == "prefill7b")))
         return
     if args.only == "gemm":
         import torch

@@ -953,10 +953,13 @@ cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool p
     return cudaErrorInvalidValue;
 }
 
+cudaError_t init_attn_prefill_attributes();
+
 cudaError_t init_attention_attributes() {
     cudaError_t err = cudaFuncSetAttribute(attn_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)decode_smem_bytes(64));
     if (err != cudaSuccess) return err;
+    if ((err = init_attn_prefill_attributes()) != cudaSuccess) return err;
     err = cudaFuncSetAttribute(attn_decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)decode_smem_bytes(128));
     if (err != cudaSuccess) return err;
@@ -984,62 +987,99 @@ cudaError_t init_attention_attributes() {
 // ---------------------------------------------------------------------------
 // Prefill
 // ---------------------------------------------------------------------------
-constexpr int kQTile = 32;
-constexpr int kKTile = 32;
+// Causal attention for T > 1 rows ("量化 llama 的一次前向", forward：mask 什么时候建):
+// query t (position index_pos + t) sees cache positions j <= index_pos + t.
+// CTA = one query head x 16 query rows; 4 threads per query row, each holding
+// HD/4 dims of q and of the output. The CTA's KV range [0, kv_end) is cut into
+// tiles of KT positions which four groups of 64 threads take in turn (group
+// g: tiles g, g + 4, ...), each group double-buffering its tiles in shared
+// memory with cp.async and keeping its own online-softmax state (m, l, o) per
+// query row; the four states are merged at the end (o = sum_g e^(m_g - M) o_g
+// / sum_g e^(m_g - M) l_g). The serial chain per CTA is a quarter of the tiles.
+constexpr int kPfQ = 16;                    // query rows per CTA
+constexpr int kPfGroups = 4;                // KV groups per CTA
+constexpr int kPfGroupThreads = kPfQ * 4;   // 4 threads per query row
+constexpr int kPfThreads = kPfGroups * kPfGroupThreads;
 
 template <int HD>
-__global__ void __launch_bounds__(128) attn_prefill_kernel(const float* __restrict__ q, const float* __restrict__ kc,
-                                                           const float* __restrict__ vc, int T, int index_pos,
-                                                           int n_head, int n_kv, int cache_stride, float scale,
-                                                           float* __restrict__ out) {
-    constexpr int DS = HD / 4;  // dims per thread
-    __shared__ __align__(16) float Ks[kKTile][HD + 4];
-    __shared__ __align__(16) float Vs[kKTile][HD + 4];
-    pdl_wait();
-    pdl_launch_dependents();
+struct PfCfg {
+    static constexpr int KT = HD == 64 ? 32 : 16;  // positions per tile
+    static constexpr int LD = HD + 4;              // floats per shared row
+    static constexpr int TILE = KT * LD;           // floats of one K (or V) tile
+    static constexpr size_t kSmem = (size_t)kPfGroups * 2 * 2 * TILE * sizeof(float);  // groups x stages x {K,V}
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const float* __restrict__ q,
+                                                                  const float* __restrict__ kc,
+                                                                  const float* __restrict__ vc, int T, int index_pos,
+                                                                  int n_head, int n_kv, int cache_stride, float scale,
+                                                                  float* __restrict__ out) {
+    using C = PfCfg<HD>;
+    constexpr int KT = C::KT, LD = C::LD, DS = HD / 4;
+    extern __shared__ __align__(16) float pf_smem[];
+    const int tid = threadIdx.x, g = tid / kPfGroupThreads, gt = tid % kPfGroupThreads;
+    const int r = gt >> 2, c = gt & 3;  // query row within the CTA, dim quarter
     const int h = blockIdx.x, qt = blockIdx.y;
     const int G = n_head / n_kv, kh = h / G;
-    const int tid = threadIdx.x, r = tid >> 2, c = tid & 3;
-    const int i = qt * kQTile + r;
+    const int i = qt * kPfQ + r;
+    float* ring = pf_smem + (size_t)g * 2 * 2 * C::TILE;  // this group's [stage][K|V][KT][LD]
+    const float* kbase = kc + (int64_t)kh * cache_stride * HD;
+    const float* vbase = vc + (int64_t)kh * cache_stride * HD;
+    const int kv_end = index_pos + min(T, (qt + 1) * kPfQ);
+    const int n_tiles = (kv_end + KT - 1) / KT;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // copy tile `t` of K and V into stage `st` (rows past kv_end zero-filled)
+    auto issue = [&](int t, int st) {
+        if (t < n_tiles) {
+            float* ks = ring + st * 2 * C::TILE;
+            float* vs = ks + C::TILE;
+            for (int f = gt; f < KT * (HD / 4); f += kPfGroupThreads) {
+                const int row = f / (HD / 4), cc = f % (HD / 4);
+                const int j = t * KT + row;
+                const bool ok = j < kv_end;
+                const int64_t off = (int64_t)(ok ? j : 0) * HD + cc * 4;
+                cp_async16(ks + row * LD + cc * 4, kbase + off, ok ? 16u : 0u);
+                cp_async16(vs + row * LD + cc * 4, vbase + off, ok ? 16u : 0u);
+            }
+        }
+        cp_async_commit();
+    };
+
     float qv[DS], o[DS];
 #pragma unroll
     for (int d = 0; d < DS; ++d) {
-        qv[d] = i < T ? q[((int64_t)i * n_head + h) * HD + c * DS + d] : 0.0f;
+        qv[d] = i < T ? q[((int64_t)i * n_head + h) * HD + c * DS + d] * scale : 0.0f;
         o[d] = 0.0f;
     }
     float m = -INFINITY, l = 0.0f;
-    const int kv_end = index_pos + min(T, (qt + 1) * kQTile);
-    const float* kbase = kc + (int64_t)kh * cache_stride * HD;
-    const float* vbase = vc + (int64_t)kh * cache_stride * HD;
-    for (int j0 = 0; j0 < kv_end; j0 += kKTile) {
-        const int nt = min(kKTile, kv_end - j0);
-        for (int f = tid; f < kKTile * (HD / 4); f += 128) {
-            const int row = f / (HD / 4), cc = f % (HD / 4);
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (row < nt) {
-                kv = *reinterpret_cast<const float4*>(kbase + (int64_t)(j0 + row) * HD + cc * 4);
-                vv = *reinterpret_cast<const float4*>(vbase + (int64_t)(j0 + row) * HD + cc * 4);
-            }
-            *reinterpret_cast<float4*>(&Ks[row][cc * 4]) = kv;
-            *reinterpret_cast<float4*>(&Vs[row][cc * 4]) = vv;
-        }
-        __syncthreads();
-        float s[kKTile];
+
+    issue(g, 0);
+    for (int t = g, it = 0; t < n_tiles; t += kPfGroups, ++it) {
+        issue(t + kPfGroups, (it + 1) & 1);
+        cp_async_wait<1>();
+        named_bar_sync(1 + g, kPfGroupThreads);  // tile t of every thread in the group has landed
+        const float* ks = ring + (it & 1) * 2 * C::TILE;
+        const float* vs = ks + C::TILE;
+        float s[KT];
         float mt = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < kKTile; ++jj) {
+        for (int jj = 0; jj < KT; ++jj) {
             float p = 0.0f;
 #pragma unroll
             for (int d = 0; d < DS; d += 4) {
-                const float4 kk = *reinterpret_cast<const float4*>(&Ks[jj][c * DS + d]);
+                const float4 kk = *reinterpret_cast<const float4*>(ks + jj * LD + c * DS + d);
                 p = fmaf(qv[d], kk.x, p); p = fmaf(qv[d + 1], kk.y, p);
                 p = fmaf(qv[d + 2], kk.z, p); p = fmaf(qv[d + 3], kk.w, p);
             }
             p += __shfl_xor_sync(0xffffffffu, p, 1);
             p += __shfl_xor_sync(0xffffffffu, p, 2);
-            const int j = j0 + jj;
-            const bool vis = (jj < nt) && (j <= index_pos + i) && (i < T);
-            s[jj] = vis ? p * scale : -INFINITY;
+            const int j = t * KT + jj;
+            const bool vis = (j < kv_end) && (j <= index_pos + i) && (i < T);
+            s[jj] = vis ? p : -INFINITY;
             mt = fmaxf(mt, s[jj]);
         }
         const float m_new = fmaxf(m, mt);
@@ -1049,38 +1089,82 @@ __global__ void __launch_bounds__(128) attn_prefill_kernel(const float* __restri
 #pragma unroll
             for (int d = 0; d < DS; ++d) o[d] *= corr;
 #pragma unroll
-            for (int jj = 0; jj < kKTile; ++jj) {
+            for (int jj = 0; jj < KT; ++jj) {
                 const float p = expf(s[jj] - m_new);
                 l += p;
 #pragma unroll
                 for (int d = 0; d < DS; d += 4) {
-                    const float4 vv = *reinterpret_cast<const float4*>(&Vs[jj][c * DS + d]);
+                    const float4 vv = *reinterpret_cast<const float4*>(vs + jj * LD + c * DS + d);
                     o[d] = fmaf(p, vv.x, o[d]); o[d + 1] = fmaf(p, vv.y, o[d + 1]);
                     o[d + 2] = fmaf(p, vv.z, o[d + 2]); o[d + 3] = fmaf(p, vv.w, o[d + 3]);
                 }
             }
             m = m_new;
         }
-        __syncthreads();
+        named_bar_sync(1 + g, kPfGroupThreads);  // the stage is read before it is refilled
     }
-    if (i < T) {
-        const float inv = 1.0f / l;
+    cp_async_wait<0>();
+    __syncthreads();  // every group has left its ring: the shared memory holds the partial states now
+
+    // partial states: o_g [group][row][HD], m_g and l_g [group][row]
+    float* po = pf_smem;
+    float* pm = po + kPfGroups * kPfQ * HD;
+    float* pl = pm + kPfGroups * kPfQ;
 #pragma unroll
-        for (int d = 0; d < DS; ++d) out[((int64_t)i * n_head + h) * HD + c * DS + d] = o[d] * inv;
+    for (int d = 0; d < DS; ++d) po[(g * kPfQ + r) * HD + c * DS + d] = o[d];
+    if (c == 0) {
+        pm[g * kPfQ + r] = m;
+        pl[g * kPfQ + r] = l;
     }
+    __syncthreads();
+    // merge: thread -> (row, HD / 16 dims)
+    constexpr int DM = HD * kPfQ / kPfThreads;
+    const int mr = tid / (HD / DM), md = (tid % (HD / DM)) * DM;
+    const int mi = qt * kPfQ + mr;
+    if (mi < T) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int gg = 0; gg < kPfGroups; ++gg) M = fmaxf(M, pm[gg * kPfQ + mr]);
+        float wsum = 0.0f, acc[DM];
+#pragma unroll
+        for (int d = 0; d < DM; ++d) acc[d] = 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < kPfGroups; ++gg) {
+            const float mg = pm[gg * kPfQ + mr];
+            const float w = mg == -INFINITY ? 0.0f : expf(mg - M);
+            wsum = fmaf(w, pl[gg * kPfQ + mr], wsum);
+#pragma unroll
+            for (int d = 0; d < DM; ++d) acc[d] = fmaf(w, po[(gg * kPfQ + mr) * HD + md + d], acc[d]);
+        }
+        const float inv = 1.0f / wsum;
+#pragma unroll
+        for (int d = 0; d < DM; ++d) out[((int64_t)mi * n_head + h) * HD + md + d] = acc[d] * inv;
+    }
+}
+
+static_assert(PfCfg<64>::kSmem >= (size_t)(kPfGroups * kPfQ * (64 + 2)) * sizeof(float), "merge space");
+static_assert(PfCfg<128>::kSmem >= (size_t)(kPfGroups * kPfQ * (128 + 2)) * sizeof(float), "merge space");
+
+cudaError_t init_attn_prefill_attributes() {
+    cudaError_t err = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)PfCfg<64>::kSmem);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)PfCfg<128>::kSmem);
+    return err;
 }
 
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache, int T,
                                 int index_pos, int n_head, int n_head_kv, int head_dim, int cache_stride,
                                 float* out, bool pdl, cudaStream_t s) {
-    dim3 grid(n_head, (T + kQTile - 1) / kQTile);
+    dim3 grid(n_head, (T + kPfQ - 1) / kPfQ);
     const float scale = 1.0f / sqrtf((float)head_dim);
     if (head_dim == 64)
-        return launch_ex(attn_prefill_kernel<64>, grid, dim3(128), 0, s, pdl, q, k_cache, v_cache, T, index_pos,
-                         n_head, n_head_kv, cache_stride, scale, out);
+        return launch_ex(attn_prefill_kernel<64>, grid, dim3(kPfThreads), PfCfg<64>::kSmem, s, pdl, q, k_cache,
+                         v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
     if (head_dim == 128)
-        return launch_ex(attn_prefill_kernel<128>, grid, dim3(128), 0, s, pdl, q, k_cache, v_cache, T, index_pos,
-                         n_head, n_head_kv, cache_stride, scale, out);
+        return launch_ex(attn_prefill_kernel<128>, grid, dim3(kPfThreads), PfCfg<128>::kSmem, s, pdl, q, k_cache,
+                         v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
     return cudaErrorInvalidValue;
 }
 
