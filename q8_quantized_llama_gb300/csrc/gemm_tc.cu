@@ -54,6 +54,11 @@ constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
 constexpr int kStXlo = kTileBytes, kStCodes = 2 * kTileBytes, kStScales = kStCodes + 4096;
 constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
 constexpr int kTcSmem = kTcStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kPartStride = kTcBN + 4;                   // floats per row of a partial tile in shared memory
+// split-K: a receive buffer of the S partials of this rank's rows, [S][128 / S][kPartStride]
+constexpr int kRecvBytes = kTcBM * kPartStride * 4;
+constexpr int kTcSmemSplit = kTcSmem + kRecvBytes;
+static_assert(kTcSmemSplit <= 227 * 1024, "shared memory of the split-K kernel");
 // tensor memory: accumulator columns [0, 128), then per stage A_hi (32) and A_lo (32)
 constexpr int kTmemCols = 512;
 constexpr int kTmemA = kTcBN;
@@ -174,14 +179,20 @@ __device__ __forceinline__ void tc_epilogue_one(const EpiArgs& e, int m, int row
     }
 }
 
-constexpr int kPartStride = kTcBN + 4;  // floats per row of a partial tile in shared memory
-static_assert(kTcBM * kPartStride * 4 <= kTcStages * kStageBytes, "partial tile fits the stages");
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // SPLIT: the CTAs of a cluster (blockIdx.z = cluster rank) take equal shares
-// of the k-blocks; each stores its partial tile in its shared memory and,
-// after a cluster barrier, rank z sums rows [z * 128 / S, (z + 1) * 128 / S)
-// over the S partials (in rank order, through distributed shared memory) and
-// applies the epilogue to them.
+// of the k-blocks. Rank z owns rows [z * 128 / S, (z + 1) * 128 / S) of the
+// tile: every rank sends the partial rows of each owner straight from tensor
+// memory into slot [its rank] of the owner's receive buffer (asynchronous
+// stores that count bytes on the owner's mbarrier), and the owner sums the S
+// slots in rank order and applies the epilogue. A cluster barrier arrived at
+// start and waited before the first send makes every peer's mbarrier valid;
+// one arrived after the owner's data is complete and waited before exit keeps
+// every CTA alive until all sends have landed.
 template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     q8_gemm_tc_kernel(PackedQ8 W, const __grid_constant__ CUtensorMap xmap, int m, EpiArgs e, int* err) {
@@ -190,6 +201,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
     __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and x_lo
     __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
+    __shared__ __align__(8) uint64_t acc_bar;               // every MMA of the CTA complete (used once)
+    __shared__ __align__(8) uint64_t recv_bar;              // split-K: peers' partial rows landed
     __shared__ uint32_t tmem_holder;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -209,52 +222,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&conv_bar[s], kTcGroupWarps);
             mbar_init(&done_bar[s], 1);
         }
+        mbar_init(&acc_bar, 1);
+        mbar_init(&recv_bar, 1);
         fence_mbar_init();
     }
     if (warp == kTcMmaWarp) tmem_alloc(&tmem_holder, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (SPLIT) cluster_arrive();  // waited before the first send
     const uint32_t tmem = tmem_holder;
     bool alive = true;  // cleared by a wait that ran out; later waits are skipped
 
     if (warp == kTcProducerWarp) {
-        if (lane == 0) {
-            const uint32_t stage_tx = (uint32_t)kTileBytes + (uint32_t)valid_tiles * (1024u + 64u);
-            auto issue_weights = [&](int kb) {
-                uint8_t* st = smem + (kb % kTcStages) * kStageBytes;
-                uint64_t* bar = &full_bar[kb % kTcStages];
-                mbar_arrive_expect_tx(bar, stage_tx);
-                const int kbg = kb0 + kb;
-                for (int t = 0; t < valid_tiles; ++t) {
-                    bulk_g2s(st + kStCodes + t * 1024, W.qs + ((int64_t)(tile0 + t) * k * 32 + (int64_t)kbg * 1024),
-                             1024u, bar);
-                    bulk_g2s(st + kStScales + t * 64,
-                             reinterpret_cast<const uint8_t*>(W.d) + ((int64_t)(tile0 + t) * nb_all + kbg) * 64, 64u,
-                             bar);
-                }
-            };
-            auto issue_x = [&](int kb) {
+        // lane 0 registers a stage's bytes, then lanes 0..3 copy the codes of
+        // row tile `lane`, lanes 8..11 its scales and lane 16 the x tile
+        const uint32_t stage_tx = (uint32_t)kTileBytes + (uint32_t)valid_tiles * (1024u + 64u);
+        auto issue_weights = [&](int kb) {
+            uint8_t* st = smem + (kb % kTcStages) * kStageBytes;
+            uint64_t* bar = &full_bar[kb % kTcStages];
+            if (lane == 0) mbar_arrive_expect_tx(bar, stage_tx);
+            __syncwarp();
+            const int kbg = kb0 + kb;
+            const int t = lane & 7;
+            if (lane < 4 && t < valid_tiles)
+                bulk_g2s(st + kStCodes + t * 1024, W.qs + ((int64_t)(tile0 + t) * k * 32 + (int64_t)kbg * 1024),
+                         1024u, bar);
+            else if (lane >= 8 && lane < 12 && t < valid_tiles)
+                bulk_g2s(st + kStScales + t * 64,
+                         reinterpret_cast<const uint8_t*>(W.d) + ((int64_t)(tile0 + t) * nb_all + kbg) * 64, 64u,
+                         bar);
+        };
+        auto issue_x = [&](int kb) {
+            if (lane == 16)
                 tma_load_2d(smem + (kb % kTcStages) * kStageBytes, &xmap, (kb0 + kb) * 32, t0,
                             &full_bar[kb % kTcStages]);
-            };
-            // the first stages' weights stream before the dependency on the previous kernel
-            const int pre = min(kTcStages, nb);
-            for (int kb = 0; kb < pre; ++kb) issue_weights(kb);
-            pdl_wait();
-            for (int kb = 0; kb < pre; ++kb) issue_x(kb);
-            for (int kb = pre; kb < nb; ++kb) {
-                const int s = kb % kTcStages;
-                if (alive) alive = mbar_wait_bounded(&done_bar[s], ((kb / kTcStages) - 1) & 1, err, 13);
-                issue_weights(kb);
-                issue_x(kb);
-            }
-            // every copy has landed before the CTA may exit
+        };
+        // the first stages' weights stream before the dependency on the previous kernel
+        const int pre = min(kTcStages, nb);
+        for (int kb = 0; kb < pre; ++kb) issue_weights(kb);
+        pdl_wait();
+        for (int kb = 0; kb < pre; ++kb) issue_x(kb);
+        for (int kb = pre; kb < nb; ++kb) {
+            const int s = kb % kTcStages;
+            if (lane == 0 && alive) alive = mbar_wait_bounded(&done_bar[s], ((kb / kTcStages) - 1) & 1, err, 13);
+            __syncwarp();
+            issue_weights(kb);
+            issue_x(kb);
+        }
+        // every copy has landed before the CTA may exit
+        if (lane == 0)
             for (int kb = max(0, nb - kTcStages); kb < nb; ++kb)
                 if (alive) alive = mbar_wait_bounded(&full_bar[kb % kTcStages], (kb / kTcStages) & 1, err, 14);
-        } else {
-            pdl_wait();
-        }
         __syncwarp();
     } else if (warp == kTcMmaWarp) {
         pdl_wait();
@@ -274,6 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 mma_commit(&done_bar[s]);
             }
+            mma_commit(&acc_bar);  // tracks every MMA issued above
         }
         __syncwarp();
     } else {
@@ -328,9 +348,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv_bar[s]);
         }
-        // all MMAs are complete once the last stage's commit has arrived
-        if (nb > 0 && alive)
-            alive = mbar_wait_bounded(&done_bar[(nb - 1) % kTcStages], ((nb - 1) / kTcStages) & 1, err, 12);
+        // the accumulator is final once the single-use commit after the last k-block has arrived (a
+        // stage's "done" barrier could be two phases behind for the group that did not convert the
+        // last k-block, where a parity wait cannot tell the phases apart)
+        if (alive) alive = mbar_wait_bounded(&acc_bar, 0, err, 12);
         tc_fence_after();
     }
 
@@ -355,46 +376,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else {
-        // partial tile -> own shared memory (the stages are free now)
-        float* part = reinterpret_cast<float*>(smem);  // [128 rows][kPartStride]
-        __syncthreads();                              // every converter has left the stages
+        const int rows_per = kTcBM / S;
+        float* recv = reinterpret_cast<float*>(smem + kTcStages * kStageBytes);  // [S][rows_per][kPartStride]
+        if (tid == 0 && alive)
+            mbar_arrive_expect_tx(&recv_bar, (uint32_t)((S - 1) * rows_per * kTcBN * 4));
+        cluster_wait();  // every peer's receive barrier is initialised
         if (reader) {
             const int row = quarter * 32 + lane;
+            const int owner = row / rows_per, orow = row - owner * rows_per;
+            float* dst = recv + ((size_t)z * rows_per + orow) * kPartStride;
             for (int c0 = half * kColsPer; c0 < (half + 1) * kColsPer; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4*>(part + row * kPartStride + c0 + j) =
-                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 f = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    if (owner == z) *reinterpret_cast<float4*>(dst + c0 + j) = f;
+                    else st_async_f32x4(dst + c0 + j, (uint32_t)owner, f, &recv_bar);
+                }
             }
         }
-        cluster_sync();
-        // rank z sums its rows over the S partials; thread -> (row pair, 4 tokens)
-        const int rows_per = kTcBM / S;
+        if (alive) alive = mbar_wait_bounded(&recv_bar, 0, err, 16);
+        __syncthreads();  // this rank's own slot is written too
+        cluster_arrive();  // waited before exit: every send in the cluster has landed by then
+        // rank z sums its rows over the S slots in rank order; thread -> (row pair, 4 tokens)
         const int ra = z * rows_per;
         for (int f = tid; f < (rows_per / 2) * (kTcBN / 4); f += kTcThreads) {
             const int rp = f % (rows_per / 2), t = (f / (rows_per / 2)) * 4;
-            const int lr = ra + 2 * rp;
+            const int lr = 2 * rp;
             float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
             for (int zz = 0; zz < S; ++zz) {
-                const float4 a = ld_dsmem_f32x4(part + lr * kPartStride + t, (uint32_t)zz);
-                const float4 b = ld_dsmem_f32x4(part + (lr + 1) * kPartStride + t, (uint32_t)zz);
-                v0.x += a.x; v0.y += a.y; v0.z += a.z; v0.w += a.w;
-                v1.x += b.x; v1.y += b.y; v1.z += b.z; v1.w += b.w;
+                const float4 a4 = *reinterpret_cast<const float4*>(recv + ((size_t)zz * rows_per + lr) * kPartStride + t);
+                const float4 b4 =
+                    *reinterpret_cast<const float4*>(recv + ((size_t)zz * rows_per + lr + 1) * kPartStride + t);
+                v0.x += a4.x; v0.y += a4.y; v0.z += a4.z; v0.w += a4.w;
+                v1.x += b4.x; v1.y += b4.y; v1.z += b4.z; v1.w += b4.w;
             }
             const float e0[4] = {v0.x, v0.y, v0.z, v0.w}, e1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (EPI == EPI_QKV || EPI == EPI_SILU) {
-                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr, e0[j], e1[j]);
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + ra + lr, e0[j], e1[j]);
                 } else {
-                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr, e0[j], 0.f);
-                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + lr + 1, e1[j], 0.f);
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + ra + lr, e0[j], 0.f);
+                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + t + j, m0 + ra + lr + 1, e1[j], 0.f);
                 }
             }
         }
-        cluster_sync();  // peers keep their shared memory until every rank has read it
+        cluster_wait();
     }
     tc_fence_before();
     __syncthreads();
@@ -458,7 +487,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gy, gx, S);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = (size_t)kTcSmem;
+    cfg.dynamicSmemBytes = (size_t)kTcSmemSplit;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
@@ -481,7 +510,8 @@ static cudaError_t gemm_tc_attr() {
     cudaError_t err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kTcSmem);
     if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        err = cudaFuncSetAttribute(q8_gemm_tc_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kTcSmemSplit);
     return err;
 }
 
