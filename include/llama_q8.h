@@ -270,8 +270,8 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
  * workspace: device scratch of llama_q8_attention_workspace_bytes(...) bytes
  * (split-KV partial results and completion counters); its counters must be
  * zero before the first call and are left zero by every call; calls sharing a
- * workspace must not overlap on the GPU. k_cache and v_cache must be 16-byte
- * aligned (LQ8_ERR_ARG otherwise). */
+ * workspace must not overlap on the GPU. q, k_cache, v_cache and out must be
+ * 16-byte aligned (LQ8_ERR_ARG otherwise). */
 size_t llama_q8_attention_workspace_bytes(int32_t n_head, int32_t n_head_kv, int32_t head_dim,
                                           int32_t cache_stride);
 llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const float* v_cache,

@@ -989,55 +989,60 @@ cudaError_t init_attention_attributes() {
 // ---------------------------------------------------------------------------
 // Causal attention for T > 1 rows ("量化 llama 的一次前向", forward：mask 什么时候建):
 // query t (position index_pos + t) sees cache positions j <= index_pos + t.
-// CTA = one query head x 16 query rows; 4 threads per query row, each holding
-// HD/4 dims of q and of the output. The CTA's KV range [0, kv_end) is cut into
-// tiles of KT positions which four groups of 64 threads take in turn (group
-// g: tiles g, g + 4, ...), each group double-buffering its tiles in shared
-// memory with cp.async and keeping its own online-softmax state (m, l, o) per
-// query row; the four states are merged at the end (o = sum_g e^(m_g - M) o_g
-// / sum_g e^(m_g - M) l_g). The serial chain per CTA is a quarter of the tiles.
-constexpr int kPfQ = 16;                    // query rows per CTA
-constexpr int kPfGroups = 4;                // KV groups per CTA
-constexpr int kPfGroupThreads = kPfQ * 4;   // 4 threads per query row
-constexpr int kPfThreads = kPfGroups * kPfGroupThreads;
-
-template <int HD>
+// CTA = one query head x R = 16 * RT query rows, 256 threads as a 16 x 16 grid
+// (ty = tid / 16, tx = tid % 16). Per KV tile of KT positions:
+//  - scores: thread (ty, tx) computes rows RT * ty + i (i < RT) against keys
+//    tx + 16 k (k < KT / 16), q and k read as float4 from shared rows padded
+//    by 4 floats (lanes tx = 0..7 hit distinct 16-byte bank groups);
+//  - online softmax: a row's maximum is reduced over its 16 tx lanes (one
+//    half-warp) with shuffles; the row sums stay per thread until the end;
+//  - P = e^(s - m) goes to shared memory, read back only by the same half-warp
+//    (the rows it owns), so a warp barrier suffices;
+//  - output: thread (ty, tx) accumulates its RT rows x HD / 16 dims (float4
+//    groups tx and tx + 16) over the tile's keys.
+// K/V tiles are double-buffered with cp.async across the whole CTA.
+template <int HD, int RT>
 struct PfCfg {
-    static constexpr int KT = HD == 64 ? 32 : 16;  // positions per tile
-    static constexpr int LD = HD + 4;              // floats per shared row
-    static constexpr int TILE = KT * LD;           // floats of one K (or V) tile
-    static constexpr size_t kSmem = (size_t)kPfGroups * 2 * 2 * TILE * sizeof(float);  // groups x stages x {K,V}
+    static constexpr int R = 16 * RT;              // query rows per CTA
+    static constexpr int KT = HD == 64 ? 64 : 32;  // positions per tile
+    static constexpr int KPT = KT / 16;            // keys per thread (scores)
+    static constexpr int DG = HD / 64;             // float4 dim groups per thread (output)
+    static constexpr int LD = HD + 4;              // floats per q / k / v row in shared memory
+    static constexpr int LDP = KT + 4;             // floats per P row
+    static constexpr int kQ = 0, kK = R * LD, kV = kK + 2 * KT * LD, kP = kV + 2 * KT * LD;
+    static constexpr size_t kSmem = (size_t)(kP + R * LDP) * sizeof(float);
 };
+constexpr int kPfThreads = 256;
 
-template <int HD>
-__global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const float* __restrict__ q,
-                                                                  const float* __restrict__ kc,
-                                                                  const float* __restrict__ vc, int T, int index_pos,
-                                                                  int n_head, int n_kv, int cache_stride, float scale,
-                                                                  float* __restrict__ out) {
-    using C = PfCfg<HD>;
-    constexpr int KT = C::KT, LD = C::LD, DS = HD / 4;
+template <int HD, int RT>
+__global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float* __restrict__ q,
+                                                                     const float* __restrict__ kc,
+                                                                     const float* __restrict__ vc, int T,
+                                                                     int index_pos, int n_head, int n_kv,
+                                                                     int cache_stride, float scale,
+                                                                     float* __restrict__ out) {
+    using C = PfCfg<HD, RT>;
+    constexpr int R = C::R, KT = C::KT, KPT = C::KPT, DG = C::DG, LD = C::LD, LDP = C::LDP;
     extern __shared__ __align__(16) float pf_smem[];
-    const int tid = threadIdx.x, g = tid / kPfGroupThreads, gt = tid % kPfGroupThreads;
-    const int r = gt >> 2, c = gt & 3;  // query row within the CTA, dim quarter
-    const int h = blockIdx.x, qt = blockIdx.y;
-    const int G = n_head / n_kv, kh = h / G;
-    const int i = qt * kPfQ + r;
-    float* ring = pf_smem + (size_t)g * 2 * 2 * C::TILE;  // this group's [stage][K|V][KT][LD]
+    float* Qs = pf_smem + C::kQ;
+    float* Ps = pf_smem + C::kP;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int h = blockIdx.x, t0 = blockIdx.y * R;
+    const int kh = h / (n_head / n_kv);
     const float* kbase = kc + (int64_t)kh * cache_stride * HD;
     const float* vbase = vc + (int64_t)kh * cache_stride * HD;
-    const int kv_end = index_pos + min(T, (qt + 1) * kPfQ);
+    const int kv_end = index_pos + min(T, t0 + R);
     const int n_tiles = (kv_end + KT - 1) / KT;
 
     pdl_wait();
     pdl_launch_dependents();
 
-    // copy tile `t` of K and V into stage `st` (rows past kv_end zero-filled)
+    // copy tile `t` of K and V into stage `st` (positions past kv_end zero-filled)
     auto issue = [&](int t, int st) {
         if (t < n_tiles) {
-            float* ks = ring + st * 2 * C::TILE;
-            float* vs = ks + C::TILE;
-            for (int f = gt; f < KT * (HD / 4); f += kPfGroupThreads) {
+            float* ks = pf_smem + C::kK + st * KT * LD;
+            float* vs = pf_smem + C::kV + st * KT * LD;
+            for (int f = tid; f < KT * (HD / 4); f += kPfThreads) {
                 const int row = f / (HD / 4), cc = f % (HD / 4);
                 const int j = t * KT + row;
                 const bool ok = j < kv_end;
@@ -1048,123 +1053,169 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const float* _
         }
         cp_async_commit();
     };
-
-    float qv[DS], o[DS];
-#pragma unroll
-    for (int d = 0; d < DS; ++d) {
-        qv[d] = i < T ? q[((int64_t)i * n_head + h) * HD + c * DS + d] * scale : 0.0f;
-        o[d] = 0.0f;
+    issue(0, 0);
+    // q rows of this CTA, pre-scaled by 1/sqrt(head_dim); rows past T are zero
+    for (int f = tid; f < R * (HD / 4); f += kPfThreads) {
+        const int row = f / (HD / 4), cc = f % (HD / 4);
+        const int t = t0 + row;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < T) v = *reinterpret_cast<const float4*>(q + ((int64_t)t * n_head + h) * HD + cc * 4);
+        v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
+        *reinterpret_cast<float4*>(Qs + row * LD + cc * 4) = v;
     }
-    float m = -INFINITY, l = 0.0f;
 
-    issue(g, 0);
-    for (int t = g, it = 0; t < n_tiles; t += kPfGroups, ++it) {
-        issue(t + kPfGroups, (it + 1) & 1);
+    float o[RT][DG][4], m[RT], l[RT];
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.0f;
+#pragma unroll
+        for (int g = 0; g < DG; ++g) o[i][g][0] = o[i][g][1] = o[i][g][2] = o[i][g][3] = 0.0f;
+    }
+
+    for (int t = 0; t < n_tiles; ++t) {
+        issue(t + 1, (t + 1) & 1);
         cp_async_wait<1>();
-        named_bar_sync(1 + g, kPfGroupThreads);  // tile t of every thread in the group has landed
-        const float* ks = ring + (it & 1) * 2 * C::TILE;
-        const float* vs = ks + C::TILE;
-        float s[KT];
-        float mt = -INFINITY;
+        __syncthreads();  // tile t (and, at t = 0, the q rows) visible to every thread
+        const float* ks = pf_smem + C::kK + (t & 1) * KT * LD;
+        const float* vs = pf_smem + C::kV + (t & 1) * KT * LD;
+        float sc[RT][KPT];
 #pragma unroll
-        for (int jj = 0; jj < KT; ++jj) {
-            float p = 0.0f;
+        for (int i = 0; i < RT; ++i)
 #pragma unroll
-            for (int d = 0; d < DS; d += 4) {
-                const float4 kk = *reinterpret_cast<const float4*>(ks + jj * LD + c * DS + d);
-                p = fmaf(qv[d], kk.x, p); p = fmaf(qv[d + 1], kk.y, p);
-                p = fmaf(qv[d + 2], kk.z, p); p = fmaf(qv[d + 3], kk.w, p);
-            }
-            p += __shfl_xor_sync(0xffffffffu, p, 1);
-            p += __shfl_xor_sync(0xffffffffu, p, 2);
-            const int j = t * KT + jj;
-            const bool vis = (j < kv_end) && (j <= index_pos + i) && (i < T);
-            s[jj] = vis ? p : -INFINITY;
-            mt = fmaxf(mt, s[jj]);
+            for (int k = 0; k < KPT; ++k) sc[i][k] = 0.0f;
+#pragma unroll 4
+        for (int d = 0; d < HD; d += 4) {
+            float4 qv[RT], kv[KPT];
+#pragma unroll
+            for (int i = 0; i < RT; ++i) qv[i] = *reinterpret_cast<const float4*>(Qs + (ty * RT + i) * LD + d);
+#pragma unroll
+            for (int k = 0; k < KPT; ++k) kv[k] = *reinterpret_cast<const float4*>(ks + (tx + 16 * k) * LD + d);
+#pragma unroll
+            for (int i = 0; i < RT; ++i)
+#pragma unroll
+                for (int k = 0; k < KPT; ++k) {
+                    sc[i][k] = fmaf(qv[i].x, kv[k].x, sc[i][k]);
+                    sc[i][k] = fmaf(qv[i].y, kv[k].y, sc[i][k]);
+                    sc[i][k] = fmaf(qv[i].z, kv[k].z, sc[i][k]);
+                    sc[i][k] = fmaf(qv[i].w, kv[k].w, sc[i][k]);
+                }
         }
-        const float m_new = fmaxf(m, mt);
-        if (m_new != -INFINITY) {
-            const float corr = expf(m - m_new);
-            l *= corr;
+        // mask, row maxima over the half-warp, P into shared memory
 #pragma unroll
-            for (int d = 0; d < DS; ++d) o[d] *= corr;
+        for (int i = 0; i < RT; ++i) {
+            const int row = ty * RT + i;
+            const int last = index_pos + t0 + row;  // last visible position of this row
+            const bool row_ok = t0 + row < T;
+            float mt = -INFINITY;
 #pragma unroll
-            for (int jj = 0; jj < KT; ++jj) {
-                const float p = expf(s[jj] - m_new);
-                l += p;
+            for (int k = 0; k < KPT; ++k) {
+                const int j = t * KT + tx + 16 * k;
+                if (!(row_ok && j <= last && j < kv_end)) sc[i][k] = -INFINITY;
+                mt = fmaxf(mt, sc[i][k]);
+            }
 #pragma unroll
-                for (int d = 0; d < DS; d += 4) {
-                    const float4 vv = *reinterpret_cast<const float4*>(vs + jj * LD + c * DS + d);
-                    o[d] = fmaf(p, vv.x, o[d]); o[d + 1] = fmaf(p, vv.y, o[d + 1]);
-                    o[d + 2] = fmaf(p, vv.z, o[d + 2]); o[d + 3] = fmaf(p, vv.w, o[d + 3]);
+            for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            const float m_new = fmaxf(m[i], mt);
+            const float corr = m_new == -INFINITY ? 1.0f : expf(m[i] - m_new);
+            float ps = 0.0f;
+#pragma unroll
+            for (int k = 0; k < KPT; ++k) {
+                const float pk = m_new == -INFINITY ? 0.0f : expf(sc[i][k] - m_new);
+                ps += pk;
+                Ps[row * LDP + tx + 16 * k] = pk;
+            }
+            l[i] = l[i] * corr + ps;
+            m[i] = m_new;
+#pragma unroll
+            for (int g = 0; g < DG; ++g) {
+                o[i][g][0] *= corr; o[i][g][1] *= corr; o[i][g][2] *= corr; o[i][g][3] *= corr;
+            }
+        }
+        __syncwarp();  // a half-warp reads back only the P rows it wrote
+#pragma unroll 2
+        for (int j = 0; j < KT; j += 4) {
+            float4 pv[RT];
+#pragma unroll
+            for (int i = 0; i < RT; ++i) pv[i] = *reinterpret_cast<const float4*>(Ps + (ty * RT + i) * LDP + j);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+                for (int g = 0; g < DG; ++g) {
+                    const float4 vv = *reinterpret_cast<const float4*>(vs + (j + jj) * LD + (tx + 16 * g) * 4);
+#pragma unroll
+                    for (int i = 0; i < RT; ++i) {
+                        const float pj = jj == 0 ? pv[i].x : (jj == 1 ? pv[i].y : (jj == 2 ? pv[i].z : pv[i].w));
+                        o[i][g][0] = fmaf(pj, vv.x, o[i][g][0]);
+                        o[i][g][1] = fmaf(pj, vv.y, o[i][g][1]);
+                        o[i][g][2] = fmaf(pj, vv.z, o[i][g][2]);
+                        o[i][g][3] = fmaf(pj, vv.w, o[i][g][3]);
+                    }
                 }
             }
-            m = m_new;
         }
-        named_bar_sync(1 + g, kPfGroupThreads);  // the stage is read before it is refilled
+        __syncthreads();  // the stage and P are read before they are refilled
     }
     cp_async_wait<0>();
-    __syncthreads();  // every group has left its ring: the shared memory holds the partial states now
-
-    // partial states: o_g [group][row][HD], m_g and l_g [group][row]
-    float* po = pf_smem;
-    float* pm = po + kPfGroups * kPfQ * HD;
-    float* pl = pm + kPfGroups * kPfQ;
+    // row sums over the half-warp, then o / l
 #pragma unroll
-    for (int d = 0; d < DS; ++d) po[(g * kPfQ + r) * HD + c * DS + d] = o[d];
-    if (c == 0) {
-        pm[g * kPfQ + r] = m;
-        pl[g * kPfQ + r] = l;
-    }
-    __syncthreads();
-    // merge: thread -> (row, HD / 16 dims)
-    constexpr int DM = HD * kPfQ / kPfThreads;
-    const int mr = tid / (HD / DM), md = (tid % (HD / DM)) * DM;
-    const int mi = qt * kPfQ + mr;
-    if (mi < T) {
-        float M = -INFINITY;
+    for (int i = 0; i < RT; ++i) {
+        float li = l[i];
 #pragma unroll
-        for (int gg = 0; gg < kPfGroups; ++gg) M = fmaxf(M, pm[gg * kPfQ + mr]);
-        float wsum = 0.0f, acc[DM];
+        for (int off = 8; off > 0; off >>= 1) li += __shfl_xor_sync(0xffffffffu, li, off);
+        const int t = t0 + ty * RT + i;
+        if (t < T) {
+            const float inv = 1.0f / li;
 #pragma unroll
-        for (int d = 0; d < DM; ++d) acc[d] = 0.0f;
-#pragma unroll
-        for (int gg = 0; gg < kPfGroups; ++gg) {
-            const float mg = pm[gg * kPfQ + mr];
-            const float w = mg == -INFINITY ? 0.0f : expf(mg - M);
-            wsum = fmaf(w, pl[gg * kPfQ + mr], wsum);
-#pragma unroll
-            for (int d = 0; d < DM; ++d) acc[d] = fmaf(w, po[(gg * kPfQ + mr) * HD + md + d], acc[d]);
+            for (int g = 0; g < DG; ++g)
+                *reinterpret_cast<float4*>(out + ((int64_t)t * n_head + h) * HD + (tx + 16 * g) * 4) =
+                    make_float4(o[i][g][0] * inv, o[i][g][1] * inv, o[i][g][2] * inv, o[i][g][3] * inv);
         }
-        const float inv = 1.0f / wsum;
-#pragma unroll
-        for (int d = 0; d < DM; ++d) out[((int64_t)mi * n_head + h) * HD + md + d] = acc[d] * inv;
     }
 }
 
-static_assert(PfCfg<64>::kSmem >= (size_t)(kPfGroups * kPfQ * (64 + 2)) * sizeof(float), "merge space");
-static_assert(PfCfg<128>::kSmem >= (size_t)(kPfGroups * kPfQ * (128 + 2)) * sizeof(float), "merge space");
+template <int HD, int RT>
+static cudaError_t pf_attr() {
+    return cudaFuncSetAttribute(attn_prefill_kernel<HD, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)PfCfg<HD, RT>::kSmem);
+}
 
 cudaError_t init_attn_prefill_attributes() {
-    cudaError_t err = cudaFuncSetAttribute(attn_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)PfCfg<64>::kSmem);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)PfCfg<128>::kSmem);
+    cudaError_t err = pf_attr<64, 1>();
+    if (err == cudaSuccess) err = pf_attr<64, 4>();
+    if (err == cudaSuccess) err = pf_attr<128, 1>();
+    if (err == cudaSuccess) err = pf_attr<128, 4>();
     return err;
+}
+
+template <int HD, int RT>
+static cudaError_t pf_launch(const float* q, const float* k_cache, const float* v_cache, int T, int index_pos,
+                             int n_head, int n_head_kv, int cache_stride, float* out, bool pdl, cudaStream_t s) {
+    constexpr int R = PfCfg<HD, RT>::R;
+    const dim3 grid(n_head, (T + R - 1) / R);
+    const float scale = 1.0f / sqrtf((float)HD);
+    return launch_ex(attn_prefill_kernel<HD, RT>, grid, dim3(kPfThreads), PfCfg<HD, RT>::kSmem, s, pdl, q, k_cache,
+                     v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
 }
 
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache, int T,
                                 int index_pos, int n_head, int n_head_kv, int head_dim, int cache_stride,
                                 float* out, bool pdl, cudaStream_t s) {
-    dim3 grid(n_head, (T + kPfQ - 1) / kPfQ);
-    const float scale = 1.0f / sqrtf((float)head_dim);
+    // 64 rows per CTA when that still gives every SM a CTA, else 16
+    static int sms = 0;
+    if (sms <= 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    const bool big = (int64_t)n_head * ((T + 63) / 64) >= sms;
     if (head_dim == 64)
-        return launch_ex(attn_prefill_kernel<64>, grid, dim3(kPfThreads), PfCfg<64>::kSmem, s, pdl, q, k_cache,
-                         v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
+        return big ? pf_launch<64, 4>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s)
+                   : pf_launch<64, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
     if (head_dim == 128)
-        return launch_ex(attn_prefill_kernel<128>, grid, dim3(kPfThreads), PfCfg<128>::kSmem, s, pdl, q, k_cache,
-                         v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
+        return big ? pf_launch<128, 4>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s)
+                   : pf_launch<128, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
     return cudaErrorInvalidValue;
 }
 

@@ -1115,8 +1115,8 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
     if ((int64_t)index_pos + T > cache_stride) return LQ8_ERR_CTX;
     if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
     if (n_head / n_head_kv > 8) return LQ8_ERR_UNSUPPORTED;
-    // K/V rows are fetched in 16-byte pieces: 16-byte aligned caches only
-    if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return LQ8_ERR_ARG;
+    // q, K/V rows and outputs move in 16-byte pieces: 16-byte aligned buffers only
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out) & 15) return LQ8_ERR_ARG;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
     cudaError_t err;
     if (T == 1) {

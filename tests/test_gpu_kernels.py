@@ -220,12 +220,13 @@ def test_attention_decode_7b(kv_len):
     _attention_case(1, kv_len - 1, 32, 8, 128, 4096, seed=kv_len + 1)
 
 
-@pytest.mark.parametrize("T,index_pos", [(203, 0), (64, 512), (2, 0), (13, 33), (33, 0)])
+# 16 query rows per CTA for these; (1100, 0) and (1030, 7) give 64 rows per CTA
+@pytest.mark.parametrize("T,index_pos", [(203, 0), (64, 512), (2, 0), (13, 33), (33, 0), (1100, 0), (1030, 7)])
 def test_attention_prefill_135m(T, index_pos):
     _attention_case(T, index_pos, 9, 3, 64, 4096, seed=T + index_pos)
 
 
-@pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8)])
+@pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8), (300, 100)])
 def test_attention_prefill_7b(T, index_pos):
     _attention_case(T, index_pos, 32, 8, 128, 4096, seed=T * 3 + index_pos)
 
