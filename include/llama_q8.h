@@ -81,7 +81,19 @@ typedef struct llama_q8_config {
                               layer (norm, Q/K/V, attention and W_o fused; gate/up; down),
                               5 = one 16-CTA cluster kernel per layer; 2-5 give
                               LQ8_ERR_UNSUPPORTED at load when the model does not fit */
+    int32_t rope_style;   /* 0: rope_i, dims 2i and 2i+1 form a pair (the Llama convention);
+                             1: NEOX, dim i pairs with dim i + head_dim/2; both at angle
+                             p * theta^(-2i/head_dim) ("量化 llama 的一次前向", RoPE：两种约定，
+                             按架构名选). Other values -> LQ8_ERR_ARG */
 } llama_q8_config;
+
+/* The rotary convention the pages' loader picks from general.architecture:
+ * 1 (NEOX) for the architectures it lists, 0 (rope_i) for any other name, -1
+ * for NULL. The pages print five names of that list (qwen, qwen2, falcon,
+ * phi3, stablelm) and say it has about twenty; this function knows the five
+ * printed ones, and a file of another listed architecture sets rope_style
+ * itself. */
+int32_t llama_q8_rope_style_for_arch(const char* general_architecture);
 
 typedef struct llama_q8_layer_weights {
     const float* attn_norm;   /* [n_embd] f32 */
@@ -106,7 +118,12 @@ typedef struct llama_q8_weights {
 typedef struct llama_q8_ctx llama_q8_ctx;
 
 /* Build a context on CUDA device `device`: copy and repack every tensor into
- * the library's device layout, build the rotary cos/sin table
+ * the library's device layout (with rope_style 1, each head's Q and K rows
+ * are stored interleaved — row i and row i + head_dim/2 side by side — so the
+ * NEOX pairs become adjacent and the same fused rotation serves both
+ * conventions; attention scores are unchanged because q and k share the
+ * permutation, and llama_q8_read_kv returns K in the natural order), build
+ * the rotary cos/sin table
  * [max_seq, head_dim/2] (angle p * theta^(-2i/head_dim), computed in double,
  * stored f32), allocate the KV cache [n_layer][n_head_kv][max_seq][head_dim]
  * for K and for V, and create the context's stream. `*out` receives the

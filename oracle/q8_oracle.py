@@ -317,8 +317,11 @@ class ModelWeights:
         return rms_norm(x, self.t[name], self.cfg["rms_eps"])
 
     def _rope(self, x, positions):
+        """rope_i, or NEOX when cfg["rope_style"] == 1 (the loader's choice by
+        architecture name, [QL] "RoPE：两种约定，按架构名选")."""
         self.counters["rope"] += 1
-        return rope_i(x, positions, self.cfg["rope_theta"])
+        rope = rope_neox if int(self.cfg.get("rope_style", 0)) == 1 else rope_i
+        return rope(x, positions, self.cfg["rope_theta"])
 
     # -- state ------------------------------------------------------------
     def clear_kv_cache(self):

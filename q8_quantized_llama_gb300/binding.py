@@ -31,7 +31,7 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul", "llama_q8_matmul_ex",
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
            "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode",
-           "llama_q8_selftest_wait_timeout")
+           "llama_q8_selftest_wait_timeout", "llama_q8_rope_style_for_arch")
 
 
 class Q8Error(RuntimeError):
@@ -48,7 +48,8 @@ class llama_q8_config(C.Structure):
     _fields_ = [("n_layer", C.c_int32), ("n_embd", C.c_int32), ("n_head", C.c_int32),
                 ("n_head_kv", C.c_int32), ("head_dim", C.c_int32), ("n_ff", C.c_int32),
                 ("n_vocab", C.c_int32), ("max_seq", C.c_int32), ("rms_eps", C.c_float),
-                ("rope_theta", C.c_float), ("tied_output", C.c_int32), ("decode_kernel", C.c_int32)]
+                ("rope_theta", C.c_float), ("tied_output", C.c_int32), ("decode_kernel", C.c_int32),
+                ("rope_style", C.c_int32)]
 
 
 class llama_q8_layer_weights(C.Structure):
@@ -88,6 +89,7 @@ def lib() -> C.CDLL:
         "llama_q8_stream": (vp, [vp]),
         "llama_q8_decode_kernel_count": (i32, [vp]),
         "llama_q8_status_str": (C.c_char_p, [i32]),
+        "llama_q8_rope_style_for_arch": (i32, [C.c_char_p]),
         "llama_q8_quantize": (i32, [vp, i64, i64, vp, vp]),
         "llama_q8_packed_bytes": (sz, [i64, i64]),
         "llama_q8_pack": (i32, [vp, i64, i64, vp, vp]),
@@ -129,11 +131,16 @@ def check(status: int, where: str) -> None:
         raise Q8Error(status, where)
 
 
+def rope_style_for_arch(arch: str | None) -> int:
+    """0 (rope_i) or 1 (NEOX) for a general.architecture name; -1 for None."""
+    return int(lib().llama_q8_rope_style_for_arch(None if arch is None else arch.encode()))
+
+
 def make_config(cfg: dict) -> llama_q8_config:
     return llama_q8_config(cfg["n_layer"], cfg["n_embd"], cfg["n_head"], cfg["n_head_kv"], cfg["head_dim"],
                            cfg["n_ff"], cfg["n_vocab"], cfg.get("max_seq", 4096), cfg.get("rms_eps", 1e-5),
                            cfg.get("rope_theta", 10000.0), int(cfg.get("tied_output", 1)),
-                           int(cfg.get("decode_kernel", 0)))
+                           int(cfg.get("decode_kernel", 0)), int(cfg.get("rope_style", 0)))
 
 
 _LAYER_KEYS = ("attn_norm", "ffn_norm", "attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up",

@@ -585,6 +585,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
     if (C.decode_kernel < 0 || C.decode_kernel > 5) return LQ8_ERR_ARG;
+    if (C.rope_style != 0 && C.rope_style != 1) return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -640,8 +641,10 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     uint8_t* staging = nullptr;
     if (!w->on_device) LOAD_CK(cudaMalloc(&staging, max_aos));
 
+    // neox_heads > 0: rows are that many heads of head_dim rows; row i and row
+    // i + head_dim/2 of each head go to rows 2i and 2i+1 (the NEOX pairs side by side)
     auto pack = [&](const void* src, int64_t rows, int64_t k, uint8_t* dst, int64_t dst_rows, int64_t off,
-                    int64_t stride) -> cudaError_t {
+                    int64_t stride, int neox_heads = 0) -> cudaError_t {
         const uint8_t* s = reinterpret_cast<const uint8_t*>(src);
         cudaError_t err = cudaSuccess;
         if (!w->on_device) {
@@ -649,7 +652,17 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
             if (err != cudaSuccess) return err;
             s = staging;
         }
-        err = launch_pack(s, rows, k, dst, dst_rows, off, stride, c->stream);
+        if (neox_heads > 0) {
+            const int64_t hd = C.head_dim, half = hd / 2, row_bytes = (k / 32) * 34;
+            for (int hh = 0; hh < neox_heads && err == cudaSuccess; ++hh) {
+                err = launch_pack(s + hh * hd * row_bytes, half, k, dst, dst_rows, off + hh * hd, 2, c->stream);
+                if (err == cudaSuccess)
+                    err = launch_pack(s + (hh * hd + half) * row_bytes, half, k, dst, dst_rows, off + hh * hd + 1, 2,
+                                      c->stream);
+            }
+        } else {
+            err = launch_pack(s, rows, k, dst, dst_rows, off, stride, c->stream);
+        }
         if (err != cudaSuccess) return err;
         if (!w->on_device) err = cudaStreamSynchronize(c->stream);  // staging is reused
         return err;
@@ -664,8 +677,10 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         uint8_t* p_o = p_qkv + b_qkv;
         uint8_t* p_gu = p_o + b_o;
         uint8_t* p_down = p_gu + b_gu;
-        cudaError_t err = pack(LW.attn_q, c->q_rows, h, p_qkv, qkv_rows, 0, 1);
-        if (err == cudaSuccess) err = pack(LW.attn_k, c->kv_rows, h, p_qkv, qkv_rows, c->q_rows, 1);
+        const int neox = C.rope_style == 1;
+        cudaError_t err = pack(LW.attn_q, c->q_rows, h, p_qkv, qkv_rows, 0, 1, neox ? C.n_head : 0);
+        if (err == cudaSuccess)
+            err = pack(LW.attn_k, c->kv_rows, h, p_qkv, qkv_rows, c->q_rows, 1, neox ? C.n_head_kv : 0);
         if (err == cudaSuccess) err = pack(LW.attn_v, c->kv_rows, h, p_qkv, qkv_rows, c->q_rows + c->kv_rows, 1);
         if (err == cudaSuccess) err = pack(LW.attn_output, h, c->q_rows, p_o, h, 0, 1);
         if (err == cudaSuccess) err = pack(LW.ffn_gate, F, h, p_gu, 2 * (int64_t)F, 0, 2);
@@ -1021,10 +1036,29 @@ llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0,
                                     cudaMemcpyDeviceToHost, ctx->stream));
     }
     LQ8_CK(ctx, cudaStreamSynchronize(ctx->stream));
+    if (ctx->cfg.rope_style == 1) {  // K rows are stored with the NEOX pairs interleaved: undo it
+        std::vector<float> row(hd);
+        for (size_t r = 0; r < (size_t)ctx->cfg.n_head_kv * n; ++r) {
+            float* kr = k_out + r * hd;
+            for (int i = 0; i < hd / 2; ++i) {
+                row[i] = kr[2 * i];
+                row[i + hd / 2] = kr[2 * i + 1];
+            }
+            std::copy(row.begin(), row.end(), kr);
+        }
+    }
     return LQ8_OK;
 }
 
 void* llama_q8_stream(llama_q8_ctx* ctx) { return ctx ? (void*)ctx->stream : nullptr; }
+
+int32_t llama_q8_rope_style_for_arch(const char* arch) {
+    if (!arch) return -1;
+    static const char* const kNeox[] = {"qwen", "qwen2", "falcon", "phi3", "stablelm"};
+    for (const char* a : kNeox)
+        if (std::strcmp(arch, a) == 0) return 1;
+    return 0;
+}
 
 int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx) { return ctx ? ctx->decode_kernels : 0; }
 

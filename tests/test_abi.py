@@ -65,7 +65,8 @@ def test_config_validation_without_a_gpu(B):
     for bad, status in [(dict(head_dim=96), B.LQ8_ERR_UNSUPPORTED), (dict(n_embd=500), B.LQ8_ERR_UNSUPPORTED),
                         (dict(n_head_kv=4), B.LQ8_ERR_ARG), (dict(n_layer=0), B.LQ8_ERR_ARG),
                         (dict(tied_output=0), B.LQ8_ERR_ARG), (dict(decode_kernel=6), B.LQ8_ERR_ARG),
-                        (dict(decode_kernel=-1), B.LQ8_ERR_ARG)]:
+                        (dict(decode_kernel=-1), B.LQ8_ERR_ARG), (dict(rope_style=2), B.LQ8_ERR_ARG),
+                        (dict(rope_style=-1), B.LQ8_ERR_ARG)]:
         c = B.make_config(dict(cfg, **bad))
         w, keep = B.make_weights(cfg, t, on_device=False)
         out = C.c_void_p()
@@ -78,3 +79,14 @@ def test_size_queries(B):
     assert B.llama_q8_packed_bytes(10, 31) == 0
     assert B.llama_q8_attention_workspace_bytes(9, 3, 64, 4096) > 0
     assert B.llama_q8_attention_workspace_bytes(9, 4, 64, 4096) == 0
+
+
+def test_rope_style_by_architecture_name(B):
+    """The loader's choice of rotary convention by general.architecture: NEOX
+    for the names the pages print from its list, rope_i for llama and any
+    other name ("量化 llama 的一次前向", RoPE：两种约定，按架构名选)."""
+    for arch in ("qwen", "qwen2", "falcon", "phi3", "stablelm"):
+        assert B.rope_style_for_arch(arch) == 1, arch
+    for arch in ("llama", "Qwen2", "qwen3moe", "", "mistral"):
+        assert B.rope_style_for_arch(arch) == 0, arch
+    assert B.rope_style_for_arch(None) == -1

@@ -368,3 +368,32 @@ def test_generate_loop_positions(tiny_tensors):
     assert len(out) == 5 and len(logits) == 5
     assert m.cache_len() == 5 + 4
     assert out[0] == O.argmax_lowest(logits[0])
+
+
+def test_neox_forward_equals_rope_i_with_interleaved_rows(tiny_tensors):
+    """NEOX RoPE pairs dim i with dim i + hd/2 at the angle rope_i gives pair
+    (2i, 2i+1) ([QL] "RoPE：两种约定，按架构名选"), and attention scores are
+    sums over dims: so the NEOX model must equal the rope_i model whose Q and K
+    rows are reordered within each head to (0, hd/2, 1, hd/2 + 1, ...). A
+    wrong pairing, angle or sign in either rotation breaks this."""
+    cfg = dict(TINY, rope_style=1)
+    hd = cfg["head_dim"]
+    perm = np.empty(hd, np.int64)
+    perm[0::2] = np.arange(hd // 2)
+    perm[1::2] = np.arange(hd // 2) + hd // 2
+    t2 = dict(tiny_tensors)
+    for li in range(cfg["n_layer"]):
+        for name, heads in (("attn_q", cfg["n_head"]), ("attn_k", cfg["n_head_kv"])):
+            blob = tiny_tensors[f"blk.{li}.{name}.weight"]
+            rows = np.concatenate([hh * hd + perm for hh in range(heads)])
+            t2[f"blk.{li}.{name}.weight"] = blob[rows]
+    ids = synth.prompt_ids(11, cfg["n_vocab"], 3)
+    neox = O.ModelWeights(cfg, tiny_tensors)
+    inter = O.ModelWeights(TINY, t2)
+    a, b = neox.forward(ids, 0), inter.forward(ids, 0)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-5 * float(np.max(np.abs(a))))
+    a, b = neox.forward([5], 11), inter.forward([5], 11)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-5 * float(np.max(np.abs(a))))
+    # and the conventions do differ on this model
+    plain = O.ModelWeights(TINY, tiny_tensors).forward(ids, 0)
+    assert float(np.max(np.abs(plain - neox.forward(ids, 0)))) > 1e-3 * float(np.max(np.abs(plain)))
