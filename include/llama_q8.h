@@ -50,7 +50,8 @@ typedef enum llama_q8_status {
     LQ8_ERR_CUDA = 5,        /* a CUDA runtime call or a kernel launch failed */
     LQ8_ERR_OOM = 6,         /* device or pinned-host allocation failed */
     LQ8_ERR_STATE = 7,       /* context already failed, or call order violated */
-    LQ8_ERR_UNSUPPORTED = 8  /* shape outside what the kernels implement */
+    LQ8_ERR_UNSUPPORTED = 8, /* shape outside what the kernels implement */
+    LQ8_ERR_FORMAT = 9       /* GGUF file unreadable, not GGUF, or missing a key or tensor */
 } llama_q8_status;
 
 /* Q8_0 block: 32 consecutive weights of one row along the input dimension,
@@ -132,6 +133,36 @@ typedef struct llama_q8_ctx llama_q8_ctx;
  * from_gguf). */
 llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights* w,
                               int32_t device, llama_q8_ctx** out);
+
+/* from_gguf: read a GGUF file's header ("生成一个 token", 读 GGUF: magic,
+ * version, metadata key/values, tensor directory; the weights are not read)
+ * and fill *cfg the way the pages' loader does ("量化 llama 的一次前向",
+ * from_gguf：键名写死了 llama.): n_layer = llama.block_count, n_embd =
+ * llama.embedding_length, n_head = llama.attention.head_count, n_head_kv =
+ * llama.attention.head_count_kv (head_count when absent), head_dim = n_embd /
+ * n_head, n_ff = llama.feed_forward_length, n_vocab = token_embd.weight's row
+ * count, max_seq = 4096, rms_eps = llama.attention.layer_norm_rms_epsilon
+ * (1e-5 when absent), rope_theta = llama.rope.freq_base (10000 when absent),
+ * tied_output = no output.weight in the file, rope_style from
+ * general.architecture (llama_q8_rope_style_for_arch), decode_kernel 0. Every
+ * tensor the model needs is checked: present under its GGUF name
+ * (token_embd.weight, output_norm.weight, output.weight optional,
+ * blk.{i}.attn_norm / ffn_norm / attn_q / attn_k / attn_v / attn_output /
+ * ffn_gate / ffn_up / ffn_down .weight), Q8_0 for matrices and F32 for norms
+ * (LQ8_ERR_UNSUPPORTED otherwise), with the extents the hyperparameters give
+ * and inside the file. n_tensors and data_offset (either may be NULL) receive
+ * the directory's size and where the data region starts. No GPU is used.
+ * Errors: LQ8_ERR_ARG (NULL path or cfg), LQ8_ERR_FORMAT (unreadable, not
+ * GGUF v2/v3, a missing llama.* key, a missing or malformed tensor),
+ * LQ8_ERR_UNSUPPORTED. */
+llama_q8_status llama_q8_gguf_config(const char* path, llama_q8_config* cfg, int64_t* n_tensors,
+                                     int64_t* data_offset);
+
+/* llama_q8_gguf_config, then llama_q8_load of the file's tensors (mapped
+ * read-only, copied to device `device` and unmapped before returning) with
+ * the given decode_kernel. */
+llama_q8_status llama_q8_load_gguf(const char* path, int32_t device, int32_t decode_kernel,
+                                   llama_q8_ctx** out);
 
 /* forward(ids, index_pos): run T tokens (host ids[T]) starting at position
  * index_pos and write the f32 logits of the LAST position to host

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libllama_q8.so")
 STATUS = {0: "LQ8_OK", 1: "LQ8_ERR_ARG", 2: "LQ8_ERR_POS", 3: "LQ8_ERR_CTX", 4: "LQ8_ERR_TOKEN",
           5: "LQ8_ERR_CUDA", 6: "LQ8_ERR_OOM", 7: "LQ8_ERR_STATE", 8: "LQ8_ERR_UNSUPPORTED"}
 LQ8_OK, LQ8_ERR_ARG, LQ8_ERR_POS, LQ8_ERR_CTX, LQ8_ERR_TOKEN = 0, 1, 2, 3, 4
-LQ8_ERR_CUDA, LQ8_ERR_OOM, LQ8_ERR_STATE, LQ8_ERR_UNSUPPORTED = 5, 6, 7, 8
+LQ8_ERR_CUDA, LQ8_ERR_OOM, LQ8_ERR_STATE, LQ8_ERR_UNSUPPORTED, LQ8_ERR_FORMAT = 5, 6, 7, 8, 9
 
 # Every symbol include/llama_q8.h declares.
 EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llama_q8_generate",
@@ -31,7 +31,8 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_packed_bytes", "llama_q8_pack", "llama_q8_matmul", "llama_q8_matmul_ex",
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
            "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode",
-           "llama_q8_selftest_wait_timeout", "llama_q8_rope_style_for_arch")
+           "llama_q8_selftest_wait_timeout", "llama_q8_rope_style_for_arch", "llama_q8_gguf_config",
+           "llama_q8_load_gguf")
 
 
 class Q8Error(RuntimeError):
@@ -90,6 +91,8 @@ def lib() -> C.CDLL:
         "llama_q8_decode_kernel_count": (i32, [vp]),
         "llama_q8_status_str": (C.c_char_p, [i32]),
         "llama_q8_rope_style_for_arch": (i32, [C.c_char_p]),
+        "llama_q8_gguf_config": (i32, [C.c_char_p, vp, vp, vp]),
+        "llama_q8_load_gguf": (i32, [C.c_char_p, i32, i32, vp]),
         "llama_q8_quantize": (i32, [vp, i64, i64, vp, vp]),
         "llama_q8_packed_bytes": (sz, [i64, i64]),
         "llama_q8_pack": (i32, [vp, i64, i64, vp, vp]),
@@ -136,6 +139,23 @@ def rope_style_for_arch(arch: str | None) -> int:
     return int(lib().llama_q8_rope_style_for_arch(None if arch is None else arch.encode()))
 
 
+def gguf_config_status(path: str):
+    """(status, config dict or None, tensor count, data offset) of llama_q8_gguf_config."""
+    c = llama_q8_config()
+    n = C.c_int64(0)
+    off = C.c_int64(0)
+    st = lib().llama_q8_gguf_config(path.encode(), C.byref(c), C.byref(n), C.byref(off))
+    cfg = {f: getattr(c, f) for f, _ in llama_q8_config._fields_} if st == LQ8_OK else None
+    return st, cfg, n.value, off.value
+
+
+def gguf_config(path: str):
+    """(config dict, tensor count, data offset) of a GGUF file; raises Q8Error."""
+    st, cfg, n, off = gguf_config_status(path)
+    check(st, "llama_q8_gguf_config")
+    return cfg, n, off
+
+
 def make_config(cfg: dict) -> llama_q8_config:
     return llama_q8_config(cfg["n_layer"], cfg["n_embd"], cfg["n_head"], cfg["n_head_kv"], cfg["head_dim"],
                            cfg["n_ff"], cfg["n_vocab"], cfg.get("max_seq", 4096), cfg.get("rms_eps", 1e-5),
@@ -171,6 +191,17 @@ class Model:
         check(L.llama_q8_load(C.byref(c), C.byref(w), device, C.byref(out)), "llama_q8_load")
         self.ctx = out
         del keep
+
+    @classmethod
+    def from_gguf(cls, path: str, device: int = 0, decode_kernel: int = 0) -> "Model":
+        """llama_q8_load_gguf: the model of a GGUF file (config from its llama.* keys)."""
+        cfg = gguf_config(path)[0]
+        out = C.c_void_p()
+        check(lib().llama_q8_load_gguf(path.encode(), device, decode_kernel, C.byref(out)), "llama_q8_load_gguf")
+        self = cls.__new__(cls)
+        self.cfg = dict(cfg, decode_kernel=decode_kernel)
+        self.ctx = out
+        return self
 
     def close(self):
         if getattr(self, "ctx", None):

@@ -571,6 +571,7 @@ const char* llama_q8_status_str(llama_q8_status s) {
         case LQ8_ERR_OOM: return "out of memory";
         case LQ8_ERR_STATE: return "context unusable or call out of order";
         case LQ8_ERR_UNSUPPORTED: return "unsupported shape";
+        case LQ8_ERR_FORMAT: return "not a readable GGUF Llama file";
     }
     return "unknown status";
 }
