@@ -15,9 +15,12 @@
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
 // Q8_0 block; one 128-byte swizzle row of f32). Warp roles:
-//  - producer warp: per k-block one 2-D tensor copy of the activation tile
-//    (128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B layout)
-//    and bulk copies of the codes (1 KiB per 32-row tile) and scales;
+//  - producer warp: per k-block three tensor copies: the activation tile
+//    (2-D, 128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B
+//    layout), and the codes and scales of the CTA's four 32-row tiles (3-D
+//    views [tile][k-block][1 KiB or 64 B] of the packed weights, one box each;
+//    tiles past the matrix read as zeros). One copy instruction costs ~60 ns
+//    of issue, so the count per stage bounds the stage rate;
 //  - two groups of 8 converter warps, taking k-blocks in turn: dequantise the
 //    weights, split them into hi/lo and write them into tensor memory
 //    (tcgen05.st; A operand, row r in lane r), and write x_lo next to the
@@ -42,27 +45,33 @@ namespace lq8 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
-constexpr int kTcStages = 4;
+// Stages in flight (6 measured no faster: the MMA issue is the pacing step).
+// The count stays a multiple of the converter groups: each stage is always
+// converted by the same group, whose parity waits then never see a barrier
+// two phases behind.
+constexpr int kTcStagesMax = 4;
+constexpr int kTcStagesSplit = 4;
 constexpr int kTcConvGroups = 2;                      // converter groups, taking k-blocks in turn
 constexpr int kTcGroupWarps = 8;                      // warps of one group (one k-block)
 constexpr int kTcConvWarps = kTcConvGroups * kTcGroupWarps;
 constexpr int kTcThreads = (kTcConvWarps + 2) * 32;  // converters, producer, MMA issuer
-static_assert(kTcStages % kTcConvGroups == 0, "each stage is converted by one group");
+static_assert(kTcStagesMax % kTcConvGroups == 0 && kTcStagesSplit % kTcConvGroups == 0,
+              "each stage is converted by one group");
 constexpr int kTcProducerWarp = kTcConvWarps, kTcMmaWarp = kTcConvWarps + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
 // one stage: x tile (hi as loaded), x_lo tile, codes of 4 row tiles, their scales
 constexpr int kStXlo = kTileBytes, kStCodes = 2 * kTileBytes, kStScales = kStCodes + 4096;
 constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
-constexpr int kTcSmem = kTcStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kTcSmem = kTcStagesMax * kStageBytes + 1024;  // + alignment slack
 constexpr int kPartStride = kTcBN + 4;                   // floats per row of a partial tile in shared memory
 // split-K: a receive buffer of the S partials of this rank's rows, [S][128 / S][kPartStride]
 constexpr int kRecvBytes = kTcBM * kPartStride * 4;
-constexpr int kTcSmemSplit = kTcSmem + kRecvBytes;
-static_assert(kTcSmemSplit <= 227 * 1024, "shared memory of the split-K kernel");
+constexpr int kTcSmemSplit = kTcStagesSplit * kStageBytes + 1024 + kRecvBytes;
+static_assert(kTcSmem <= 227 * 1024 && kTcSmemSplit <= 227 * 1024, "shared memory per CTA");
 // tensor memory: accumulator columns [0, 128), then per stage A_hi (32) and A_lo (32)
 constexpr int kTmemCols = 512;
 constexpr int kTmemA = kTcBN;
-static_assert(kTmemA + kTcStages * 64 <= kTmemCols, "tensor memory columns");
+static_assert(kTmemA + kTcStagesMax * 64 <= kTmemCols, "tensor memory columns");
 
 // ---- tcgen05 wrappers ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
@@ -131,6 +140,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 3-D tensor copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 2-D tensor copy global -> shared, completing on an mbarrier; coordinates in
 // elements (x innermost).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -195,9 +214,11 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // every CTA alive until all sends have landed.
 template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    q8_gemm_tc_kernel(PackedQ8 W, const __grid_constant__ CUtensorMap xmap, int m, EpiArgs e, int* err) {
+    q8_gemm_tc_kernel(PackedQ8 W, const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap dmap, int m, EpiArgs e, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kTcStages = SPLIT ? kTcStagesSplit : kTcStagesMax;
     __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
     __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and x_lo
     __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
@@ -235,23 +256,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool alive = true;  // cleared by a wait that ran out; later waits are skipped
 
     if (warp == kTcProducerWarp) {
-        // lane 0 registers a stage's bytes, then lanes 0..3 copy the codes of
-        // row tile `lane`, lanes 8..11 its scales and lane 16 the x tile
-        const uint32_t stage_tx = (uint32_t)kTileBytes + (uint32_t)valid_tiles * (1024u + 64u);
+        // lane 0 registers a stage's bytes (full boxes: tiles past the matrix
+        // arrive as zeros), then lane 17 copies the codes of the four tiles,
+        // lane 18 their scales and lane 16 the x tile
+        constexpr uint32_t stage_tx = (uint32_t)kTileBytes + 4u * (1024u + 64u);
         auto issue_weights = [&](int kb) {
             uint8_t* st = smem + (kb % kTcStages) * kStageBytes;
             uint64_t* bar = &full_bar[kb % kTcStages];
             if (lane == 0) mbar_arrive_expect_tx(bar, stage_tx);
             __syncwarp();
-            const int kbg = kb0 + kb;
-            const int t = lane & 7;
-            if (lane < 4 && t < valid_tiles)
-                bulk_g2s(st + kStCodes + t * 1024, W.qs + ((int64_t)(tile0 + t) * k * 32 + (int64_t)kbg * 1024),
-                         1024u, bar);
-            else if (lane >= 8 && lane < 12 && t < valid_tiles)
-                bulk_g2s(st + kStScales + t * 64,
-                         reinterpret_cast<const uint8_t*>(W.d) + ((int64_t)(tile0 + t) * nb_all + kbg) * 64, 64u,
-                         bar);
+            if (lane == 17) tma_load_3d(st + kStCodes, &qmap, 0, kb0 + kb, tile0, bar);
+            else if (lane == 18) tma_load_3d(st + kStScales, &dmap, 0, kb0 + kb, tile0, bar);
         };
         auto issue_x = [&](int kb) {
             if (lane == 16)
@@ -450,10 +465,7 @@ static int gemm_tc_splits(int tiles, int nb) {
 // dependency on the driver library).
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
-// Tensor map of the activations X[m][ldx] (f32, k columns used): boxes of 32
-// columns x 128 rows with the 128-byte swizzle; rows past m read as zeros.
-static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, int ldx) {
-    if (((uintptr_t)X & 15) || (ldx & 3) || ldx < k) return cudaErrorInvalidValue;
+static cudaError_t get_encode_tiled() {
     if (!g_encode_tiled) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -463,6 +475,15 @@ static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, in
             return cudaErrorNotSupported;
         g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    return cudaSuccess;
+}
+
+// Tensor map of the activations X[m][ldx] (f32, k columns used): boxes of 32
+// columns x 128 rows with the 128-byte swizzle; rows past m read as zeros.
+static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, int ldx) {
+    if (((uintptr_t)X & 15) || (ldx & 3) || ldx < k) return cudaErrorInvalidValue;
+    cudaError_t e = get_encode_tiled();
+    if (e != cudaSuccess) return e;
     const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
     const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
     const cuuint32_t box[2] = {32, (cuuint32_t)kTcBN};
@@ -473,17 +494,43 @@ static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D views of the packed weights as 32-bit words: codes [tile][k-block][256]
+// (1 KiB per 32-row tile and k-block) and scales [tile][k-block][16] (64 B);
+// one box = the CTA's four tiles at one k-block, tiles past the matrix zero.
+static cudaError_t make_w_maps(CUtensorMap* qmap, CUtensorMap* dmap, const PackedQ8& W) {
+    if (((uintptr_t)W.qs | (uintptr_t)W.d) & 15) return cudaErrorInvalidValue;
+    cudaError_t e = get_encode_tiled();
+    if (e != cudaSuccess) return e;
+    const cuuint64_t tiles = (cuuint64_t)(W.rows_pad / 32), nb = (cuuint64_t)(W.k / 32);
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const cuuint64_t qdims[3] = {256, nb, tiles};
+    const cuuint64_t qstrides[2] = {1024, nb * 1024};
+    const cuuint32_t qbox[3] = {256, 1, 4};
+    CUresult r = g_encode_tiled(qmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<int8_t*>(W.qs), qdims, qstrides,
+                                qbox, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const cuuint64_t ddims[3] = {16, nb, tiles};
+    const cuuint64_t dstrides[2] = {64, nb * 64};
+    const cuuint32_t dbox[3] = {16, 1, 4};
+    r = g_encode_tiled(dmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<__half*>(W.d), ddims, dstrides, dbox, elem,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int EPI>
 static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
                                int* err, cudaStream_t s) {
-    CUtensorMap xmap;
+    CUtensorMap xmap, qmap, dmap;
     cudaError_t merr = make_x_map(&xmap, X, m, W.k, ldx);
+    if (merr == cudaSuccess) merr = make_w_maps(&qmap, &dmap, W);
     if (merr != cudaSuccess) return merr;
     const int gx = (W.rows_pad + kTcBM - 1) / kTcBM, gy = (m + kTcBN - 1) / kTcBN;
     const int S = gemm_tc_splits(gx * gy, W.k / 32);
     if (S == 1)
         return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gy, gx), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
-                         xmap, m, e, err);
+                         xmap, qmap, dmap, m, e, err);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gy, gx, S);
     cfg.blockDim = dim3(kTcThreads);
@@ -502,7 +549,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, m, e, err);
+    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, qmap, dmap, m, e, err);
 }
 
 template <int EPI>
