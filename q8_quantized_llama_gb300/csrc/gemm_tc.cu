@@ -52,12 +52,14 @@ constexpr int kTcBN = 128;
 constexpr int kTcStagesMax = 4;
 constexpr int kTcStagesSplit = 4;
 constexpr int kTcConvGroups = 2;                      // converter groups, taking k-blocks in turn
-constexpr int kTcGroupWarps = 8;                      // warps of one group (one k-block)
+constexpr int kTcGroupWarps = 4;                      // warps of one group (one k-block, 32 rows each)
 constexpr int kTcConvWarps = kTcConvGroups * kTcGroupWarps;
-constexpr int kTcThreads = (kTcConvWarps + 2) * 32;  // converters, producer, MMA issuer
+constexpr int kTcAccWarps = 8;                        // accumulator warps: 4 lane quarters x 2 column halves
+constexpr int kTcAccWarp0 = kTcConvWarps;
+constexpr int kTcThreads = (kTcConvWarps + kTcAccWarps + 2) * 32;  // + producer, MMA issuer
 static_assert(kTcStagesMax % kTcConvGroups == 0 && kTcStagesSplit % kTcConvGroups == 0,
               "each stage is converted by one group");
-constexpr int kTcProducerWarp = kTcConvWarps, kTcMmaWarp = kTcConvWarps + 1;
+constexpr int kTcProducerWarp = kTcConvWarps + kTcAccWarps, kTcMmaWarp = kTcProducerWarp + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
 // one stage: x tile (hi as loaded), x_lo tile, codes of 4 row tiles, their scales
 constexpr int kStXlo = kTileBytes, kStCodes = 2 * kTileBytes, kStScales = kStCodes + 4096;
@@ -68,10 +70,11 @@ constexpr int kPartStride = kTcBN + 4;                   // floats per row of a 
 constexpr int kRecvBytes = kTcBM * kPartStride * 4;
 constexpr int kTcSmemSplit = kTcStagesSplit * kStageBytes + 1024 + kRecvBytes;
 static_assert(kTcSmem <= 227 * 1024 && kTcSmemSplit <= 227 * 1024, "shared memory per CTA");
-// tensor memory: accumulator columns [0, 128), then per stage A_hi (32) and A_lo (32)
+// tensor memory: two block-partial buffers of 128 columns, then per stage the
+// 32 codes of each row (A operand)
 constexpr int kTmemCols = 512;
-constexpr int kTmemA = kTcBN;
-static_assert(kTmemA + kTcStagesMax * 64 <= kTmemCols, "tensor memory columns");
+constexpr int kTmemA = 2 * kTcBN;
+static_assert(kTmemA + kTcStagesMax * 32 <= kTmemCols, "tensor memory columns");
 
 // ---- tcgen05 wrappers ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
@@ -222,7 +225,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
     __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and x_lo
     __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
-    __shared__ __align__(8) uint64_t acc_bar;               // every MMA of the CTA complete (used once)
+    __shared__ __align__(8) uint64_t part_full[2];          // a block partial is in tensor memory
+    __shared__ __align__(8) uint64_t part_empty[2];         // the accumulator warps have read it
     __shared__ __align__(8) uint64_t recv_bar;              // split-K: peers' partial rows landed
     __shared__ uint32_t tmem_holder;
 
@@ -243,7 +247,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&conv_bar[s], kTcGroupWarps);
             mbar_init(&done_bar[s], 1);
         }
-        mbar_init(&acc_bar, 1);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(&part_full[p], 1);
+            mbar_init(&part_empty[p], kTcAccWarps);
+        }
         mbar_init(&recv_bar, 1);
         fence_mbar_init();
     }
@@ -294,31 +301,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pdl_wait();
         if (lane == 0) {
             for (int kb = 0; kb < nb; ++kb) {
-                const int s = kb % kTcStages;
+                const int s = kb % kTcStages, p = kb & 1;
                 if (alive) alive = mbar_wait_bounded(&conv_bar[s], (kb / kTcStages) & 1, err, 15);
+                // the partial buffer of k-block kb - 2 has been read by the accumulator warps
+                if (kb >= 2 && alive) alive = mbar_wait_bounded(&part_empty[p], ((kb >> 1) - 1) & 1, err, 17);
                 tc_fence_after();
                 const uint32_t xs = smem_u32(smem + s * kStageBytes);
-                const uint32_t a = tmem + (uint32_t)(kTmemA + s * 64);
+                const uint32_t a = tmem + (uint32_t)(kTmemA + s * 32);
+                const uint32_t d = tmem + (uint32_t)(p * kTcBN);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t b_hi = sw128_desc(xs + kk * 32), b_lo = sw128_desc(xs + kStXlo + kk * 32);
-                    mma_tf32_ts(tmem, a + kk * 8, b_hi, (kb | kk) != 0);
-                    mma_tf32_ts(tmem, a + kk * 8, b_lo, 1u);
-                    mma_tf32_ts(tmem, a + 32 + kk * 8, b_hi, 1u);
+                    mma_tf32_ts(d, a + kk * 8, b_hi, kk != 0);
+                    mma_tf32_ts(d, a + kk * 8, b_lo, 1u);
                 }
                 mma_commit(&done_bar[s]);
+                mma_commit(&part_full[p]);
             }
-            mma_commit(&acc_bar);  // tracks every MMA issued above
         }
         __syncwarp();
+    } else if (warp >= kTcConvWarps) {
+        pdl_wait();  // accumulator warps: they write the outputs
     } else {
         pdl_wait();
         if (tid == 0) pdl_launch_dependents();
-        // converter group g takes k-blocks g, g + G, ...; within it warp w
-        // converts row r = 32 * (w % 4) + lane of the CTA's 128 weight rows,
-        // k half (w / 4) % 2
+        // converter group g takes k-blocks g, g + G, ...; warp w of the group
+        // writes the 32 codes (as exact f32) of row r = 32 * (w % 4) + lane
         const int group = warp / kTcGroupWarps, gtid = tid - group * kTcGroupWarps * 32;
-        const int quarter = warp & 3, khalf = (warp >> 2) & 1;
+        const int quarter = warp & 3;
         const bool row_ok = quarter < valid_tiles;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         for (int kb = group; kb < nb; kb += kTcConvGroups) {
@@ -326,28 +336,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 11);
             tc_fence_after();
             uint8_t* st = smem + s * kStageBytes;
-            uint32_t hi[16], lo[16];
-            {
-                uint4 qa = make_uint4(0u, 0u, 0u, 0u);
-                float da = 0.f;
-                if (row_ok) {
-                    qa = *reinterpret_cast<const uint4*>(st + kStCodes + quarter * 1024 + khalf * 512 + lane * 16);
-                    da = __half2float(reinterpret_cast<const __half*>(st + kStScales)[quarter * 32 + lane]);
-                }
-                float w[16];
-                dequant16(qa, da, w);
+            const uint32_t a = tmem + lane_base + (uint32_t)(kTmemA + s * 32);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    hi[i] = tf32_rna_bits(w[i]);
-                    lo[i] = __float_as_uint(w[i] - __uint_as_float(hi[i]));
-                }
+            for (int h = 0; h < 2; ++h) {
+                uint4 qa = make_uint4(0u, 0u, 0u, 0u);
+                if (row_ok) qa = *reinterpret_cast<const uint4*>(st + kStCodes + quarter * 1024 + h * 512 + lane * 16);
+                float w[16];
+                dequant16(qa, 1.0f, w);  // the codes themselves: exact in tf32
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(w[i]);
+                tmem_st16(a + h * 16, u);
             }
-            const uint32_t a = tmem + lane_base + (uint32_t)(kTmemA + s * 64 + khalf * 16);
-            tmem_st16(a, hi);
-            tmem_st16(a + 32, lo);
             // x_lo: elementwise, so the swizzled positions of the x tile carry over
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kTileBytes / (kTcGroupWarps * 32 * 16); ++i) {
                 const int off = (gtid + i * kTcGroupWarps * 32) * 16;
                 const float4 x = *reinterpret_cast<const float4*>(st + off);
                 float4 xl;
@@ -363,30 +366,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv_bar[s]);
         }
-        // the accumulator is final once the single-use commit after the last k-block has arrived (a
-        // stage's "done" barrier could be two phases behind for the group that did not convert the
-        // last k-block, where a parity wait cannot tell the phases apart)
-        if (alive) alive = mbar_wait_bounded(&acc_bar, 0, err, 12);
-        tc_fence_after();
     }
 
-    // ---- epilogue: converter warp w reads TMEM lanes 32*(w%4).. and token
-    // columns [w/4 * 128/P, (w/4 + 1) * 128/P) of P = kTcConvWarps / 4 parts
-    constexpr int kColsPer = kTcBN / (kTcConvWarps / 4);
-    static_assert(kColsPer % 16 == 0, "epilogue column part");
-    const int quarter = warp & 3, half = warp >> 2;
-    const bool reader = warp < kTcConvWarps;
-    const int r = m0 + quarter * 32 + lane;
-    if (!SPLIT) {
-        if (reader) {
-            for (int c0 = half * kColsPer; c0 < (half + 1) * kColsPer; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+    // ---- accumulator warps: warp 8 + w holds rows 32*(w%4) + lane and token
+    // columns [64*(w/4), 64*(w/4) + 64) of the tile in registers; per k-block
+    // it reads the block partial from tensor memory, frees the buffer and adds
+    // it times the block scale d of its row
+    const int aw = warp - kTcAccWarp0;
+    const bool accw = aw >= 0 && aw < kTcAccWarps;
+    const int quarter = aw & 3, half = aw >> 2;
+    constexpr int kColsPer = kTcBN / 2;
+    float acc[kColsPer];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float other =
-                        (EPI == EPI_QKV || EPI == EPI_SILU) ? __shfl_xor_sync(0xffffffffu, v[j], 1) : 0.f;
-                    tc_epilogue_one<EPI>(e, m, W.rows, t0 + c0 + j, r, v[j], other);
+    for (int j = 0; j < kColsPer; ++j) acc[j] = 0.0f;
+    if (accw) {
+        const bool row_ok = quarter < valid_tiles;
+        const __half* drow = W.d + ((int64_t)(tile0 + (row_ok ? quarter : 0)) * nb_all + kb0) * 32 + lane;
+        float dnext = row_ok ? __half2float(drow[0]) : 0.0f;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        for (int kb = 0; kb < nb; ++kb) {
+            const int p = kb & 1;
+            const float d = dnext;
+            if (kb + 1 < nb && row_ok) dnext = __half2float(drow[(int64_t)(kb + 1) * 32]);
+            if (alive) alive = mbar_wait_bounded(&part_full[p], (kb >> 1) & 1, err, 12);
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < kColsPer; c += 16) {
+                float t16[16];
+                tmem_ld16(tmem + lane_base + (uint32_t)(p * kTcBN + half * kColsPer + c), t16);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[c + j] = fmaf(d, t16[j], acc[c + j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&part_empty[p]);
+        }
+    }
+
+    if (!SPLIT) {
+        // the finished tile goes back to tensor memory (partial buffer 0: every
+        // MMA is complete, and each accumulator warp overwrites only the region
+        // it alone read), then all 16 converter and accumulator warps apply the
+        // epilogue, 32 token columns each: warp w reads lanes 32*(w%4) and
+        // columns [32*(w/4), 32*(w/4) + 32)
+        if (accw) {
+            const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+#pragma unroll
+            for (int c = 0; c < kColsPer; c += 16) {
+                uint32_t u[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(acc[c + j]);
+                tmem_st16(tmem + lane_base + (uint32_t)(half * kColsPer + c), u);
+            }
+            tmem_wait_st();
+        }
+        if (warp < kTcConvWarps + kTcAccWarps) {
+            tc_fence_before();
+            named_bar_sync(1, (kTcConvWarps + kTcAccWarps) * 32);
+            tc_fence_after();
+            const int eq = warp & 3, part = warp >> 2;
+            const int r = m0 + eq * 32 + lane;
+            for (int c0 = part * 32; c0 < part * 32 + 32; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)c0, v);
+                if (EPI == EPI_RESIDUAL) {
+                    // the 16 residual reads first, then the 16 writes: no chain of dependent round trips
+                    float y0[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = t0 + c0 + j;
+                        y0[j] = (t < m && r < W.rows) ? e.y[(int64_t)t * e.ldy + r] : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = t0 + c0 + j;
+                        if (t < m && r < W.rows) e.y[(int64_t)t * e.ldy + r] = y0[j] + v[j];
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float other =
+                            (EPI == EPI_QKV || EPI == EPI_SILU) ? __shfl_xor_sync(0xffffffffu, v[j], 1) : 0.f;
+                        tc_epilogue_one<EPI>(e, m, W.rows, t0 + c0 + j, r, v[j], other);
+                    }
                 }
             }
         }
@@ -396,19 +458,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tid == 0 && alive)
             mbar_arrive_expect_tx(&recv_bar, (uint32_t)((S - 1) * rows_per * kTcBN * 4));
         cluster_wait();  // every peer's receive barrier is initialised
-        if (reader) {
+        if (accw) {
             const int row = quarter * 32 + lane;
             const int owner = row / rows_per, orow = row - owner * rows_per;
-            float* dst = recv + ((size_t)z * rows_per + orow) * kPartStride;
-            for (int c0 = half * kColsPer; c0 < (half + 1) * kColsPer; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+            float* dst = recv + ((size_t)z * rows_per + orow) * kPartStride + half * kColsPer;
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 f = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    if (owner == z) *reinterpret_cast<float4*>(dst + c0 + j) = f;
-                    else st_async_f32x4(dst + c0 + j, (uint32_t)owner, f, &recv_bar);
-                }
+            for (int j = 0; j < kColsPer; j += 4) {
+                const float4 f = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                if (owner == z) *reinterpret_cast<float4*>(dst + j) = f;
+                else st_async_f32x4(dst + j, (uint32_t)owner, f, &recv_bar);
             }
         }
         if (alive) alive = mbar_wait_bounded(&recv_bar, 0, err, 16);
