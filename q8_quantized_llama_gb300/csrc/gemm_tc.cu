@@ -4,37 +4,38 @@
 // token", prefill 和 decode：同一个 forward，不同的路: many rows go to the
 // matrix-matrix kernel).
 //
-// Precision: split-TF32 ("3xTF32"). A dequantised weight d*q (f32, at most 18
-// significant bits) is exactly hi + lo with hi = w rounded to tf32 and
-// lo = w - hi (at most 8 bits, exact in tf32). An activation x is read by the
-// MMA as tf32 (its low 13 mantissa bits ignored: x_hi = x truncated) and
-// x_lo = x - x_hi is exact in f32 (below 2^-10 |x|; the MMA keeps its top 11
-// bits). Three MMAs per k-step, w_hi.x_hi + w_hi.x_lo + w_lo.x_hi, accumulate
-// in f32 in TMEM; the truncated x_lo and the dropped w_lo.x_lo leave each
-// product off by less than 2^-19 relative.
+// Precision: the int8 codes q of a Q8_0 block are exact in tf32, and the
+// block scale d is one number per (row, k-block), so the tensor cores compute
+// per k-block the block partial P = sum_k q.x with the activation split as
+// x = x_hi + x_lo (x_hi = the tensor core's truncated tf32 reading of x, x_lo
+// = x - x_hi exact in f32, of which the MMA keeps the top 11 bits): two MMAs
+// per k-step, f32 accumulation in TMEM. Accumulator warps then add d.P to the
+// running sums in registers. Each product q.x is off by less than 2^-20
+// relative (the truncated x_lo), plus one f32 rounding per block partial.
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
-// Q8_0 block; one 128-byte swizzle row of f32). Warp roles:
+// Q8_0 block; one 128-byte swizzle row of f32). Warp roles (18 warps):
 //  - producer warp: per k-block three tensor copies: the activation tile
 //    (2-D, 128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B
 //    layout), and the codes and scales of the CTA's four 32-row tiles (3-D
 //    views [tile][k-block][1 KiB or 64 B] of the packed weights, one box each;
-//    tiles past the matrix read as zeros). One copy instruction costs ~60 ns
-//    of issue, so the count per stage bounds the stage rate;
-//  - two groups of 8 converter warps, taking k-blocks in turn: dequantise the
-//    weights, split them into hi/lo and write them into tensor memory
-//    (tcgen05.st; A operand, row r in lane r), and write x_lo next to the
-//    activation tile in shared memory. A group's chain per k-block (loads,
-//    tensor-memory stores and their completion, proxy fence) is latency
-//    bound; two groups keep two k-blocks in conversion at once;
-//  - MMA warp: one thread issues the 12 MMAs of a k-block with A read from
-//    tensor memory and commits them to the stage's "done" barrier, which frees
-//    the stage for the producer.
-// Stages are handed on with mbarriers (no CTA-wide barrier in the k loop), so
-// copies, conversion and MMAs of different k-blocks overlap. Token tiles vary
-// fastest in the grid: the CTAs that share a weight tile run at the same time
-// and read it from DRAM once. The epilogue reads TMEM with tcgen05.ld (warp w
-// reads lanes 32*(w%4)) and applies the shared epilogues.
+//    tiles past the matrix read as zeros);
+//  - two groups of 4 converter warps, taking k-blocks in turn: write each
+//    row's 32 codes as f32 into tensor memory (tcgen05.st; A operand, row r in
+//    lane r) and x_lo beside the activation tile in shared memory (generic
+//    stores, then a proxy fence for the tensor core);
+//  - MMA warp: one thread issues the 8 MMAs of a k-block (A from tensor
+//    memory) into one of two block-partial buffers and commits them to the
+//    stage's "done" barrier (frees the stage for the producer) and to the
+//    buffer's "full" barrier;
+//  - 8 accumulator warps (4 lane quarters x 2 column halves): per k-block read
+//    the block partial, free the buffer, and add it times the row's d (read
+//    from global memory one block ahead) into 64 registers.
+// Stages and buffers are handed on with mbarriers (no CTA-wide barrier in the
+// k loop). Token tiles vary fastest in the grid: the CTAs that share a weight
+// tile run at the same time and read it from DRAM once. At the end the
+// accumulators return the tile to tensor memory and all 16 converter and
+// accumulator warps apply the epilogue, 32 token columns each.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

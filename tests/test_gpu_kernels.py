@@ -89,8 +89,9 @@ def _matmul_case(rows, k, m, seed):
     # f32 accumulation: the matrix-vector kernel sums 32-code blocks, then at
     # most k/256 blocks per warp, then 8 warp partials; the matrix-matrix
     # kernel sums the k products in one chain. Bound = (chain + 8) u sum|w x|.
-    # Rows > 16 run on the tensor cores in split-TF32: each product carries
-    # less than 2^-19 relative error on top of the f32 accumulation.
+    # Rows > 16 run on the tensor cores (codes times x split into tf32 hi and
+    # lo, block sums scaled by d): each product carries less than 2^-19
+    # relative error on top of the f32 accumulation.
     chain = (k // 256 + 40) if m == 1 else (k + 8)
     split = 2.0 ** -19 if m > 16 else 0.0
     tol = ((chain + 8) * U + split) * mag + 1e-30
@@ -153,10 +154,11 @@ def test_matmul_tensor_core_7b_prefill_shapes(rows, k):
 @pytest.mark.parametrize("rows,k,m", [(256, 512, 40), (4096, 256, 300)])
 def test_matmul_tensor_core_split_precision_one_hot(rows, k, m):
     """Weight rows with a single nonzero: every output is one product w * x
-    with no accumulation error, so the split-TF32 bound of a single product
-    (< 2^-19 relative) must hold element by element. A weight or activation
-    split that did not match the tensor core's reading of tf32 operands would
-    leave errors near 2^-11."""
+    with no accumulation error, so the tensor-core bound of a single product
+    (< 2^-19 relative) must hold element by element. An activation split that
+    did not match the tensor core's reading of tf32 operands, or a block
+    scale applied to the wrong row or block, would leave errors near 2^-11 or
+    worse."""
     B = binding()
     cols = (np.arange(rows) * 37 + 5) % k
     w = np.zeros((rows, k), np.float32)
