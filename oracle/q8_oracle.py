@@ -18,7 +18,7 @@ Sources, all candle 0.11.0 documentation pages:
   [OT] "生成一个 token" (candle / 01-overview / one-token)
   [SP] "速度" (pytorch-to-candle / 09-deploy / speed)
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   R1 Q8_0 block: the pages give only byte counts ([OT] "实验程序" file size,
      [OT] "读 GGUF" data offset, [SP] "CPU GGUF" 136.3 MiB). Blocks of 32
      along the input dim; d = max|w| / 127 in f32; q = round(w / d) with an
