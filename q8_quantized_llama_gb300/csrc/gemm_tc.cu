@@ -178,13 +178,6 @@ __device__ __forceinline__ void dequant16(const uint4& q, float d, float (&w)[16
     }
 }
 
-// w rounded to the nearest tf32 value (low 13 mantissa bits zero).
-__device__ __forceinline__ uint32_t tf32_rna_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent and the 10 mantissa bits of tf32
 
 // Epilogue of one output element pair/element (row r of W, token t).
