@@ -63,7 +63,7 @@ class Reader {
     bool pod(T* v) { return bytes(v, sizeof(T)); }
     bool str(std::string* s) {
         uint64_t n = 0;
-        if (!pod(&n) || n > (1ull << 30)) return false;
+        if (!pod(&n) || n > (1ull << 24)) return false;  // keys and string values: at most 16 MiB
         s->resize(n);
         return bytes(&(*s)[0], n);
     }
@@ -204,7 +204,11 @@ llama_q8_status check_tensor(const Gguf& g, const std::string& name, uint32_t ty
     for (size_t d = 2; d < t.dims.size(); ++d)
         if (t.dims[d] != 1) return LQ8_ERR_FORMAT;
     if (t.dims[0] != inner || o != outer) return LQ8_ERR_FORMAT;
-    if (g.data_offset + t.offset + tensor_bytes(t) > g.file_bytes) return LQ8_ERR_FORMAT;
+    // inside the file, without wrapping: extents are bounded by the checked hyperparameters
+    const uint64_t bytes = tensor_bytes(t);
+    if (g.data_offset > g.file_bytes || t.offset > g.file_bytes - g.data_offset ||
+        bytes > g.file_bytes - g.data_offset - t.offset)
+        return LQ8_ERR_FORMAT;
     return LQ8_OK;
 }
 
@@ -218,6 +222,9 @@ llama_q8_status config_from(const Gguf& g, llama_q8_config* c) {
         return LQ8_ERR_FORMAT;
     if (!get_int(g, "llama.attention.head_count_kv", &n_head_kv)) n_head_kv = n_head;
     if (n_layer <= 0 || n_embd <= 0 || n_head <= 0 || n_head_kv <= 0 || n_ff <= 0 || n_embd % n_head)
+        return LQ8_ERR_FORMAT;
+    // bounds that keep every size product far from overflow (llama_q8_load checks the shapes it runs)
+    if (n_layer > 4096 || n_embd > (1 << 20) || n_ff > (1 << 22) || n_head > 4096 || n_head_kv > n_head)
         return LQ8_ERR_FORMAT;
     std::memset(c, 0, sizeof(*c));
     c->n_layer = (int32_t)n_layer;
@@ -236,7 +243,9 @@ llama_q8_status config_from(const Gguf& g, llama_q8_config* c) {
                         ? llama_q8_rope_style_for_arch(arch->second.str.c_str())
                         : 0;
     auto e = g.tensors.find("token_embd.weight");
-    if (e == g.tensors.end() || e->second.dims.size() < 2) return LQ8_ERR_FORMAT;
+    if (e == g.tensors.end() || e->second.dims.size() < 2 || e->second.dims[1] == 0 ||
+        e->second.dims[1] > (1u << 24))
+        return LQ8_ERR_FORMAT;
     c->n_vocab = (int32_t)e->second.dims[1];
     c->tied_output = g.tensors.count("output.weight") ? 0 : 1;
     const uint64_t h = (uint64_t)n_embd, V = (uint64_t)c->n_vocab, F = (uint64_t)n_ff;

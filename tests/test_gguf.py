@@ -131,6 +131,40 @@ def test_errors(B, tmp_path):
     assert B.gguf_config_status(str(p))[0] == B.LQ8_ERR_FORMAT
 
 
+def test_truncated_and_corrupted_files_fail_cleanly(B, tmp_path):
+    """Every truncation of a small file and seeded byte corruptions of its
+    header give a status (never a crash or an out-of-file read); a corrupted
+    tensor offset near 2^64 is rejected rather than wrapping the bounds check."""
+    p = tmp_path / "g.gguf"
+    off = _tiny_file(p)
+    raw = p.read_bytes()
+    ok = B.gguf_config_status(str(p))[0]
+    assert ok == B.LQ8_OK
+    for cut in list(range(0, off, 97)) + [off - 1, off + 1, len(raw) - 1]:
+        p.write_bytes(raw[:cut])
+        assert B.gguf_config_status(str(p))[0] in (B.LQ8_ERR_FORMAT, B.LQ8_ERR_UNSUPPORTED), cut
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        bad = bytearray(raw)
+        for _ in range(int(rng.integers(1, 4))):
+            i = int(rng.integers(4, off))
+            bad[i] = int(rng.integers(0, 256))
+        p.write_bytes(bytes(bad))
+        assert B.gguf_config_status(str(p))[0] in (B.LQ8_OK, B.LQ8_ERR_FORMAT, B.LQ8_ERR_UNSUPPORTED)
+    # the last tensor's offset field (the 8 bytes before the header padding) set near 2^64
+    tensors = G.model_tensors(TINY, zero_blobs(dict(TINY, tied_output=0)))
+    huge = bytearray(raw)
+    name = tensors[-1][0].encode()
+    pos = raw.rfind(name)
+    assert pos > 0
+    rank_at = pos + len(name)
+    rank = int.from_bytes(raw[rank_at:rank_at + 4], "little")
+    off_at = rank_at + 4 + 8 * rank + 4
+    huge[off_at:off_at + 8] = (2**64 - 64).to_bytes(8, "little")
+    p.write_bytes(bytes(huge))
+    assert B.gguf_config_status(str(p))[0] == B.LQ8_ERR_FORMAT
+
+
 @pytest.mark.gpu
 def test_model_from_file_equals_model_from_arrays(B, tmp_path):
     from oracle import q8_oracle as O
