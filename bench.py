@@ -60,6 +60,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--cpu-baseline-threads", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode", "decode7b", "prefill", "prefill7b"],
                    default=None,
                    help="run one kernel workload only (used for ncu captures)")
@@ -213,8 +214,9 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline_worker(seconds: float):
-    """Runs in a fresh interpreter: the oracle on a bounded sample of the workload."""
+def cpu_baseline_worker(seconds: float, threads: int = 0):
+    """Runs in a fresh interpreter: the oracle on a bounded sample of the
+    workload (threads > 0: the BLAS/OpenMP thread count the parent set)."""
     from q8_quantized_llama_gb300 import synth
     O, cfg, model = oracle_model()
     prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
@@ -228,21 +230,26 @@ def cpu_baseline_worker(seconds: float):
         d_s += time.perf_counter() - t0
         pos += 1
         n += 1
-    print(json.dumps({"value": n / d_s, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+    print(json.dumps({"value": n / d_s, "unit": "tokens/s", "cores": threads or cpu_threads(), "kind": "oracle",
                       "prefill_tok_s": PROMPT_LEN / p_s,
                       "sample": f"135M Q8_0 oracle (numpy f64): one 203-token prefill and the first {n} of the "
                                 f"128 greedy decode steps"}))
 
 
-def run_cpu_baseline(seconds: float):
+def run_cpu_baseline(seconds: float, threads: int = 0):
+    """The oracle timed in a subprocess on all host cores, or (threads > 0) with
+    the BLAS and OpenMP pools held to that many threads."""
     env = dict(os.environ)
+    if threads > 0:
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[var] = str(threads)
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
-                        "--cpu-baseline-seconds", str(seconds)], capture_output=True, text=True, env=env,
-                       timeout=600)
+                        "--cpu-baseline-seconds", str(seconds), "--cpu-baseline-threads", str(threads)],
+                       capture_output=True, text=True, env=env, timeout=600)
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
             return json.loads(line)
-    return {"value": None, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+    return {"value": None, "unit": "tokens/s", "cores": threads or cpu_threads(), "kind": "oracle",
             "sample": "failed: " + r.stderr[-300:]}
 
 
@@ -665,6 +672,8 @@ def run_ours(args):
         }
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)
+            # the same oracle on one thread, a shorter sample (context for the all-cores figure)
+            out["cpu_baseline_single_thread"] = run_cpu_baseline(min(10.0, args.cpu_baseline_seconds / 2), threads=1)
     model.close()
     if world > 1:
         import torch.distributed as dist
@@ -676,7 +685,7 @@ def run_ours(args):
 def main():
     args = parse_args()
     if args.cpu_baseline_worker:
-        cpu_baseline_worker(args.cpu_baseline_seconds)
+        cpu_baseline_worker(args.cpu_baseline_seconds, args.cpu_baseline_threads)
         return
     if args.impl == "reference":
         run_reference(args)
