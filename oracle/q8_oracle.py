@@ -218,7 +218,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray | No
     kr = repeat_kv(np.asarray(k, np.float32), n_rep).astype(np.float64)
     vr = repeat_kv(np.asarray(v, np.float32), n_rep).astype(np.float64)
     q64 = np.asarray(q, np.float32).astype(np.float64)
-    att = np.einsum("thd,jhd->htj", q64, kr) / math.sqrt(hd)
+    # scores[h, t, j] = q[t, h] . k[j, h] / sqrt(hd): one f64 matrix product per head
+    att = np.matmul(q64.transpose(1, 0, 2), kr.transpose(1, 2, 0)) / math.sqrt(hd)
     if mask is not None:
         if mask.shape != (T, kv_len):
             raise ValueError(
@@ -227,7 +228,8 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, mask: np.ndarray | No
     m = np.max(att, axis=-1, keepdims=True)
     e = np.exp(att - m)
     p = e / np.sum(e, axis=-1, keepdims=True)
-    o = np.einsum("htj,jhd->thd", p, vr)
+    # o[t, h] = sum_j p[h, t, j] v[j, h]
+    o = np.matmul(p, vr.transpose(1, 0, 2)).transpose(1, 0, 2)
     return o.astype(np.float32)
 
 
