@@ -337,9 +337,9 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
  * [head_dim]; out[n_head][head_dim]. One cluster of 16 CTAs per KV head (8
  * when the clusters of all KV heads cannot be resident together) splits the
  * positions, streams K/V rows with bulk async copies and merges its partial
- * results through distributed shared memory, so no scratch memory is needed. k_cache and v_cache must be
- * 16-byte aligned (LQ8_ERR_ARG otherwise); other errors as
- * llama_q8_attention. Enqueues on `stream` and returns. */
+ * results through distributed shared memory, so no scratch memory is needed. q, k_cache,
+ * v_cache and out must be 16-byte aligned (LQ8_ERR_ARG otherwise); other
+ * errors as llama_q8_attention. Enqueues on `stream` and returns. */
 llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache,
                                           int32_t kv_len, int32_t n_head, int32_t n_head_kv,
                                           int32_t head_dim, int32_t cache_stride, float* out,
@@ -360,7 +360,9 @@ llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, 
  * scratch need exceeds 2 MiB (n_head_kv * ceil(cache_stride/64) * group *
  * (head_dim + 2) floats, plus counters) return LQ8_ERR_UNSUPPORTED, as do
  * head_dim other than 64/128 and groups above 8; kv_len > cache_stride is
- * LQ8_ERR_CTX. The first call on each device looks up the array's device
+ * LQ8_ERR_CTX. q, k_cache, v_cache and out must be 16-byte aligned (the
+ * kernel moves them in 16-byte pieces): LQ8_ERR_ARG otherwise, before any
+ * launch. The first call on each device looks up the array's device
  * address (and sets the kernel's shared-memory limit): make that first call
  * before any stream capture. All calls share the one array, so calls that
  * overlap on the GPU (other streams, other threads) race and give wrong

@@ -3,16 +3,24 @@
 // Decode (T = 1): the fused single-token kernel the pages describe for the
 // Metal path ("生成一个 token", prefill 和 decode：同一个 forward，不同的路:
 // q k^T, scale, softmax and the product with v in one kernel, the query heads
-// of a group sharing their KV head inside it). Here the cache is split into
-// 64-position chunks, one CTA per (KV head, chunk), all query heads of the
-// group handled by that CTA so each K/V row is read from HBM once; the last
-// CTA of a KV head (completion counter) merges the chunk results with the
-// usual max/sum rescaling. No repeat_kv copy and no cat.
+// of a group sharing their KV head inside it). Two forms, neither with a
+// repeat_kv copy or a cat:
+//  - attn_decode_kernel (split-KV with a workspace): the cache is split into
+//    64-position chunks, one CTA per (KV head, chunk), all query heads of the
+//    group handled by that CTA so each K/V row is read from HBM once; the last
+//    CTA of a KV head (completion counter) merges the chunk results with the
+//    usual max/sum rescaling;
+//  - attn_decode_cluster_kernel (the decode step's form, no scratch): one
+//    thread-block cluster per KV head splits the positions, streams K/V rows
+//    with bulk async copies and merges its partials through distributed
+//    shared memory (optionally applying the head's W_o column slice).
 //
-// Prefill (T > 1): a causal flash-style kernel, one CTA per (query head,
-// 32-query tile), streaming 32-position K/V tiles through shared memory with
-// an online softmax; query t sees positions <= index_pos + t ("量化 llama 的一次
-// 前向", forward：mask 什么时候建 — the mask is a predicate here, never built).
+// Prefill (T > 1): attn_prefill_kernel<HD, RT>, a causal flash-style kernel,
+// one CTA per (query head, 16*RT query rows) with 256 threads as a 16 x 16
+// grid, register-blocked scores, K/V tiles of 64 positions (head_dim 64) or
+// 32 (head_dim 128) double-buffered in shared memory, online softmax; query t
+// sees positions <= index_pos + t ("量化 llama 的一次前向", forward：mask
+// 什么时候建 — the mask is a predicate here, never built).
 #include <mutex>
 
 #include "attn_core.cuh"
@@ -1248,7 +1256,7 @@ cudaError_t noalloc_scratch(void** out) {
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
-        err = init_attention_attributes();
+        err = ensure_kernel_attributes();
         if (err != cudaSuccess) return err;
         g_noalloc_ptr[dev] = p;
     }
@@ -1267,6 +1275,8 @@ extern "C" llama_q8_status llama_q8_attention_decode_noalloc(const float* q, con
     if (!q || !k_cache || !v_cache || !out || kv_len <= 0 || n_head <= 0 || n_head_kv <= 0 ||
         n_head % n_head_kv || cache_stride <= 0)
         return LQ8_ERR_ARG;
+    // the kernel reads q, K and V and writes out as 16-byte vectors
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out) & 15) return LQ8_ERR_ARG;
     if (kv_len > cache_stride) return LQ8_ERR_CTX;
     if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
     if (n_head / n_head_kv > kMaxGroup) return LQ8_ERR_UNSUPPORTED;

@@ -18,6 +18,7 @@
 #include <fcntl.h>
 #include <unistd.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -159,10 +160,19 @@ llama_q8_status parse(const char* path, Gguf* g) {
             if (ok) g->tensors[name] = t;
         }
         if (!ok) break;
+        // general.alignment, when present, must be an integer power of two no
+        // larger than 64 KiB: anything else would make the rounding below
+        // undefined or let it wrap into the header.
         uint64_t align = 32;
         auto a = g->kv.find("general.alignment");
-        if (a != g->kv.end() && a->second.type != kString && a->second.type != kArray && a->second.num >= 1)
-            align = (uint64_t)a->second.num;
+        if (a != g->kv.end()) {
+            const double v = a->second.num;
+            if (a->second.type == kString || a->second.type == kArray || !(v >= 1.0 && v <= 65536.0) ||
+                v != (double)(uint64_t)v)
+                break;
+            align = (uint64_t)v;
+            if (align & (align - 1)) break;
+        }
         const uint64_t end = r.pos();
         g->data_offset = (end + align - 1) / align * align;
         if (std::fseek(f, 0, SEEK_END) != 0) break;
@@ -173,10 +183,16 @@ llama_q8_status parse(const char* path, Gguf* g) {
     return st;
 }
 
+// An integer-valued key. Values that are not finite, not integral or beyond
+// +-2^53 (where a double stops holding every integer) are rejected before the
+// conversion, which would otherwise be undefined.
 bool get_int(const Gguf& g, const std::string& key, int64_t* out) {
     auto it = g.kv.find(key);
     if (it == g.kv.end() || it->second.type == kString || it->second.type == kArray) return false;
-    *out = (int64_t)it->second.num;
+    const double v = it->second.num;
+    if (!(v >= -9007199254740992.0 && v <= 9007199254740992.0)) return false;
+    if (v != std::trunc(v)) return false;
+    *out = (int64_t)v;
     return true;
 }
 
@@ -220,7 +236,10 @@ llama_q8_status config_from(const Gguf& g, llama_q8_config* c) {
     if (!get_int(g, "llama.block_count", &n_layer) || !get_int(g, "llama.embedding_length", &n_embd) ||
         !get_int(g, "llama.attention.head_count", &n_head) || !get_int(g, "llama.feed_forward_length", &n_ff))
         return LQ8_ERR_FORMAT;
-    if (!get_int(g, "llama.attention.head_count_kv", &n_head_kv)) n_head_kv = n_head;
+    if (!get_int(g, "llama.attention.head_count_kv", &n_head_kv)) {
+        if (g.kv.count("llama.attention.head_count_kv")) return LQ8_ERR_FORMAT;  // present but not an integer
+        n_head_kv = n_head;
+    }
     if (n_layer <= 0 || n_embd <= 0 || n_head <= 0 || n_head_kv <= 0 || n_ff <= 0 || n_embd % n_head)
         return LQ8_ERR_FORMAT;
     // bounds that keep every size product far from overflow (llama_q8_load checks the shapes it runs)

@@ -107,6 +107,8 @@ cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int e
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                            int* err, cudaStream_t s);
 cudaError_t init_gemm_tc_attributes();
+// Every kernel's attributes on the current device, once per device (runtime.cu).
+cudaError_t ensure_kernel_attributes();
 // Rows above which the matrix-matrix product runs on the tensor cores.
 constexpr int kTensorCoreMinRows = 16;
 inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,

@@ -24,14 +24,15 @@ using namespace lq8;
 namespace lq8 {
 cudaError_t init_gemv_attributes();
 cudaError_t init_attention_attributes();
-}  // namespace lq8
 
 namespace {
-
 constexpr int kMaxDevices = 64;
 std::mutex g_init_mu;
 bool g_init_done[kMaxDevices] = {};
+}  // namespace
 
+// Kernel attributes (shared-memory limits, cluster permissions) of every
+// kernel, set once per device under one lock.
 cudaError_t ensure_kernel_attributes() {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -45,6 +46,9 @@ cudaError_t ensure_kernel_attributes() {
     if (err == cudaSuccess) g_init_done[dev] = true;
     return err;
 }
+}  // namespace lq8
+
+namespace {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -1126,8 +1130,8 @@ llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, 
     if (kv_len > cache_stride) return LQ8_ERR_CTX;
     if (head_dim != 64 && head_dim != 128) return LQ8_ERR_UNSUPPORTED;
     if (n_head / n_head_kv > 8) return LQ8_ERR_UNSUPPORTED;
-    // K/V rows are fetched by bulk async copies: 16-byte aligned caches only
-    if (((uintptr_t)k_cache | (uintptr_t)v_cache) & 15) return LQ8_ERR_ARG;
+    // K/V rows and q are fetched by bulk async copies or 16-byte loads: 16-byte aligned buffers only
+    if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out) & 15) return LQ8_ERR_ARG;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
     cudaError_t err = launch_attn_decode_cluster(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride,
                                                  kv_len, nullptr, out, false, nullptr, (cudaStream_t)stream);

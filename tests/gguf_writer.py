@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import struct
 
-T_U32, T_I32, T_F32, T_BOOL, T_STRING, T_ARRAY, T_U64 = 4, 5, 6, 7, 8, 9, 10
+T_U32, T_I32, T_F32, T_BOOL, T_STRING, T_ARRAY, T_U64, T_F64 = 4, 5, 6, 7, 8, 9, 10, 12
 TENSOR_F32, TENSOR_Q5_0, TENSOR_Q8_0 = 0, 6, 8
 
 
@@ -27,6 +27,8 @@ def _value(t: int, v) -> bytes:
         return struct.pack("<Q", v)
     if t == T_F32:
         return struct.pack("<f", v)
+    if t == T_F64:
+        return struct.pack("<d", v)
     if t == T_BOOL:
         return struct.pack("<B", 1 if v else 0)
     if t == T_STRING:

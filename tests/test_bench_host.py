@@ -38,10 +38,15 @@ def test_decode_bytes_7b():
 
 
 def test_hbm_peak_reads_the_measured_file(tmp_path, monkeypatch):
+    # a measured-peaks file with a known copy bandwidth: the measured branch
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6543.2, "bf16_tflops": 1900.0}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peak, kind = bench.hbm_peak()
-    d = json.load(open(bench.os.path.join(bench.ROOT, "MEASURED_PEAKS.json")))
-    assert kind == "measured" and peak == pytest.approx(float(d["hbm_gbs"]))
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))   # no file: the stated fallback
+    assert kind == "measured" and peak == pytest.approx(6543.2)
+    # no file: the stated fallback
+    empty = tmp_path / "empty"
+    empty.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(empty))
     peak, kind = bench.hbm_peak()
     assert kind == "fallback" and peak == bench.FALLBACK_HBM_GBS
 

@@ -97,6 +97,32 @@ def test_alignment_key(B, tmp_path):
     assert got_off == off and off % 256 == 0 and n == 2 * 9 + 2
 
 
+def test_bad_alignment_and_integer_keys_are_rejected(B, tmp_path):
+    """general.alignment must be an integer power of two up to 64 KiB, and the
+    integer hyperparameters finite integers within +-2^53; anything else is a
+    format error, never an undefined conversion or a wrapped data offset."""
+    def status(kv):
+        p = tmp_path / "al.gguf"
+        _tiny_file(p, kv=kv)
+        return B.gguf_config_status(str(p))[0]
+
+    base = G.llama_kv(TINY)
+    for bad in ((G.T_U32, 0), (G.T_U32, 48), (G.T_U32, 1 << 17), (G.T_U64, 2**64 - 1),
+                (G.T_F32, 32.5), (G.T_F32, float("inf")), (G.T_F32, float("nan")), (G.T_F64, 2.0**63)):
+        assert status(base + [("general.alignment", bad[0], bad[1])]) == B.LQ8_ERR_FORMAT, bad
+    assert status(base + [("general.alignment", G.T_STRING, "32")]) == B.LQ8_ERR_FORMAT
+
+    def with_key(key, t, v):
+        return [x for x in base if x[0] != key] + [(key, t, v)]
+
+    for key in ("llama.block_count", "llama.embedding_length", "llama.attention.head_count_kv"):
+        for t, v in ((G.T_F32, float("nan")), (G.T_F32, float("inf")), (G.T_F32, 2.5), (G.T_F64, 1e300),
+                     (G.T_F64, -1e300)):
+            assert status(with_key(key, t, v)) == B.LQ8_ERR_FORMAT, (key, t, v)
+    # an integral value given as a float is still an integer
+    assert status(with_key("llama.block_count", G.T_F32, 2.0)) == B.LQ8_OK
+
+
 def test_extra_metadata_arrays_are_skipped(B, tmp_path):
     kv = G.llama_kv(TINY) + [("tokenizer.ggml.tokens", G.T_ARRAY, (G.T_STRING, ["a", "bb", "<s>"] * 50)),
                              ("tokenizer.ggml.token_type", G.T_ARRAY, (G.T_I32, list(range(150)))),
