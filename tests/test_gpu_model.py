@@ -178,24 +178,35 @@ def test_device_resident_api(m135):
     assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
 
 
-@pytest.mark.parametrize("variant", ["front", "three", "layer"])
-def test_fused_decode_kernels_at_long_context(m135, variant):
-    """Decode steps at positions near the 4096 limit: the one-kernel layer and
-    the fused layer front give the logits and tokens of the five-kernel
-    layer."""
-    model, layered = m135[variant], m135["layered"]
-    prompt = synth.prompt_ids(3900, V, 6)
-    a = model.forward(prompt, 0)
-    b = layered.forward(prompt, 0)
-    ok, err, bound = logits_close(a, b)
-    assert ok, (err, bound)
-    tok = int(np.argmax(a))
-    pos = len(prompt)
-    for _ in range(4):
-        a = model.forward([tok], pos)
-        b = layered.forward([tok], pos)
-        ok, err, bound = logits_close(a, b)
-        assert ok, (pos, err, bound)
-        assert int(np.argmax(a)) == int(np.argmax(b))
-        tok = int(np.argmax(a))
+LONG_PROMPT = 3900
+
+
+@pytest.fixture(scope="module")
+def long_run(m135):
+    """The oracle's greedy run from a 3900-token prompt to the end of the
+    4096-position cache: prefill, then decode steps at positions 3900..4095."""
+    prompt = synth.prompt_ids(LONG_PROMPT, V, 6)
+    ids, logits = m135["oracle"].generate(prompt, CFG["max_seq"] - LONG_PROMPT)
+    return prompt, ids, logits
+
+
+def test_long_context_decode_matches_oracle(either, long_run):
+    """Decode steps near the 4096-position limit ([QL] from_gguf: the rotary
+    table and the cache end at 4096) against the oracle, every step: logits
+    within tolerance and identical greedy tokens, up to the last position."""
+    model, _ = either
+    prompt, ref_ids, ref_logits = long_run
+    logits = model.forward(prompt, 0)
+    ok, err, bound = logits_close(logits, ref_logits[0])
+    assert ok, ("prefill", err, bound)
+    got = [int(np.argmax(logits))]
+    pos = LONG_PROMPT
+    for step in range(1, len(ref_logits)):
+        logits = model.forward([got[-1]], pos)
         pos += 1
+        ok, err, bound = logits_close(logits, ref_logits[step])
+        assert ok, (pos - 1, err, bound)
+        got.append(int(np.argmax(logits)))
+        assert got[-1] == ref_ids[step], (pos - 1, got[-1], ref_ids[step])
+    assert model.cache_len() == CFG["max_seq"]
+    assert got == ref_ids
