@@ -41,13 +41,11 @@ SEED = 0
 PAGES_DECODE_MS = 7.40
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# decode step's kernels, from the ncu captures summarised under profiles/ (the
-# kernel sources they were taken on are the committed ones). The layer front's
-# figure is at kv_len 205; its K/V part grows by 1536 bytes per position.
-NCU_TRAFFIC = {
-    "layer_front_qkv_attn_o": {"bytes": 1322752, "kv_len": 205, "profile": "profiles/layer_front_135m_decode.md"},
-    "decode_mlp": {"bytes": 2865920, "kv_len": None, "profile": "profiles/decode_mlp_135m.md"},
-}
+# decode step's kernels from one ncu capture of the current kernel sources
+# (135M model, decode steps after the 203-token prompt, kv_len stated); the
+# K/V part grows by n_kv * head_dim * 8 bytes per cached position.
+NCU_TRAFFIC = {}
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops x max SM clock
 L2_BYTES = 126 * 2 ** 20
 
 
@@ -61,7 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--cpu-baseline-threads", type=int, default=0, help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode", "decode7b", "prefill", "prefill7b"],
+    p.add_argument("--cpu-baseline-config", choices=["c0", "c1", "c4"], default="c1", help=argparse.SUPPRESS)
+    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode", "decode7b", "prefill", "prefill7b",
+                                      "sweep", "attnprefill", "profile"],
                    default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
@@ -186,12 +186,13 @@ class ClockSampler:
 # CPU oracle legs
 # ----------------------------------------------------------------------------
 
-def oracle_model():
+def oracle_model(big: bool = False):
+    """The oracle's model: the 135M shape (seed 0), or the 7B shape (seed 1)."""
     from oracle import q8_oracle as O
     from q8_quantized_llama_gb300 import synth
-    cfg = dict(synth.MODEL_135M)
+    cfg = dict(synth.MODEL_7B if big else synth.MODEL_135M)
     t = {}
-    for name, w, kind in synth.iter_model_weights_f32(cfg, SEED):
+    for name, w, kind in synth.iter_model_weights_f32(cfg, 1 if big else SEED):
         t[name] = O.quantize_q8_0(w) if kind == "matrix" else w
     return O, cfg, O.ModelWeights(cfg, t, weight_cache="f64")
 
@@ -214,53 +215,75 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline_worker(seconds: float, threads: int = 0):
-    """Runs in a fresh interpreter: the oracle on a bounded sample of the
-    workload (threads > 0: the BLAS/OpenMP thread count the parent set)."""
+# The oracle's configurations: model, prompt length, decode steps of the full
+# run, and the decode steps of the bounded sample (C4: prefill + the first 16
+# decode steps; the full 256 would take far longer than a bench run).
+ORACLE_CONFIGS = {
+    "c0": (False, 13, 20, 20),
+    "c1": (False, PROMPT_LEN, DECODE_STEPS, DECODE_STEPS),
+    "c4": (True, 512, 256, 16),
+}
+
+
+def cpu_baseline_worker(seconds: float, threads: int = 0, config: str = "c1"):
+    """Runs in a fresh interpreter: the oracle on a bounded sample of one
+    configuration (threads > 0: the BLAS/OpenMP thread count the parent set)."""
     from q8_quantized_llama_gb300 import synth
-    O, cfg, model = oracle_model()
-    prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
+    big, n_prompt, n_full, n_sample = ORACLE_CONFIGS[config]
+    O, cfg, model = oracle_model(big)
+    prompt = synth.prompt_ids(n_prompt, cfg["n_vocab"], 1 if big else SEED)
     t_start = time.perf_counter()
-    p_s, _ = oracle_step(O, model, prompt, 0)
+    t0 = time.perf_counter()
     nxt = O.argmax_lowest(model.forward(prompt, 0))
-    pos, n, d_s = PROMPT_LEN, 0, 0.0
-    while n < DECODE_STEPS and time.perf_counter() - t_start < seconds:
+    p_s = time.perf_counter() - t0
+    pos, n, d_s = n_prompt, 0, 0.0
+    while n < n_sample and time.perf_counter() - t_start < seconds:
         t0 = time.perf_counter()
         nxt = O.argmax_lowest(model.forward([nxt], pos))
         d_s += time.perf_counter() - t0
         pos += 1
         n += 1
-    print(json.dumps({"value": n / d_s, "unit": "tokens/s", "cores": threads or cpu_threads(), "kind": "oracle",
-                      "prefill_tok_s": PROMPT_LEN / p_s,
-                      "sample": f"135M Q8_0 oracle (numpy f64): one 203-token prefill and the first {n} of the "
-                                f"128 greedy decode steps"}))
+    name = "7B" if big else "135M"
+    print(json.dumps({"value": n / d_s if n else None, "unit": "tokens/s", "cores": threads or cpu_threads(),
+                      "kind": "oracle", "config": config, "prefill_tok_s": n_prompt / p_s,
+                      "decode_ms_per_token": 1000 * d_s / n if n else None,
+                      "sample": f"{name} Q8_0 oracle (numpy f64): one {n_prompt}-token prefill and the first {n} "
+                                f"of the {n_full} greedy decode steps"}))
 
 
-def run_cpu_baseline(seconds: float, threads: int = 0):
+def run_cpu_baseline(seconds: float, threads: int = 0, config: str = "c1", timeout: float = 600.0):
     """The oracle timed in a subprocess on all host cores, or (threads > 0) with
     the BLAS and OpenMP pools held to that many threads."""
     env = dict(os.environ)
     if threads > 0:
         for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
             env[var] = str(threads)
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
-                        "--cpu-baseline-seconds", str(seconds), "--cpu-baseline-threads", str(threads)],
-                       capture_output=True, text=True, env=env, timeout=600)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker",
+                            "--cpu-baseline-seconds", str(seconds), "--cpu-baseline-threads", str(threads),
+                            "--cpu-baseline-config", config],
+                           capture_output=True, text=True, env=env, timeout=timeout)
+    except subprocess.TimeoutExpired:
+        return {"value": None, "unit": "tokens/s", "cores": threads or cpu_threads(), "kind": "oracle",
+                "config": config, "sample": f"not finished within {timeout:.0f} s"}
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
             return json.loads(line)
     return {"value": None, "unit": "tokens/s", "cores": threads or cpu_threads(), "kind": "oracle",
-            "sample": "failed: " + r.stderr[-300:]}
+            "config": config, "sample": "failed: " + r.stderr[-300:]}
 
 
 def run_reference(args):
+    """The oracle as it stands on the workload of the headline metric: each
+    step one 203-token prefill and all 128 greedy decode steps (decode
+    tokens/s over the timed steps)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     from q8_quantized_llama_gb300 import synth
     O, cfg, model = oracle_model()
     prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
-    n_dec = 2
+    n_dec = DECODE_STEPS
     for _ in range(args.warmup):
         oracle_step(O, model, prompt, n_dec)
     pre, dec = [], []
@@ -269,14 +292,15 @@ def run_reference(args):
         pre.append(p_s)
         dec.append(d_s)
     value = n_dec * args.steps / sum(dec)
-    sample = (f"135M Q8_0 oracle (numpy f64) per step: one 203-token prefill + the first {n_dec} of the 128 "
-              f"greedy decode steps")
+    sample = (f"135M Q8_0 oracle (numpy f64), each step the whole workload: one 203-token prefill + all "
+              f"{n_dec} greedy decode steps")
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1000 * (sum(pre) + sum(dec)) / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": "135M-shaped Q8_0 Llama seed 0, 203-token random prompt prefill + greedy decode",
-                      "prompt": PROMPT_LEN, "decode_steps_per_step": n_dec},
+           "config": {"workload": "135M-shaped Q8_0 Llama (30x576, 9/3 heads, FFN 1536, vocab 49152, seed 0): "
+                                  "203-token random prompt prefill + 128 greedy decode steps, fresh KV cache",
+                      "prompt": PROMPT_LEN, "decode_steps": n_dec},
            "decode_ms_per_token": 1000 * sum(dec) / (n_dec * args.steps),
            "prefill_tok_s": PROMPT_LEN * args.steps / sum(pre),
            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
@@ -289,8 +313,8 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def gpu_model(torch, B, synth, device):
-    cfg = dict(synth.MODEL_135M)
+def gpu_model(torch, B, synth, device, head_splits=0):
+    cfg = dict(synth.MODEL_135M, head_splits=head_splits)
     t = {}
     for name, w, kind in synth.iter_model_weights_f32(cfg, SEED):
         dw = torch.from_numpy(w).to(device)
@@ -378,7 +402,7 @@ def prefill_only(torch, B, synth, device, args, big: bool):
     return out
 
 
-def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3):
+def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=256, reps=3):
     """Greedy decode of the Llama-7B-shaped Q8_0 model (32 x 4096, 32/8 heads of
     128, FFN 14336, vocab 32000, untied head) after a 512-token prefill: the
     decode step streams 7.55 GB of weights, so this is where the matrix-vector
@@ -410,6 +434,10 @@ def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3
         torch.cuda.synchronize()
         pre.append(e[0].elapsed_time(e[1]))
         dec.append(e[1].elapsed_time(e[2]) / n_decode)
+    # per-kernel in-graph times: the instrumented graph over 64 steps after the prompt
+    model.prefill_async(d_prompt, prompt_len, 0, d_next)
+    model.sync()
+    fams, prof_step_us = decode_timeline(model, cfg, 64, peak)
     model.close()
     torch.cuda.empty_cache()
     ms = statistics.median(dec)
@@ -418,7 +446,8 @@ def decode_7b(torch, B, synth, device, peak, prompt_len=512, n_decode=64, reps=3
     return {"workload": f"7B-shaped Q8_0 Llama, {prompt_len}-token prefill + {n_decode} greedy decode steps",
             "decode_ms_per_token": ms, "decode_tok_s": 1000.0 / ms, "prefill_ms": statistics.median(pre),
             "prefill_tok_s": prompt_len / (statistics.median(pre) / 1000),
-            "weights_bytes": w, "kv_bytes_mean": kv, "roofline_ms": roof_ms, "frac": roof_ms / ms}
+            "weights_bytes": w, "kv_bytes_mean": kv, "roofline_ms": roof_ms, "frac": roof_ms / ms,
+            "instrumented_step_us": prof_step_us, "kernels": fams}
 
 
 def gemv_7b_roofline(torch, B, synth, device, peak):
@@ -497,6 +526,129 @@ def gemm_microbench(torch, B, synth, device):
         del packed, x, y
         torch.cuda.empty_cache()
     return out
+
+
+def linear_sweep(torch, B, synth, device, peak):
+    """The Q8_0 linear sweep: x [rows, K] (N(0,1) f32) times each 135M
+    projection shape at rows 1, 8 and 203 — [576->576] (q, o), [576->192]
+    (k, v), [576->1536] (gate, up), [1536->576] (down), [576->49152] (lm_head)
+    — plus the 7B shapes [1,4096]x[4096,4096] and x[4096,14336]. Each timed
+    launch reads its own copy of the weights, rotating over enough copies to
+    exceed L2 (>= 256 MB), so the weights stream from HBM; rows = 1 launches
+    are chained the way the decode step chains them. GB/s counts the algorithmic
+    bytes (N*K*34/32 + 4*K*rows + 4*N*rows); rows = 203 also TFLOP/s."""
+    out = []
+    s = torch.cuda.current_stream()
+    shapes = [(r, n, k) for r in (1, 8, 203) for n, k in ((576, 576), (192, 576), (1536, 576), (576, 1536),
+                                                            (49152, 576))]
+    shapes += [(1, 4096, 4096), (1, 14336, 4096)]
+    for rows, n, k in shapes:
+        w = synth.weight_matrix_f32(n, k, 9, stream=n + k)
+        dw = torch.from_numpy(w).to(device)
+        q = torch.empty((n, k // 32 * 34), dtype=torch.uint8, device=device)
+        B.llama_q8_quantize(dw, n, k, q)
+        nbytes = B.llama_q8_packed_bytes(n, k)
+        ncopy = max(2, min(1024, -(-256 * 2 ** 20 // nbytes)))
+        packed = torch.empty((ncopy, nbytes), dtype=torch.uint8, device=device)
+        for c in range(ncopy):
+            B.llama_q8_pack(q, n, k, packed[c])
+        del dw, q
+        x = torch.from_numpy(synth.normal_f32((rows, k), 9, 2)).to(device)
+        y = torch.empty((rows, n), dtype=torch.float32, device=device)
+        flags = B.LQ8_MATMUL_EARLY_WEIGHTS if rows == 1 else 0
+        launches = max(ncopy, 200) if rows == 1 else max(ncopy, 50)
+        for i in range(min(ncopy, 16)):
+            B.llama_q8_matmul_ex(packed[i], n, k, x, rows, y, flags, s.cuda_stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for i in range(launches):
+            B.llama_q8_matmul_ex(packed[i % ncopy], n, k, x, rows, y, flags, s.cuda_stream)
+        e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000 / launches
+        algo = n * k * 34 / 32 + 4 * k * rows + 4 * n * rows
+        rec = {"shape": f"[{rows},{k}]x[{k},{n}]", "us": us, "gbs": algo / (us * 1e-6) / 1e9,
+               "frac": algo / (us * 1e-6) / 1e9 / peak, "weight_copies": ncopy}
+        if rows == 203:
+            rec["tflops"] = 2.0 * rows * n * k / (us * 1e-6) / 1e12
+        out.append(rec)
+        del packed, x, y
+        torch.cuda.empty_cache()
+    return out
+
+
+def attention_prefill_bench(torch, B, synth, device):
+    """Causal prefill attention (llama_q8_attention, T > 1): T = 203 at
+    position 0 and T = 64 at position 512, at the 135M shape (9/3 heads of 64)
+    and the 7B shape (32/8 heads of 128), cache stride 4096. Algorithmic
+    FLOP = 4 * n_head * head_dim * sum over queries of the visible positions
+    (q k^T and p v); the kernel runs on the FP32 CUDA cores, so the fraction is
+    of the FP32 FMA rate at the maximum SM clock."""
+    out = []
+    s = torch.cuda.current_stream()
+    for nh, nkv, hd in ((9, 3, 64), (32, 8, 128)):
+        stride = 4096
+        kc = torch.from_numpy(synth.normal_f32((nkv, stride, hd), 3, 1)).to(device)
+        vc = torch.from_numpy(synth.normal_f32((nkv, stride, hd), 3, 2)).to(device)
+        for T, pos in ((203, 0), (64, 512)):
+            q = torch.from_numpy(synth.normal_f32((T, nh, hd), 3, 3)).to(device)
+            o = torch.empty((T, nh, hd), dtype=torch.float32, device=device)
+            for _ in range(3):
+                B.llama_q8_attention(q, kc, vc, T, pos, nh, nkv, hd, stride, o, None, 0, s.cuda_stream)
+            n = 50
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(s)
+            for _ in range(n):
+                B.llama_q8_attention(q, kc, vc, T, pos, nh, nkv, hd, stride, o, None, 0, s.cuda_stream)
+            e1.record(s)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000 / n
+            visible = sum(pos + i + 1 for i in range(T))
+            flops = 4.0 * nh * hd * visible
+            tf = flops / (us * 1e-6) / 1e12
+            out.append({"heads": f"{nh}/{nkv}x{hd}", "T": T, "index_pos": pos, "us": us, "tflops": tf,
+                        "frac_fp32": tf / FP32_FMA_TFLOPS})
+        del kc, vc
+        torch.cuda.empty_cache()
+    return out
+
+
+def decode_timeline(model, cfg, n_steps, peak):
+    """Per-family timeline of the decode step from the instrumented copy of
+    the CUDA graph (llama_q8_profile_decode): exclusive time per launch (the
+    step's time spent on it: from its dependency wait returning to the next
+    launch's), span, algorithmic bytes, GB/s over both."""
+    prof = model.profile_decode(n_steps)
+    total_ms = sum(v[1] for v in prof.values())
+    fams = {}
+    for name, (n, ms, span_ms, nbytes) in prof.items():
+        if n == 0:
+            continue
+        fams[name] = {"launches": n, "us_per_launch": 1000 * ms / n, "span_us_per_launch": 1000 * span_ms / n,
+                      "bytes_per_launch": nbytes / n, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                      "gbs_over_span": nbytes / (span_ms * 1e-3) / 1e9, "share": ms / total_ms,
+                      "us_per_token": 1000 * ms / n_steps}
+    return fams, 1000 * total_ms / n_steps
+
+
+def lm_head_variants(torch, B, synth, device, peak, prompt, n_steps):
+    """The lm_head + argmax GEMV in the decode graph, row-parallel (persistent
+    CTAs over 32-row tiles) against split-K (each tile's 576-wide range over a
+    2-CTA cluster): its in-graph exclusive time from the timeline."""
+    res = {}
+    for name, splits in (("row_parallel", 0), ("split_k2", 2)):
+        cfg, model = gpu_model(torch, B, synth, device, head_splits=splits)
+        model.forward_argmax(prompt, 0)
+        fams, step_us = decode_timeline(model, cfg, n_steps, peak)
+        h = fams["gemv_head_argmax"]
+        res[name] = {"us_per_launch": h["us_per_launch"], "gbs": h["gbs"], "frac": h["gbs"] / peak,
+                     "step_us": step_us}
+        model.close()
+        torch.cuda.empty_cache()
+    res["kept"] = min(("row_parallel", "split_k2"), key=lambda k: res[k]["us_per_launch"])
+    return res
 
 
 def attention_microbench(torch, B, synth, device, peak):
@@ -616,19 +768,21 @@ def run_ours(args):
             e2e_dec.append(time.perf_counter() - t0)
     e2e_value, _ = aggregate_throughput(DECODE_STEPS * args.steps, sum(e2e_dec), world, device)
 
-    # per-kernel timing of the decode step (eager launches with event pairs)
+    # the decode step's timeline: the instrumented copy of the same CUDA graph (PDL chaining intact)
     model.forward_argmax(prompt, 0)
-    prof = model.profile_decode(DECODE_STEPS)
-    step_ms = sum(v[1] for v in prof.values()) / DECODE_STEPS
-    dom_name = max(prof, key=lambda k: prof[k][1])
-    dl, dms, dbytes = prof[dom_name]
-    dom_gbs = (dbytes / dl) / (dms / dl * 1e-3) / 1e9
+    fams, prof_step_us = decode_timeline(model, cfg, DECODE_STEPS, peak)
+    dom_name = max(fams, key=lambda k: fams[k]["share"])
+    dom = fams[dom_name]
     weights_bytes, kv_bytes = decode_bytes(cfg, PROMPT_LEN + (DECODE_STEPS + 1) / 2)
+    traffic = NCU_TRAFFIC.get(dom_name)
 
     out = None
     if rank == 0:
+        lm_head = lm_head_variants(torch, B, synth, device, peak, prompt, DECODE_STEPS)
         gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
         attn = attention_microbench(torch, B, synth, device, peak)
+        attn_pf = attention_prefill_bench(torch, B, synth, device)
+        sweep = linear_sweep(torch, B, synth, device, peak)
         gemm = gemm_microbench(torch, B, synth, device)
         model7 = decode_7b(torch, B, synth, device, peak)
         dec_tok_ms = [d / DECODE_STEPS for d in dec_ms]
@@ -651,29 +805,41 @@ def run_ours(args):
                     "h2d_bytes_per_step": 4 * (PROMPT_LEN + DECODE_STEPS),
                     "d2h_bytes_per_step": 16 * (1 + DECODE_STEPS)},
             "gpu_launches": gpu_launches,
-            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": dom_gbs / peak, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "traffic": NCU_TRAFFIC.get(dom_name, {}).get("bytes"),
-                         "traffic_source": NCU_TRAFFIC.get(dom_name),
-                         "algorithmic_bytes_per_launch": dbytes / dl,
-                         "note": "algorithmic bytes per launch / mean event-timed launch duration, eager decode; "
-                                 "the kernel is latency-bound (a chain of dependent steps), see profiles/"},
+            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": dom["gbs"] / peak, "peak_source": f"{peak_kind} HBM copy bandwidth (burst)",
+                         "traffic": traffic["bytes"] if traffic else None,
+                         "traffic_kv_len": traffic["kv_len"] if traffic else None,
+                         "algorithmic_bytes_per_launch": dom["bytes_per_launch"],
+                         "duration_us": dom["us_per_launch"], "span_us": dom["span_us_per_launch"],
+                         "share_of_step": dom["share"],
+                         "timing": "the decode graph's instrumented copy (same kernels and PDL chaining; each "
+                                   "launch stamps %globaltimer at entry and when its dependency wait returns); "
+                                   "duration = exclusive time per launch, averaged over 128 steps x 30 layers",
+                         "note": "latency-bound: the kernel is a chain of dependent phases (norm, Q/K/V rows, "
+                                 "row exchange, attention, partial exchange, W_o) for ~1.4 MB of bytes"},
             "decode_step_roofline": {"weights_bytes": weights_bytes, "kv_bytes_mean": kv_bytes,
                                      "roofline_us": (weights_bytes + kv_bytes) / (peak * 1e9) * 1e6,
                                      "graph_step_us": 1000 * statistics.median(dec_tok_ms),
+                                     "instrumented_step_us": prof_step_us,
                                      "frac": ((weights_bytes + kv_bytes) / (peak * 1e9) * 1e6)
                                      / (1000 * statistics.median(dec_tok_ms))},
-            "kernels": {k: {"launches": v[0], "ms": v[1], "gbs": (v[2] / (v[1] * 1e-3) / 1e9) if v[1] else None,
-                            "share": v[1] / (step_ms * DECODE_STEPS)} for k, v in prof.items() if v[0] > 0},
+            "kernels": fams,
+            "lm_head": lm_head,
             "gemv_7b": gemv7,
             "attention_decode": attn,
+            "attention_prefill": attn_pf,
+            "linear_sweep": sweep,
             "gemm_prefill": gemm,
             "decode_7b": model7,
         }
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = run_cpu_baseline(args.cpu_baseline_seconds)
-            # the same oracle on one thread, a shorter sample (context for the all-cores figure)
-            out["cpu_baseline_single_thread"] = run_cpu_baseline(min(10.0, args.cpu_baseline_seconds / 2), threads=1)
+            # the same oracle on one thread, and on the two other configurations
+            out["cpu_baseline_legs"] = {
+                "c1_single_thread": run_cpu_baseline(max(15.0, args.cpu_baseline_seconds), threads=1),
+                "c0": run_cpu_baseline(args.cpu_baseline_seconds, config="c0"),
+                "c4": run_cpu_baseline(600.0, config="c4", timeout=900.0),
+            }
     model.close()
     if world > 1:
         import torch.distributed as dist
@@ -685,7 +851,7 @@ def run_ours(args):
 def main():
     args = parse_args()
     if args.cpu_baseline_worker:
-        cpu_baseline_worker(args.cpu_baseline_seconds, args.cpu_baseline_threads)
+        cpu_baseline_worker(args.cpu_baseline_seconds, args.cpu_baseline_threads, args.cpu_baseline_config)
         return
     if args.impl == "reference":
         run_reference(args)
@@ -705,6 +871,33 @@ def main():
         from q8_quantized_llama_gb300 import synth
         B.lib()
         print(json.dumps(prefill_only(torch, B, synth, torch.device("cuda", 0), args, args.only == "prefill7b")))
+        return
+    if args.only in ("sweep", "attnprefill"):
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        dev = torch.device("cuda", 0)
+        if args.only == "sweep":
+            print(json.dumps({"linear_sweep": linear_sweep(torch, B, synth, dev, hbm_peak()[0])}))
+        else:
+            print(json.dumps({"attention_prefill": attention_prefill_bench(torch, B, synth, dev)}))
+        return
+    if args.only == "profile":
+        import torch
+        torch.cuda.set_device(0)
+        from q8_quantized_llama_gb300 import binding as B
+        from q8_quantized_llama_gb300 import synth
+        B.lib()
+        dev = torch.device("cuda", 0)
+        cfg, model = gpu_model(torch, B, synth, dev)
+        prompt = synth.prompt_ids(PROMPT_LEN, cfg["n_vocab"], SEED)
+        model.forward_argmax(prompt, 0)
+        fams, step_us = decode_timeline(model, cfg, DECODE_STEPS, hbm_peak()[0])
+        print(json.dumps({"instrumented_step_us": step_us, "kernels": fams,
+                          "lm_head": lm_head_variants(torch, B, synth, dev, hbm_peak()[0], prompt, DECODE_STEPS)}))
+        model.close()
         return
     if args.only == "gemm":
         import torch

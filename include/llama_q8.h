@@ -77,15 +77,21 @@ typedef struct llama_q8_config {
     int32_t decode_kernel; /* decode step: 0 = automatic (two kernels per layer when each KV
                               head's Q/K/V rows and W_o slice fit a cluster and the MLP fits
                               8-CTA clusters, else three, four or five), 1 = five per-layer
-                              kernels, 2 = embedding and all layers as ONE cluster kernel,
-                              3 = four per layer (attention applying W_o), 4 = three per
-                              layer (norm, Q/K/V, attention and W_o fused; gate/up; down),
-                              5 = one 16-CTA cluster kernel per layer; 2-5 give
-                              LQ8_ERR_UNSUPPORTED at load when the model does not fit */
+                              kernels, 3 = four per layer (attention applying W_o), 4 = three
+                              per layer (norm, Q/K/V, attention and W_o fused; gate/up; down);
+                              3-4 give LQ8_ERR_UNSUPPORTED at load when the model does not
+                              fit; 2 and 5 (one cluster kernel for the whole step / per layer)
+                              are not built (measured slower): LQ8_ERR_UNSUPPORTED */
     int32_t rope_style;   /* 0: rope_i, dims 2i and 2i+1 form a pair (the Llama convention);
                              1: NEOX, dim i pairs with dim i + head_dim/2; both at angle
                              p * theta^(-2i/head_dim) ("量化 llama 的一次前向", RoPE：两种约定，
                              按架构名选). Other values -> LQ8_ERR_ARG */
+    int32_t head_splits;  /* lm_head matrix-vector product of the decode step and of the
+                             prefill's last row: 0 = row-parallel (persistent CTAs, each
+                             taking whole 32-row tiles over the full n_embd); 2..8 = split-K,
+                             each tile's n_embd range split over a cluster of that many CTAs
+                             whose partial sums meet in distributed shared memory. Other
+                             values, or more splits than n_embd / 32, -> LQ8_ERR_ARG */
 } llama_q8_config;
 
 /* The rotary convention the pages' loader picks from general.architecture:
@@ -227,28 +233,38 @@ llama_q8_status llama_q8_read_kv(llama_q8_ctx* ctx, int32_t layer, int32_t pos0,
 void* llama_q8_stream(llama_q8_ctx* ctx);
 
 /* Number of kernel launches one decode step makes (the CUDA-graph nodes):
- * n_layer * {5, 4, 3, 2, 1} + 2 with per-layer kernels (see decode_kernel), 2
- * with the one-cluster whole-step kernel (layers, then lm_head + argmax). */
+ * n_layer * {5, 4, 3, 2} + 2 (embedding, per-layer kernels, lm_head + argmax;
+ * see decode_kernel). */
 int32_t llama_q8_decode_kernel_count(const llama_q8_ctx* ctx);
 
 /* Cumulative number of kernel launches this context has issued; a CUDA-graph
  * decode step counts as its llama_q8_decode_kernel_count() kernels. */
 int64_t llama_q8_launch_count(const llama_q8_ctx* ctx);
 
-/* Per-kernel timing of the decode step, in the spirit of the per-span self
- * times on "量化 llama 的一次前向" (一个 decode 步里时间去了哪): runs n_steps
- * greedy decode steps EAGERLY (the same kernels the graph holds, one launch
- * at a time, a CUDA event pair around each launch on the context stream),
- * continuing from the current cached length and advancing it like
- * llama_q8_decode_async. For each kernel family it reports the launches, the
- * summed event time and the algorithmic bytes (weights read once, activations,
- * KV rows read, outputs written). stats: host array of max_stats entries;
- * *n_stats receives the number of families. Requires a non-empty cache and
- * cached length + n_steps <= max_seq. */
+/* Per-kernel timeline of the decode step, in the spirit of the per-span self
+ * times on "量化 llama 的一次前向" (一个 decode 步里时间去了哪). Replays an
+ * instrumented copy of the CUDA-graph decode step n_steps times (greedy
+ * decode, continuing from the current cached length and advancing it like
+ * llama_q8_decode_async): the same kernels, launch order and programmatic
+ * dependent launches as the step llama_q8_decode_async replays, each launch
+ * also recording on the GPU's global nanosecond timer when its first CTA
+ * started and when its grid dependency wait first returned (that is, when the
+ * previous launch had completed); a one-CTA stamp kernel after the lm_head
+ * closes the step. Per kernel family: launches; ms = summed exclusive time
+ * (from the return of the launch's dependency wait to that of the next
+ * launch: these add up to the step); span_ms = summed time from the launch's
+ * first CTA entry to the next launch's wait return (includes the part that
+ * overlapped the previous kernel); bytes = summed algorithmic bytes (weights
+ * read once, activations, the K/V rows read at the step's cache length,
+ * outputs written). stats: host array of max_stats (>= 10) entries; *n_stats
+ * receives the number of families. Requires a non-empty cache and cached
+ * length + n_steps <= max_seq. Allocates a small device and pinned host
+ * buffer for the stamps. */
 typedef struct llama_q8_kernel_stat {
     char name[32];
     int32_t launches;
     double ms;
+    double span_ms;
     double bytes;
 } llama_q8_kernel_stat;
 llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llama_q8_kernel_stat* stats,

@@ -42,7 +42,8 @@ class Q8Error(RuntimeError):
 
 
 class llama_q8_kernel_stat(C.Structure):
-    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int32), ("ms", C.c_double), ("bytes", C.c_double)]
+    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int32), ("ms", C.c_double), ("span_ms", C.c_double),
+                ("bytes", C.c_double)]
 
 
 class llama_q8_config(C.Structure):
@@ -50,7 +51,7 @@ class llama_q8_config(C.Structure):
                 ("n_head_kv", C.c_int32), ("head_dim", C.c_int32), ("n_ff", C.c_int32),
                 ("n_vocab", C.c_int32), ("max_seq", C.c_int32), ("rms_eps", C.c_float),
                 ("rope_theta", C.c_float), ("tied_output", C.c_int32), ("decode_kernel", C.c_int32),
-                ("rope_style", C.c_int32)]
+                ("rope_style", C.c_int32), ("head_splits", C.c_int32)]
 
 
 class llama_q8_layer_weights(C.Structure):
@@ -160,7 +161,8 @@ def make_config(cfg: dict) -> llama_q8_config:
     return llama_q8_config(cfg["n_layer"], cfg["n_embd"], cfg["n_head"], cfg["n_head_kv"], cfg["head_dim"],
                            cfg["n_ff"], cfg["n_vocab"], cfg.get("max_seq", 4096), cfg.get("rms_eps", 1e-5),
                            cfg.get("rope_theta", 10000.0), int(cfg.get("tied_output", 1)),
-                           int(cfg.get("decode_kernel", 0)), int(cfg.get("rope_style", 0)))
+                           int(cfg.get("decode_kernel", 0)), int(cfg.get("rope_style", 0)),
+                           int(cfg.get("head_splits", 0)))
 
 
 _LAYER_KEYS = ("attn_norm", "ffn_norm", "attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up",
@@ -273,11 +275,13 @@ class Model:
         return int(lib().llama_q8_launch_count(self.ctx))
 
     def profile_decode(self, n_steps: int):
-        """Per-kernel-family {name: (launches, ms, bytes)} over n_steps eager decode steps."""
+        """Per-kernel-family timeline of n_steps decode steps of the instrumented
+        graph: {name: (launches, exclusive ms, span ms, bytes)}."""
         stats = (llama_q8_kernel_stat * 16)()
         n = C.c_int32()
         check(lib().llama_q8_profile_decode(self.ctx, n_steps, stats, 16, C.byref(n)), "llama_q8_profile_decode")
-        return {stats[i].name.decode(): (stats[i].launches, stats[i].ms, stats[i].bytes) for i in range(n.value)}
+        return {stats[i].name.decode(): (stats[i].launches, stats[i].ms, stats[i].span_ms, stats[i].bytes)
+                for i in range(n.value)}
 
 
 # ---- device-level entry points ------------------------------------------------

@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
     __shared__ __align__(8) uint64_t wo_bar;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) stamp_at(fo.stamp, 0);
     const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
     const int G = n_head / n_kv;
     const int nbk = G * HD / 32;                       // W_o column blocks of this group
@@ -302,7 +303,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
 
     // ---- consumers ---------------------------------------------------------------------
     pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
+    if (tid == 0) {
+        pdl_launch_dependents();
+        stamp_at(fo.stamp, 1);
+    }
     for (int i = tid; i < GP * HD; i += kCaCT) Q[i] = i < G * HD ? q[(int64_t)kh * G * HD + i] : 0.0f;
     named_bar_sync(1, kCaCT);
     float4 qr[GP];
@@ -443,6 +447,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     __shared__ __align__(8) uint64_t rows_bar, part_bar;  // completed by st.async bytes
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) stamp_at(fa.stamp, 0);
     const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
     const int n_head = fa.n_head, n_kv = fa.n_kv, G = n_head / n_kv;
     const int h = fa.wqkv.k, nbx = h >> 5;
@@ -547,7 +552,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
         gpre[u] = i < h ? fa.g[i] : 0.0f;
     }
     pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
+    if (tid == 0) {
+        pdl_launch_dependents();
+        stamp_at(fa.stamp, 1);
+    }
     // x * g into XN and the sum of squares; the scale 1/rms multiplies the finished
     // projection rows, so no barrier waits on the reduction before the products.
     float r_norm;
@@ -796,11 +804,11 @@ static int ca_cluster_size(int n_kv, int G, const AttnOproj* fo) {
 template <int HD, int GP, bool FO>
 static cudaError_t ca_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv, int cache_stride,
                              int kv_len, const DevState* st, float* out, const AttnOproj* fo, bool pdl, int* err,
-                             cudaStream_t s) {
+                             cudaStream_t s, unsigned long long* stamp) {
     const int G = n_head / n_kv;
     const float scale = 1.0f / sqrtf((float)HD);
-    const AttnOproj none{};
-    const AttnOproj& f = FO ? *fo : none;
+    AttnOproj f = FO ? *fo : AttnOproj{};
+    f.stamp = stamp;
     cudaLaunchAttribute attrs[2];
     if (ca_cluster_size<HD, GP, FO>(n_kv, G, fo) == 16) {
         const int wo = FO ? fo_wo_bytes(f.wo.rows_pad, G, HD, 16) : 0;
@@ -817,27 +825,29 @@ static cudaError_t ca_launch(const float* q, const float* kc, const float* vc, i
 template <bool FO>
 static cudaError_t ca_dispatch(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                                int head_dim, int cache_stride, int kv_len, const DevState* st, float* out,
-                               const AttnOproj* fo, bool pdl, int* err, cudaStream_t s) {
+                               const AttnOproj* fo, bool pdl, int* err, cudaStream_t s,
+                               unsigned long long* stamp) {
     if (n_head_kv <= 0 || n_head % n_head_kv || n_head / n_head_kv > kMaxGroup) return cudaErrorInvalidValue;
     const bool wide = n_head / n_head_kv > 4;
     if (head_dim == 64)
         return wide ? ca_launch<64, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
-                                           pdl, err, s)
+                                           pdl, err, s, stamp)
                     : ca_launch<64, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
-                                           pdl, err, s);
+                                           pdl, err, s, stamp);
     if (head_dim == 128)
         return wide ? ca_launch<128, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
-                                            fo, pdl, err, s)
+                                            fo, pdl, err, s, stamp)
                     : ca_launch<128, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
-                                            fo, pdl, err, s);
+                                            fo, pdl, err, s, stamp);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
-                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s) {
+                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s,
+                                       unsigned long long* stamp) {
     return ca_dispatch<false>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, kv_len, st, out,
-                              nullptr, pdl, err, s);
+                              nullptr, pdl, err, s, stamp);
 }
 
 // The O projection fits the decode attention kernel when every CTA's W_o
@@ -859,11 +869,11 @@ bool attn_oproj_fused_supported(int n_head, int n_kv, int head_dim, const Packed
 
 cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                               int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
-                              int part_stride, bool pdl, int* err, cudaStream_t s) {
+                              int part_stride, bool pdl, int* err, cudaStream_t s, unsigned long long* stamp) {
     if (!st) return cudaErrorInvalidValue;
-    const AttnOproj fo{Wo, part, part_stride};
+    const AttnOproj fo{Wo, part, part_stride, nullptr};
     return ca_dispatch<true>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, 0, st, nullptr, &fo,
-                             pdl, err, s);
+                             pdl, err, s, stamp);
 }
 
 // ---- fused layer front: host side --------------------------------------------------------

@@ -60,6 +60,7 @@ struct AttnOproj {
     PackedQ8 wo;
     float* part;
     int part_stride;
+    unsigned long long* stamp;  // timeline stamps (instrumented decode graph), or null
 };
 constexpr int kFoMaxWoBytes = 32 * 1024;  // W_o bytes one CTA may hold
 __host__ __device__ inline int fo_tiles_per_cta(int rows_pad, int cl) { return (rows_pad / 32 + cl - 1) / cl; }

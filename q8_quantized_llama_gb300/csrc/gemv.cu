@@ -20,6 +20,10 @@
 // Programmatic dependent launch: the producer starts streaming weights (which
 // no kernel writes) before the grid waits on its predecessor, so the weight
 // reads of a decode step overlap the tail of the previous kernel.
+#include <algorithm>
+#include <map>
+#include <mutex>
+
 #include "epilogue.cuh"
 #include "ptx.cuh"
 
@@ -68,11 +72,13 @@ __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, c
 }
 
 // Epilogue on the 32 rows of a tile (warp-wide; lane = row within the tile).
-// pre: for EPI_RESIDUAL, the residual value of this lane's row, read right
-// after the grid dependency wait so that its latency overlaps the products.
+// pre: for EPI_RESIDUAL, the residual value of this lane's row, read before
+// the tile's products so that its latency overlaps them. For EPI_ARGMAX the
+// logits are stored and the tile's best packed key (value, lowest index) is
+// folded into *best (warp-uniform); the CTA publishes it once at the end.
 template <int EPI>
-__device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, int n_tiles,
-                                              float pre) {
+__device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, float pre,
+                                              unsigned long long* best) {
     const int r = tile * 32 + lane;
     const bool valid = r < rows;
     if (EPI == EPI_STORE) {
@@ -94,25 +100,34 @@ __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int ti
             const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
             key = other > key ? other : key;
         }
-        if (lane == 0) {
-            atomicMax(e.best_key, key);
-            __threadfence();
-            const unsigned int ticket = atomicAdd(e.done_count, 1u);
-            if (ticket == (unsigned)(n_tiles - 1)) {
-                __threadfence();
-                const unsigned long long best = atomicExch(e.best_key, 0ull);
-                atomicExch(e.done_count, 0u);
-                const int tok = argmax_key_index(best);
-                DevState* st = e.st;
-                st->token = tok;
-                if (e.out_ids) e.out_ids[st->n_out] = tok;
-                st->n_out += 1;
-                st->pos = e.pos_after >= 0 ? e.pos_after : st->pos + 1;
-            }
-        }
+        *best = key > *best ? key : *best;
     }
 }
 
+// Greedy token: every publishing CTA adds its best key; the last one to arrive
+// (ticket) reads the maximum, resets the accumulators for the next launch and
+// writes the token and position to the step state. One thread.
+__device__ __forceinline__ void argmax_publish(const EpiArgs& e, unsigned long long best, unsigned int n_pub) {
+    atomicMax(e.best_key, best);
+    __threadfence();
+    const unsigned int ticket = atomicAdd(e.done_count, 1u);
+    if (ticket == n_pub - 1) {
+        __threadfence();
+        const unsigned long long key = atomicExch(e.best_key, 0ull);
+        atomicExch(e.done_count, 0u);
+        const int tok = argmax_key_index(key);
+        DevState* st = e.st;
+        st->token = tok;
+        if (e.out_ids) e.out_ids[st->n_out] = tok;
+        st->n_out += 1;
+        st->pos = e.pos_after >= 0 ? e.pos_after : st->pos + 1;
+    }
+}
+
+// Grid: with S == 1 a persistent set of CTAs (at most what is resident at
+// once), each taking row tiles blockIdx.x, blockIdx.x + gridDim.x, ... and
+// streaming their weights through one continuous ring; with S > 1 one cluster
+// of S CTAs per tile, rank r taking the r-th part of the block range.
 template <int EPI, bool NORM, typename RG>
 __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     constexpr int kStages = RG::kStages, kStageBlocks = RG::kStageBlocks;
@@ -123,17 +138,22 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ __align__(8) uint64_t empty[kStages];
     __shared__ __align__(8) uint64_t xbar;
-    __shared__ float red[kCWarps][33];
+    __shared__ float red[2][kCWarps][32];  // per-warp tile sums, by tile parity
+    __shared__ float ssq[kCWarps];          // per-warp sums of squares (fused norm)
     __shared__ float part[32];
 
     const PackedQ8& W = a.W;
     const int k = W.k, nb = k >> 5;
     const int S = a.splits;
-    const int tile = blockIdx.x / S, split = blockIdx.x % S;
+    const int tiles = W.rows_pad >> 5;
+    const int cl_id = blockIdx.x / S, split = blockIdx.x % S, n_cl = gridDim.x / S;
+    const int my_tiles = cl_id < tiles ? (tiles - cl_id + n_cl - 1) / n_cl : 0;
     const int b0 = (split * nb) / S, b1 = ((split + 1) * nb) / S;
     const int nblk = b1 - b0;
-    const int n_stage = (nblk + kStageBlocks - 1) / kStageBlocks;
+    const int n_stage = (nblk + kStageBlocks - 1) / kStageBlocks;  // per tile
+    const int total = my_tiles * n_stage;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) stamp_at(a.e.stamp, 0);
 
     // The activation vector goes to shared memory by one bulk copy issued after
     // the grid dependency wait: the whole vector when the fused RMSNorm needs
@@ -152,25 +172,26 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
-    float res_pre = 0.0f;  // EPI_RESIDUAL: residual of the row this lane finishes (warp 0 of split 0)
 
     if (warp == kCWarps) {
-        // ---- producer: stream this unit's codes and scales -------------------
+        // ---- producer: stream the codes and scales of every tile of this CTA ----
         if (lane == 0) {
-            const uint8_t* gcodes = reinterpret_cast<const uint8_t*>(W.qs) + (size_t)tile * k * 32;
-            const uint8_t* gscales = reinterpret_cast<const uint8_t*>(W.d) + (size_t)tile * nb * 64;
-            auto issue_stage = [&](int j) {
-                const int slot = j % kStages;
-                if (j >= kStages) mbar_wait_bounded(&empty[slot], ((j / kStages) - 1) & 1, a.err, 9);
+            const uint8_t* qs = reinterpret_cast<const uint8_t*>(W.qs);
+            const uint8_t* ds = reinterpret_cast<const uint8_t*>(W.d);
+            auto issue_stage = [&](int g) {
+                const int slot = g % kStages;
+                if (g >= kStages) mbar_wait_bounded(&empty[slot], ((g / kStages) - 1) & 1, a.err, 9);
+                const int tile = cl_id + (g / n_stage) * n_cl, j = g % n_stage;
                 const int bs = b0 + j * kStageBlocks;
                 const int nbs = min(kStageBlocks, b1 - bs);
                 uint8_t* dst = stages + slot * kStageBytes;
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbs * 1024 + nbs * 64));
-                bulk_g2s(dst, gcodes + (size_t)bs * 1024, nbs * 1024, &full[slot]);
-                bulk_g2s(dst + kStageCodeBytes, gscales + (size_t)bs * 64, nbs * 64, &full[slot]);
+                bulk_g2s(dst, qs + (size_t)tile * k * 32 + (size_t)bs * 1024, nbs * 1024, &full[slot]);
+                bulk_g2s(dst + kStageCodeBytes, ds + (size_t)tile * nb * 64 + (size_t)bs * 64, nbs * 64,
+                         &full[slot]);
             };
-            const int first = min(kStages, n_stage);
-            for (int j = 0; j < first; ++j) issue_stage(j);  // weights: no kernel writes them
+            const int first = min(kStages, total);
+            for (int g = 0; g < first; ++g) issue_stage(g);  // weights: no kernel writes them
             pdl_wait();                                      // x: written by the preceding kernel
             const int xoff = x_full ? 0 : x0, xcnt = x_full ? k : xn;
             mbar_arrive_expect_tx(&xbar, (uint32_t)(xcnt * 4 * (1 + np)));
@@ -178,7 +199,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             for (int p = 0; p < np; ++p)
                 bulk_g2s(xs + (size_t)(p + 1) * k, a.pre.part + (size_t)p * a.pre.part_stride, (uint32_t)(k * 4),
                          &xbar);
-            for (int j = first; j < n_stage; ++j) issue_stage(j);
+            for (int g = first; g < total; ++g) issue_stage(g);
         }
     } else {
         // ---- consumers --------------------------------------------------------
@@ -194,13 +215,13 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             }
         }
         pdl_wait();
-        if (tid == 0) pdl_launch_dependents();
-        constexpr int kCT = kCWarps * 32;
-        if (EPI == EPI_RESIDUAL && split == 0 && warp == 0) {
-            const int r = tile * 32 + lane;
-            if (r < W.rows) res_pre = a.e.res ? a.e.res[r] : a.e.y[r];
+        if (tid == 0) {
+            pdl_launch_dependents();
+            stamp_at(a.e.stamp, 1);
         }
+        constexpr int kCT = kCWarps * 32;
         mbar_wait_bounded(&xbar, 0, a.err, 13);
+        float rscale = 1.0f;
         if (NORM) {
             // x (+ the partials, in order) -> sum of squares for the scale, and x * g in
             // place; the scale 1/rms multiplies the finished dot products in the epilogue,
@@ -228,7 +249,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 *reinterpret_cast<float4*>(xs + i) = v;
             }
             ss = warp_sum(ss);
-            if (lane == 0) red[warp][32] = ss;
+            if (lane == 0) ssq[warp] = ss;
             named_bar_sync(1, kCT);
             if (x_full) {  // split unit: scale this unit's slice after every sum has landed
                 for (int i = tid * 4, u = 0; i < xn; i += kCT * 4, ++u) {
@@ -243,53 +264,73 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 }
                 named_bar_sync(1, kCT);
             }
-        }
-
-        float acc = 0.0f;
-        for (int j = 0; j < n_stage; ++j) {
-            const int slot = j % kStages;
-            mbar_wait_bounded(&full[slot], (j / kStages) & 1, a.err, 10);
-            const int bs = j * kStageBlocks;  // relative to b0
-            const int nbs = min(kStageBlocks, nblk - bs);
-            const uint8_t* st = stages + slot * kStageBytes;
-#pragma unroll
-            for (int bi = warp; bi < kStageBlocks; bi += kCWarps) {
-                if (bi < nbs) {
-                    const uint4 q0 = *reinterpret_cast<const uint4*>(st + bi * 1024 + lane * 16);
-                    const uint4 q1 = *reinterpret_cast<const uint4*>(st + bi * 1024 + 512 + lane * 16);
-                    const float d =
-                        __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[bi * 32 + lane]);
-                    acc = fmaf(d, block_dot32(q0, q1, xslice + (bs + bi) * 32), acc);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-        red[warp][lane] = acc;
-        named_bar_sync(1, kCT);
-        if (warp == 0) {
-            float v = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kCWarps; ++w) v += red[w][lane];
-            part[lane] = v;
-        }
-    }
-
-    // ---- cluster reduction and epilogue ---------------------------------------
-    __syncwarp();
-    if (S > 1) cluster_sync(); else __syncthreads();
-    if (split == 0 && warp == 0) {
-        float v = part[lane];
-        for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
-        if (NORM) {  // 1 / rms of the (full) input, from this CTA's warp sums
             float t = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kCWarps; ++w) t += red[w][32];
-            v *= 1.0f / sqrtf(t / (float)k + a.eps);
+            for (int w = 0; w < kCWarps; ++w) t += ssq[w];
+            rscale = 1.0f / sqrtf(t / (float)k + a.eps);
         }
-        gemv_epilogue<EPI>(a.e, W.rows, tile, lane, v, W.rows_pad / 32, res_pre);
+
+        unsigned long long best = 0ull;  // EPI_ARGMAX, warp 0
+        float res_pre = 0.0f;            // EPI_RESIDUAL: residual of the row this lane finishes
+        for (int ti = 0; ti < my_tiles; ++ti) {
+            const int tile = cl_id + ti * n_cl;
+            if (EPI == EPI_RESIDUAL && split == 0 && warp == 0) {
+                const int r = tile * 32 + lane;
+                if (r < W.rows) res_pre = a.e.res ? a.e.res[r] : a.e.y[r];
+            }
+            float acc = 0.0f;
+            for (int j = 0; j < n_stage; ++j) {
+                const int g = ti * n_stage + j;
+                const int slot = g % kStages;
+                mbar_wait_bounded(&full[slot], (g / kStages) & 1, a.err, 10);
+                const int bs = j * kStageBlocks;  // relative to b0
+                const int nbs = min(kStageBlocks, nblk - bs);
+                const uint8_t* st = stages + slot * kStageBytes;
+#pragma unroll
+                for (int bi = warp; bi < kStageBlocks; bi += kCWarps) {
+                    if (bi < nbs) {
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(st + bi * 1024 + lane * 16);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>(st + bi * 1024 + 512 + lane * 16);
+                        const float d =
+                            __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[bi * 32 + lane]);
+                        acc = fmaf(d, block_dot32(q0, q1, xslice + (bs + bi) * 32), acc);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+            red[ti & 1][warp][lane] = acc;
+            named_bar_sync(1, kCT);
+            if (warp == 0) {
+                float v = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kCWarps; ++w) v += red[ti & 1][w][lane];
+                if (S == 1)
+                    gemv_epilogue<EPI>(a.e, W.rows, tile, lane, NORM ? v * rscale : v, res_pre, &best);
+                else
+                    part[lane] = v;  // one tile per cluster: reduced below
+            }
+        }
+        if (S > 1) {
+            // ---- cluster reduction and epilogue (one tile per cluster) -------------
+            __syncwarp();
+            cluster_sync();
+            if (split == 0 && warp == 0 && my_tiles > 0) {
+                float v = part[lane];
+                for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
+                gemv_epilogue<EPI>(a.e, W.rows, cl_id, lane, NORM ? v * rscale : v, res_pre, &best);
+            }
+            cluster_sync();  // peers keep their shared memory until the leader has read it
+        }
+        if (EPI == EPI_ARGMAX && split == 0 && tid == 0) argmax_publish(a.e, best, (unsigned)n_cl);
+        return;
     }
-    if (S > 1) cluster_sync();  // peers keep their shared memory until the leader has read it
+    // the producer warp joins the cluster barriers of a split launch
+    if (S > 1) {
+        __syncwarp();
+        cluster_sync();
+        cluster_sync();
+    }
 }
 
 // Splits per tile: enough CTAs to cover the GPU in one wave, at least 16
@@ -314,12 +355,32 @@ static int sm_count_current() {
     return g_sm_count[dev];
 }
 
+// CTAs of one instantiation resident per SM with `smem` bytes of dynamic
+// shared memory (occupancy query, remembered per kernel and size).
+static int resident_ctas(void (*kernel)(GemvArgs), size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, size_t>, int> known;
+    std::lock_guard<std::mutex> lock(mu);
+    const std::pair<const void*, size_t> key((const void*)kernel, smem);
+    auto it = known.find(key);
+    if (it != known.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kGemvThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    n = n > 0 ? n : 1;
+    known[key] = n;
+    return n;
+}
+
 template <int EPI, bool NORM, typename RG>
 static cudaError_t gemv_launch_ring(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
-                                    bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+                                    bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre, int force_splits) {
     constexpr int kStages = RG::kStages, kStageBytes = RG::kStageBytes;
     const int tiles = W.rows_pad / 32, nb = W.k / 32;
-    const int S = gemv_splits(tiles, nb, sm_count_current(), RG::kCtasPerSm);
+    const int sms = sm_count_current();
+    const int S = force_splits > 0 ? force_splits : gemv_splits(tiles, nb, sms, RG::kCtasPerSm);
     const int max_blk = (nb + S - 1) / S;
     const int n_part = (NORM && pre) ? pre->n_part : 0;
     // x (its slice, or all of it for the norm) and the added partials
@@ -327,8 +388,12 @@ static cudaError_t gemv_launch_ring(const PackedQ8& W, const float* x, const flo
     const size_t smem = (size_t)kStages * kStageBytes + x_floats * sizeof(float);
     if (smem > (size_t)kGemvMaxSmem) return cudaErrorInvalidValue;
     GemvArgs a{W, x, g, eps, e, S, err, (NORM && pre) ? *pre : GemvPreSum{}};
+    // S == 1: persistent CTAs, as many as are resident at once (each takes every
+    // grid-th row tile); S > 1: one cluster per tile
+    int grid = tiles * S;
+    if (S == 1) grid = std::min(tiles, sms * resident_ctas(q8_gemv_kernel<EPI, NORM, RG>, smem));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles * S);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -353,11 +418,11 @@ static cudaError_t gemv_launch_ring(const PackedQ8& W, const float* x, const flo
 
 template <int EPI, bool NORM>
 static cudaError_t gemv_launch_one(const PackedQ8& W, const float* x, const float* g, float eps, const EpiArgs& e,
-                                   bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+                                   bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre, int force_splits) {
     const int tiles = W.rows_pad / 32;
     if (tiles >= 2 * sm_count_current())
-        return gemv_launch_ring<EPI, NORM, RingWide>(W, x, g, eps, e, pdl, err, s, pre);
-    return gemv_launch_ring<EPI, NORM, RingDeep>(W, x, g, eps, e, pdl, err, s, pre);
+        return gemv_launch_ring<EPI, NORM, RingWide>(W, x, g, eps, e, pdl, err, s, pre, force_splits);
+    return gemv_launch_ring<EPI, NORM, RingDeep>(W, x, g, eps, e, pdl, err, s, pre, force_splits);
 }
 
 template <int EPI>
@@ -394,24 +459,28 @@ size_t gemv_max_k() {
 }
 
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre) {
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre,
+                        int force_splits) {
     const bool norm = norm_g != nullptr;
+    if (force_splits < 0 || force_splits > 8 || (force_splits > 0 && W.k / 32 < force_splits))
+        return cudaErrorInvalidValue;
+    const int f = force_splits;
     switch (epi) {
         case EPI_STORE:
-            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
-                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
+            return norm ? gemv_launch_one<EPI_STORE, true>(W, x, norm_g, eps, e, pdl, err, s, pre, f)
+                        : gemv_launch_one<EPI_STORE, false>(W, x, norm_g, eps, e, pdl, err, s, pre, f);
         case EPI_RESIDUAL:
-            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
-                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
+            return norm ? gemv_launch_one<EPI_RESIDUAL, true>(W, x, norm_g, eps, e, pdl, err, s, pre, f)
+                        : gemv_launch_one<EPI_RESIDUAL, false>(W, x, norm_g, eps, e, pdl, err, s, pre, f);
         case EPI_QKV:
-            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
-                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
+            return norm ? gemv_launch_one<EPI_QKV, true>(W, x, norm_g, eps, e, pdl, err, s, pre, f)
+                        : gemv_launch_one<EPI_QKV, false>(W, x, norm_g, eps, e, pdl, err, s, pre, f);
         case EPI_SILU:
-            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
-                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
+            return norm ? gemv_launch_one<EPI_SILU, true>(W, x, norm_g, eps, e, pdl, err, s, pre, f)
+                        : gemv_launch_one<EPI_SILU, false>(W, x, norm_g, eps, e, pdl, err, s, pre, f);
         case EPI_ARGMAX:
-            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, pdl, err, s, pre)
-                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, pdl, err, s, pre);
+            return norm ? gemv_launch_one<EPI_ARGMAX, true>(W, x, norm_g, eps, e, pdl, err, s, pre, f)
+                        : gemv_launch_one<EPI_ARGMAX, false>(W, x, norm_g, eps, e, pdl, err, s, pre, f);
     }
     return cudaErrorInvalidValue;
 }

@@ -50,6 +50,8 @@ struct EpiArgs {
     DevState* st = nullptr;
     int32_t* out_ids = nullptr;
     int pos_after = -1;  // >= 0: state->pos := pos_after; < 0: state->pos += 1
+    // matrix-vector kernel: timeline stamps of this launch (instrumented decode graph), or null
+    unsigned long long* stamp = nullptr;
 };
 
 // Launch with an optional programmatic-dependent-launch attribute (the kernel
@@ -80,7 +82,12 @@ cudaError_t launch_quantize(const float* w, int64_t rows, int64_t k, uint8_t* ou
 cudaError_t launch_pack(const uint8_t* q8, int64_t rows, int64_t k, uint8_t* packed_base,
                         int64_t dst_rows, int64_t row_offset, int64_t row_stride, cudaStream_t s);
 cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const DevState* st_token,
-                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s);
+                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s,
+                         unsigned long long* stamp = nullptr);
+// One 32-thread CTA that stamps its entry and the return of its grid dependency
+// wait: placed after the last kernel of the instrumented decode graph, its wait
+// returns when that kernel has completed.
+cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
                            cudaStream_t s);
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
@@ -97,8 +104,12 @@ struct GemvPreSum {
     int part_stride = 0;
     float* x_sum_out = nullptr;
 };
+// force_splits: 0 = automatic (persistent row-parallel CTAs when the row tiles
+// fill the GPU, else the block range of each tile split over a cluster);
+// 2..8 = split every tile's block range over a cluster of that many CTAs.
 cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, float eps, int epi,
-                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre = nullptr);
+                        const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre = nullptr,
+                        int force_splits = 0);
 size_t gemv_max_k();
 // gemm.cu (m > 1): CUDA-core kernel for a few rows
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
@@ -125,7 +136,8 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
                                bool pdl, cudaStream_t s);
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
-                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s);
+                                       const DevState* st, float* out, bool pdl, int* err, cudaStream_t s,
+                                       unsigned long long* stamp = nullptr);
 // Decode attention whose clusters also apply the O projection: cluster kh
 // writes part[kh][0..rows) = W_o[:, columns of its query heads] o, the n_kv
 // partials summing to W_o o (added to the residual by the next kernel).
@@ -153,27 +165,9 @@ struct FrontArgs {
     float* part;           // [n_kv][part_stride] partials of W_o o
     int part_stride;
     int* err;
+    unsigned long long* stamp;  // timeline stamps (instrumented decode graph), or null
 };
 int layer_front_cluster_size(const FrontArgs& fa, int head_dim);  // 0: not supported
-
-// decode_layer.cu: a whole decode layer as one 16-CTA cluster kernel (small models).
-struct LayerKArgs {
-    const float* x_in;   // [h] residual stream in (written by the preceding kernel)
-    float* x_out;        // [h] residual stream out (a different buffer)
-    const float* g_attn; // [h] RMSNorm weights
-    const float* g_ffn;
-    float eps;
-    PackedQ8 wqkv, wo, wgu, wdown;  // [Wq;Wk;Wv], W_o, row-interleaved [Wg;Wu], W_down
-    float* kc;           // layer K cache [n_kv][stride][hd]
-    float* vc;
-    const float* rope_cos;  // [stride][hd/2]
-    const float* rope_sin;
-    int n_head, n_kv, stride;
-    const DevState* st;
-    float scale;
-    int* err;
-};
-bool decode_layer_supported(const LayerKArgs& la, int head_dim);
 
 // mlp.cu: the MLP half of a decode layer as one kernel (clusters of 8 CTAs).
 struct MlpArgs {
@@ -187,40 +181,18 @@ struct MlpArgs {
     float* xr_out;           // [h] x + W_o o (written by the first CTA): the next residual base
     float* mlp_part;         // [clusters][h] partials of W_down a, one per cluster
     int* err;
+    unsigned long long* stamp;  // timeline stamps (instrumented decode graph), or null
 };
 int decode_mlp_clusters(int h, int ff, int gu_rows);  // 0: not supported
 cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s);
-cudaError_t launch_decode_layer(const LayerKArgs& la, int head_dim, bool pdl, cudaStream_t s);
 cudaError_t launch_layer_front(const FrontArgs& fa, int head_dim, int cl, bool pdl, cudaStream_t s);
 cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                               int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
-                              int part_stride, bool pdl, int* err, cudaStream_t s);
+                              int part_stride, bool pdl, int* err, cudaStream_t s,
+                              unsigned long long* stamp = nullptr);
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache,
                                 int T, int index_pos, int n_head, int n_head_kv, int head_dim,
                                 int cache_stride, float* out, bool pdl, cudaStream_t s);
-
-// decode_cluster.cu: the per-layer part of a decode step as one cluster
-struct LayerPtrs {
-    PackedQ8 qkv, o, gu, down;
-    const float* attn_norm;
-    const float* ffn_norm;
-    float* kc;  // [n_kv][max_seq][hd]
-    float* vc;
-};
-struct ClusterStepArgs {
-    const LayerPtrs* layers;
-    int n_layer;
-    PackedQ8 embd;
-    int n_vocab, h, n_head, n_kv, hd, ff, max_seq;
-    float eps, scale;
-    const float* rope_cos;
-    const float* rope_sin;
-    DevState* st;
-    float* x_out;  // final residual stream for the lm_head kernel
-    int* err;
-};
-int decode_cluster_size(int h, int n_head, int n_kv, int hd, int ff);
-cudaError_t launch_decode_cluster(int cl, const ClusterStepArgs& args, cudaStream_t s);
 
 PackedQ8 packed_view(const uint8_t* base, int64_t rows, int64_t k);
 

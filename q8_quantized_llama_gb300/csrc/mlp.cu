@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
     extern __shared__ __align__(128) float smf[];
     __shared__ __align__(8) uint64_t w_bar, red_bar;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) stamp_at(ma.stamp, 0);
     const int c = blockIdx.x;                 // block column of W_down = a entries [32c, 32c + 32)
     const int q = (int)cluster_rank();        // rank in the cluster
     const int cl_id = c / kMlpCl;
@@ -103,7 +104,10 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
         gpre[u] = i < h ? *reinterpret_cast<const float4*>(ma.g + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
+    if (tid == 0) {
+        pdl_launch_dependents();
+        stamp_at(ma.stamp, 1);
+    }
     float ss = 0.0f;
 #pragma unroll
     for (int u = 0; u < kGPre; ++u) {

@@ -40,6 +40,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Timeline stamps of one launch of the instrumented decode graph (null in
+// every other launch): stamp[0] = earliest CTA entry, stamp[1] = earliest
+// return from the grid dependency wait, on the global nanosecond timer.
+__device__ __forceinline__ void stamp_at(unsigned long long* stamp, int i) {
+    if (stamp) atomicMin(stamp + i, (unsigned long long)global_timer_ns());
+}
 // Wait for the phase with the given parity to complete, for at most ~1 s.
 // On timeout, record `code` in *err (if given) and return false; callers then
 // carry on through their remaining barriers so that no thread is left waiting.

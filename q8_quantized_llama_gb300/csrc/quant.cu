@@ -104,9 +104,11 @@ cudaError_t launch_pack(const uint8_t* q8, int64_t rows, int64_t k, uint8_t* pac
 // st_err->err and row 0 is used.
 // ---------------------------------------------------------------------------
 __global__ void embed_kernel(PackedQ8 E, const int32_t* __restrict__ ids, const DevState* st_token,
-                             DevState* st_err, float* __restrict__ x, int n_vocab) {
+                             DevState* st_err, float* __restrict__ x, int n_vocab, unsigned long long* stamp) {
+    if (threadIdx.x == 0) stamp_at(stamp, 0);
     pdl_wait();
     pdl_launch_dependents();
+    if (threadIdx.x == 0) stamp_at(stamp, 1);
     const int t = blockIdx.x;
     int id = ids ? ids[t] : st_token->token;
     if (id < 0 || id >= n_vocab) {
@@ -132,8 +134,19 @@ __global__ void embed_kernel(PackedQ8 E, const int32_t* __restrict__ ids, const 
 }
 
 cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const DevState* st_token,
-                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s) {
-    return launch_ex(embed_kernel, dim3(T), dim3(128), 0, s, pdl, E, ids, st_token, st_err, x, n_vocab);
+                         DevState* st_err, float* x, int n_vocab, bool pdl, cudaStream_t s,
+                         unsigned long long* stamp) {
+    return launch_ex(embed_kernel, dim3(T), dim3(128), 0, s, pdl, E, ids, st_token, st_err, x, n_vocab, stamp);
+}
+
+__global__ void stamp_kernel(unsigned long long* stamp) {
+    if (threadIdx.x == 0) stamp_at(stamp, 0);
+    pdl_wait();
+    if (threadIdx.x == 0) stamp_at(stamp, 1);
+}
+
+cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s) {
+    return launch_ex(stamp_kernel, dim3(1), dim3(32), 0, s, true, stamp);
 }
 
 // ---------------------------------------------------------------------------

@@ -52,54 +52,24 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Event-pair timing of individual launches (llama_q8_profile_decode). The
-// events are recorded as external event nodes of a captured graph, so each
-// kernel's time is taken on the GPU's own clock, free of host launch gaps.
-struct Profiler {
+// Layout of one decode step for llama_q8_profile_decode: the family and the
+// algorithmic bytes of each launch, in launch order (K/V bytes are per cached
+// position and scaled by the step's cache length when the timeline is read).
+struct StepLayout {
     struct Rec {
         int family;
         double bytes;       // algorithmic bytes of the launch, fixed part
         double kv_per_pos;  // plus this many bytes per cached position (K/V reads)
-        cudaEvent_t a, b;
     };
     std::vector<Rec> recs;
-    cudaStream_t s = nullptr;
-    cudaEvent_t cur_a = nullptr;
-    int cur = -1;
-    double cur_bytes = 0, cur_kv = 0;
-    cudaError_t begin(int family, double bytes, double kv_per_pos) {
-        cur = family;
-        cur_bytes = bytes;
-        cur_kv = kv_per_pos;
-        cudaError_t e = cudaEventCreate(&cur_a);
-        if (e == cudaSuccess) e = cudaEventRecordWithFlags(cur_a, s, cudaEventRecordExternal);
-        return e;
-    }
-    cudaError_t end() {
-        cudaEvent_t b = nullptr;
-        cudaError_t e = cudaEventCreate(&b);
-        if (e == cudaSuccess) e = cudaEventRecordWithFlags(b, s, cudaEventRecordExternal);
-        recs.push_back({cur, cur_bytes, cur_kv, cur_a, b});
-        cur_a = nullptr;
-        return e;
-    }
-    ~Profiler() {
-        for (auto& r : recs) {
-            cudaEventDestroy(r.a);
-            cudaEventDestroy(r.b);
-        }
-        if (cur_a) cudaEventDestroy(cur_a);
-    }
 };
 
 enum Family {
-    F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_CLUSTER, F_ATTN_O, F_FRONT, F_LAYER, F_MLP,
-    F_COUNT
+    F_EMBED = 0, F_QKV, F_ATTN, F_OPROJ, F_GATEUP, F_DOWN, F_HEAD, F_ATTN_O, F_FRONT, F_MLP, F_COUNT
 };
 const char* kFamilyNames[F_COUNT] = {"embed", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_residual",
                                      "gemv_gate_up_silu", "gemv_down_residual", "gemv_head_argmax",
-                                     "decode_cluster_layers", "attn_oproj_residual", "layer_front_qkv_attn_o",
-                                     "decode_layer_cluster", "decode_mlp"};
+                                     "attn_oproj_residual", "layer_front_qkv_attn_o", "decode_mlp"};
 
 struct LayerDev {
     const float* attn_norm;
@@ -129,7 +99,6 @@ struct llama_q8_ctx {
     float* d_a = nullptr;
     float* d_part = nullptr;  // decode: per-KV-head partials of W_o o
     float* d_xsum = nullptr;  // decode: x + W_o o, the residual of the down projection
-    float* d_x2 = nullptr;    // decode with the layer kernel: odd layers' residual stream
     float* d_xr = nullptr;    // decode with the MLP kernel: x + W_o o of the last layer
     float* d_mlp = nullptr;   // decode with the MLP kernel: per-cluster partials of W_down a
     float* d_logits = nullptr;
@@ -151,12 +120,9 @@ struct llama_q8_ctx {
 
     int len = 0;
     int64_t launches = 0;
-    int cluster = 0;                     // > 0: decode layers run as one cluster of this many CTAs
     bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
     int front_cl = 0;                    // > 0: norm + QKV + attention + W_o as one kernel (this cluster size)
-    bool layer_kernel = false;           // each decode layer as one 16-CTA cluster kernel
     int mlp_clusters = 0;                // > 0: gate/up + down as one kernel with this many 8-CTA clusters
-    LayerPtrs* d_layer_ptrs = nullptr;   // per-layer pointers for that kernel
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
     int decode_kernels = 0;
@@ -181,9 +147,9 @@ void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
-                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_x2, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
+                   c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
                    c->d_out_ids,
-                   c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_layer_ptrs};
+                   c->d_state, c->d_best, c->d_done, c->d_attn_ws};
     for (void* p : dev)
         if (p) cudaFree(p);
     void* host[] = {c->h_ids, c->h_out, c->h_logits, c->h_state};
@@ -256,97 +222,29 @@ FrontArgs front_args(llama_q8_ctx* c, int l) {
     return fa;
 }
 
-LayerKArgs layer_args(llama_q8_ctx* c, int l) {
-    const llama_q8_config& cfg = c->cfg;
-    const LayerDev& L = c->layers[l];
-    LayerKArgs la{};
-    la.x_in = (l & 1) ? c->d_x2 : c->d_x;
-    la.x_out = (l & 1) ? c->d_x : c->d_x2;
-    la.g_attn = L.attn_norm;
-    la.g_ffn = L.ffn_norm;
-    la.eps = cfg.rms_eps;
-    la.wqkv = L.qkv;
-    la.wo = L.o;
-    la.wgu = L.gu;
-    la.wdown = L.down;
-    la.kc = c->kcache(l);
-    la.vc = c->vcache(l);
-    la.rope_cos = c->d_rope_cos;
-    la.rope_sin = c->d_rope_sin;
-    la.n_head = cfg.n_head;
-    la.n_kv = cfg.n_head_kv;
-    la.stride = cfg.max_seq;
-    la.st = c->d_state;
-    la.scale = 1.0f / sqrtf((float)cfg.head_dim);
-    la.err = &c->d_state->err;
-    return la;
-}
-
-cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof = nullptr) {
+cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, StepLayout* layout = nullptr,
+                                unsigned long long* stamps = nullptr) {
     const llama_q8_config& cfg = c->cfg;
     cudaStream_t s = c->stream;
-    const bool pdl = prof == nullptr;
+    const bool pdl = true;
     const int64_t h = cfg.n_embd, F = cfg.n_ff, qr = c->q_rows, kvr = c->kv_rows;
     int n = 0;
     cudaError_t err = cudaSuccess;
+    unsigned long long* stp = nullptr;  // this launch's two stamps (instrumented graph only)
     auto run = [&](int fam, double bytes, double kv_per_pos, auto&& launch) {
         if (err != cudaSuccess) return;
-        if (prof) err = prof->begin(fam, bytes, kv_per_pos);
-        if (err == cudaSuccess) err = launch();
-        if (err == cudaSuccess && prof) err = prof->end();
+        stp = stamps ? stamps + 2 * n : nullptr;
+        if (layout) layout->recs.push_back({fam, bytes, kv_per_pos});
+        err = launch();
         ++n;
     };
-    if (c->cluster > 0) {
-        // embedding + all layers in one cluster kernel, then the lm_head on the whole GPU
-        double wbytes = 0.0;
-        for (int l = 0; l < cfg.n_layer; ++l)
-            wbytes += q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + q8_bytes(2 * F, h) + q8_bytes(h, F) + 8.0 * h;
-        ClusterStepArgs a{};
-        a.layers = c->d_layer_ptrs;
-        a.n_layer = cfg.n_layer;
-        a.embd = c->embd;
-        a.n_vocab = cfg.n_vocab;
-        a.h = cfg.n_embd;
-        a.n_head = cfg.n_head;
-        a.n_kv = cfg.n_head_kv;
-        a.hd = cfg.head_dim;
-        a.ff = cfg.n_ff;
-        a.max_seq = cfg.max_seq;
-        a.eps = cfg.rms_eps;
-        a.scale = 1.0f / sqrtf((float)cfg.head_dim);
-        a.rope_cos = c->d_rope_cos;
-        a.rope_sin = c->d_rope_sin;
-        a.st = c->d_state;
-        a.x_out = c->d_x;
-        a.err = &c->d_state->err;
-        run(F_CLUSTER, wbytes + q8_bytes(1, h) + 4.0 * h, 8.0 * (double)cfg.n_head_kv * cfg.head_dim * cfg.n_layer,
-            [&] { return launch_decode_cluster(c->cluster, a, s); });
-        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
-            return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
-                               &c->d_state->err, s);
-        });
-        if (n_kernels) *n_kernels = n;
-        return err;
-    }
-    run(F_EMBED, q8_bytes(1, h) + 4.0 * h, 0.0,
-        [&] { return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, pdl, s); });
-    if (c->layer_kernel) {
-        // every layer as one cluster kernel; the residual stream alternates between two buffers
-        const double lbytes = q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + q8_bytes(2 * F, h) + q8_bytes(h, F) +
-                              16.0 * h;
-        for (int l = 0; l < cfg.n_layer; ++l) {
-            const LayerKArgs la = layer_args(c, l);
-            run(F_LAYER, lbytes, 8.0 * (double)cfg.n_head_kv * cfg.head_dim,
-                [&] { return launch_decode_layer(la, cfg.head_dim, pdl, s); });
-        }
-        float* xf = (cfg.n_layer & 1) ? c->d_x2 : c->d_x;
-        run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
-            return launch_gemv(c->head, xf, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
-                               &c->d_state->err, s);
-        });
-        if (n_kernels) *n_kernels = n;
-        return err;
-    }
+    auto stamped = [&](EpiArgs x) {
+        x.stamp = stp;
+        return x;
+    };
+    run(F_EMBED, q8_bytes(1, h) + 4.0 * h, 0.0, [&] {
+        return launch_embed(c->embd, nullptr, 1, c->d_state, c->d_state, c->d_x, cfg.n_vocab, pdl, s, stp);
+    });
     for (int l = 0; l < cfg.n_layer; ++l) {
         const LayerDev& L = c->layers[l];
         EpiArgs e = qkv_epi(c, l);
@@ -357,19 +255,22 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
             // attention + W_o per KV head (partials), the sum folded into the gate/up kernel's norm,
             // and the down projection's residual taken from that sum
             if (c->front_cl > 0) {
-                const FrontArgs fa = front_args(c, l);
+                FrontArgs fa = front_args(c, l);
                 run(F_FRONT, q8_bytes(qr + 2 * kvr, h) + q8_bytes(h, qr) + 8.0 * h + 4.0 * h * cfg.n_head_kv,
-                    8.0 * (double)cfg.n_head_kv * cfg.head_dim,
-                    [&] { return launch_layer_front(fa, cfg.head_dim, c->front_cl, pdl, s); });
+                    8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
+                        fa.stamp = stp;
+                        return launch_layer_front(fa, cfg.head_dim, c->front_cl, pdl, s);
+                    });
             } else {
                 run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0, [&] {
-                    return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s);
+                    return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, stamped(e), pdl,
+                                       &c->d_state->err, s);
                 });
                 run(F_ATTN_O, 4.0 * qr + q8_bytes(h, qr) + 4.0 * h * cfg.n_head_kv,
                     8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
                         return launch_attn_oproj(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
                                                  cfg.head_dim, cfg.max_seq, c->d_state, L.o, c->d_part, (int)h, pdl,
-                                                 &c->d_state->err, s);
+                                                 &c->d_state->err, s, stp);
                     });
             }
             if (c->mlp_clusters > 0) {
@@ -385,7 +286,10 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
                 ma.mlp_part = c->d_mlp;
                 ma.err = &c->d_state->err;
                 run(F_MLP, q8_bytes(2 * F, h) + q8_bytes(h, F) + 4.0 * h * (3 + cfg.n_head_kv + c->mlp_clusters), 0.0,
-                    [&] { return launch_decode_mlp(ma, pdl, s); });
+                    [&] {
+                        ma.stamp = stp;
+                        return launch_decode_mlp(ma, pdl, s);
+                    });
                 continue;
             }
             EpiArgs g;
@@ -396,31 +300,41 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
             pre.part_stride = (int)h;
             pre.x_sum_out = c->d_xsum;
             run(F_GATEUP, q8_bytes(2 * F, h) + 4.0 * h * (2 + cfg.n_head_kv) + 4.0 * F, 0.0, [&] {
-                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s,
-                                   &pre);
+                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, stamped(g), pdl,
+                                   &c->d_state->err, s, &pre);
             });
             EpiArgs rd;
             rd.y = c->d_x;
             rd.res = c->d_xsum;
             run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
-                [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, rd, pdl, &c->d_state->err, s); });
+                [&] {
+                    return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, stamped(rd), pdl, &c->d_state->err, s);
+                });
         } else {
             run(F_QKV, q8_bytes(qr + 2 * kvr, h) + 8.0 * h + 4.0 * (qr + 2 * kvr), 0.0,
-                [&] { return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, e, pdl, &c->d_state->err, s); });
+                [&] {
+                    return launch_gemv(L.qkv, c->d_x, L.attn_norm, cfg.rms_eps, EPI_QKV, stamped(e), pdl,
+                                       &c->d_state->err, s);
+                });
             run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
                 return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
                                                   cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
-                                                  &c->d_state->err, s);
+                                                  &c->d_state->err, s, stp);
             });
             run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h, 0.0,
-                [&] { return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
+                [&] {
+                    return launch_gemv(L.o, c->d_o, nullptr, 0.f, EPI_RESIDUAL, stamped(r), pdl, &c->d_state->err, s);
+                });
             EpiArgs g;
             g.a_out = c->d_a;
             run(F_GATEUP, q8_bytes(2 * F, h) + 8.0 * h + 4.0 * F, 0.0, [&] {
-                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, g, pdl, &c->d_state->err, s);
+                return launch_gemv(L.gu, c->d_x, L.ffn_norm, cfg.rms_eps, EPI_SILU, stamped(g), pdl,
+                                   &c->d_state->err, s);
             });
             run(F_DOWN, q8_bytes(h, F) + 4.0 * F + 8.0 * h, 0.0,
-                [&] { return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, r, pdl, &c->d_state->err, s); });
+                [&] {
+                    return launch_gemv(L.down, c->d_a, nullptr, 0.f, EPI_RESIDUAL, stamped(r), pdl, &c->d_state->err, s);
+                });
         }
     }
     if (c->mlp_clusters > 0) {  // the last layer's residual = its base + the MLP's cluster partials
@@ -429,15 +343,17 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, Profiler* prof 
         pre.n_part = c->mlp_clusters;
         pre.part_stride = (int)h;
         run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * h * c->mlp_clusters + 4.0 * cfg.n_vocab, 0.0, [&] {
-            return launch_gemv(c->head, c->d_xr, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
-                               &c->d_state->err, s, &pre);
+            return launch_gemv(c->head, c->d_xr, c->out_norm, cfg.rms_eps, EPI_ARGMAX, stamped(head_epi(c, -1)), pdl,
+                               &c->d_state->err, s, &pre, cfg.head_splits);
         });
     } else {
         run(F_HEAD, q8_bytes(cfg.n_vocab, h) + 8.0 * h + 4.0 * cfg.n_vocab, 0.0, [&] {
-            return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, head_epi(c, -1), pdl,
-                               &c->d_state->err, s);
+            return launch_gemv(c->head, c->d_x, c->out_norm, cfg.rms_eps, EPI_ARGMAX, stamped(head_epi(c, -1)), pdl,
+                               &c->d_state->err, s, nullptr, cfg.head_splits);
         });
     }
+    // the instrumented graph ends with a stamp kernel whose wait returns when the lm_head has completed
+    if (err == cudaSuccess && stamps) err = launch_stamp(stamps + 2 * n, s);
     if (n_kernels) *n_kernels = n;
     return err;
 }
@@ -471,7 +387,7 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
     }
     if (err == cudaSuccess)
         err = launch_gemv(c->head, c->d_x + (size_t)(T - 1) * h, c->out_norm, cfg.rms_eps, EPI_ARGMAX,
-                          head_epi(c, index_pos + T), true, &c->d_state->err, s);
+                          head_epi(c, index_pos + T), true, &c->d_state->err, s, nullptr, cfg.head_splits);
     return err;
 }
 
@@ -590,7 +506,13 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         return LQ8_ERR_ARG;
     if (C.n_head % C.n_head_kv != 0) return LQ8_ERR_ARG;
     if (C.decode_kernel < 0 || C.decode_kernel > 5) return LQ8_ERR_ARG;
+    // 2 and 5 (one cluster kernel for the whole step / per layer) were measured
+    // slower than the per-layer kernels and are not built
+    if (C.decode_kernel == 2 || C.decode_kernel == 5) return LQ8_ERR_UNSUPPORTED;
     if (C.rope_style != 0 && C.rope_style != 1) return LQ8_ERR_ARG;
+    if (C.head_splits < 0 || C.head_splits == 1 || C.head_splits > 8 ||
+        (C.head_splits > 0 && C.n_embd > 0 && C.n_embd / 32 < C.head_splits))
+        return LQ8_ERR_ARG;
     if (!C.tied_output && !w->output) return LQ8_ERR_ARG;
     for (int l = 0; l < C.n_layer; ++l) {
         const llama_q8_layer_weights& L = w->layers[l];
@@ -755,7 +677,6 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_a, sizeof(float) * T * F));
     LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
     LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
-    LOAD_CK(cudaMalloc(&c->d_x2, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_xr, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_mlp, sizeof(float) * h * (F / 32 / 8 + 1)));
     LOAD_CK(cudaMalloc(&c->d_logits, sizeof(float) * V));
@@ -775,16 +696,9 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMallocHost(&c->h_logits, sizeof(float) * V));
     LOAD_CK(cudaMallocHost(&c->h_state, sizeof(DevState)));
     LOAD_CK(cudaStreamSynchronize(c->stream));
-    // decode path: the whole layer stack as one cluster when asked for and it fits
-    // decode_kernel: 0 automatic (three per layer when the model fits, else four, else five), 1 five
-    // per layer, 2 one cluster kernel for the whole step, 3 four per layer, 4 three per layer, 5 one
-    // cluster kernel per layer (measured slower than three per layer on the models here)
+    // decode_kernel: 0 automatic (two per layer when the model fits, else three, four or five),
+    // 1 five per layer, 3 four per layer, 4 three per layer
     bool unsupported = false;
-    if (C.decode_kernel == 5) {
-        c->layer_kernel = decode_layer_supported(layer_args(c, 0), hd);
-        cudaGetLastError();
-        unsupported = !c->layer_kernel;
-    }
     if (C.decode_kernel == 0 || C.decode_kernel == 3 || C.decode_kernel == 4) {
         c->fuse_o = attn_oproj_fused_supported(C.n_head, C.n_head_kv, hd, c->layers[0].o);
         cudaGetLastError();
@@ -798,30 +712,6 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         free_ctx_memory(c);
         delete c;
         return LQ8_ERR_UNSUPPORTED;
-    }
-    if (C.decode_kernel == 2) {
-        c->cluster = decode_cluster_size(h, C.n_head, C.n_head_kv, hd, F);
-        cudaGetLastError();
-        if (c->cluster <= 0) {
-            free_ctx_memory(c);
-            delete c;
-            return LQ8_ERR_UNSUPPORTED;
-        }
-    }
-    if (c->cluster > 0) {
-        std::vector<LayerPtrs> lp(L);
-        for (int l = 0; l < L; ++l) {
-            lp[l].qkv = c->layers[l].qkv;
-            lp[l].o = c->layers[l].o;
-            lp[l].gu = c->layers[l].gu;
-            lp[l].down = c->layers[l].down;
-            lp[l].attn_norm = c->layers[l].attn_norm;
-            lp[l].ffn_norm = c->layers[l].ffn_norm;
-            lp[l].kc = c->kcache(l);
-            lp[l].vc = c->vcache(l);
-        }
-        LOAD_CK(cudaMalloc(&c->d_layer_ptrs, sizeof(LayerPtrs) * L));
-        LOAD_CK(cudaMemcpy(c->d_layer_ptrs, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice));
     }
     LOAD_CK(ensure_decode_graph(c));
 #undef LOAD_CK
@@ -934,22 +824,44 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
     if (ctx->len == 0) return LQ8_ERR_STATE;
     if ((int64_t)ctx->len + n_steps > ctx->cfg.max_seq) return LQ8_ERR_CTX;
     LQ8_CK(ctx, cudaSetDevice(ctx->device));
-    Profiler prof;
-    prof.s = ctx->stream;
-    int n = 0;
-    LQ8_CK(ctx, cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t lerr = enqueue_decode_step(ctx, &n, &prof);
-    cudaGraph_t g = nullptr;
-    cudaError_t cerr = cudaStreamEndCapture(ctx->stream, &g);
-    if (lerr != cudaSuccess || cerr != cudaSuccess) {
-        if (g) cudaGraphDestroy(g);
-        ctx->failed = true;
-        return LQ8_ERR_CUDA;
+    // the instrumented copy of the decode graph: the same launches with their stamp slots set
+    const int nk = ctx->decode_kernels;
+    const size_t slots = 2 * (size_t)(nk + 1);
+    const size_t sbytes = slots * sizeof(unsigned long long);
+    unsigned long long* d_st = nullptr;
+    unsigned long long* h_st = nullptr;
+    LQ8_CK(ctx, cudaMalloc(&d_st, sbytes));
+    if (cudaMallocHost(&h_st, sbytes * (size_t)n_steps) != cudaSuccess) {
+        cudaFree(d_st);
+        return LQ8_ERR_OOM;
     }
+    StepLayout layout;
+    int n = 0;
     cudaGraphExec_t exec = nullptr;
-    cerr = cudaGraphInstantiate(&exec, g, 0);
-    cudaGraphDestroy(g);
-    if (cerr != cudaSuccess) {
+    cudaError_t err = cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal);
+    if (err == cudaSuccess) {
+        cudaError_t lerr = enqueue_decode_step(ctx, &n, &layout, d_st);
+        cudaGraph_t g = nullptr;
+        err = cudaStreamEndCapture(ctx->stream, &g);
+        if (err == cudaSuccess) err = lerr;
+        if (err == cudaSuccess && n != nk) err = cudaErrorUnknown;
+        if (err == cudaSuccess) err = cudaGraphInstantiate(&exec, g, 0);
+        if (g) cudaGraphDestroy(g);
+    }
+    if (err == cudaSuccess) err = launch_set_state(ctx->d_state, -1, -1, 0, ctx->stream);
+    ctx->launches += 1;
+    for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
+        err = cudaMemsetAsync(d_st, 0xff, sbytes, ctx->stream);
+        if (err == cudaSuccess) err = cudaGraphLaunch(exec, ctx->stream);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(h_st + (size_t)i * slots, d_st, sbytes, cudaMemcpyDeviceToHost, ctx->stream);
+        ctx->launches += nk + 1;
+    }
+    if (err == cudaSuccess) err = cudaStreamSynchronize(ctx->stream);
+    if (exec) cudaGraphExecDestroy(exec);
+    cudaFree(d_st);
+    if (err != cudaSuccess) {
+        cudaFreeHost(h_st);
         ctx->failed = true;
         return LQ8_ERR_CUDA;
     }
@@ -958,31 +870,34 @@ llama_q8_status llama_q8_profile_decode(llama_q8_ctx* ctx, int32_t n_steps, llam
         std::strncpy(stats[f].name, kFamilyNames[f], sizeof(stats[f].name) - 1);
         stats[f].launches = 0;
         stats[f].ms = 0.0;
+        stats[f].span_ms = 0.0;
         stats[f].bytes = 0.0;
     }
-    cudaError_t err = launch_set_state(ctx->d_state, -1, -1, 0, ctx->stream);
-    ctx->launches += 1;
-    for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
-        err = cudaGraphLaunch(exec, ctx->stream);
-        if (err == cudaSuccess) err = cudaStreamSynchronize(ctx->stream);
-        ctx->launches += n;
+    // Launch k's exclusive time runs from the first return of its dependency
+    // wait (its predecessor has completed) to that of launch k + 1 (it has
+    // completed); its span starts at its first CTA's entry instead.
+    bool complete = true;
+    for (int i = 0; i < n_steps; ++i) {
+        const unsigned long long* t = h_st + (size_t)i * slots;
         const double kv_len = (double)(ctx->len + i + 1);  // the step's token sits at len + i
-        for (const auto& r : prof.recs) {
-            float ms = 0.f;
-            if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, r.a, r.b);
+        for (int k = 0; k < nk; ++k) {
+            const unsigned long long e0 = t[2 * k], w0 = t[2 * k + 1], w1 = t[2 * k + 3];
+            if (e0 == ~0ull || w0 == ~0ull || w1 == ~0ull || w1 < w0 || w1 < e0) {
+                complete = false;
+                continue;
+            }
+            const StepLayout::Rec& r = layout.recs[k];
             stats[r.family].launches += 1;
-            stats[r.family].ms += ms;
+            stats[r.family].ms += (double)(w1 - w0) * 1e-6;
+            stats[r.family].span_ms += (double)(w1 - e0) * 1e-6;
             stats[r.family].bytes += r.bytes + r.kv_per_pos * kv_len;
         }
     }
-    cudaGraphExecDestroy(exec);
-    if (err != cudaSuccess) {
-        ctx->failed = true;
-        return LQ8_ERR_CUDA;
-    }
-    *n_stats = F_COUNT;
+    cudaFreeHost(h_st);
     ctx->len += n_steps;
-    return LQ8_OK;
+    if (!complete) return LQ8_ERR_STATE;
+    *n_stats = F_COUNT;
+    return device_status(ctx);
 }
 
 llama_q8_status llama_q8_sync(llama_q8_ctx* ctx) {

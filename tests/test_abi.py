@@ -66,7 +66,12 @@ def test_config_validation_without_a_gpu(B):
                         (dict(n_head_kv=4), B.LQ8_ERR_ARG), (dict(n_layer=0), B.LQ8_ERR_ARG),
                         (dict(tied_output=0), B.LQ8_ERR_ARG), (dict(decode_kernel=6), B.LQ8_ERR_ARG),
                         (dict(decode_kernel=-1), B.LQ8_ERR_ARG), (dict(rope_style=2), B.LQ8_ERR_ARG),
-                        (dict(rope_style=-1), B.LQ8_ERR_ARG)]:
+                        (dict(rope_style=-1), B.LQ8_ERR_ARG),
+                        # the one-cluster whole-step and per-layer forms are not built
+                        (dict(decode_kernel=2), B.LQ8_ERR_UNSUPPORTED), (dict(decode_kernel=5), B.LQ8_ERR_UNSUPPORTED),
+                        # split-K lm_head: 2..8 CTAs, no more than n_embd / 32
+                        (dict(head_splits=1), B.LQ8_ERR_ARG), (dict(head_splits=9), B.LQ8_ERR_ARG),
+                        (dict(head_splits=-1), B.LQ8_ERR_ARG)]:
         c = B.make_config(dict(cfg, **bad))
         w, keep = B.make_weights(cfg, t, on_device=False)
         out = C.c_void_p()

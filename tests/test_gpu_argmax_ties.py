@@ -6,7 +6,8 @@ every logit value occurs at many indices spread over the whole vocabulary
 (and so over many CTAs of the lm_head kernel). The duplicated rows must give
 bit-identical logits, and the greedy token must be the lowest index holding
 the maximum — for the prefill, the CUDA-graph decode step and the device-fed
-generation loop, with the head untied (output.weight) and tied (token_embd).
+generation loop, with the head untied (output.weight) and tied (token_embd),
+row-parallel and split-K over a 2-CTA cluster.
 """
 import numpy as np
 import pytest
@@ -27,11 +28,11 @@ def _periodic(w):
     return np.ascontiguousarray(w[np.arange(rows) % PERIOD])
 
 
-@pytest.mark.parametrize("tied", [0, 1])
-def test_argmax_returns_lowest_index_among_equal_maxima(tied):
+@pytest.mark.parametrize("tied,head_splits", [(0, 0), (1, 0), (0, 2)])
+def test_argmax_returns_lowest_index_among_equal_maxima(tied, head_splits):
     require_gpu()
     B = binding()
-    cfg = dict(BASE, tied_output=tied)
+    cfg = dict(BASE, tied_output=tied, head_splits=head_splits)
     host = synth.model_weights_f32(cfg, 7)
     head = "token_embd.weight" if tied else "output.weight"
     host[head] = _periodic(host[head])

@@ -28,10 +28,9 @@ def m135():
     models = {
         "front": B.Model(CFG, dev_t, on_device=True),                          # automatic: two kernels per layer
         "three": B.Model(dict(CFG, decode_kernel=4), dev_t, on_device=True),   # front, gate/up, down
-        "layer": B.Model(dict(CFG, decode_kernel=5), dev_t, on_device=True),   # one cluster kernel per layer
         "four": B.Model(dict(CFG, decode_kernel=3), dev_t, on_device=True),    # attention applies W_o
         "layered": B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True), # five kernels per layer
-        "cluster": B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True), # one-cluster decode step
+        "splitk": B.Model(dict(CFG, head_splits=2), dev_t, on_device=True),    # split-K lm_head
     }
     del dev_t
     torch.cuda.empty_cache()
@@ -42,7 +41,7 @@ def m135():
             m.close()
 
 
-@pytest.fixture(params=["front", "three", "four", "layered", "layer", "cluster"])
+@pytest.fixture(params=["front", "three", "four", "layered", "splitk"])
 def either(request, m135):
     return m135[request.param], m135["oracle"]
 
@@ -158,7 +157,7 @@ def test_prefill_and_decode_paths_agree(either):
 
 
 def test_device_resident_api(m135):
-    model, layered, cluster = m135["front"], m135["layered"], m135["cluster"]
+    model, layered = m135["front"], m135["layered"]
     prompt = synth.prompt_ids(203, V, 0)
     ref = model.generate(prompt, 16)
     d_ids = torch.from_numpy(prompt).cuda()
@@ -172,10 +171,8 @@ def test_device_resident_api(m135):
     assert model.cache_len() == 203 + 16
     assert model.decode_kernel_count() == 1 + 2 * CFG["n_layer"] + 1   # layer front + MLP
     assert m135["three"].decode_kernel_count() == 1 + 3 * CFG["n_layer"] + 1
-    assert m135["layer"].decode_kernel_count() == 1 + CFG["n_layer"] + 1
     assert m135["four"].decode_kernel_count() == 1 + 4 * CFG["n_layer"] + 1
     assert layered.decode_kernel_count() == 1 + 5 * CFG["n_layer"] + 1
-    assert cluster.decode_kernel_count() == 2                            # layers in one cluster + lm_head
 
 
 LONG_PROMPT = 3900
@@ -210,3 +207,27 @@ def test_long_context_decode_matches_oracle(either, long_run):
         assert got[-1] == ref_ids[step], (pos - 1, got[-1], ref_ids[step])
     assert model.cache_len() == CFG["max_seq"]
     assert got == ref_ids
+
+
+@pytest.mark.parametrize("variant", ["front", "layered"])
+def test_decode_timeline_profile(m135, variant):
+    """The instrumented copy of the decode graph (timeline stamps on every
+    launch) computes the same greedy tokens as the product graph, and reports
+    every launch of every step: exclusive times that add up to the step and
+    spans that contain them."""
+    model = m135[variant]
+    prompt = synth.prompt_ids(203, V, 0)
+    ref = model.generate(prompt, 17)
+    assert model.forward_argmax(prompt, 0) == ref[0]
+    prof = model.profile_decode(16)                       # decode steps 1..16, instrumented
+    assert model.cache_len() == 203 + 16
+    d_out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    model.decode_async(1, d_out)                          # step 17 on the product graph
+    model.sync()
+    assert int(d_out.cpu()[0]) == ref[17]
+    launches = sum(v[0] for v in prof.values())
+    assert launches == 16 * model.decode_kernel_count()
+    for name, (n, ms, span_ms, nbytes) in prof.items():
+        if n:
+            assert 0.0 < ms <= span_ms and nbytes > 0, name
+    assert prof["embed"][0] == 16 and prof["gemv_head_argmax"][0] == 16

@@ -2,8 +2,8 @@
 i + head_dim/2, the convention the pages' loader picks for the architectures it
 lists, "量化 llama 的一次前向", RoPE：两种约定，按架构名选) against the oracle's
 NEOX forward: identical greedy tokens and logits within tolerance for the
-two-kernel decode layer, the five-kernel layer and the one-cluster step, the
-tensor-core prefill, and the K/V cache in natural dim order."""
+two-, three- and five-kernel decode layers, the tensor-core prefill, and the
+K/V cache in natural dim order."""
 import numpy as np
 import pytest
 
@@ -27,7 +27,7 @@ def neox():
     models = {
         "auto": B.Model(CFG, dev_t, on_device=True),
         "layered": B.Model(dict(CFG, decode_kernel=1), dev_t, on_device=True),
-        "cluster": B.Model(dict(CFG, decode_kernel=2), dev_t, on_device=True),
+        "three": B.Model(dict(CFG, decode_kernel=4), dev_t, on_device=True),
     }
     del dev_t
     torch.cuda.empty_cache()
@@ -36,7 +36,7 @@ def neox():
         m.close()
 
 
-@pytest.mark.parametrize("form", ["auto", "layered", "cluster"])
+@pytest.mark.parametrize("form", ["auto", "three", "layered"])
 def test_neox_generation_matches_oracle(neox, form):
     models, ora_t = neox
     model = models[form]
