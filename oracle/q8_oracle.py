@@ -34,6 +34,10 @@ Readings where the pages are silent:
   R5 Attention scale 1 / sqrt(head_dim), applied as a division in f64.
   R6 Activations are never quantised: Q8_0 weights times f32 activations.
   R7 Greedy argmax returns the lowest index among equal maxima.
+  R13 Q5_0 / Q4_K / Q6_K blocks: the pages give their names, their timings
+     and the byte census of a Q4_K_M file ([SP] "CPU GGUF"), not their
+     layouts; those follow the published GGUF block definitions, and their
+     byte sizes reproduce the census.
 
 Parity pins (tests/test_oracle_pins.py): every public function here is pinned
 against byte counts printed on the pages, hand-computed fixtures under
@@ -108,6 +112,123 @@ def dequantize_q8_0(blob: np.ndarray, rows: int, k: int) -> np.ndarray:
     dh, q = q8_0_scales_and_codes(blob, rows, k)
     w = dh.astype(np.float32)[..., None] * q.reshape(rows, k // QK8_0, QK8_0).astype(np.float32)
     return w.reshape(rows, k)
+
+
+# --------------------------------------------------------------------------
+# Other GGUF block formats (reading R13): Q5_0, Q4_K, Q6_K
+# --------------------------------------------------------------------------
+# [SP] "CPU GGUF：decode 快，prefill 慢" times QMatMul in Q5_0, Q4K and Q6K and
+# lists the tensor census of the 135M Q4_K_M file (Q4K 16 tensors 7.6 MiB,
+# Q5_0 166 tensors 51.2 MiB, Q6K 14 tensors 9.7 MiB, Q8_0 15 tensors 30.3 MiB);
+# it notes that K-quant blocks hold 256 weights, so rows of 576 fall back to
+# Q5_0. The pages do not print the layouts inside a block; they are read from
+# the published GGUF block definitions, and the byte sizes below reproduce the
+# census exactly (tests/test_oracle_pins.py).
+GGUF_TYPE_Q5_0, GGUF_TYPE_Q8_0, GGUF_TYPE_Q4_K, GGUF_TYPE_Q6_K = 6, 8, 12, 14
+# type -> (weights per block, bytes per block)
+BLOCK_FORMATS = {GGUF_TYPE_Q5_0: (32, 22), GGUF_TYPE_Q8_0: (32, 34), GGUF_TYPE_Q4_K: (256, 144),
+                 GGUF_TYPE_Q6_K: (256, 210)}
+
+
+def block_format_row_bytes(gguf_type: int, k: int) -> int:
+    """Bytes one row of k weights occupies in a block format."""
+    qk, nbytes = BLOCK_FORMATS[gguf_type]
+    if k % qk:
+        raise ValueError(f"row length {k} is not a multiple of the block size {qk}")
+    return k // qk * nbytes
+
+
+def _blocks(blob, rows, k, gguf_type):
+    qk, nbytes = BLOCK_FORMATS[gguf_type]
+    return np.ascontiguousarray(blob, dtype=np.uint8).reshape(rows, k // qk, nbytes)
+
+
+def _f16(b2: np.ndarray) -> np.ndarray:
+    """Little-endian fp16 in the last axis (2 bytes) -> f64."""
+    return np.ascontiguousarray(b2).view("<f2")[..., 0].astype(np.float64)
+
+
+def dequantize_q5_0(blob: np.ndarray, rows: int, k: int) -> np.ndarray:
+    """Q5_0 -> f64 [rows, k]. Block of 32 weights, 22 bytes: fp16 scale d, a
+    32-bit little-endian word qh whose bit j is the fifth bit of weight j, and
+    16 bytes qs whose byte j holds the low four bits of weight j (low nibble)
+    and of weight j + 16 (high nibble). w_j = d * (code_j - 16)."""
+    b = _blocks(blob, rows, k, GGUF_TYPE_Q5_0)
+    d = _f16(b[..., 0:2])
+    qh = np.ascontiguousarray(b[..., 2:6]).view("<u4")[..., 0].astype(np.int64)
+    qs = b[..., 6:22].astype(np.int64)
+    low = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)                   # weights 0..15, 16..31
+    high = (qh[..., None] >> np.arange(32)) & 1
+    q = (low | (high << 4)) - 16
+    return (d[..., None] * q).reshape(rows, k)
+
+
+def q4_k_scales_mins(sc12: np.ndarray):
+    """The eight 6-bit (scale, min) pairs packed into a Q4_K block's 12 bytes:
+    sub-blocks 0-3 take the low six bits of bytes j (scale) and j + 4 (min);
+    sub-blocks 4-7 take the low / high nibble of byte j + 4 for the low four
+    bits and the top two bits of bytes j - 4 (scale) and j (min)."""
+    b = sc12.astype(np.int64)
+    sc = np.empty(b.shape[:-1] + (8,), np.int64)
+    mn = np.empty_like(sc)
+    for j in range(4):
+        sc[..., j] = b[..., j] & 63
+        mn[..., j] = b[..., j + 4] & 63
+    for j in range(4, 8):
+        sc[..., j] = (b[..., j + 4] & 0x0F) | ((b[..., j - 4] >> 6) << 4)
+        mn[..., j] = (b[..., j + 4] >> 4) | ((b[..., j] >> 6) << 4)
+    return sc, mn
+
+
+def dequantize_q4_k(blob: np.ndarray, rows: int, k: int, parts: bool = False):
+    """Q4_K -> f64 [rows, k]. Block of 256 weights, 144 bytes: fp16 d, fp16
+    dmin, 12 bytes of packed 6-bit (scale, min) pairs for eight sub-blocks of
+    32, then 128 bytes of 4-bit codes: bytes [32c, 32c + 32) hold sub-block 2c
+    in their low nibbles and sub-block 2c + 1 in their high nibbles.
+    w = d * scale_s * q - dmin * min_s. parts=True returns the two terms
+    (d * scale * q, dmin * min) separately."""
+    b = _blocks(blob, rows, k, GGUF_TYPE_Q4_K)
+    d = _f16(b[..., 0:2])
+    dmin = _f16(b[..., 2:4])
+    sc, mn = q4_k_scales_mins(b[..., 4:16])
+    qs = b[..., 16:144].astype(np.int64).reshape(rows, k // 256, 4, 32)
+    q = np.stack([qs & 0x0F, qs >> 4], axis=3).reshape(rows, k // 256, 8, 32)   # [.., sub-block, 32]
+    scaled = d[..., None, None] * sc[..., None] * q
+    offset = np.broadcast_to((dmin[..., None] * mn)[..., None], scaled.shape)
+    if parts:
+        return scaled.reshape(rows, k), np.ascontiguousarray(offset).reshape(rows, k)
+    return (scaled - offset).reshape(rows, k)
+
+
+def dequantize_q6_k(blob: np.ndarray, rows: int, k: int) -> np.ndarray:
+    """Q6_K -> f64 [rows, k]. Block of 256 weights, 210 bytes: 128 bytes ql
+    (low four bits), 64 bytes qh (top two bits), 16 int8 scales (one per 16
+    weights), fp16 d. Each half h of 128 weights uses ql[64h, 64h + 64) and
+    qh[32h, 32h + 32): for l < 32, weights 128h + 32g + l (g = 0..3) take the
+    low (g even) or high (g odd) nibble of ql[64h + l + 32 (g % 2)] and bits
+    2g, 2g + 1 of qh[32h + l]. w_t = d * scale[t // 16] * (code_t - 32)."""
+    b = _blocks(blob, rows, k, GGUF_TYPE_Q6_K)
+    nb = k // 256
+    ql = b[..., 0:128].astype(np.int64).reshape(rows, nb, 2, 64)
+    qh = b[..., 128:192].astype(np.int64).reshape(rows, nb, 2, 32)
+    scales = np.ascontiguousarray(b[..., 192:208]).view(np.int8).astype(np.int64)
+    d = _f16(b[..., 208:210])
+    codes = np.empty((rows, nb, 2, 4, 32), np.int64)
+    for g in range(4):
+        nib = ql[..., 32 * (g % 2): 32 * (g % 2) + 32]
+        low = (nib & 0x0F) if g < 2 else (nib >> 4)
+        codes[..., g, :] = low | (((qh >> (2 * g)) & 3) << 4)
+    q = codes.reshape(rows, nb, 256) - 32
+    w = d[..., None] * np.repeat(scales, 16, axis=-1) * q
+    return w.reshape(rows, k)
+
+
+def dequantize_block_format(gguf_type: int, blob: np.ndarray, rows: int, k: int) -> np.ndarray:
+    """Any of the block formats above (and Q8_0) -> f64 [rows, k]."""
+    if gguf_type == GGUF_TYPE_Q8_0:
+        return dequantize_q8_0(blob, rows, k).astype(np.float64)
+    return {GGUF_TYPE_Q5_0: dequantize_q5_0, GGUF_TYPE_Q4_K: dequantize_q4_k,
+            GGUF_TYPE_Q6_K: dequantize_q6_k}[gguf_type](blob, rows, k)
 
 
 # --------------------------------------------------------------------------
