@@ -325,6 +325,47 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
 llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, const float* x,
                                    int64_t m, float* y, int32_t flags, void* stream);
 
+/* Other GGUF block formats in the matrix-vector product ("速度", CPU GGUF：
+ * decode 快，prefill 慢: the pages time QMatMul in Q5_0, Q4K and Q6K and find a
+ * 135M Q4_K_M file mostly Q5_0, with Q4K / Q6K for the down projections whose
+ * rows of 1536 are a multiple of the 256-weight K-quant block). gguf_type is
+ * the GGUF tensor type id: 6 = Q5_0 (32 weights in 22 bytes: fp16 d, 32 bits
+ * of fifth bits, 16 bytes of low nibbles; w = d (q - 16)), 12 = Q4_K (256
+ * weights in 144 bytes: fp16 d and dmin, 12 bytes of 6-bit scales and mins for
+ * eight sub-blocks of 32, 128 bytes of 4-bit codes; w = d sc q - dmin m),
+ * 14 = Q6_K (256 weights in 210 bytes: 128 bytes of low nibbles, 64 of top
+ * two bits, 16 int8 scales per 16 weights, fp16 d; w = d sc (q - 32)); 8 =
+ * Q8_0 routes to the calls above. Layouts inside the blocks are the
+ * published GGUF definitions. A [rows, k] matrix is rows * (k / block)
+ * blocks, row-major, as in the file; k must be a multiple of the block size
+ * (LQ8_ERR_ARG). Other types: LQ8_ERR_UNSUPPORTED. */
+#define LLAMA_Q8_GGUF_Q5_0 6
+#define LLAMA_Q8_GGUF_Q8_0 8
+#define LLAMA_Q8_GGUF_Q4_K 12
+#define LLAMA_Q8_GGUF_Q6_K 14
+
+/* Bytes of the library's device layout of a [rows, k] matrix of gguf_type
+ * (rows padded to a multiple of 32; the same bytes per block otherwise); 0
+ * for an unsupported type or a k that is not a multiple of the block. */
+size_t llama_q8_packed_bytes_fmt(int32_t gguf_type, int64_t rows, int64_t k);
+
+/* Repack device blocks[rows][k / block][block bytes] into the device layout
+ * (packed: llama_q8_packed_bytes_fmt bytes, device memory, caller-owned; the
+ * padding rows are zeroed). Each (32-row tile, block) becomes one contiguous
+ * record whose fields are regrouped by row. Enqueues on `stream`. */
+llama_q8_status llama_q8_pack_fmt(int32_t gguf_type, const void* blocks, int64_t rows, int64_t k, void* packed,
+                                  void* stream);
+
+/* y[rows] = W x for one token (the decode product): x[k] and y[rows] f32
+ * device memory, W packed by llama_q8_pack_fmt. Codes are converted to f32
+ * exactly and multiplied in f32 with f32 accumulation; Q4_K subtracts
+ * dmin * m * (sum of x over the sub-block). packed and x must be 16-byte
+ * aligned (LQ8_ERR_ARG); k above the shared-memory limit of the kernel
+ * (>= 32768 for every type) gives LQ8_ERR_UNSUPPORTED. flags: as
+ * llama_q8_matmul_ex (LQ8_MATMUL_EARLY_WEIGHTS). Enqueues on `stream`. */
+llama_q8_status llama_q8_matvec_fmt(int32_t gguf_type, const void* packed, int64_t rows, int64_t k, const float* x,
+                                    float* y, int32_t flags, void* stream);
+
 /* Grouped-query attention over a KV cache: for each of T queries at
  * positions index_pos + t, out = softmax(q k^T / sqrt(head_dim) + mask) v,
  * query head h reading KV head h / (n_head / n_head_kv). q[T][n_head][head_dim];

@@ -32,7 +32,8 @@ EXPORTS = ("llama_q8_load", "llama_q8_forward", "llama_q8_forward_argmax", "llam
            "llama_q8_attention_workspace_bytes", "llama_q8_attention", "llama_q8_launch_count",
            "llama_q8_profile_decode", "llama_q8_attention_decode_noalloc", "llama_q8_attention_decode",
            "llama_q8_selftest_wait_timeout", "llama_q8_rope_style_for_arch", "llama_q8_gguf_config",
-           "llama_q8_load_gguf")
+           "llama_q8_load_gguf", "llama_q8_packed_bytes_fmt", "llama_q8_pack_fmt", "llama_q8_matvec_fmt")
+GGUF_Q5_0, GGUF_Q8_0, GGUF_Q4_K, GGUF_Q6_K = 6, 8, 12, 14
 
 
 class Q8Error(RuntimeError):
@@ -106,6 +107,9 @@ def lib() -> C.CDLL:
         "llama_q8_attention_decode": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "llama_q8_profile_decode": (i32, [vp, i32, C.POINTER(llama_q8_kernel_stat), i32, C.POINTER(i32)]),
         "llama_q8_selftest_wait_timeout": (i32, [C.POINTER(i32)]),
+        "llama_q8_packed_bytes_fmt": (sz, [i32, i64, i64]),
+        "llama_q8_pack_fmt": (i32, [i32, vp, i64, i64, vp, vp]),
+        "llama_q8_matvec_fmt": (i32, [i32, vp, i64, i64, vp, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -315,6 +319,19 @@ def llama_q8_selftest_wait_timeout() -> int:
 def llama_q8_matmul_ex(packed, rows: int, k: int, x, m: int, y, flags: int, stream=0) -> None:
     check(lib().llama_q8_matmul_ex(ptr(packed), rows, k, ptr(x), m, ptr(y), flags, stream or None),
           "llama_q8_matmul_ex")
+
+
+def llama_q8_packed_bytes_fmt(gguf_type: int, rows: int, k: int) -> int:
+    return int(lib().llama_q8_packed_bytes_fmt(gguf_type, rows, k))
+
+
+def llama_q8_pack_fmt(gguf_type: int, blocks, rows: int, k: int, packed, stream=0) -> None:
+    check(lib().llama_q8_pack_fmt(gguf_type, ptr(blocks), rows, k, ptr(packed), stream or None), "llama_q8_pack_fmt")
+
+
+def llama_q8_matvec_fmt(gguf_type: int, packed, rows: int, k: int, x, y, flags: int = 0, stream=0) -> None:
+    check(lib().llama_q8_matvec_fmt(gguf_type, ptr(packed), rows, k, ptr(x), ptr(y), flags, stream or None),
+          "llama_q8_matvec_fmt")
 
 
 def llama_q8_attention_workspace_bytes(n_head: int, n_head_kv: int, head_dim: int, cache_stride: int) -> int:

@@ -551,6 +551,14 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
         const int i = tid + u * kCaCT;
         gpre[u] = i < h ? fa.g[i] : 0.0f;
     }
+    // the rotary row of this position (the table is constant and pos was written
+    // two or more launches back): into shared memory before the wait, so the
+    // rotation after the projections reads no global memory
+    __shared__ float rope_cs[2][HD / 2];
+    if (tid < HD / 2) {
+        rope_cs[0][tid] = fa.rope_cos[(int64_t)pos * (HD / 2) + tid];
+        rope_cs[1][tid] = fa.rope_sin[(int64_t)pos * (HD / 2) + tid];
+    }
     pdl_wait();
     if (tid == 0) {
         pdl_launch_dependents();
@@ -562,9 +570,28 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     {
         float ss = 0.0f;
         const bool keep = fa.x_store && kh == 0 && rank == 0;
+        // x and every partial of each element are requested before any is used,
+        // so the whole input costs one memory round trip
+        constexpr int kMaxParts = 8;
+        float xin[kGPre], xp[kGPre][kMaxParts];
+#pragma unroll
+        for (int u = 0; u < kGPre; ++u) {
+            const int i = tid + u * kCaCT;
+            xin[u] = i < h ? fa.x[i] : 0.0f;
+#pragma unroll
+            for (int p = 0; p < kMaxParts; ++p)
+                xp[u][p] = (i < h && p < fa.n_xparts) ? fa.xparts[(size_t)p * h + i] : 0.0f;
+        }
         for (int i = tid, u = 0; i < h; i += kCaCT, ++u) {
-            float v = fa.x[i];
-            for (int p = 0; p < fa.n_xparts; ++p) v += fa.xparts[(size_t)p * h + i];
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kGPre; ++w)
+                if (w == u) {
+                    v = xin[w];
+#pragma unroll
+                    for (int p = 0; p < kMaxParts; ++p)
+                        if (p < fa.n_xparts) v += xp[w][p];
+                }
             if (keep) fa.x_store[i] = v;
             ss = fmaf(v, v, ss);
             float gg = 0.0f;
@@ -588,9 +615,8 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
     // ---- this CTA's projection tiles; rotated rows to every CTA of the cluster ----------
     mbar_wait_bounded(&wq_bar, 0, fa.err, 25);
     {
-        const int half = HD >> 1;
-        const float* cosr = fa.rope_cos + (int64_t)pos * half;
-        const float* sinr = fa.rope_sin + (int64_t)pos * half;
+        const float* cosr = rope_cs[0];
+        const float* sinr = rope_cs[1];
         int u = 0;
         for (int i = rank; i < n_qkv; i += CL, ++u) {
             const uint8_t* tw = WQ + (size_t)u * nbx * 1088;

@@ -111,6 +111,17 @@ cudaError_t launch_gemv(const PackedQ8& W, const float* x, const float* norm_g, 
                         const EpiArgs& e, bool pdl, int* err, cudaStream_t s, const GemvPreSum* pre = nullptr,
                         int force_splits = 0);
 size_t gemv_max_k();
+// gemv_formats.cu: the matrix-vector product for other GGUF block formats
+// (GGUF type ids), on the library's repacked layout of each.
+constexpr int kGgufQ5_0 = 6, kGgufQ8_0 = 8, kGgufQ4_K = 12, kGgufQ6_K = 14;
+bool fmt_supported(int type);                        // Q5_0, Q4_K, Q6_K
+int fmt_block_weights(int type);                     // 32 or 256
+int64_t fmt_packed_bytes(int type, int64_t rows, int64_t k);
+int64_t fmt_max_k(int type);
+cudaError_t launch_pack_fmt(int type, const uint8_t* src, int64_t rows, int64_t k, uint8_t* dst, cudaStream_t s);
+cudaError_t launch_gemv_fmt(int type, const uint8_t* packed, int rows, int k, const float* x, float* y, bool pdl,
+                            int* err, cudaStream_t s);
+cudaError_t init_gemv_fmt_attributes();
 // gemm.cu (m > 1): CUDA-core kernel for a few rows
 cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
                         const EpiArgs& e, bool pdl, cudaStream_t s);

@@ -109,14 +109,31 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
         stamp_at(ma.stamp, 1);
     }
     float ss = 0.0f;
+    // x and every attention partial are requested before any is used: one round trip
+    constexpr int kMaxParts = 8;
+    float4 xin[kGPre], xp[kGPre][kMaxParts];
+#pragma unroll
+    for (int u = 0; u < kGPre; ++u) {
+        const int i = tid * 4 + u * kMlpCT * 4;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        xin[u] = i < h ? *reinterpret_cast<const float4*>(ma.x + i) : z;
+#pragma unroll
+        for (int p = 0; p < kMaxParts; ++p)
+            xp[u][p] = (i < h && p < ma.n_attn_part)
+                           ? *reinterpret_cast<const float4*>(ma.attn_part + (size_t)p * h + i)
+                           : z;
+    }
 #pragma unroll
     for (int u = 0; u < kGPre; ++u) {
         const int i = tid * 4 + u * kMlpCT * 4;
         if (i < h) {
-            float4 v = *reinterpret_cast<const float4*>(ma.x + i);
-            for (int p = 0; p < ma.n_attn_part; ++p) {
-                const float4 w = *reinterpret_cast<const float4*>(ma.attn_part + (size_t)p * h + i);
-                v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+            float4 v = xin[u];
+#pragma unroll
+            for (int p = 0; p < kMaxParts; ++p) {
+                if (p < ma.n_attn_part) {
+                    const float4 w = xp[u][p];
+                    v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+                }
             }
             if (c == 0) *reinterpret_cast<float4*>(ma.xr_out + i) = v;
             ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);

@@ -43,6 +43,7 @@ cudaError_t ensure_kernel_attributes() {
     err = init_gemv_attributes();
     if (err == cudaSuccess) err = init_attention_attributes();
     if (err == cudaSuccess) err = init_gemm_tc_attributes();
+    if (err == cudaSuccess) err = init_gemv_fmt_attributes();
     if (err == cudaSuccess) g_init_done[dev] = true;
     return err;
 }
@@ -705,6 +706,8 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
         if (C.decode_kernel != 3 && c->fuse_o) c->front_cl = layer_front_cluster_size(front_args(c, 0), hd);
         cudaGetLastError();
         if (C.decode_kernel == 0 && c->front_cl > 0) c->mlp_clusters = decode_mlp_clusters(h, F, c->layers[0].gu.rows);
+        // the front and MLP kernels read at most 8 partials of their input
+        if (c->mlp_clusters > 8 || C.n_head_kv > 8) c->mlp_clusters = 0;
         cudaGetLastError();
         unsupported = (C.decode_kernel == 3 && !c->fuse_o) || (C.decode_kernel == 4 && c->front_cl == 0);
     }
@@ -1034,6 +1037,43 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
         err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
+}
+
+size_t llama_q8_packed_bytes_fmt(int32_t gguf_type, int64_t rows, int64_t k) {
+    if (gguf_type == kGgufQ8_0) return llama_q8_packed_bytes(rows, k);
+    if (!fmt_supported(gguf_type) || rows <= 0 || k <= 0 || k % fmt_block_weights(gguf_type)) return 0;
+    return (size_t)fmt_packed_bytes(gguf_type, rows, k);
+}
+
+llama_q8_status llama_q8_pack_fmt(int32_t gguf_type, const void* blocks, int64_t rows, int64_t k, void* packed,
+                                  void* stream) {
+    if (gguf_type == kGgufQ8_0) return llama_q8_pack(blocks, rows, k, packed, stream);
+    if (!blocks || !packed || rows <= 0 || k <= 0) return LQ8_ERR_ARG;
+    if (!fmt_supported(gguf_type)) return LQ8_ERR_UNSUPPORTED;
+    if (k % fmt_block_weights(gguf_type)) return LQ8_ERR_ARG;
+    if (rows > (1 << 30) || k > (1 << 30)) return LQ8_ERR_UNSUPPORTED;
+    return launch_pack_fmt(gguf_type, reinterpret_cast<const uint8_t*>(blocks), rows, k,
+                           reinterpret_cast<uint8_t*>(packed), (cudaStream_t)stream) == cudaSuccess
+               ? LQ8_OK
+               : LQ8_ERR_CUDA;
+}
+
+llama_q8_status llama_q8_matvec_fmt(int32_t gguf_type, const void* packed, int64_t rows, int64_t k, const float* x,
+                                    float* y, int32_t flags, void* stream) {
+    if (gguf_type == kGgufQ8_0) return llama_q8_matmul_ex(packed, rows, k, x, 1, y, flags, stream);
+    if (!packed || !x || !y || rows <= 0 || k <= 0) return LQ8_ERR_ARG;
+    if (!fmt_supported(gguf_type)) return LQ8_ERR_UNSUPPORTED;
+    if (k % fmt_block_weights(gguf_type)) return LQ8_ERR_ARG;
+    if (flags & ~LQ8_MATMUL_EARLY_WEIGHTS) return LQ8_ERR_ARG;
+    // records and x are fetched by bulk async copies: 16-byte aligned only
+    if (((uintptr_t)packed | (uintptr_t)x) & 15) return LQ8_ERR_ARG;
+    if (rows > (1 << 30) || k > fmt_max_k(gguf_type)) return LQ8_ERR_UNSUPPORTED;
+    if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
+    const bool early = (flags & LQ8_MATMUL_EARLY_WEIGHTS) != 0;
+    return launch_gemv_fmt(gguf_type, reinterpret_cast<const uint8_t*>(packed), (int)rows, (int)k, x, y, early,
+                           nullptr, (cudaStream_t)stream) == cudaSuccess
+               ? LQ8_OK
+               : LQ8_ERR_CUDA;
 }
 
 llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache, int32_t kv_len,

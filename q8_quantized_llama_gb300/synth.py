@@ -109,3 +109,22 @@ def normal_f32(shape, seed: int, stream: int = 0, std: float = 1.0) -> np.ndarra
 def weight_matrix_f32(rows: int, k: int, seed: int, stream: int = 0) -> np.ndarray:
     """One N(0, 0.02) f32 weight matrix [rows, k] for the isolated linear sweep."""
     return normal_f32((rows, k), seed, 0x3000 + stream, WEIGHT_STD)
+
+
+# Other GGUF block formats: (weights per block, bytes per block, byte offsets of
+# the fp16 scale fields). Random blocks are random bytes with those fields
+# replaced by finite fp16 values of a typical magnitude.
+_BLOCK_FORMATS = {6: (32, 22, (0,)), 12: (256, 144, (0, 2)), 14: (256, 210, (208,))}
+
+
+def random_blocks(gguf_type: int, rows: int, k: int, seed: int, stream: int = 0) -> np.ndarray:
+    """uint8 [rows, k / block * block bytes] of random Q5_0 (6), Q4_K (12) or
+    Q6_K (14) blocks: every code, scale and min byte uniform, fp16 scales
+    |N(0, 1)| * 2^-7 (so weights stay of order 0.1)."""
+    qk, nbytes, f16_at = _BLOCK_FORMATS[gguf_type]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0xB10C, gguf_type, stream])))
+    blocks = rng.integers(0, 256, size=(rows, k // qk, nbytes), dtype=np.uint8)
+    for off in f16_at:
+        scale = (np.abs(rng.standard_normal((rows, k // qk))) * 2.0 ** -7).astype("<f2")
+        blocks[..., off:off + 2] = scale.view(np.uint8).reshape(rows, k // qk, 2)
+    return blocks.reshape(rows, k // qk * nbytes)
