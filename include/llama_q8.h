@@ -307,7 +307,8 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
  * matrix, f32 x and y. m == 1 runs the matrix-vector kernel, m > 1 a
  * matrix-matrix kernel (the dispatch "生成一个 token" describes for
  * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32): up to 16 rows on the CUDA
- * cores with f32 accumulation, more rows on the tcgen05 tensor cores: per
+ * cores with f32 accumulation (each 32-row weight tile streamed once and
+ * multiplied with every row of x), more rows on the tcgen05 tensor cores: per
  * Q8_0 block the int8 codes (exact in tf32) times x split into tf32 hi and lo
  * parts (two TF32 products per step, f32 accumulation in tensor memory), the
  * block sums scaled by d and added in f32; less than 2^-19 relative error per

@@ -355,6 +355,230 @@ static int sm_count_current() {
     return g_sm_count[dev];
 }
 
+// ---------------------------------------------------------------------------
+// Few token rows (prefill chunks of 2..16 tokens): the same weight stream,
+// each 32-row tile read once and multiplied with every token row. Lane = weight
+// row; per 32-weight block the lane turns its codes into f32 once and takes the
+// dot product with each token's x block (broadcast shared-memory reads).
+// Grid: one CTA per (tile, split), the block range of a tile split over a
+// cluster when the tiles cannot fill the GPU or the token rows' slices of x
+// would not fit in shared memory; the leader adds the peers' partial sums in
+// rank order.
+// ---------------------------------------------------------------------------
+constexpr int kRowsMax = 16;
+
+struct GemvRowsArgs {
+    PackedQ8 W;
+    const float* X;  // [m][ldx]
+    int m, ldx;
+    EpiArgs e;
+    int splits;
+    int* err;
+};
+
+template <int EPI>
+__device__ __forceinline__ void rows_epilogue(const EpiArgs& e, int rows, int tile, int lane, int t, float v) {
+    const int r = tile * 32 + lane;
+    const bool valid = r < rows;
+    if (EPI == EPI_STORE) {
+        if (valid) e.y[(int64_t)t * e.ldy + r] = v;
+    } else if (EPI == EPI_RESIDUAL) {
+        if (valid) e.y[(int64_t)t * e.ldy + r] += v;
+    } else if (EPI == EPI_QKV) {
+        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+        if (!(lane & 1) && valid) epi_qkv_pair(e, t, e.pos0 + t, r, v, other);
+    } else if (EPI == EPI_SILU) {
+        const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+        if (!(lane & 1) && valid) e.a_out[(int64_t)t * e.lda + (r >> 1)] = silu_f32(v) * up;
+    }
+}
+
+template <int EPI, typename RG>
+__global__ void __launch_bounds__(kGemvThreads) q8_gemv_rows_kernel(GemvRowsArgs a) {
+    constexpr int kStages = RG::kStages, kStageBlocks = RG::kStageBlocks;
+    constexpr int kStageCodeBytes = RG::kStageCodeBytes, kStageBytes = RG::kStageBytes;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    float* xs = reinterpret_cast<float*>(smem + kStages * kStageBytes);  // [m][xn]
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ __align__(8) uint64_t empty[kStages];
+    __shared__ __align__(8) uint64_t xbar;
+    __shared__ float red[kCWarps][kRowsMax][32];
+    __shared__ float part[kRowsMax][32];
+
+    const PackedQ8& W = a.W;
+    const int k = W.k, nb = k >> 5, m = a.m;
+    const int S = a.splits;
+    const int tile = blockIdx.x / S, split = blockIdx.x % S;
+    const int b0 = (split * nb) / S, b1 = ((split + 1) * nb) / S;
+    const int nblk = b1 - b0, xn = nblk * 32;
+    const int n_stage = (nblk + kStageBlocks - 1) / kStageBlocks;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCWarps);
+        }
+        mbar_init(&xbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCWarps) {
+        if (lane == 0) {
+            const uint8_t* gcodes = reinterpret_cast<const uint8_t*>(W.qs) + (size_t)tile * k * 32;
+            const uint8_t* gscales = reinterpret_cast<const uint8_t*>(W.d) + (size_t)tile * nb * 64;
+            auto issue_stage = [&](int j) {
+                const int slot = j % kStages;
+                if (j >= kStages) mbar_wait_bounded(&empty[slot], ((j / kStages) - 1) & 1, a.err, 14);
+                const int bs = b0 + j * kStageBlocks;
+                const int nbs = min(kStageBlocks, b1 - bs);
+                uint8_t* dst = stages + slot * kStageBytes;
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)(nbs * 1024 + nbs * 64));
+                bulk_g2s(dst, gcodes + (size_t)bs * 1024, nbs * 1024, &full[slot]);
+                bulk_g2s(dst + kStageCodeBytes, gscales + (size_t)bs * 64, nbs * 64, &full[slot]);
+            };
+            const int first = min(kStages, n_stage);
+            for (int j = 0; j < first; ++j) issue_stage(j);  // weights: no kernel writes them
+            pdl_wait();                                      // x: written by the preceding kernel
+            mbar_arrive_expect_tx(&xbar, (uint32_t)(m * xn * 4));
+            for (int t = 0; t < m; ++t)
+                bulk_g2s(xs + (size_t)t * xn, a.X + (size_t)t * a.ldx + b0 * 32, (uint32_t)(xn * 4), &xbar);
+            for (int j = first; j < n_stage; ++j) issue_stage(j);
+        }
+    } else {
+        pdl_wait();
+        if (tid == 0) pdl_launch_dependents();
+        mbar_wait_bounded(&xbar, 0, a.err, 15);
+        float acc[kRowsMax];
+#pragma unroll
+        for (int t = 0; t < kRowsMax; ++t) acc[t] = 0.0f;
+        for (int j = 0; j < n_stage; ++j) {
+            const int slot = j % kStages;
+            mbar_wait_bounded(&full[slot], (j / kStages) & 1, a.err, 16);
+            const int bs = j * kStageBlocks;  // relative to b0
+            const int nbs = min(kStageBlocks, nblk - bs);
+            const uint8_t* st = stages + slot * kStageBytes;
+            for (int bi = warp; bi < nbs; bi += kCWarps) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(st + bi * 1024 + lane * 16);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(st + bi * 1024 + 512 + lane * 16);
+                const float d = __half2float(reinterpret_cast<const __half*>(st + kStageCodeBytes)[bi * 32 + lane]);
+                // the 32 codes as 16 exact f32 pairs, once for every token row
+                uint64_t w[16];
+                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t u = qw[i] ^ 0x80808080u;
+                    w[2 * i] = codes2_f2<0>(u);
+                    w[2 * i + 1] = codes2_f2<2>(u);
+                }
+                const float* xb = xs + (bs + bi) * 32;
+#pragma unroll
+                for (int t = 0; t < kRowsMax; ++t) {
+                    if (t < m) {
+                        const float4* x4 = reinterpret_cast<const float4*>(xb + (size_t)t * xn);
+                        uint64_t s0 = 0, s1 = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 xv = x4[i];
+                            s0 = fma_f2(w[2 * i], pack_f2(xv.x, xv.y), s0);
+                            s1 = fma_f2(w[2 * i + 1], pack_f2(xv.z, xv.w), s1);
+                        }
+                        acc[t] = fmaf(d, (f2_lo(s0) + f2_hi(s0)) + (f2_lo(s1) + f2_hi(s1)), acc[t]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+#pragma unroll
+        for (int t = 0; t < kRowsMax; ++t)
+            if (t < m) red[warp][t][lane] = acc[t];
+        named_bar_sync(1, kCWarps * 32);
+        // warp w finishes token rows w, w + 8: the sum over the eight warps
+        for (int t = warp; t < m; t += kCWarps) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w2 = 0; w2 < kCWarps; ++w2) v += red[w2][t][lane];
+            if (S == 1)
+                rows_epilogue<EPI>(a.e, W.rows, tile, lane, t, v);
+            else
+                part[t][lane] = v;
+        }
+        if (S > 1) {
+            cluster_sync();
+            if (split == 0) {
+                for (int t = warp; t < m; t += kCWarps) {
+                    float v = part[t][lane];
+                    for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[t][lane], (uint32_t)rnk);
+                    rows_epilogue<EPI>(a.e, W.rows, tile, lane, t, v);
+                }
+            }
+            cluster_sync();  // peers keep their shared memory until the leader has read it
+        }
+        return;
+    }
+    if (S > 1) {
+        __syncwarp();
+        cluster_sync();
+        cluster_sync();
+    }
+}
+
+template <int EPI>
+static cudaError_t gemv_rows_launch(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
+                                    int* err, cudaStream_t s) {
+    using RG = RingDeep;
+    constexpr size_t ring = (size_t)RG::kStages * RG::kStageBytes;
+    const int tiles = W.rows_pad / 32, nb = W.k / 32;
+    const int sms = sm_count_current();
+    // splits: fill the GPU (at most one CTA per SM per tile-split, 8 blocks per split
+    // at least) and make the token rows' x slices fit beside the ring
+    int S = 1;
+    // dynamic shared memory beside the kernel's ~19 KB of static arrays
+    constexpr size_t kRowsMaxSmem = 200 * 1024;
+    auto fits = [&](int sp) { return ring + (size_t)m * ((nb + sp - 1) / sp) * 32 * 4 <= kRowsMaxSmem; };
+    while (S < 8 && (!fits(S) || (tiles * (S + 1) <= sms && nb / (S + 1) >= 8))) ++S;
+    if (!fits(S)) return cudaErrorInvalidValue;
+    const size_t smem = ring + (size_t)m * ((nb + S - 1) / S) * 32 * 4;
+    GemvRowsArgs a{W, X, m, ldx, e, S, err};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int n = 0;
+    if (S > 1) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = S;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, q8_gemv_rows_kernel<EPI, RG>, a);
+}
+
+cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
+                             int* err, cudaStream_t s) {
+    if (m < 1 || m > kRowsMax || ldx % 4) return cudaErrorInvalidValue;
+    switch (epi) {
+        case EPI_STORE: return gemv_rows_launch<EPI_STORE>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_RESIDUAL: return gemv_rows_launch<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_QKV: return gemv_rows_launch<EPI_QKV>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_SILU: return gemv_rows_launch<EPI_SILU>(W, X, m, ldx, e, pdl, err, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 // CTAs of one instantiation resident per SM with `smem` bytes of dynamic
 // shared memory (occupancy query, remembered per kernel and size).
 static int resident_ctas(void (*kernel)(GemvArgs), size_t smem) {
@@ -435,6 +659,9 @@ static cudaError_t gemv_set_attr() {
     one(q8_gemv_kernel<EPI, false, RingWide>);
     one(q8_gemv_kernel<EPI, true, RingDeep>);
     one(q8_gemv_kernel<EPI, false, RingDeep>);
+    if (EPI != EPI_ARGMAX && err == cudaSuccess)
+        err = cudaFuncSetAttribute(q8_gemv_rows_kernel<EPI == EPI_ARGMAX ? EPI_STORE : EPI, RingDeep>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
     return err;
 }
 

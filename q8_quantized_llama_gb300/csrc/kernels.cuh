@@ -122,9 +122,9 @@ cudaError_t launch_pack_fmt(int type, const uint8_t* src, int64_t rows, int64_t 
 cudaError_t launch_gemv_fmt(int type, const uint8_t* packed, int rows, int k, const float* x, float* y, bool pdl,
                             int* err, cudaStream_t s);
 cudaError_t init_gemv_fmt_attributes();
-// gemm.cu (m > 1): CUDA-core kernel for a few rows
-cudaError_t launch_gemm(const PackedQ8& W, const float* X, int m, int ldx, int epi,
-                        const EpiArgs& e, bool pdl, cudaStream_t s);
+// gemv.cu, 2 <= m <= 16 token rows: each weight tile streamed once for all rows
+cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
+                             int* err, cudaStream_t s);
 // gemm_tc.cu: tcgen05 split-TF32 kernel for many rows
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                            int* err, cudaStream_t s);
@@ -136,7 +136,7 @@ constexpr int kTensorCoreMinRows = 16;
 inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,
                                       bool pdl, int* err, cudaStream_t s) {
     return m > kTensorCoreMinRows ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s)
-                                  : launch_gemm(W, X, m, ldx, epi, e, pdl, s);
+                                  : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
 }
 
 // attention.cu

@@ -117,6 +117,14 @@ def test_matmul_ragged_edges(rows, k, m):
     _matmul_case(rows, k, m, seed=4)
 
 
+@pytest.mark.parametrize("rows,k,m", [(576, 1536, 13), (960, 576, 16), (33, 96, 5), (4096, 14336, 16),
+                                      (14336, 4096, 8), (49152, 576, 2)])
+def test_matmul_few_rows(rows, k, m):
+    """2..16 token rows: every weight tile streamed once for all rows, the block
+    range split over a cluster when the rows' slices of x need it (k = 14336)."""
+    _matmul_case(rows, k, m, seed=6)
+
+
 def test_matmul_early_weights_chain_equals_serial_calls():
     """A chain of matrix-vector calls whose weight streams start before the
     previous call ends (each call reading the previous call's output) gives
