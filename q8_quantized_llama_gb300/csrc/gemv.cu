@@ -366,6 +366,8 @@ static int sm_count_current() {
 // rank order.
 // ---------------------------------------------------------------------------
 constexpr int kRowsMax = 16;
+// dynamic shared memory of the few-rows kernel, beside its ~19 KB of static arrays
+constexpr int kRowsMaxSmem = 200 * 1024;
 
 struct GemvRowsArgs {
     PackedQ8 W;
@@ -536,9 +538,7 @@ static cudaError_t gemv_rows_launch(const PackedQ8& W, const float* X, int m, in
     // splits: fill the GPU (at most one CTA per SM per tile-split, 8 blocks per split
     // at least) and make the token rows' x slices fit beside the ring
     int S = 1;
-    // dynamic shared memory beside the kernel's ~19 KB of static arrays
-    constexpr size_t kRowsMaxSmem = 200 * 1024;
-    auto fits = [&](int sp) { return ring + (size_t)m * ((nb + sp - 1) / sp) * 32 * 4 <= kRowsMaxSmem; };
+    auto fits = [&](int sp) { return ring + (size_t)m * ((nb + sp - 1) / sp) * 32 * 4 <= (size_t)kRowsMaxSmem; };
     while (S < 8 && (!fits(S) || (tiles * (S + 1) <= sms && nb / (S + 1) >= 8))) ++S;
     if (!fits(S)) return cudaErrorInvalidValue;
     const size_t smem = ring + (size_t)m * ((nb + S - 1) / S) * 32 * 4;
@@ -661,7 +661,7 @@ static cudaError_t gemv_set_attr() {
     one(q8_gemv_kernel<EPI, false, RingDeep>);
     if (EPI != EPI_ARGMAX && err == cudaSuccess)
         err = cudaFuncSetAttribute(q8_gemv_rows_kernel<EPI == EPI_ARGMAX ? EPI_STORE : EPI, RingDeep>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsMaxSmem);
     return err;
 }
 
