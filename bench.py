@@ -654,7 +654,9 @@ def lm_head_variants(torch, B, synth, device, peak, prompt, n_steps):
 def attention_microbench(torch, B, synth, device, peak):
     """GQA decode attention at the 135M shape (9/3 heads of 64) and the 7B
     shape (32/8 heads of 128), kv_len 32..4096, the decode step's kernel
-    (llama_q8_attention_decode). 100 launches, each on its own cache copy so
+    (llama_q8_attention_decode with a workspace, as the decode step passes the
+    context's: long contexts split each KV head over several clusters). 100
+    launches, each on its own cache copy so
     that the K/V rows stream from HBM (one 4096-position cache is 6.3 / 33.6
     MB), are captured in a CUDA graph and replayed: the per-launch time is the
     kernel plus the graph's launch-to-launch gap, without host overhead."""
@@ -666,11 +668,13 @@ def attention_microbench(torch, B, synth, device, peak):
         vc = [torch.randn(nkv * stride * hd, device=device) for _ in range(ncopy)]
         q = torch.randn(nh * hd, device=device)
         o = torch.empty(nh * hd, device=device)
+        ws_bytes = B.llama_q8_attention_workspace_bytes(nh, nkv, hd, stride)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
         for kv in (32, 256, 1024, 4096):
             s = torch.cuda.current_stream()
             for i in range(8):
                 B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
-                                            s.cuda_stream)
+                                            s.cuda_stream, ws, ws_bytes)
             torch.cuda.synchronize()
             n = 100
             g = torch.cuda.CUDAGraph()
@@ -678,7 +682,7 @@ def attention_microbench(torch, B, synth, device, peak):
             with torch.cuda.graph(g, stream=cs):
                 for i in range(n):
                     B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
-                                                cs.cuda_stream)
+                                                cs.cuda_stream, ws, ws_bytes)
             g.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

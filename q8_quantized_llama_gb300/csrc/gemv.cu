@@ -78,7 +78,7 @@ __device__ __forceinline__ float block_dot32(const uint4& q0, const uint4& q1, c
 // folded into *best (warp-uniform); the CTA publishes it once at the end.
 template <int EPI>
 __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int tile, int lane, float v, float pre,
-                                              unsigned long long* best) {
+                                              unsigned long long* best, float2 cs) {
     const int r = tile * 32 + lane;
     const bool valid = r < rows;
     if (EPI == EPI_STORE) {
@@ -88,7 +88,7 @@ __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int ti
     } else if (EPI == EPI_QKV) {
         const float other = __shfl_xor_sync(0xffffffffu, v, 1);
         const int pos = e.state ? e.state->pos : e.pos0;
-        if (!(lane & 1) && valid) epi_qkv_pair(e, 0, pos, r, v, other);
+        if (!(lane & 1) && valid) epi_qkv_pair_cs(e, 0, pos, r, v, other, cs);
     } else if (EPI == EPI_SILU) {
         const float up = __shfl_xor_sync(0xffffffffu, v, 1);
         if (!(lane & 1) && valid) e.a_out[r >> 1] = silu_f32(v) * up;
@@ -214,6 +214,12 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 gpre[u] = i < xn ? *reinterpret_cast<const float4*>(a.g + x0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+        // QKV: the rotary (cos, sin) of the first tile's row pairs, before the wait
+        // (the table is constant and the position was written two or more launches back)
+        float2 cs = make_float2(1.0f, 0.0f);
+        const int qkv_pos = (EPI == EPI_QKV) ? (a.e.state ? a.e.state->pos : a.e.pos0) : 0;
+        if (EPI == EPI_QKV && warp == 0 && split == 0 && my_tiles > 0 && cl_id * 32 + lane < W.rows)
+            cs = rope_cs_for_row(a.e, qkv_pos, (cl_id * 32 + lane) & ~1);
         pdl_wait();
         if (tid == 0) {
             pdl_launch_dependents();
@@ -278,6 +284,8 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
                 const int r = tile * 32 + lane;
                 if (r < W.rows) res_pre = a.e.res ? a.e.res[r] : a.e.y[r];
             }
+            if (EPI == EPI_QKV && ti > 0 && split == 0 && warp == 0 && tile * 32 + lane < W.rows)
+                cs = rope_cs_for_row(a.e, qkv_pos, (tile * 32 + lane) & ~1);  // used after the tile's products
             float acc = 0.0f;
             for (int j = 0; j < n_stage; ++j) {
                 const int g = ti * n_stage + j;
@@ -306,7 +314,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
 #pragma unroll
                 for (int w = 0; w < kCWarps; ++w) v += red[ti & 1][w][lane];
                 if (S == 1)
-                    gemv_epilogue<EPI>(a.e, W.rows, tile, lane, NORM ? v * rscale : v, res_pre, &best);
+                    gemv_epilogue<EPI>(a.e, W.rows, tile, lane, NORM ? v * rscale : v, res_pre, &best, cs);
                 else
                     part[lane] = v;  // one tile per cluster: reduced below
             }
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_kernel(GemvArgs a) {
             if (split == 0 && warp == 0 && my_tiles > 0) {
                 float v = part[lane];
                 for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[lane], (uint32_t)rnk);
-                gemv_epilogue<EPI>(a.e, W.rows, cl_id, lane, NORM ? v * rscale : v, res_pre, &best);
+                gemv_epilogue<EPI>(a.e, W.rows, cl_id, lane, NORM ? v * rscale : v, res_pre, &best, cs);
             }
             cluster_sync();  // peers keep their shared memory until the leader has read it
         }
