@@ -44,7 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 # decode step's kernels from one ncu capture of the current kernel sources
 # (135M model, decode steps after the 203-token prompt, kv_len stated); the
 # K/V part grows by n_kv * head_dim * 8 bytes per cached position.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # 3 launches (layers 0-2 of decode step 21, kv_len 224), mean of 1,343,232 / 1,356,288 / 1,356,544 B read, 0 written
+    "layer_front_qkv_attn_o": {"bytes": 1352021, "kv_len": 224, "kv_bytes_per_pos": 1536},
+}
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops x max SM clock
 L2_BYTES = 126 * 2 ** 20
 
@@ -654,9 +657,7 @@ def lm_head_variants(torch, B, synth, device, peak, prompt, n_steps):
 def attention_microbench(torch, B, synth, device, peak):
     """GQA decode attention at the 135M shape (9/3 heads of 64) and the 7B
     shape (32/8 heads of 128), kv_len 32..4096, the decode step's kernel
-    (llama_q8_attention_decode with a workspace, as the decode step passes the
-    context's: long contexts split each KV head over several clusters). 100
-    launches, each on its own cache copy so
+    (llama_q8_attention_decode). 100 launches, each on its own cache copy so
     that the K/V rows stream from HBM (one 4096-position cache is 6.3 / 33.6
     MB), are captured in a CUDA graph and replayed: the per-launch time is the
     kernel plus the graph's launch-to-launch gap, without host overhead."""
@@ -668,13 +669,11 @@ def attention_microbench(torch, B, synth, device, peak):
         vc = [torch.randn(nkv * stride * hd, device=device) for _ in range(ncopy)]
         q = torch.randn(nh * hd, device=device)
         o = torch.empty(nh * hd, device=device)
-        ws_bytes = B.llama_q8_attention_workspace_bytes(nh, nkv, hd, stride)
-        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
         for kv in (32, 256, 1024, 4096):
             s = torch.cuda.current_stream()
             for i in range(8):
                 B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
-                                            s.cuda_stream, ws, ws_bytes)
+                                            s.cuda_stream)
             torch.cuda.synchronize()
             n = 100
             g = torch.cuda.CUDAGraph()
@@ -682,7 +681,7 @@ def attention_microbench(torch, B, synth, device, peak):
             with torch.cuda.graph(g, stream=cs):
                 for i in range(n):
                     B.llama_q8_attention_decode(q, kc[i % ncopy], vc[i % ncopy], kv, nh, nkv, hd, stride, o,
-                                                cs.cuda_stream, ws, ws_bytes)
+                                                cs.cuda_stream)
             g.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -779,6 +778,10 @@ def run_ours(args):
     dom = fams[dom_name]
     weights_bytes, kv_bytes = decode_bytes(cfg, PROMPT_LEN + (DECODE_STEPS + 1) / 2)
     traffic = NCU_TRAFFIC.get(dom_name)
+    mean_kv = PROMPT_LEN + (DECODE_STEPS + 1) / 2
+    traffic_bytes = None
+    if traffic:  # scaled from the captured kv_len to the timed steps' mean, as the algorithmic bytes are
+        traffic_bytes = traffic["bytes"] + traffic["kv_bytes_per_pos"] * (mean_kv - traffic["kv_len"])
 
     out = None
     if rank == 0:
@@ -811,8 +814,10 @@ def run_ours(args):
             "gpu_launches": gpu_launches,
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                          "frac": dom["gbs"] / peak, "peak_source": f"{peak_kind} HBM copy bandwidth (burst)",
-                         "traffic": traffic["bytes"] if traffic else None,
-                         "traffic_kv_len": traffic["kv_len"] if traffic else None,
+                         "traffic": traffic_bytes,
+                         "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of the same kernel "
+                                            f"at kv_len {traffic['kv_len']}, scaled by {traffic['kv_bytes_per_pos']} "
+                                            f"B per position to the mean kv_len {mean_kv}") if traffic else None,
                          "algorithmic_bytes_per_launch": dom["bytes_per_launch"],
                          "duration_us": dom["us_per_launch"], "span_us": dom["span_us_per_launch"],
                          "share_of_step": dom["share"],

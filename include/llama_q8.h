@@ -395,20 +395,13 @@ llama_q8_status llama_q8_attention(const float* q, const float* k_cache, const f
  * [head_dim]; out[n_head][head_dim]. One cluster of 16 CTAs per KV head (8
  * when the clusters of all KV heads cannot be resident together) splits the
  * positions, streams K/V rows with bulk async copies and merges its partial
- * results through distributed shared memory. workspace: optional (NULL: one
- * cluster per KV head and no scratch memory); when given, device memory of
- * at least llama_q8_attention_workspace_bytes(...) bytes whose counters are
- * zero (every call leaves them zero; calls sharing it must not overlap on
- * the GPU), and contexts of more than 128 positions per CTA then split each
- * KV head over up to 4 clusters (as many as are resident together), the last
- * cluster of a head merging their results from the workspace in a fixed
- * order. q, k_cache, v_cache, out and the workspace must be 16-byte aligned
- * (LQ8_ERR_ARG otherwise); other errors as llama_q8_attention. Enqueues on
- * `stream` and returns. */
+ * results through distributed shared memory, so no scratch memory is needed. q, k_cache,
+ * v_cache and out must be 16-byte aligned (LQ8_ERR_ARG otherwise); other
+ * errors as llama_q8_attention. Enqueues on `stream` and returns. */
 llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache,
                                           int32_t kv_len, int32_t n_head, int32_t n_head_kv,
                                           int32_t head_dim, int32_t cache_stride, float* out,
-                                          void* workspace, size_t workspace_bytes, void* stream);
+                                          void* stream);
 
 /* Allocation-free single-token attention. No counterpart on the pages: it is
  * a service to callers that cannot allocate device memory — a host that

@@ -104,7 +104,7 @@ def lib() -> C.CDLL:
         "llama_q8_attention": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
         "llama_q8_launch_count": (i64, [vp]),
         "llama_q8_attention_decode_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
-        "llama_q8_attention_decode": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, sz, vp]),
+        "llama_q8_attention_decode": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]),
         "llama_q8_profile_decode": (i32, [vp, i32, C.POINTER(llama_q8_kernel_stat), i32, C.POINTER(i32)]),
         "llama_q8_selftest_wait_timeout": (i32, [C.POINTER(i32)]),
         "llama_q8_packed_bytes_fmt": (sz, [i32, i64, i64]),
@@ -346,12 +346,10 @@ def llama_q8_attention(q, k_cache, v_cache, T: int, index_pos: int, n_head: int,
 
 
 def llama_q8_attention_decode(q, k_cache, v_cache, kv_len: int, n_head: int, n_head_kv: int, head_dim: int,
-                              cache_stride: int, out, stream=0, workspace=None, workspace_bytes: int = 0) -> None:
-    """Single-token attention with the decode step's cluster kernel (optional
-    workspace: long contexts split each KV head over several clusters)."""
+                              cache_stride: int, out, stream=0) -> None:
+    """Single-token attention with the decode step's cluster kernel."""
     check(lib().llama_q8_attention_decode(ptr(q), ptr(k_cache), ptr(v_cache), kv_len, n_head, n_head_kv, head_dim,
-                                          cache_stride, ptr(out), ptr(workspace), workspace_bytes, stream or None),
-          "llama_q8_attention_decode")
+                                          cache_stride, ptr(out), stream or None), "llama_q8_attention_decode")
 
 
 def llama_q8_attention_decode_noalloc(q, k_cache, v_cache, kv_len: int, n_head: int, n_head_kv: int,

@@ -21,7 +21,6 @@
 // 32 (head_dim 128) double-buffered in shared memory, online softmax; query t
 // sees positions <= index_pos + t ("量化 llama 的一次前向", forward：mask
 // 什么时候建 — the mask is a predicate here, never built).
-#include <algorithm>
 #include <mutex>
 
 #include "attn_core.cuh"
@@ -35,9 +34,6 @@ constexpr int kChunk = 64;       // positions per decode CTA
 constexpr int kDecThreads = 128;
 
 static inline int max_splits_for(int cache_stride) { return (cache_stride + kChunk - 1) / kChunk; }
-// The workspace starts with one completion counter per KV head, 256 bytes for
-// up to 64 heads (the cluster kernel's per-cluster results follow them).
-constexpr int kAttnCounterFloats = 64;
 
 size_t attn_workspace_bytes(int n_head, int n_head_kv, int head_dim, int cache_stride) {
     const int G = n_head / n_head_kv;
@@ -242,8 +238,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) stamp_at(fo.stamp, 0);
-    const int parts = FO ? 1 : fo.parts;
-    const int kh = blockIdx.x / CL / parts, part = blockIdx.x / CL % parts, rank = blockIdx.x % CL;
+    const int kh = blockIdx.x / CL, rank = blockIdx.x % CL;
     const int G = n_head / n_kv;
     const int nbk = G * HD / 32;                       // W_o column blocks of this group
     const int tiles = FO ? fo.wo.rows_pad >> 5 : 0;
@@ -259,11 +254,8 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
     uint8_t* WO = reinterpret_cast<uint8_t*>(smf + pl.wo);
 
     const int kv_len = st ? st->pos + 1 : kv_len_host;
-    // clusters in use for this KV head: one per kCaPartMinRows * CL positions, at most `parts`
-    const int n_use = parts > 1 ? max(1, min(parts, kv_len / (kCaPartMinRows * CL))) : 1;
-    if (part >= n_use) return;  // the whole cluster: nothing to do at this context length
-    const int per = (kv_len + n_use * CL - 1) / (n_use * CL);
-    const int j_begin = min(kv_len, (part * CL + rank) * per), j_end = min(kv_len, j_begin + per);
+    const int per = (kv_len + CL - 1) / CL;
+    const int j_begin = min(kv_len, rank * per), j_end = min(kv_len, j_begin + per);
     // The newest position is written by the preceding kernel (the QKV
     // epilogue) in the decode step; every older row may be read before the
     // grid dependency wait.
@@ -347,11 +339,6 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
     }
     cluster_sync();
     if (rank == 0) {
-        // the cluster's result; with several clusters per head, unnormalised (acc, M, L) to the workspace
-        const int stride_p = G * HD + 2 * G;
-        float* mine = nullptr;
-        if (!FO && n_use > 1)
-            mine = fo.ws + kAttnCounterFloats + ((size_t)kh * parts + part) * stride_p;
         for (int e = tid; e < G * HD; e += kCaCT) {
             const int g = e / HD;
             float M = -INFINITY;
@@ -365,49 +352,12 @@ __global__ void __launch_bounds__(kCaThreads, 1) attn_decode_cluster_kernel(
                 Lsum = fmaf(wgt, PLs[r * G + g], Lsum);
                 acc = fmaf(wgt, PO[r * G * HD + e], acc);
             }
+            const float val = acc / Lsum;
             if (FO) {
-                const float val = acc / Lsum;
 #pragma unroll
                 for (int r = 0; r < CL; ++r) st_dsmem_f32(&OM[e], (uint32_t)r, val);
-            } else if (mine) {
-                mine[e] = acc;
-                if (e % HD == 0) {
-                    mine[G * HD + g] = M;
-                    mine[G * HD + G + g] = Lsum;
-                }
             } else {
-                out[(int64_t)kh * G * HD + e] = acc / Lsum;
-            }
-        }
-        if (!FO && mine) {
-            // the last cluster of this head to finish merges the n_use results in order
-            __shared__ int last;
-            __threadfence();
-            named_bar_sync(1, kCaCT);
-            if (tid == 0) {
-                unsigned int* counter = reinterpret_cast<unsigned int*>(fo.ws) + kh;
-                last = atomicAdd(counter, 1u) == (unsigned int)(n_use - 1);
-                if (last) {
-                    __threadfence();
-                    atomicExch(counter, 0u);
-                }
-            }
-            named_bar_sync(1, kCaCT);
-            if (last) {
-                const float* base = fo.ws + kAttnCounterFloats + (size_t)kh * parts * stride_p;
-                for (int e = tid; e < G * HD; e += kCaCT) {
-                    const int g = e / HD;
-                    float M = -INFINITY;
-                    for (int c = 0; c < n_use; ++c) M = fmaxf(M, __ldcg(base + c * stride_p + G * HD + g));
-                    float Lsum = 0.0f, acc = 0.0f;
-                    for (int c = 0; c < n_use; ++c) {
-                        const float m_c = __ldcg(base + c * stride_p + G * HD + g);
-                        const float wgt = m_c == -INFINITY ? 0.0f : expf(m_c - M);
-                        Lsum = fmaf(wgt, __ldcg(base + c * stride_p + G * HD + G + g), Lsum);
-                        acc = fmaf(wgt, __ldcg(base + c * stride_p + e), acc);
-                    }
-                    out[(int64_t)kh * G * HD + e] = acc / Lsum;
-                }
+                out[(int64_t)kh * G * HD + e] = val;
             }
         }
     }
@@ -807,10 +757,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
 }
 
 template <int HD, int CL, int GP, bool FO>
-static cudaLaunchConfig_t ca_config(int n_clusters, int G, int wo_bytes, cudaStream_t s, cudaLaunchAttribute* attrs,
+static cudaLaunchConfig_t ca_config(int n_kv, int G, int wo_bytes, cudaStream_t s, cudaLaunchAttribute* attrs,
                                     bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_clusters * CL);
+    cfg.gridDim = dim3(n_kv * CL);
     cfg.blockDim = dim3(kCaThreads);
     cfg.dynamicSmemBytes = (size_t)ca_plan<HD>(G, GP, CL, wo_bytes).floats * 4;
     cfg.stream = s;
@@ -880,36 +830,20 @@ static int ca_cluster_size(int n_kv, int G, const AttnOproj* fo) {
 template <int HD, int GP, bool FO>
 static cudaError_t ca_launch(const float* q, const float* kc, const float* vc, int n_head, int n_kv, int cache_stride,
                              int kv_len, const DevState* st, float* out, const AttnOproj* fo, bool pdl, int* err,
-                             cudaStream_t s, unsigned long long* stamp, float* ws, size_t ws_bytes) {
+                             cudaStream_t s, unsigned long long* stamp) {
     const int G = n_head / n_kv;
     const float scale = 1.0f / sqrtf((float)HD);
     AttnOproj f = FO ? *fo : AttnOproj{};
     f.stamp = stamp;
-    const int cl = ca_cluster_size<HD, GP, FO>(n_kv, G, fo);
-    // long contexts: up to 4 clusters per KV head, as many as are resident with
-    // the other heads' (16-CTA clusters: the occupancy query; 8-CTA: ~2 per GPC)
-    int parts = 1;
-    if (!FO && ws && n_kv <= kAttnCounterFloats) {
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int resident = cl == 16 ? ca_max16<HD, GP, FO>(G, 0) : sms / 8 - 1;
-        parts = std::max(1, std::min(4, resident / n_kv));
-        while (parts > 1 && ws_bytes < (size_t)kAttnCounterFloats * 4 +
-                                            (size_t)n_kv * parts * (G * HD + 2 * G) * sizeof(float))
-            --parts;
-    }
-    f.ws = parts > 1 ? ws : nullptr;
-    f.parts = parts;
     cudaLaunchAttribute attrs[2];
-    if (cl == 16) {
+    if (ca_cluster_size<HD, GP, FO>(n_kv, G, fo) == 16) {
         const int wo = FO ? fo_wo_bytes(f.wo.rows_pad, G, HD, 16) : 0;
-        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP, FO>(n_kv * parts, G, wo, s, attrs, pdl);
+        cudaLaunchConfig_t cfg = ca_config<HD, 16, GP, FO>(n_kv, G, wo, s, attrs, pdl);
         return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 16, GP, FO>, q, kc, vc, n_head, n_kv,
                                   cache_stride, kv_len, st, scale, out, f, err);
     }
     const int wo = FO ? fo_wo_bytes(f.wo.rows_pad, G, HD, 8) : 0;
-    cudaLaunchConfig_t cfg = ca_config<HD, 8, GP, FO>(n_kv * parts, G, wo, s, attrs, pdl);
+    cudaLaunchConfig_t cfg = ca_config<HD, 8, GP, FO>(n_kv, G, wo, s, attrs, pdl);
     return cudaLaunchKernelEx(&cfg, attn_decode_cluster_kernel<HD, 8, GP, FO>, q, kc, vc, n_head, n_kv, cache_stride,
                               kv_len, st, scale, out, f, err);
 }
@@ -918,28 +852,28 @@ template <bool FO>
 static cudaError_t ca_dispatch(const float* q, const float* k_cache, const float* v_cache, int n_head, int n_head_kv,
                                int head_dim, int cache_stride, int kv_len, const DevState* st, float* out,
                                const AttnOproj* fo, bool pdl, int* err, cudaStream_t s,
-                               unsigned long long* stamp, float* ws = nullptr, size_t ws_bytes = 0) {
+                               unsigned long long* stamp) {
     if (n_head_kv <= 0 || n_head % n_head_kv || n_head / n_head_kv > kMaxGroup) return cudaErrorInvalidValue;
     const bool wide = n_head / n_head_kv > 4;
     if (head_dim == 64)
         return wide ? ca_launch<64, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
-                                           pdl, err, s, stamp, ws, ws_bytes)
+                                           pdl, err, s, stamp)
                     : ca_launch<64, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out, fo,
-                                           pdl, err, s, stamp, ws, ws_bytes);
+                                           pdl, err, s, stamp);
     if (head_dim == 128)
         return wide ? ca_launch<128, 8, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
-                                            fo, pdl, err, s, stamp, ws, ws_bytes)
+                                            fo, pdl, err, s, stamp)
                     : ca_launch<128, 4, FO>(q, k_cache, v_cache, n_head, n_head_kv, cache_stride, kv_len, st, out,
-                                            fo, pdl, err, s, stamp, ws, ws_bytes);
+                                            fo, pdl, err, s, stamp);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
                                        const DevState* st, float* out, bool pdl, int* err, cudaStream_t s,
-                                       unsigned long long* stamp, void* ws, size_t ws_bytes) {
+                                       unsigned long long* stamp) {
     return ca_dispatch<false>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, kv_len, st, out,
-                              nullptr, pdl, err, s, stamp, reinterpret_cast<float*>(ws), ws_bytes);
+                              nullptr, pdl, err, s, stamp);
 }
 
 // The O projection fits the decode attention kernel when every CTA's W_o
@@ -963,7 +897,7 @@ cudaError_t launch_attn_oproj(const float* q, const float* k_cache, const float*
                               int head_dim, int cache_stride, const DevState* st, const PackedQ8& Wo, float* part,
                               int part_stride, bool pdl, int* err, cudaStream_t s, unsigned long long* stamp) {
     if (!st) return cudaErrorInvalidValue;
-    const AttnOproj fo{Wo, part, part_stride, nullptr, nullptr, 1};
+    const AttnOproj fo{Wo, part, part_stride, nullptr};
     return ca_dispatch<true>(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride, 0, st, nullptr, &fo,
                              pdl, err, s, stamp);
 }

@@ -61,15 +61,7 @@ struct AttnOproj {
     float* part;
     int part_stride;
     unsigned long long* stamp;  // timeline stamps (instrumented decode graph), or null
-    // Long contexts (no O projection): `parts` clusters per KV head split the
-    // positions, each writing its merged but unnormalised result to ws; the
-    // last cluster of a head (completion counter in ws) merges them. ws: the
-    // split-KV workspace (counters first, zero between launches), or null.
-    float* ws;
-    int parts;
 };
-// Positions per CTA above which a long context uses more than one cluster per KV head.
-constexpr int kCaPartMinRows = 128;
 constexpr int kFoMaxWoBytes = 32 * 1024;  // W_o bytes one CTA may hold
 __host__ __device__ inline int fo_tiles_per_cta(int rows_pad, int cl) { return (rows_pad / 32 + cl - 1) / cl; }
 __host__ __device__ inline int fo_wo_bytes(int rows_pad, int G, int hd, int cl) {

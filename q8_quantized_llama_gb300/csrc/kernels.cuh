@@ -145,13 +145,10 @@ cudaError_t launch_attn_decode(const float* q, const float* k_cache, const float
                                int n_head, int n_head_kv, int head_dim, int cache_stride,
                                int kv_len, const DevState* st, float* out, void* workspace,
                                bool pdl, cudaStream_t s);
-// ws (optional, at least attn_workspace_bytes(...), counters zero): lets long
-// contexts split each KV head's positions over several clusters.
 cudaError_t launch_attn_decode_cluster(const float* q, const float* k_cache, const float* v_cache, int n_head,
                                        int n_head_kv, int head_dim, int cache_stride, int kv_len,
                                        const DevState* st, float* out, bool pdl, int* err, cudaStream_t s,
-                                       unsigned long long* stamp = nullptr, void* ws = nullptr,
-                                       size_t ws_bytes = 0);
+                                       unsigned long long* stamp = nullptr);
 // Decode attention whose clusters also apply the O projection: cluster kh
 // writes part[kh][0..rows) = W_o[:, columns of its query heads] o, the n_kv
 // partials summing to W_o o (added to the residual by the next kernel).

@@ -320,9 +320,7 @@ cudaError_t enqueue_decode_step(llama_q8_ctx* c, int* n_kernels, StepLayout* lay
             run(F_ATTN, 8.0 * qr, 8.0 * (double)cfg.n_head_kv * cfg.head_dim, [&] {
                 return launch_attn_decode_cluster(c->d_q, c->kcache(l), c->vcache(l), cfg.n_head, cfg.n_head_kv,
                                                   cfg.head_dim, cfg.max_seq, 0, c->d_state, c->d_o, pdl,
-                                                  &c->d_state->err, s, stp, c->d_attn_ws,
-                                                  attn_workspace_bytes(cfg.n_head, cfg.n_head_kv, cfg.head_dim,
-                                                                       cfg.max_seq));
+                                                  &c->d_state->err, s, stp);
             });
             run(F_OPROJ, q8_bytes(h, qr) + 4.0 * qr + 8.0 * h, 0.0,
                 [&] {
@@ -1080,7 +1078,7 @@ llama_q8_status llama_q8_matvec_fmt(int32_t gguf_type, const void* packed, int64
 
 llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, const float* v_cache, int32_t kv_len,
                                          int32_t n_head, int32_t n_head_kv, int32_t head_dim, int32_t cache_stride,
-                                         float* out, void* workspace, size_t workspace_bytes, void* stream) {
+                                         float* out, void* stream) {
     if (!q || !k_cache || !v_cache || !out || kv_len <= 0 || n_head <= 0 || n_head_kv <= 0 ||
         n_head % n_head_kv || cache_stride <= 0)
         return LQ8_ERR_ARG;
@@ -1090,13 +1088,8 @@ llama_q8_status llama_q8_attention_decode(const float* q, const float* k_cache, 
     // K/V rows and q are fetched by bulk async copies or 16-byte loads: 16-byte aligned buffers only
     if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out) & 15) return LQ8_ERR_ARG;
     if (ensure_kernel_attributes() != cudaSuccess) return LQ8_ERR_CUDA;
-    // the workspace, when given, must be the full split-KV size (its counters zero)
-    if (workspace && (workspace_bytes < attn_workspace_bytes(n_head, n_head_kv, head_dim, cache_stride) ||
-                      ((uintptr_t)workspace & 15)))
-        return LQ8_ERR_ARG;
     cudaError_t err = launch_attn_decode_cluster(q, k_cache, v_cache, n_head, n_head_kv, head_dim, cache_stride,
-                                                 kv_len, nullptr, out, false, nullptr, (cudaStream_t)stream,
-                                                 nullptr, workspace, workspace ? workspace_bytes : 0);
+                                                 kv_len, nullptr, out, false, nullptr, (cudaStream_t)stream);
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
 

@@ -201,11 +201,6 @@ def _attention_case(T, index_pos, nh, nkv, hd, stride, seed, entry="attention"):
     dq, dk, dv = to_dev(q), to_dev(kc), to_dev(vc)
     if entry == "attention":
         B.llama_q8_attention(dq, dk, dv, T, index_pos, nh, nkv, hd, stride, out, ws, ws_bytes)
-    elif entry == "decode_ws":   # several clusters per KV head at long contexts
-        B.llama_q8_attention_decode(dq, dk, dv, kv_len, nh, nkv, hd, stride, out, workspace=ws,
-                                    workspace_bytes=ws_bytes)
-        torch.cuda.synchronize()
-        assert int(ws[:256].view(torch.int32).abs().sum()) == 0   # counters left zero
     else:
         B.llama_q8_attention_decode(dq, dk, dv, kv_len, nh, nkv, hd, stride, out)
     torch.cuda.synchronize()
@@ -254,15 +249,6 @@ def test_attention_decode_cluster_135m(kv_len):
 @pytest.mark.parametrize("kv_len", [1, 32, 768, 1024, 4096])
 def test_attention_decode_cluster_7b(kv_len):
     _attention_case(1, kv_len - 1, 32, 8, 128, 4096, seed=kv_len + 9, entry="decode")
-
-
-@pytest.mark.parametrize("nh,nkv,hd,kv_len", [(9, 3, 64, 4096), (9, 3, 64, 2049), (9, 3, 64, 1000),
-                                             (32, 8, 128, 4096), (32, 8, 128, 2048), (32, 8, 128, 3000),
-                                             (16, 2, 64, 4095), (8, 8, 128, 2048)])
-def test_attention_decode_cluster_with_workspace(nh, nkv, hd, kv_len):
-    """With a workspace, long contexts split each KV head's positions over
-    several clusters whose results the last one merges; short ones do not."""
-    _attention_case(1, kv_len - 1, nh, nkv, hd, 4096, seed=nh * 5 + kv_len, entry="decode_ws")
 
 
 @pytest.mark.parametrize("nh,nkv,hd,kv_len", [(4, 4, 64, 100), (8, 1, 128, 777), (16, 2, 64, 4095),
