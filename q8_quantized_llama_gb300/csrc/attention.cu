@@ -620,19 +620,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
         int u = 0;
         for (int i = rank; i < n_qkv; i += CL, ++u) {
             const uint8_t* tw = WQ + (size_t)u * nbx * 1088;
-            float acc = 0.0f;
-            for (int b = warp; b < nbx; b += kCaWarps) {
-                const uint4 q0 = *reinterpret_cast<const uint4*>(tw + b * 1024 + lane * 16);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(tw + b * 1024 + 512 + lane * 16);
-                const float d = __half2float(reinterpret_cast<const __half*>(tw + nbx * 1024)[b * 32 + lane]);
-                const float4* x4 = reinterpret_cast<const float4*>(XN + b * 32);
-                uint64_t a0 = 0, a1 = 0;
-                a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
-                a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
-                a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
-                a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
-                acc = fmaf(d, (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)), acc);
-            }
+            const float acc = tile_blocks_dot(tw, nbx, warp, kCaWarps, nbx, lane, XN);
             RED2[warp * 33 + lane] = acc;
             named_bar_sync(1, kCaCT);
             if (warp == 0) {

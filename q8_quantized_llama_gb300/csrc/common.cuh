@@ -83,6 +83,43 @@ __device__ __forceinline__ uint64_t dot4_acc(uint32_t w, float4 x, uint64_t acc)
     return acc;
 }
 
+// One Q8_0 block of a 32-row tile against 32 values of x (lane = row): codes
+// at blk (two 512-byte halves, 16 bytes per lane), as two packed partial sums.
+__device__ __forceinline__ float block_dot_lane(const uint8_t* blk, int lane, const float* x) {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + lane * 16);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 512 + lane * 16);
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint64_t a0 = 0, a1 = 0;
+    a0 = dot4_acc(q0.x, x4[0], a0); a1 = dot4_acc(q1.x, x4[4], a1);
+    a0 = dot4_acc(q0.y, x4[1], a0); a1 = dot4_acc(q1.y, x4[5], a1);
+    a0 = dot4_acc(q0.z, x4[2], a0); a1 = dot4_acc(q1.z, x4[6], a1);
+    a0 = dot4_acc(q0.w, x4[3], a0); a1 = dot4_acc(q1.w, x4[7], a1);
+    return (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1));
+}
+
+// sum over blocks b = b0, b0 + step, ... < b1 of d_b (codes_b . x_b) for one
+// 32-row tile held in shared memory (codes of block b at tw + 1024 b, the fp16
+// scales after nb_all blocks, x of block b at xs + 32 b). Two blocks per step
+// with independent chains, so the second block's loads and products overlap
+// the first's (the latency of these short loops is what the decode kernels
+// wait on).
+__device__ __forceinline__ float tile_blocks_dot(const uint8_t* tw, int nb_all, int b0, int step, int b1, int lane,
+                                                 const float* xs) {
+    const __half* ds = reinterpret_cast<const __half*>(tw + (size_t)nb_all * 1024);
+    float acc0 = 0.0f, acc1 = 0.0f;
+    int b = b0;
+    for (; b + step < b1; b += 2 * step) {
+        const float d0 = __half2float(ds[b * 32 + lane]);
+        const float d1 = __half2float(ds[(b + step) * 32 + lane]);
+        const float s0 = block_dot_lane(tw + (size_t)b * 1024, lane, xs + b * 32);
+        const float s1 = block_dot_lane(tw + (size_t)(b + step) * 1024, lane, xs + (b + step) * 32);
+        acc0 = fmaf(d0, s0, acc0);
+        acc1 = fmaf(d1, s1, acc1);
+    }
+    if (b < b1) acc0 = fmaf(__half2float(ds[b * 32 + lane]), block_dot_lane(tw + (size_t)b * 1024, lane, xs + b * 32), acc0);
+    return acc0 + acc1;
+}
+
 // Exact scalar code extraction (used where speed does not matter).
 __device__ __forceinline__ float code_to_f32(int8_t q) { return (float)q; }
 
