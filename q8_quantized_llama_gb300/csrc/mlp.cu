@@ -1,11 +1,12 @@
 // The MLP half of a decode layer (T = 1) as ONE kernel: RMSNorm -> gate/up +
 // SiLU -> down projection ("量化 llama 的一次前向", forward, mlp: the same
-// steps as the gate/up and down kernels, one launch). CTA c owns 32 entries
-// of the SiLU product a = silu(W_g y) * (W_u y) (the gate/up row tiles 2c and
-// 2c + 1 of the row-interleaved [W_g;W_u]) and multiplies them into block
-// column c of W_down: a partial of W_down a over all h rows. The CTAs form
-// clusters of 8; each partial row goes (st.async, completing the receiver's
-// mbarrier) to the CTA of its cluster that owns the row, which adds the 8 in
+// steps as the gate/up and down kernels, one launch). CTA c owns 16 entries
+// of the SiLU product a = silu(W_g y) * (W_u y) (gate/up row tile c of the
+// row-interleaved [W_g;W_u]) and multiplies them into the matching 16-column
+// half of W_down's block column c / 2 (one 512-byte chunk of every row tile
+// in the packed layout): a partial of W_down a over all h rows. The CTAs form
+// clusters of 16; each partial row goes (st.async, completing the receiver's
+// mbarrier) to the CTA of its cluster that owns the row, which adds the 16 in
 // rank order and writes the cluster's partial. The next kernel adds the
 // clusters' partials to the residual in a fixed order, so the result is
 // deterministic. Weights and the norm weight are requested before the grid
@@ -15,7 +16,8 @@
 
 namespace lq8 {
 
-constexpr int kMlpCl = 8;       // CTAs per cluster
+constexpr int kMlpCl = 16;      // CTAs per cluster (non-portable size)
+constexpr int kMlpProd = 16;    // SiLU products per CTA
 constexpr int kMlpWarps = 8;    // consumer warps
 constexpr int kMlpCT = kMlpWarps * 32;
 constexpr int kMlpThreads = kMlpCT + 32;
@@ -30,11 +32,11 @@ __host__ __device__ inline MlpPlan mlp_plan(int h) {
     const int nbx = h / 32, tiles_h = h / 32;
     int o = 0;
     auto take = [&](int n) { const int r = o; o += mlp_round(n); return r; };
-    p.gu = take(2 * nbx * 1088 / 4);    // two gate/up tiles: codes then scales per tile
-    p.wd = take(tiles_h * 1024 / 4);    // block column c of W_down: codes of each row tile
-    p.wds = take(tiles_h * 64 / 4);     // and their scales
+    p.gu = take(nbx * 1088 / 4);        // the gate/up tile: codes then scales
+    p.wd = take(tiles_h * 512 / 4);     // W_down: this CTA's 16-code chunk of each row tile
+    p.wds = take(tiles_h * 64 / 4);     // and the scales of its block
     p.xs = take(h);                     // x * g
-    p.a = take(32);                     // this CTA's 32 SiLU products
+    p.a = take(kMlpProd);               // this CTA's SiLU products
     p.part = take(h);                   // this CTA's partial of W_down a
     p.red_in = take(kMlpCl * mlp_rows_per_owner(h));  // partials of the rows this CTA owns
     p.red = take(kMlpWarps * 33);
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
     __shared__ __align__(8) uint64_t w_bar, red_bar;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) stamp_at(ma.stamp, 0);
-    const int c = blockIdx.x;                 // block column of W_down = a entries [32c, 32c + 32)
+    const int c = blockIdx.x;                 // a entries [16c, 16c + 16): W_down chunk c
     const int q = (int)cluster_rank();        // rank in the cluster
     const int cl_id = c / kMlpCl;
     const int h = ma.wgu.k, nbx = h >> 5, tiles_h = h >> 5;
@@ -75,21 +77,18 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
 
     if (warp == kMlpWarps) {
         if (lane == 0) {  // constant weights, before the dependency wait
-            mbar_arrive_expect_tx(&w_bar, (uint32_t)(2 * nbx * 1088 + tiles_h * 1088));
-            for (int u = 0; u < 2; ++u) {
-                const int t = 2 * c + u;
-                uint8_t* dst = GU + (size_t)u * nbx * 1088;
-                bulk_g2s(dst, reinterpret_cast<const uint8_t*>(ma.wgu.qs) + (size_t)t * h * 32,
-                         (uint32_t)(nbx * 1024), &w_bar);
-                bulk_g2s(dst + nbx * 1024, reinterpret_cast<const uint8_t*>(ma.wgu.d) + (size_t)t * nbx * 64,
-                         (uint32_t)(nbx * 64), &w_bar);
-            }
+            mbar_arrive_expect_tx(&w_bar, (uint32_t)(nbx * 1088 + tiles_h * (512 + 64)));
+            bulk_g2s(GU, reinterpret_cast<const uint8_t*>(ma.wgu.qs) + (size_t)c * h * 32, (uint32_t)(nbx * 1024),
+                     &w_bar);
+            bulk_g2s(GU + nbx * 1024, reinterpret_cast<const uint8_t*>(ma.wgu.d) + (size_t)c * nbx * 64,
+                     (uint32_t)(nbx * 64), &w_bar);
             for (int t = 0; t < tiles_h; ++t) {
-                bulk_g2s(WD + (size_t)t * 1024,
-                         reinterpret_cast<const uint8_t*>(ma.wdown.qs) + (size_t)t * ma.wdown.k * 32 + (size_t)c * 1024,
-                         1024u, &w_bar);
+                // 16-code chunk c of row tile t: block c / 2, its first or second half
+                bulk_g2s(WD + (size_t)t * 512,
+                         reinterpret_cast<const uint8_t*>(ma.wdown.qs) + (size_t)t * ma.wdown.k * 32 + (size_t)c * 512,
+                         512u, &w_bar);
                 bulk_g2s(WDS + (size_t)t * 64,
-                         reinterpret_cast<const uint8_t*>(ma.wdown.d) + ((size_t)t * nbf + c) * 64, 64u, &w_bar);
+                         reinterpret_cast<const uint8_t*>(ma.wdown.d) + ((size_t)t * nbf + (c >> 1)) * 64, 64u, &w_bar);
             }
         }
         return;
@@ -150,36 +149,31 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
     const float r_norm = 1.0f / sqrtf(t_ss / (float)h + ma.eps);
     mbar_wait_bounded(&w_bar, 0, ma.err, 51);
 
-    // ---- gate/up: warps 0-3 tile 2c, warps 4-7 tile 2c + 1; lane = row ---------------
+    // ---- gate/up: tile c, its blocks over the eight warps; lane = row ----------------------
     {
-        const int u = warp >> 2, wq = warp & 3;
-        const uint8_t* tw = GU + (size_t)u * nbx * 1088;
-        const float acc = tile_blocks_dot(tw, nbx, wq, 4, nbx, lane, XS);
+        const float acc = tile_blocks_dot(GU, nbx, warp, kMlpWarps, nbx, lane, XS);
         RED[warp * 33 + lane] = acc;
         named_bar_sync(1, kMlpCT);
-        if (wq == 0) {
+        if (warp == 0) {
             float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) v += RED[(u * 4 + w) * 33 + lane];
+            for (int w = 0; w < kMlpWarps; ++w) v += RED[w * 33 + lane];
             v *= r_norm;
             const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-            if (!(lane & 1)) A[u * 16 + (lane >> 1)] = silu_f32(v) * up;
+            if (!(lane & 1)) A[lane >> 1] = silu_f32(v) * up;
         }
         named_bar_sync(1, kMlpCT);
     }
 
-    // ---- down: block column c of W_down times a, every row tile; lane = row -----------
+    // ---- down: this CTA's 16 columns of W_down times a, every row tile; lane = row ---------
 #pragma unroll 2
     for (int t = warp; t < tiles_h; t += kMlpWarps) {
-        const uint4 q0 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 1024 + lane * 16);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 1024 + 512 + lane * 16);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 512 + lane * 16);
         const float d = __half2float(reinterpret_cast<const __half*>(WDS + (size_t)t * 64)[lane]);
         const float4* a4 = reinterpret_cast<const float4*>(A);
         uint64_t a0 = 0, a1 = 0;
-        a0 = dot4_acc(q0.x, a4[0], a0); a1 = dot4_acc(q1.x, a4[4], a1);
-        a0 = dot4_acc(q0.y, a4[1], a0); a1 = dot4_acc(q1.y, a4[5], a1);
-        a0 = dot4_acc(q0.z, a4[2], a0); a1 = dot4_acc(q1.z, a4[6], a1);
-        a0 = dot4_acc(q0.w, a4[3], a0); a1 = dot4_acc(q1.w, a4[7], a1);
+        a0 = dot4_acc(q0.x, a4[0], a0); a1 = dot4_acc(q0.y, a4[1], a1);
+        a0 = dot4_acc(q0.z, a4[2], a0); a1 = dot4_acc(q0.w, a4[3], a1);
         PART[t * 32 + lane] = d * ((f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)));
     }
     named_bar_sync(1, kMlpCT);
@@ -201,33 +195,12 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
 static constexpr int kMlpSmemLimit = 227 * 1024 - 1024;
 static bool g_mlp_attr = false;
 
-// The kernel serves the model when F / 32 is a multiple of 8 (whole
-// clusters), h <= 2048 with h / 8 rows per owner a multiple of 4, and the
-// shared-memory plan fits.
-int decode_mlp_clusters(int h, int ff, int gu_rows) {
-    if (h % 32 || ff % 32 || gu_rows != 2 * ff || h > 2048 || (h / kMlpCl) % 4) return 0;
-    if ((ff / 32) % kMlpCl) return 0;
-    const size_t smem = (size_t)mlp_plan(h).floats * 4;
-    if (smem > (size_t)kMlpSmemLimit) return 0;
-    if (!g_mlp_attr) {
-        if (cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlpSmemLimit) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        g_mlp_attr = true;
-    }
-    return (ff / 32) / kMlpCl;
-}
-
-cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s) {
-    const int h = ma.wgu.k, ff = ma.wdown.k;
+static cudaLaunchConfig_t mlp_config(int grid, size_t smem, cudaStream_t s, cudaLaunchAttribute* attrs, bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ff / 32);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kMlpThreads);
-    cfg.dynamicSmemBytes = (size_t)mlp_plan(h).floats * 4;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = kMlpCl;
     attrs[0].val.clusterDim.y = 1;
@@ -240,6 +213,42 @@ cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s) {
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
+    return cfg;
+}
+
+// The kernel serves the model when F / 16 is a multiple of 16 (whole
+// clusters), h <= 2048 with h / 16 rows per owner a multiple of 4, the
+// shared-memory plan fits, and all the clusters can be resident at once.
+int decode_mlp_clusters(int h, int ff, int gu_rows) {
+    if (h % 64 || ff % 32 || gu_rows != 2 * ff || h > 2048 || (h / kMlpCl) % 4) return 0;
+    if ((ff / kMlpProd) % kMlpCl) return 0;
+    const size_t smem = (size_t)mlp_plan(h).floats * 4;
+    if (smem > (size_t)kMlpSmemLimit) return 0;
+    if (!g_mlp_attr) {
+        if (cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlpSmemLimit) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_mlp_attr = true;
+    }
+    const int clusters = (ff / kMlpProd) / kMlpCl;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = mlp_config(kMlpCl, smem, 0, attrs, false);
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, decode_mlp_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return resident >= clusters ? clusters : 0;
+}
+
+cudaError_t launch_decode_mlp(const MlpArgs& ma, bool pdl, cudaStream_t s) {
+    const int h = ma.wgu.k, ff = ma.wdown.k;
+    cudaLaunchAttribute attrs[2];
+    cudaLaunchConfig_t cfg = mlp_config(ff / kMlpProd, (size_t)mlp_plan(h).floats * 4, s, attrs, pdl);
     return cudaLaunchKernelEx(&cfg, decode_mlp_kernel, ma);
 }
 
