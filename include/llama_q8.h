@@ -76,7 +76,7 @@ typedef struct llama_q8_config {
     int32_t tied_output;  /* 1: the head is token_embd (no output.weight) */
     int32_t decode_kernel; /* decode step: 0 = automatic (two kernels per layer when each KV
                               head's Q/K/V rows and W_o slice fit a cluster and the MLP fits
-                              8-CTA clusters, else three, four or five), 1 = five per-layer
+                              16-CTA clusters, else three, four or five), 1 = five per-layer
                               kernels, 3 = four per layer (attention applying W_o), 4 = three
                               per layer (norm, Q/K/V, attention and W_o fused; gate/up; down);
                               3-4 give LQ8_ERR_UNSUPPORTED at load when the model does not

@@ -123,7 +123,7 @@ struct llama_q8_ctx {
     int64_t launches = 0;
     bool fuse_o = false;                 // decode attention kernel also applies W_o and the residual
     int front_cl = 0;                    // > 0: norm + QKV + attention + W_o as one kernel (this cluster size)
-    int mlp_clusters = 0;                // > 0: gate/up + down as one kernel with this many 8-CTA clusters
+    int mlp_clusters = 0;                // > 0: gate/up + down as one kernel with this many 16-CTA clusters
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
     int decode_kernels = 0;
