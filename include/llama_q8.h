@@ -192,7 +192,9 @@ llama_q8_status llama_q8_forward_argmax(llama_q8_ctx* ctx, const int32_t* ids, i
  * prompt[T] at position 0, then n_decode greedy decode steps, each feeding
  * back the previous token. out_ids (host, n_decode + 1 entries) receives the
  * token chosen by the prefill followed by one token per decode step. The
- * decode steps replay the CUDA graph back to back with the token fed back on
+ * decode steps replay the captured decode graphs back to back (one of eight
+ * steps while they fit, whose launches chain across the steps, then single
+ * steps) with the token fed back on
  * the device; the host reads the tokens once at the end. Requires
  * T + n_decode <= max_seq (LQ8_ERR_CTX). */
 llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int32_t T,

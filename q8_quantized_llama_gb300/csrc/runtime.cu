@@ -126,6 +126,10 @@ struct llama_q8_ctx {
     int mlp_clusters = 0;                // > 0: gate/up + down as one kernel with this many 16-CTA clusters
     cudaGraph_t decode_graph = nullptr;
     cudaGraphExec_t decode_exec = nullptr;
+    // kMultiSteps decode steps in one graph: the programmatic dependent launches
+    // chain across the steps too (no gap between graph launches)
+    cudaGraph_t multi_graph = nullptr;
+    cudaGraphExec_t multi_exec = nullptr;
     int decode_kernels = 0;
 
     size_t layer_cache_floats() const { return (size_t)cfg.n_head_kv * cfg.max_seq * cfg.head_dim; }
@@ -147,6 +151,8 @@ namespace {
 void free_ctx_memory(llama_q8_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     if (c->decode_graph) cudaGraphDestroy(c->decode_graph);
+    if (c->multi_exec) cudaGraphExecDestroy(c->multi_exec);
+    if (c->multi_graph) cudaGraphDestroy(c->multi_graph);
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
                    c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
                    c->d_out_ids,
@@ -405,12 +411,14 @@ llama_q8_status device_status(llama_q8_ctx* c) {
 
 int prefill_kernel_count(const llama_q8_ctx* c) { return 1 + 7 * c->cfg.n_layer + 1; }
 
-cudaError_t ensure_decode_graph(llama_q8_ctx* c) {
-    if (c->decode_exec) return cudaSuccess;
+constexpr int kMultiSteps = 8;
+
+// Capture `steps` decode steps back to back into one instantiated graph.
+cudaError_t capture_decode_steps(llama_q8_ctx* c, int steps, cudaGraph_t* graph, cudaGraphExec_t* exec, int* n_kernels) {
     cudaError_t err = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
     if (err != cudaSuccess) return err;
-    int n = 0;
-    cudaError_t lerr = enqueue_decode_step(c, &n);
+    cudaError_t lerr = cudaSuccess;
+    for (int i = 0; i < steps && lerr == cudaSuccess; ++i) lerr = enqueue_decode_step(c, n_kernels);
     cudaGraph_t g = nullptr;
     err = cudaStreamEndCapture(c->stream, &g);
     if (lerr != cudaSuccess) {
@@ -418,14 +426,32 @@ cudaError_t ensure_decode_graph(llama_q8_ctx* c) {
         return lerr;
     }
     if (err != cudaSuccess) return err;
-    err = cudaGraphInstantiate(&c->decode_exec, g, 0);
+    err = cudaGraphInstantiate(exec, g, 0);
     if (err != cudaSuccess) {
         cudaGraphDestroy(g);
         return err;
     }
-    c->decode_graph = g;
-    c->decode_kernels = n;
+    *graph = g;
     return cudaSuccess;
+}
+
+cudaError_t ensure_decode_graph(llama_q8_ctx* c) {
+    if (c->decode_exec) return cudaSuccess;
+    int n = 0;
+    cudaError_t err = capture_decode_steps(c, 1, &c->decode_graph, &c->decode_exec, &n);
+    if (err != cudaSuccess) return err;
+    c->decode_kernels = n;
+    int n8 = 0;
+    return capture_decode_steps(c, kMultiSteps, &c->multi_graph, &c->multi_exec, &n8);
+}
+
+// n decode steps on the context stream: the multi-step graph while it fits,
+// then single steps. Returns the number of kernel launches enqueued.
+cudaError_t launch_decode_steps(llama_q8_ctx* c, int n) {
+    cudaError_t err = cudaSuccess;
+    for (; n >= kMultiSteps && err == cudaSuccess; n -= kMultiSteps) err = cudaGraphLaunch(c->multi_exec, c->stream);
+    for (; n > 0 && err == cudaSuccess; --n) err = cudaGraphLaunch(c->decode_exec, c->stream);
+    return err;
 }
 
 llama_q8_status check_positions(const llama_q8_ctx* c, int T, int index_pos) {
@@ -767,7 +793,7 @@ llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int3
         LQ8_CK(ctx, enqueue_prefill(ctx, ctx->d_ids, T, 0));
         ctx->launches += 1 + prefill_kernel_count(ctx);
     }
-    for (int i = 0; i < n_decode; ++i) LQ8_CK(ctx, cudaGraphLaunch(ctx->decode_exec, ctx->stream));
+    LQ8_CK(ctx, launch_decode_steps(ctx, n_decode));
     ctx->launches += (int64_t)n_decode * ctx->decode_kernels;
     LQ8_CK(ctx, cudaMemcpyAsync(ctx->h_out, ctx->d_out_ids, sizeof(int32_t) * (n_decode + 1), cudaMemcpyDeviceToHost,
                                 ctx->stream));
@@ -810,7 +836,7 @@ llama_q8_status llama_q8_decode_async(llama_q8_ctx* ctx, int32_t n_steps, int32_
     LQ8_CK(ctx, cudaSetDevice(ctx->device));
     LQ8_CK(ctx, ensure_decode_graph(ctx));
     LQ8_CK(ctx, launch_set_state(ctx->d_state, -1, -1, 0, ctx->stream));
-    for (int i = 0; i < n_steps; ++i) LQ8_CK(ctx, cudaGraphLaunch(ctx->decode_exec, ctx->stream));
+    LQ8_CK(ctx, launch_decode_steps(ctx, n_steps));
     ctx->launches += 1 + (int64_t)n_steps * ctx->decode_kernels;
     LQ8_CK(ctx, cudaMemcpyAsync(d_out, ctx->d_out_ids, sizeof(int32_t) * n_steps, cudaMemcpyDeviceToDevice,
                                 ctx->stream));
