@@ -508,9 +508,24 @@ static int gemm_tc_splits(int tiles, int nb) {
         cudaDeviceGetAttribute(&g_tc_sms, cudaDevAttrMultiProcessorCount, dev);
         if (g_tc_sms <= 0) g_tc_sms = 148;
     }
-    int S = 1;
-    while (S < 8 && tiles * S * 2 <= g_tc_sms && nb / (S * 2) >= 2) S *= 2;
-    return S;
+    // split-K over S in {1, 2, 4, 8} CTAs of a cluster (S divides the 128 rows
+    // of a tile): the least estimated time, counted in k-blocks per wave of
+    // CTAs, with ~5 k-blocks' worth for the split's exchange and sum (the
+    // k-block pace is ~0.7 us, the split epilogue ~3-4 us), taken only when
+    // it beats the next smaller choice by more than 10%
+    constexpr int kSplitCost = 5;
+    int best = 1;
+    long best_cost = (long)((tiles + g_tc_sms - 1) / g_tc_sms) * nb;
+    for (int S = 2; S <= 8; S *= 2) {
+        if (nb / S < 2) break;
+        const long waves = ((long)tiles * S + g_tc_sms - 1) / g_tc_sms;
+        const long cost = waves * ((nb + S - 1) / S + kSplitCost);
+        if (cost * 10 < best_cost * 9) {  // a split only for a clear (> 10%) gain
+            best = S;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
