@@ -498,10 +498,11 @@ def gemv_7b_roofline(torch, B, synth, device, peak):
 
 
 def gemm_microbench(torch, B, synth, device):
-    """Q8_0 matrix-matrix products on the tensor cores: the pages' QMatMul
+    """Q8_0 matrix-matrix products: the pages' QMatMul
     shape [203,1536]x[1536,576] ("速度", CPU GGUF), the 135M prefill shapes at
-    203 rows, and 7B prefill shapes at 512 rows. Algorithmic TFLOP/s =
-    2*m*rows*k / time (the split-TF32 path issues three MMAs per product)."""
+    203 rows, and 7B prefill shapes at 512 rows, with the library's choice of
+    kernel and with each kernel forced (tensor cores, CUDA-core rows kernel).
+    Algorithmic TFLOP/s = 2*m*rows*k / time of the automatic choice."""
     out = []
     s = torch.cuda.current_stream()
     for m, rows, k in ((203, 576, 1536), (203, 960, 576), (203, 3072, 576), (512, 6144, 4096), (512, 28672, 4096),
@@ -515,17 +516,25 @@ def gemm_microbench(torch, B, synth, device):
         del dw, q
         x = torch.from_numpy(synth.normal_f32((m, k), 5, 1)).to(device)
         y = torch.empty((m, rows), dtype=torch.float32, device=device)
-        for _ in range(3):
-            B.llama_q8_matmul(packed, rows, k, x, m, y, s.cuda_stream)
-        n = 20
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        for _ in range(n):
-            B.llama_q8_matmul(packed, rows, k, x, m, y, s.cuda_stream)
-        e1.record(s)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1000 / n
-        out.append({"shape": f"[{m},{k}]x[{k},{rows}]", "us": us, "tflops": 2.0 * m * rows * k / (us * 1e-6) / 1e12})
+        rec = {"shape": f"[{m},{k}]x[{k},{rows}]"}
+        # the automatic choice first, then each kernel forced by flag
+        for key, flags in (("auto", 0), ("tensor_cores", B.LQ8_MATMUL_TENSOR_CORES),
+                           ("cuda_cores", B.LQ8_MATMUL_CUDA_CORES)):
+            for _ in range(3):
+                B.llama_q8_matmul_ex(packed, rows, k, x, m, y, flags, s.cuda_stream)
+            n = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(n):
+                B.llama_q8_matmul_ex(packed, rows, k, x, m, y, flags, s.cuda_stream)
+            e1.record(s)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000 / n
+            if key == "auto":
+                rec.update({"us": us, "tflops": 2.0 * m * rows * k / (us * 1e-6) / 1e12})
+            else:
+                rec[key + "_us"] = us
+        out.append(rec)
         del packed, x, y
         torch.cuda.empty_cache()
     return out

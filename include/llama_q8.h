@@ -325,6 +325,16 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
  * on the stream writes W; it is how the decode step chains its projections.
  * Unknown flag bits -> LQ8_ERR_ARG. */
 #define LQ8_MATMUL_EARLY_WEIGHTS 1
+/* Kernel for m > 1 token rows (m == 1 always takes the matrix-vector kernel).
+ * Neither flag: the tensor cores when m > 16, else the CUDA-core rows kernel,
+ * which streams each 32-row weight tile once per chunk of 16 token rows.
+ * LQ8_MATMUL_TENSOR_CORES / LQ8_MATMUL_CUDA_CORES force one kernel for any m
+ * > 1 (both -> LQ8_ERR_ARG; the CUDA-core kernel with more than 16 rows
+ * and k > 16896, or fewer rows and a k whose x slices do not fit its shared
+ * memory -> LQ8_ERR_UNSUPPORTED). Both compute the same product within the
+ * bounds stated above. */
+#define LQ8_MATMUL_TENSOR_CORES 2
+#define LQ8_MATMUL_CUDA_CORES 4
 llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, const float* x,
                                    int64_t m, float* y, int32_t flags, void* stream);
 

@@ -307,6 +307,8 @@ def llama_q8_matmul(packed, rows: int, k: int, x, m: int, y, stream=0) -> None:
 
 
 LQ8_MATMUL_EARLY_WEIGHTS = 1
+LQ8_MATMUL_TENSOR_CORES = 2
+LQ8_MATMUL_CUDA_CORES = 4
 
 
 def llama_q8_selftest_wait_timeout() -> int:

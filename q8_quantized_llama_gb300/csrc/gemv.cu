@@ -364,14 +364,15 @@ static int sm_count_current() {
 }
 
 // ---------------------------------------------------------------------------
-// Few token rows (prefill chunks of 2..16 tokens): the same weight stream,
-// each 32-row tile read once and multiplied with every token row. Lane = weight
-// row; per 32-weight block the lane turns its codes into f32 once and takes the
-// dot product with each token's x block (broadcast shared-memory reads).
-// Grid: one CTA per (tile, split), the block range of a tile split over a
-// cluster when the tiles cannot fill the GPU or the token rows' slices of x
-// would not fit in shared memory; the leader adds the peers' partial sums in
-// rank order.
+// Token rows on the CUDA cores (prefill chunks of 2..16 tokens, and small
+// products of more rows in chunks of 16): the same weight stream, each 32-row
+// tile read once per chunk and multiplied with every token row of the chunk.
+// Lane = weight row; per 32-weight block the lane turns its codes into f32
+// once and takes the dot product with each token's x block (broadcast
+// shared-memory reads). Grid: x = (tile, split), y = 16-token chunk; the block
+// range of a tile split over a cluster when the CTAs cannot fill the GPU or the
+// chunk's slices of x would not fit in shared memory; the leader adds the
+// peers' partial sums in rank order.
 // ---------------------------------------------------------------------------
 constexpr int kRowsMax = 16;
 // dynamic shared memory of the few-rows kernel, beside its ~19 KB of static arrays
@@ -417,7 +418,9 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_rows_kernel(GemvRowsArgs
     __shared__ float part[kRowsMax][32];
 
     const PackedQ8& W = a.W;
-    const int k = W.k, nb = k >> 5, m = a.m;
+    const int k = W.k, nb = k >> 5;
+    const int t0 = blockIdx.y * kRowsMax, m = min(kRowsMax, a.m - t0);  // this CTA's token rows
+    const float* X = a.X + (size_t)t0 * a.ldx;
     const int S = a.splits;
     const int tile = blockIdx.x / S, split = blockIdx.x % S;
     const int b0 = (split * nb) / S, b1 = ((split + 1) * nb) / S;
@@ -454,7 +457,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_rows_kernel(GemvRowsArgs
             pdl_wait();                                      // x: written by the preceding kernel
             mbar_arrive_expect_tx(&xbar, (uint32_t)(m * xn * 4));
             for (int t = 0; t < m; ++t)
-                bulk_g2s(xs + (size_t)t * xn, a.X + (size_t)t * a.ldx + b0 * 32, (uint32_t)(xn * 4), &xbar);
+                bulk_g2s(xs + (size_t)t * xn, X + (size_t)t * a.ldx + b0 * 32, (uint32_t)(xn * 4), &xbar);
             for (int j = first; j < n_stage; ++j) issue_stage(j);
         }
     } else {
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_rows_kernel(GemvRowsArgs
 #pragma unroll
             for (int w2 = 0; w2 < kCWarps; ++w2) v += red[w2][t][lane];
             if (S == 1)
-                rows_epilogue<EPI>(a.e, W.rows, tile, lane, t, v);
+                rows_epilogue<EPI>(a.e, W.rows, tile, lane, t0 + t, v);
             else
                 part[t][lane] = v;
         }
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(kGemvThreads) q8_gemv_rows_kernel(GemvRowsArgs
                 for (int t = warp; t < m; t += kCWarps) {
                     float v = part[t][lane];
                     for (int rnk = 1; rnk < S; ++rnk) v += ld_dsmem_f32(&part[t][lane], (uint32_t)rnk);
-                    rows_epilogue<EPI>(a.e, W.rows, tile, lane, t, v);
+                    rows_epilogue<EPI>(a.e, W.rows, tile, lane, t0 + t, v);
                 }
             }
             cluster_sync();  // peers keep their shared memory until the leader has read it
@@ -543,16 +546,17 @@ static cudaError_t gemv_rows_launch(const PackedQ8& W, const float* X, int m, in
     constexpr size_t ring = (size_t)RG::kStages * RG::kStageBytes;
     const int tiles = W.rows_pad / 32, nb = W.k / 32;
     const int sms = sm_count_current();
-    // splits: fill the GPU (at most one CTA per SM per tile-split, 8 blocks per split
-    // at least) and make the token rows' x slices fit beside the ring
+    const int chunks = (m + kRowsMax - 1) / kRowsMax, mc = std::min(m, kRowsMax);
+    // splits: fill the GPU (at most one CTA per SM per tile-split and chunk, 8
+    // blocks per split at least) and make the chunk's x slices fit beside the ring
     int S = 1;
-    auto fits = [&](int sp) { return ring + (size_t)m * ((nb + sp - 1) / sp) * 32 * 4 <= (size_t)kRowsMaxSmem; };
-    while (S < 8 && (!fits(S) || (tiles * (S + 1) <= sms && nb / (S + 1) >= 8))) ++S;
-    if (!fits(S)) return cudaErrorInvalidValue;
-    const size_t smem = ring + (size_t)m * ((nb + S - 1) / S) * 32 * 4;
+    auto fits = [&](int sp) { return ring + (size_t)mc * ((nb + sp - 1) / sp) * 32 * 4 <= (size_t)kRowsMaxSmem; };
+    while (S < 8 && (!fits(S) || ((int64_t)tiles * chunks * (S + 1) <= sms && nb / (S + 1) >= 8))) ++S;
+    if (!fits(S) || chunks > 65535) return cudaErrorInvalidValue;
+    const size_t smem = ring + (size_t)mc * ((nb + S - 1) / S) * 32 * 4;
     GemvRowsArgs a{W, X, m, ldx, e, S, err};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles * S);
+    cfg.gridDim = dim3(tiles * S, chunks);
     cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -575,9 +579,15 @@ static cudaError_t gemv_rows_launch(const PackedQ8& W, const float* X, int m, in
     return cudaLaunchKernelEx(&cfg, q8_gemv_rows_kernel<EPI, RG>, a);
 }
 
+bool gemv_rows_fits(int64_t m, int64_t k) {
+    constexpr size_t ring = (size_t)RingDeep::kStages * RingDeep::kStageBytes;
+    const int64_t mc = std::min<int64_t>(m, kRowsMax), nb = k / 32;
+    return ring + (size_t)mc * ((nb + 7) / 8) * 32 * 4 <= (size_t)kRowsMaxSmem;
+}
+
 cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                              int* err, cudaStream_t s) {
-    if (m < 1 || m > kRowsMax || ldx % 4) return cudaErrorInvalidValue;
+    if (m < 1 || ldx % 4) return cudaErrorInvalidValue;
     switch (epi) {
         case EPI_STORE: return gemv_rows_launch<EPI_STORE>(W, X, m, ldx, e, pdl, err, s);
         case EPI_RESIDUAL: return gemv_rows_launch<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s);

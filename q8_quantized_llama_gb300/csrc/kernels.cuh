@@ -122,21 +122,35 @@ cudaError_t launch_pack_fmt(int type, const uint8_t* src, int64_t rows, int64_t 
 cudaError_t launch_gemv_fmt(int type, const uint8_t* packed, int rows, int k, const float* x, float* y, bool pdl,
                             int* err, cudaStream_t s);
 cudaError_t init_gemv_fmt_attributes();
-// gemv.cu, 2 <= m <= 16 token rows: each weight tile streamed once for all rows
+// gemv.cu, m >= 2 token rows on the CUDA cores, in chunks of 16: each weight
+// tile streamed once per chunk for all of its rows
 cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                              int* err, cudaStream_t s);
+bool gemv_rows_fits(int64_t m, int64_t k);  // a chunk's x slices fit beside the ring (at most 8 splits)
 // gemm_tc.cu: tcgen05 split-TF32 kernel for many rows
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                            int* err, cudaStream_t s);
 cudaError_t init_gemm_tc_attributes();
 // Every kernel's attributes on the current device, once per device (runtime.cu).
 cudaError_t ensure_kernel_attributes();
-// Rows above which the matrix-matrix product runs on the tensor cores.
+// Which kernel takes a product of m > 1 token rows: the tensor cores above 16
+// rows, the CUDA-core rows kernel up to 16 (either can be forced). Measured on
+// the 135M prefill shapes at 203 rows, the tensor cores win even there, where
+// their start-up dominates: 14.5-20.6 us against 33-88 us for the rows kernel
+// in 16-row chunks.
 constexpr int kTensorCoreMinRows = 16;
+enum MatmulPath : int { MATMUL_AUTO = 0, MATMUL_TENSOR_CORES = 1, MATMUL_CUDA_CORES = 2 };
+inline bool matmul_on_tensor_cores(int m, int rows, int k, int path) {
+    (void)rows;
+    (void)k;
+    if (path == MATMUL_TENSOR_CORES) return true;
+    if (path == MATMUL_CUDA_CORES) return false;
+    return m > kTensorCoreMinRows;
+}
 inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,
-                                      bool pdl, int* err, cudaStream_t s) {
-    return m > kTensorCoreMinRows ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s)
-                                  : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
+                                      bool pdl, int* err, cudaStream_t s, int path = MATMUL_AUTO) {
+    return matmul_on_tensor_cores(m, W.rows, W.k, path) ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s)
+                                                         : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
 }
 
 // attention.cu

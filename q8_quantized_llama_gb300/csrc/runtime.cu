@@ -1045,7 +1045,10 @@ llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, con
 llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, const float* x, int64_t m, float* y,
                                    int32_t flags, void* stream) {
     if (!packed || !x || !y || rows <= 0 || k <= 0 || k % 32 || m <= 0) return LQ8_ERR_ARG;
-    if (flags & ~LQ8_MATMUL_EARLY_WEIGHTS) return LQ8_ERR_ARG;
+    if (flags & ~(LQ8_MATMUL_EARLY_WEIGHTS | LQ8_MATMUL_TENSOR_CORES | LQ8_MATMUL_CUDA_CORES)) return LQ8_ERR_ARG;
+    if ((flags & LQ8_MATMUL_TENSOR_CORES) && (flags & LQ8_MATMUL_CUDA_CORES)) return LQ8_ERR_ARG;
+    const int path = (flags & LQ8_MATMUL_TENSOR_CORES) ? MATMUL_TENSOR_CORES
+                     : (flags & LQ8_MATMUL_CUDA_CORES) ? MATMUL_CUDA_CORES : MATMUL_AUTO;
     // W and x are fetched by bulk and tensor copies: 16-byte aligned only
     if (((uintptr_t)packed | (uintptr_t)x) & 15) return LQ8_ERR_ARG;
     const bool early = (flags & LQ8_MATMUL_EARLY_WEIGHTS) != 0;
@@ -1060,7 +1063,8 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
         if ((size_t)k > gemv_max_k()) return LQ8_ERR_UNSUPPORTED;
         err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
     } else {
-        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
+        if (!matmul_on_tensor_cores((int)m, (int)rows, (int)k, path) && !gemv_rows_fits(m, k)) return LQ8_ERR_UNSUPPORTED;
+        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream, path);
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }

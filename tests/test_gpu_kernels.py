@@ -71,8 +71,16 @@ def _packed(wq_dev, rows, k):
     return packed
 
 
-def _matmul_case(rows, k, m, seed):
+def _on_tensor_cores(rows, k, m, path):
+    """The library's choice for m > 1 rows (llama_q8.h, LQ8_MATMUL_*)."""
+    if path != "auto":
+        return path == "tc"
+    return m > 16
+
+
+def _matmul_case(rows, k, m, seed, path="auto"):
     B = binding()
+    flags = {"auto": 0, "tc": B.LQ8_MATMUL_TENSOR_CORES, "cc": B.LQ8_MATMUL_CUDA_CORES}[path]
     w = synth.weight_matrix_f32(rows, k, seed, stream=rows + k)
     x = synth.normal_f32((m, k), seed, stream=m * 131 + k)
     wq = gpu_quantize(w)
@@ -80,7 +88,7 @@ def _matmul_case(rows, k, m, seed):
     packed = _packed(wq, rows, k)
     dx = to_dev(x)
     dy = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    B.llama_q8_matmul(packed, rows, k, dx, m, dy)
+    B.llama_q8_matmul_ex(packed, rows, k, dx, m, dy, flags)
     torch.cuda.synchronize()
     got = dy.cpu().numpy().astype(np.float64)
     wd = O.dequantize_q8_0(O.quantize_q8_0(w), rows, k).astype(np.float64)
@@ -89,11 +97,11 @@ def _matmul_case(rows, k, m, seed):
     # f32 accumulation: the matrix-vector kernel sums 32-code blocks, then at
     # most k/256 blocks per warp, then 8 warp partials; the matrix-matrix
     # kernel sums the k products in one chain. Bound = (chain + 8) u sum|w x|.
-    # Rows > 16 run on the tensor cores (codes times x split into tf32 hi and
-    # lo, block sums scaled by d): each product carries less than 2^-19
-    # relative error on top of the f32 accumulation.
+    # On the tensor cores (codes times x split into tf32 hi and lo, block sums
+    # scaled by d) each product carries less than 2^-19 relative error on top
+    # of the f32 accumulation.
     chain = (k // 256 + 40) if m == 1 else (k + 8)
-    split = 2.0 ** -19 if m > 16 else 0.0
+    split = 2.0 ** -19 if (m > 1 and _on_tensor_cores(rows, k, m, path)) else 0.0
     tol = ((chain + 8) * U + split) * mag + 1e-30
     assert np.all(np.isfinite(got))
     bad = np.abs(got - ref) > tol
@@ -125,6 +133,34 @@ def test_matmul_few_rows(rows, k, m):
     _matmul_case(rows, k, m, seed=6)
 
 
+@pytest.mark.parametrize("rows,k,m", [(960, 576, 203), (3072, 576, 203), (576, 1536, 203), (576, 576, 17),
+                                      (100, 96, 65), (4096, 4096, 40), (33, 14336, 31)])
+@pytest.mark.parametrize("path", ["cc", "tc"])
+def test_matmul_both_kernels_many_rows(rows, k, m, path):
+    """More than 16 token rows through each kernel, forced by flag: the
+    CUDA-core kernel in chunks of 16 rows (a ragged last chunk everywhere
+    here; 14336-wide rows split over a cluster) and the tensor cores, at the
+    135M prefill shapes of a 203-token prompt and ragged small shapes."""
+    _matmul_case(rows, k, m, seed=8, path=path)
+
+
+def test_matmul_path_flags_rejected_together():
+    B = binding()
+    rows, k, m = 64, 64, 20
+    packed = _packed(gpu_quantize(synth.weight_matrix_f32(rows, k, 9)), rows, k)
+    dx = torch.zeros((m, k), dtype=torch.float32, device="cuda")
+    dy = torch.zeros((m, rows), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.Q8Error) as e:
+        B.llama_q8_matmul_ex(packed, rows, k, dx, m, dy, B.LQ8_MATMUL_TENSOR_CORES | B.LQ8_MATMUL_CUDA_CORES)
+    assert e.value.status == B.LQ8_ERR_ARG
+    rows, k = 64, 16928  # above the CUDA-core kernel's 16896 for chunks of 16 rows
+    packed = _packed(gpu_quantize(synth.weight_matrix_f32(rows, k, 9)), rows, k)
+    dx = torch.zeros((m, k), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.Q8Error) as e:
+        B.llama_q8_matmul_ex(packed, rows, k, dx, m, dy, B.LQ8_MATMUL_CUDA_CORES)
+    assert e.value.status == B.LQ8_ERR_UNSUPPORTED
+
+
 def test_matmul_early_weights_chain_equals_serial_calls():
     """A chain of matrix-vector calls whose weight streams start before the
     previous call ends (each call reading the previous call's output) gives
@@ -151,11 +187,12 @@ def test_matmul_early_weights_chain_equals_serial_calls():
     for a, b in zip(serial, chained):
         np.testing.assert_array_equal(a, b)
     with pytest.raises(B.Q8Error):
-        B.llama_q8_matmul_ex(mats[0], rows, k, x0, 1, ys[0], 2)
+        B.llama_q8_matmul_ex(mats[0], rows, k, x0, 1, ys[0], 8)  # an unknown flag bit
 
 
 @pytest.mark.parametrize("rows,k", [(4096, 4096), (6144, 4096), (4096, 14336)])
 def test_matmul_tensor_core_7b_prefill_shapes(rows, k):
+    assert _on_tensor_cores(rows, k, 512, "auto")
     _matmul_case(rows, k, 512, seed=5)
 
 
@@ -176,7 +213,7 @@ def test_matmul_tensor_core_split_precision_one_hot(rows, k, m):
     np.testing.assert_array_equal(wq.cpu().numpy(), O.quantize_q8_0(w))
     packed = _packed(wq, rows, k)
     dy = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    B.llama_q8_matmul(packed, rows, k, to_dev(x), m, dy)
+    B.llama_q8_matmul_ex(packed, rows, k, to_dev(x), m, dy, B.LQ8_MATMUL_TENSOR_CORES)
     torch.cuda.synchronize()
     got = dy.cpu().numpy().astype(np.float64)
     wd = O.dequantize_q8_0(O.quantize_q8_0(w), rows, k).astype(np.float64)
