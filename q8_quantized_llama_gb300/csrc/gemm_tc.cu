@@ -497,29 +497,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kTcMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-static int g_tc_sms = 0;
+// CTAs of the tensor-core GEMM that can be resident at once with S CTAs per
+// cluster: one per SM without a split; with a split, the occupancy API's count
+// of co-resident S-CTA clusters (a cluster takes S SMs of one GPC, so on this
+// GPU 16 clusters of 8 do not all fit at once). Queried once per device.
+static int g_tc_capacity[64][4] = {};
 
-// k-splits per output tile: enough CTAs to cover the GPU once, at most 8 (a
-// portable cluster), at least two k-blocks per CTA.
-static int gemm_tc_splits(int tiles, int nb) {
-    if (g_tc_sms <= 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_tc_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_tc_sms <= 0) g_tc_sms = 148;
+static int gemm_tc_capacity(int S) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    const int slot = S == 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : 3;
+    int& cap = g_tc_capacity[dev][slot];
+    if (cap > 0) return cap;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    if (S == 1) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q8_gemm_tc_kernel<EPI_STORE, false>, kTcThreads,
+                                                          (size_t)kTcSmem) != cudaSuccess || per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        cap = sms * per_sm;
+        return cap;
     }
-    // split-K over S in {1, 2, 4, 8} CTAs of a cluster (S divides the 128 rows
-    // of a tile): the least estimated time, counted in k-blocks per wave of
-    // CTAs, with ~5 k-blocks' worth for the split's exchange and sum (the
-    // k-block pace is ~0.7 us, the split epilogue ~3-4 us), taken only when
-    // it beats the next smaller choice by more than 10%
-    constexpr int kSplitCost = 5;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, S);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = (size_t)kTcSmemSplit;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, q8_gemm_tc_kernel<EPI_STORE, true>, &cfg) != cudaSuccess ||
+        clusters < 1) {
+        cudaGetLastError();
+        clusters = sms / S;
+    }
+    cap = clusters * S;
+    return cap;
+}
+
+// k-splits per output tile over S in {1, 2, 4, 8} CTAs of a cluster (S divides
+// the 128 rows of a tile, at least two k-blocks per CTA): the least estimated
+// time, counted in k-blocks per wave of co-resident CTAs, with split_cost(S)
+// k-blocks' worth for the exchange of partial rows (measured with per-CTA
+// timestamps at 203 tokens: 0.64 us per k-block in steady state, ~2 us from
+// the last block partial to the peers' rows landing with S = 2, ~3.7 us with
+// S = 8), taken only when it beats the next smaller choice by more than 10%.
+static int split_cost(int S) { return 2 + S / 2; }
+
+static int gemm_tc_splits(int tiles, int nb) {
     int best = 1;
-    long best_cost = (long)((tiles + g_tc_sms - 1) / g_tc_sms) * nb;
+    const int cap1 = gemm_tc_capacity(1);
+    long best_cost = (long)((tiles + cap1 - 1) / cap1) * nb;
     for (int S = 2; S <= 8; S *= 2) {
         if (nb / S < 2) break;
-        const long waves = ((long)tiles * S + g_tc_sms - 1) / g_tc_sms;
-        const long cost = waves * ((nb + S - 1) / S + kSplitCost);
+        const int cap = gemm_tc_capacity(S);
+        const long waves = ((long)tiles * S + cap - 1) / cap;
+        const long cost = waves * ((nb + S - 1) / S + split_cost(S));
         if (cost * 10 < best_cost * 9) {  // a split only for a clear (> 10%) gain
             best = S;
             best_cost = cost;
