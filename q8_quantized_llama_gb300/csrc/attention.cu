@@ -15,11 +15,12 @@
 //    with bulk async copies and merges its partials through distributed
 //    shared memory (optionally applying the head's W_o column slice).
 //
-// Prefill (T > 1): attn_prefill_kernel<HD, RT>, a causal flash-style kernel,
-// one CTA per (query head, 16*RT query rows) with 256 threads as a 16 x 16
-// grid, register-blocked scores, K/V tiles of 64 positions (head_dim 64) or
-// 32 (head_dim 128) double-buffered in shared memory, online softmax; query t
-// sees positions <= index_pos + t ("量化 llama 的一次前向", forward：mask
+// Prefill (T > 1): attn_prefill_kernel<HD, RT, KS>, a causal flash-style
+// kernel, one CTA per (query head, 16*RT query rows) with 256 threads as a
+// 16 x 16 grid (or a cluster of KS CTAs splitting the keys, for short
+// prompts), register-blocked scores, K/V tiles of 64 positions (head_dim 64)
+// or 32 (head_dim 128) double-buffered in shared memory, online softmax; query
+// t sees positions <= index_pos + t ("量化 llama 的一次前向", forward：mask
 // 什么时候建 — the mask is a predicate here, never built).
 #include <mutex>
 
@@ -1033,6 +1034,11 @@ cudaError_t init_attention_attributes() {
 //  - output: thread (ty, tx) accumulates its RT rows x HD / 16 dims (float4
 //    groups tx and tx + 16) over the tile's keys.
 // K/V tiles are double-buffered with cp.async across the whole CTA.
+// Key split (KS > 1, short prompts whose row tiles cannot fill the GPU): a
+// cluster of KS CTAs shares one (head, row tile), rank z taking key tiles z,
+// z + KS, ...; each keeps its unnormalised output, row maxima and row sums in
+// shared memory, and rank 0 reads the peers' through distributed shared
+// memory and merges them (weights e^(m_z - M)) before the division.
 template <int HD, int RT>
 struct PfCfg {
     static constexpr int R = 16 * RT;              // query rows per CTA
@@ -1043,10 +1049,13 @@ struct PfCfg {
     static constexpr int LDP = KT + 4;             // floats per P row
     static constexpr int kQ = 0, kK = R * LD, kV = kK + 2 * KT * LD, kP = kV + 2 * KT * LD;
     static constexpr size_t kSmem = (size_t)(kP + R * LDP) * sizeof(float);
+    // key split: this CTA's unnormalised output rows, row maxima and row sums
+    static constexpr int kMO = kP + R * LDP, kMM = kMO + R * HD, kML = kMM + R;
+    static constexpr size_t kSmemSplit = (size_t)(kML + R) * sizeof(float);
 };
 constexpr int kPfThreads = 256;
 
-template <int HD, int RT>
+template <int HD, int RT, int KS>
 __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float* __restrict__ q,
                                                                      const float* __restrict__ kc,
                                                                      const float* __restrict__ vc, int T,
@@ -1059,19 +1068,22 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
     float* Qs = pf_smem + C::kQ;
     float* Ps = pf_smem + C::kP;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int h = blockIdx.x, t0 = blockIdx.y * R;
+    const int h = blockIdx.x / KS, z = blockIdx.x % KS, t0 = blockIdx.y * R;  // z: rank in the key split
     const int kh = h / (n_head / n_kv);
     const float* kbase = kc + (int64_t)kh * cache_stride * HD;
     const float* vbase = vc + (int64_t)kh * cache_stride * HD;
     const int kv_end = index_pos + min(T, t0 + R);
     const int n_tiles = (kv_end + KT - 1) / KT;
+    const int n_mine = n_tiles > z ? (n_tiles - z + KS - 1) / KS : 0;  // key tiles z, z + KS, ...
 
     pdl_wait();
     pdl_launch_dependents();
 
-    // copy tile `t` of K and V into stage `st` (positions past kv_end zero-filled)
-    auto issue = [&](int t, int st) {
-        if (t < n_tiles) {
+    // copy this CTA's key tile number `it` (tile z + it * KS) of K and V into
+    // stage `st` (positions past kv_end zero-filled)
+    auto issue = [&](int it, int st) {
+        if (it < n_mine) {
+            const int t = z + it * KS;
             float* ks = pf_smem + C::kK + st * KT * LD;
             float* vs = pf_smem + C::kV + st * KT * LD;
             for (int f = tid; f < KT * (HD / 4); f += kPfThreads) {
@@ -1105,12 +1117,13 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
         for (int g = 0; g < DG; ++g) o[i][g][0] = o[i][g][1] = o[i][g][2] = o[i][g][3] = 0.0f;
     }
 
-    for (int t = 0; t < n_tiles; ++t) {
-        issue(t + 1, (t + 1) & 1);
+    for (int it = 0; it < n_mine; ++it) {
+        const int t = z + it * KS;
+        issue(it + 1, (it + 1) & 1);
         cp_async_wait<1>();
-        __syncthreads();  // tile t (and, at t = 0, the q rows) visible to every thread
-        const float* ks = pf_smem + C::kK + (t & 1) * KT * LD;
-        const float* vs = pf_smem + C::kV + (t & 1) * KT * LD;
+        __syncthreads();  // tile t (and, at the first tile, the q rows) visible to every thread
+        const float* ks = pf_smem + C::kK + (it & 1) * KT * LD;
+        const float* vs = pf_smem + C::kV + (it & 1) * KT * LD;
         float sc[RT][KPT];
 #pragma unroll
         for (int i = 0; i < RT; ++i)
@@ -1189,15 +1202,76 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
         __syncthreads();  // the stage and P are read before they are refilled
     }
     cp_async_wait<0>();
-    // row sums over the half-warp, then o / l
+    // row sums over the half-warp
 #pragma unroll
     for (int i = 0; i < RT; ++i) {
-        float li = l[i];
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) li += __shfl_xor_sync(0xffffffffu, li, off);
+        for (int off = 8; off > 0; off >>= 1) l[i] += __shfl_xor_sync(0xffffffffu, l[i], off);
+    }
+    if (KS > 1) {
+        // key split: every rank leaves (o, m, l) in its shared memory; rank 0
+        // merges the peers' into its registers, the others are done after the
+        // second cluster barrier (which keeps their shared memory until rank 0
+        // has read it)
+        float* MO = pf_smem + C::kMO;
+        float* MM = pf_smem + C::kMM;
+        float* ML = pf_smem + C::kML;
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            const int row = ty * RT + i;
+#pragma unroll
+            for (int g = 0; g < DG; ++g)
+                *reinterpret_cast<float4*>(MO + row * HD + (tx + 16 * g) * 4) =
+                    make_float4(o[i][g][0], o[i][g][1], o[i][g][2], o[i][g][3]);
+            if (tx == 0) {
+                MM[row] = m[i];
+                ML[row] = l[i];
+            }
+        }
+        cluster_sync();
+        if (z == 0) {
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const int row = ty * RT + i;
+                float mz[KS];
+                mz[0] = m[i];
+                float mx = m[i];
+#pragma unroll
+                for (int r = 1; r < KS; ++r) {
+                    mz[r] = ld_dsmem_f32(MM + row, (uint32_t)r);
+                    mx = fmaxf(mx, mz[r]);
+                }
+                // weights e^(m_r - M); a rank that saw no visible key has m = -inf
+                const float w0 = m[i] == -INFINITY ? 0.0f : expf(m[i] - mx);
+                l[i] *= w0;
+#pragma unroll
+                for (int g = 0; g < DG; ++g) {
+                    o[i][g][0] *= w0; o[i][g][1] *= w0; o[i][g][2] *= w0; o[i][g][3] *= w0;
+                }
+#pragma unroll
+                for (int r = 1; r < KS; ++r) {
+                    const float wr = mz[r] == -INFINITY ? 0.0f : expf(mz[r] - mx);
+                    l[i] = fmaf(wr, ld_dsmem_f32(ML + row, (uint32_t)r), l[i]);
+#pragma unroll
+                    for (int g = 0; g < DG; ++g) {
+                        const float4 v = ld_dsmem_f32x4(MO + row * HD + (tx + 16 * g) * 4, (uint32_t)r);
+                        o[i][g][0] = fmaf(wr, v.x, o[i][g][0]);
+                        o[i][g][1] = fmaf(wr, v.y, o[i][g][1]);
+                        o[i][g][2] = fmaf(wr, v.z, o[i][g][2]);
+                        o[i][g][3] = fmaf(wr, v.w, o[i][g][3]);
+                    }
+                }
+            }
+        }
+        cluster_sync();
+        if (z != 0) return;
+    }
+    // o / l
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
         const int t = t0 + ty * RT + i;
         if (t < T) {
-            const float inv = 1.0f / li;
+            const float inv = 1.0f / l[i];
 #pragma unroll
             for (int g = 0; g < DG; ++g)
                 *reinterpret_cast<float4*>(out + ((int64_t)t * n_head + h) * HD + (tx + 16 * g) * 4) =
@@ -1206,34 +1280,83 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
     }
 }
 
-template <int HD, int RT>
+template <int HD, int RT, int KS>
 static cudaError_t pf_attr() {
-    return cudaFuncSetAttribute(attn_prefill_kernel<HD, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)PfCfg<HD, RT>::kSmem);
+    return cudaFuncSetAttribute(attn_prefill_kernel<HD, RT, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(KS > 1 ? PfCfg<HD, RT>::kSmemSplit : PfCfg<HD, RT>::kSmem));
 }
 
-cudaError_t init_attn_prefill_attributes() {
-    cudaError_t err = pf_attr<64, 1>();
-    if (err == cudaSuccess) err = pf_attr<64, 4>();
-    if (err == cudaSuccess) err = pf_attr<128, 1>();
-    if (err == cudaSuccess) err = pf_attr<128, 4>();
+template <int HD>
+static cudaError_t pf_attr_hd() {
+    cudaError_t err = pf_attr<HD, 4, 1>();
+    if (err == cudaSuccess) err = pf_attr<HD, 1, 1>();
+    if (err == cudaSuccess) err = pf_attr<HD, 1, 2>();
+    if (err == cudaSuccess) err = pf_attr<HD, 1, 4>();
+    if (err == cudaSuccess) err = pf_attr<HD, 1, 8>();
     return err;
 }
 
-template <int HD, int RT>
+cudaError_t init_attn_prefill_attributes() {
+    cudaError_t err = pf_attr_hd<64>();
+    if (err == cudaSuccess) err = pf_attr_hd<128>();
+    return err;
+}
+
+template <int HD, int RT, int KS>
 static cudaError_t pf_launch(const float* q, const float* k_cache, const float* v_cache, int T, int index_pos,
                              int n_head, int n_head_kv, int cache_stride, float* out, bool pdl, cudaStream_t s) {
     constexpr int R = PfCfg<HD, RT>::R;
-    const dim3 grid(n_head, (T + R - 1) / R);
     const float scale = 1.0f / sqrtf((float)HD);
-    return launch_ex(attn_prefill_kernel<HD, RT>, grid, dim3(kPfThreads), PfCfg<HD, RT>::kSmem, s, pdl, q, k_cache,
-                     v_cache, T, index_pos, n_head, n_head_kv, cache_stride, scale, out);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_head * KS, (T + R - 1) / R);
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = KS > 1 ? PfCfg<HD, RT>::kSmemSplit : PfCfg<HD, RT>::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int n = 0;
+    if (KS > 1) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = KS;
+        attrs[n].val.clusterDim.y = 1;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, attn_prefill_kernel<HD, RT, KS>, q, k_cache, v_cache, T, index_pos, n_head,
+                              n_head_kv, cache_stride, scale, out);
+}
+
+template <int HD>
+static cudaError_t pf_dispatch(const float* q, const float* k_cache, const float* v_cache, int T, int index_pos,
+                               int n_head, int n_head_kv, int cache_stride, float* out, bool pdl, cudaStream_t s,
+                               int sms) {
+    // 64 rows per CTA when that still gives every SM a CTA; else 16 rows, and
+    // when even those leave SMs idle, each row tile's keys split over a
+    // cluster of 2, 4 or 8 CTAs (two resident per SM, at least one key tile
+    // each)
+    if ((int64_t)n_head * ((T + 63) / 64) >= sms)
+        return pf_launch<HD, 4, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+    const int64_t ctas = (int64_t)n_head * ((T + 15) / 16);
+    const int tiles = (index_pos + T + PfCfg<HD, 1>::KT - 1) / PfCfg<HD, 1>::KT;
+    int ks = 1;
+    while (ks < 8 && ctas * ks * 2 <= 2 * (int64_t)sms && tiles >= ks * 2) ks *= 2;
+    switch (ks) {
+        case 2: return pf_launch<HD, 1, 2>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+        case 4: return pf_launch<HD, 1, 4>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+        case 8: return pf_launch<HD, 1, 8>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+    }
+    return pf_launch<HD, 1, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
 }
 
 cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const float* v_cache, int T,
                                 int index_pos, int n_head, int n_head_kv, int head_dim, int cache_stride,
                                 float* out, bool pdl, cudaStream_t s) {
-    // 64 rows per CTA when that still gives every SM a CTA, else 16
     static int sms = 0;
     if (sms <= 0) {
         int dev = 0;
@@ -1241,13 +1364,10 @@ cudaError_t launch_attn_prefill(const float* q, const float* k_cache, const floa
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms <= 0) sms = 148;
     }
-    const bool big = (int64_t)n_head * ((T + 63) / 64) >= sms;
     if (head_dim == 64)
-        return big ? pf_launch<64, 4>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s)
-                   : pf_launch<64, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+        return pf_dispatch<64>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s, sms);
     if (head_dim == 128)
-        return big ? pf_launch<128, 4>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s)
-                   : pf_launch<128, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+        return pf_dispatch<128>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s, sms);
     return cudaErrorInvalidValue;
 }
 

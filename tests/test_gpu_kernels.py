@@ -268,12 +268,16 @@ def test_attention_decode_7b(kv_len):
 
 
 # 16 query rows per CTA for these; (1100, 0) and (1030, 7) give 64 rows per CTA
-@pytest.mark.parametrize("T,index_pos", [(203, 0), (64, 512), (2, 0), (13, 33), (33, 0), (1100, 0), (1030, 7)])
+# prompts whose 16-row tiles leave SMs idle split each tile's keys over a
+# cluster: (203, 0) over 2 CTAs, (64, 200) over 4, (64, 512) over 8 at the 135M
+# shape; (64, 512) over 2, (16, 100) over 4, (16, 1000) over 8 at the 7B shape
+@pytest.mark.parametrize("T,index_pos", [(203, 0), (64, 512), (64, 200), (2, 0), (13, 33), (33, 0), (1100, 0),
+                                         (1030, 7)])
 def test_attention_prefill_135m(T, index_pos):
     _attention_case(T, index_pos, 9, 3, 64, 4096, seed=T + index_pos)
 
 
-@pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8), (300, 100)])
+@pytest.mark.parametrize("T,index_pos", [(512, 0), (64, 512), (5, 8), (300, 100), (16, 100), (16, 1000)])
 def test_attention_prefill_7b(T, index_pos):
     _attention_case(T, index_pos, 32, 8, 128, 4096, seed=T * 3 + index_pos)
 
