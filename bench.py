@@ -63,8 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--cpu-baseline-threads", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--cpu-baseline-config", choices=["c0", "c1", "c4"], default="c1", help=argparse.SUPPRESS)
-    p.add_argument("--only", choices=["gemv7b", "attn", "gemm", "decode", "decode7b", "prefill", "prefill7b",
-                                      "sweep", "attnprefill", "profile"],
+    p.add_argument("--only", choices=["gemv7b", "formats", "attn", "gemm", "decode", "decode7b", "prefill",
+                                      "prefill7b", "sweep", "attnprefill", "profile"],
                    default=None,
                    help="run one kernel workload only (used for ncu captures)")
     return p.parse_args(argv)
@@ -497,6 +497,54 @@ def gemv_7b_roofline(torch, B, synth, device, peak):
             "serial_us": res["serial"], "serial_frac": algo / (res["serial"] * 1e-6) / 1e9 / peak}
 
 
+def block_format_gemv_bench(torch, B, synth, device, peak):
+    """The matrix-vector product in the other GGUF block formats of a Q4_K_M
+    file ("速度", CPU GGUF：decode 快，prefill 慢: Q5_0, Q4K, Q6K), with Q8_0
+    beside them, at two shapes: [1,4096]x[4096,14336] for bandwidth (chained
+    launches rotating over 8 weight copies, 8 x 33-62 MB > L2, so each launch
+    streams its matrix from HBM) and the pages' QMatMul shape
+    [1,1536]x[1536,576] (latency bound; 64 rotating copies). Algorithmic bytes
+    = rows * k * (block bytes / block weights) + 4 k + 4 rows."""
+    formats = (("Q8_0", B.GGUF_Q8_0, 34 / 32), ("Q5_0", B.GGUF_Q5_0, 22 / 32), ("Q4_K", B.GGUF_Q4_K, 144 / 256),
+               ("Q6_K", B.GGUF_Q6_K, 210 / 256))
+    s = torch.cuda.current_stream()
+    out = []
+    for rows, k, ncopy, n in ((14336, 4096, 8, 200), (576, 1536, 64, 400)):
+        x = torch.from_numpy(synth.normal_f32((1, k), 3, 7)).to(device)
+        y = torch.empty((1, rows), dtype=torch.float32, device=device)
+        for name, t, bpw in formats:
+            if t == B.GGUF_Q8_0:
+                w = torch.from_numpy(synth.weight_matrix_f32(rows, k, 3)).to(device)
+                blob = torch.empty((rows, k // 32 * 34), dtype=torch.uint8, device=device)
+                B.llama_q8_quantize(w, rows, k, blob)
+                del w
+            else:
+                blob = torch.from_numpy(synth.random_blocks(t, rows, k, 3)).to(device)
+            nbytes = B.llama_q8_packed_bytes_fmt(t, rows, k)
+            first = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            B.llama_q8_pack_fmt(t, blob, rows, k, first)
+            del blob
+            copies = [first] + [first.clone() for _ in range(ncopy - 1)]
+            flags = B.LQ8_MATMUL_EARLY_WEIGHTS
+            for i in range(16):
+                B.llama_q8_matvec_fmt(t, copies[i % ncopy], rows, k, x, y, flags, s.cuda_stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(s)
+            for i in range(n):
+                B.llama_q8_matvec_fmt(t, copies[i % ncopy], rows, k, x, y, flags, s.cuda_stream)
+            e1.record(s)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000 / n
+            algo = rows * k * bpw + 4 * k + 4 * rows
+            gbs = algo / (us * 1e-6) / 1e9
+            out.append({"format": name, "shape": f"[1,{k}]x[{k},{rows}]", "us": us, "algorithmic_bytes": algo,
+                        "achieved_gbs": gbs, "frac": gbs / peak})
+            del copies, first
+            torch.cuda.empty_cache()
+    return out
+
+
 def gemm_microbench(torch, B, synth, device):
     """Q8_0 matrix-matrix products: the pages' QMatMul
     shape [203,1536]x[1536,576] ("速度", CPU GGUF), the 135M prefill shapes at
@@ -796,6 +844,7 @@ def run_ours(args):
     if rank == 0:
         lm_head = lm_head_variants(torch, B, synth, device, peak, prompt, DECODE_STEPS)
         gemv7 = gemv_7b_roofline(torch, B, synth, device, peak)
+        fmt_gemv = block_format_gemv_bench(torch, B, synth, device, peak)
         attn = attention_microbench(torch, B, synth, device, peak)
         attn_pf = attention_prefill_bench(torch, B, synth, device)
         sweep = linear_sweep(torch, B, synth, device, peak)
@@ -844,6 +893,7 @@ def run_ours(args):
             "kernels": fams,
             "lm_head": lm_head,
             "gemv_7b": gemv7,
+            "block_format_gemv": fmt_gemv,
             "attention_decode": attn,
             "attention_prefill": attn_pf,
             "linear_sweep": sweep,
@@ -934,13 +984,14 @@ def main():
         print(json.dumps({"attention_decode": attention_microbench(torch, B, synth, torch.device("cuda", 0),
                                                                     hbm_peak()[0])}))
         return
-    if args.only == "gemv7b":
+    if args.only in ("gemv7b", "formats"):
         import torch
         torch.cuda.set_device(0)
         from q8_quantized_llama_gb300 import binding as B
         from q8_quantized_llama_gb300 import synth
         B.lib()
-        print(json.dumps(gemv_7b_roofline(torch, B, synth, torch.device("cuda", 0), hbm_peak()[0])))
+        fn = gemv_7b_roofline if args.only == "gemv7b" else block_format_gemv_bench
+        print(json.dumps(fn(torch, B, synth, torch.device("cuda", 0), hbm_peak()[0])))
         return
     run_ours(args)
 

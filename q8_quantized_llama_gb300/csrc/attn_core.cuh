@@ -2,7 +2,7 @@
 // geometry, the producer and consumer sides of one KV head's position share
 // (two passes per window through a ring of shared-memory stages), the
 // butterfly reduce-scatter of the K pass, and distributed-shared-memory
-// stores. Included by attention.cu and decode_layer.cu.
+// stores. Included by attention.cu.
 #pragma once
 
 #include "kernels.cuh"
