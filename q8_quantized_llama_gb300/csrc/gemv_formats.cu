@@ -13,10 +13,10 @@
 //   Q6_K (6720 B): 8 chunks of ql | 4 chunks of qh | 16 int8 scales 32 x 16 | d 32 x 2
 // A tile's block range is one contiguous run of records, streamed into a
 // shared-memory ring by a producer warp with bulk async copies, as in the
-// Q8_0 kernel. Eight consumer warps take 32-weight units (a Q5_0 block, a
-// Q4_K sub-block, two Q6_K sub-blocks of 16) and turn codes into exact f32
-// with the offset folded in: bytes 0x4B0000cc are 2^23 + c, and subtracting
-// 2^23 + offset leaves c - offset.
+// Q8_0 kernel. Eight consumer warps take units (a Q5_0 block, half a Q4_K
+// block of four sub-blocks, two Q6_K sub-blocks of 16) and turn codes into
+// exact f32 with the offset folded in: bytes 0x4B0000cc are 2^23 + c, and
+// subtracting 2^23 + offset leaves c - offset.
 #include <algorithm>
 #include <map>
 #include <mutex>
@@ -37,15 +37,17 @@ template <int T>
 struct Fmt;
 template <>
 struct Fmt<kGgufQ5_0> {
-    static constexpr int kW = 32, kBytes = 22, kRec = 32 * 22, kUnits = 1, kStageRecs = 16;
+    static constexpr int kW = 32, kBytes = 22, kRec = 32 * 22, kUnits = 1, kUnitW = 32, kStageRecs = 16;
 };
 template <>
 struct Fmt<kGgufQ4_K> {
-    static constexpr int kW = 256, kBytes = 144, kRec = 32 * 144, kUnits = 8, kStageRecs = 2;
+    // a unit is half a block (four sub-blocks): the scale bytes are read and
+    // unpacked once per unit, and each 32-byte chunk pair serves two sub-blocks
+    static constexpr int kW = 256, kBytes = 144, kRec = 32 * 144, kUnits = 2, kUnitW = 128, kStageRecs = 4;
 };
 template <>
 struct Fmt<kGgufQ6_K> {
-    static constexpr int kW = 256, kBytes = 210, kRec = 32 * 210, kUnits = 8, kStageRecs = 2;
+    static constexpr int kW = 256, kBytes = 210, kRec = 32 * 210, kUnits = 8, kUnitW = 32, kStageRecs = 2;
 };
 
 // Four codes held as bytes of c (each < 256 - 2^23 rounding is exact) minus
@@ -94,33 +96,44 @@ __device__ __forceinline__ float unit_dot<kGgufQ5_0>(const uint8_t* rec, int, in
 }
 
 template <>
-__device__ __forceinline__ float unit_dot<kGgufQ4_K>(const uint8_t* rec, int s, int lane, const float* x,
+__device__ __forceinline__ float unit_dot<kGgufQ4_K>(const uint8_t* rec, int u, int lane, const float* x,
                                                      const float* xsum) {
-    // sub-block s: low (s even) or high (s odd) nibbles of qs bytes [32 (s / 2), + 32)
-    const int c = s >> 1, sh = (s & 1) * 4;
-    const uint4 q0 = lds_u4(rec + (2 * c) * 512 + lane * 16);
-    const uint4 q1 = lds_u4(rec + (2 * c + 1) * 512 + lane * 16);
-    const uint8_t* meta = rec + 4096 + lane * 16;
-    const float d = __half2float(*reinterpret_cast<const __half*>(meta));
-    const float dmin = __half2float(*reinterpret_cast<const __half*>(meta + 2));
-    const uint8_t* scb = meta + 4;
-    int sc, mn;
-    if (s < 4) {
-        sc = scb[s] & 63;
-        mn = scb[s + 4] & 63;
-    } else {
-        sc = (scb[s + 4] & 0xF) | ((scb[s - 4] >> 6) << 4);
-        mn = (scb[s + 4] >> 4) | ((scb[s] >> 6) << 4);
+    // unit u: sub-blocks 4u .. 4u + 3, the low and high nibbles of qs bytes
+    // [64u, 64u + 64) (chunks 4u .. 4u + 3). The lane's 16 metadata bytes in one
+    // load: fp16 d, fp16 dmin, then the 12 scale bytes; the unit's four 6-bit
+    // scales and minima unpacked as the bytes of one word each.
+    const uint4 meta = lds_u4(rec + 4096 + lane * 16);
+    const float d = __half2float(__ushort_as_half((unsigned short)(meta.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(meta.x >> 16)));
+    uint32_t scw, mnw;
+    if (u == 0) {  // sub-blocks 0..3: low six bits of scale bytes 0..3 and 4..7
+        scw = meta.y & 0x3F3F3F3Fu;
+        mnw = meta.z & 0x3F3F3F3Fu;
+    } else {  // sub-blocks 4..7: nibbles of bytes 8..11, top two bits from bytes 0..3 / 4..7
+        scw = (meta.w & 0x0F0F0F0Fu) | ((meta.y >> 2) & 0x30303030u);
+        mnw = ((meta.w >> 4) & 0x0F0F0F0Fu) | ((meta.z >> 2) & 0x30303030u);
     }
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    uint64_t a0 = 0, a1 = 0;
+    float qacc = 0.0f, macc = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        a0 = dot4_codes((word(q0, i) >> sh) & 0x0F0F0F0Fu, x4[i], 0.0f, a0);
-        a1 = dot4_codes((word(q1, i) >> sh) & 0x0F0F0F0Fu, x4[4 + i], 0.0f, a1);
+    for (int p = 0; p < 2; ++p) {
+        const uint4 q0 = lds_u4(rec + (4 * u + 2 * p) * 512 + lane * 16);      // weights 0..15 of sub-blocks 2p, 2p + 1
+        const uint4 q1 = lds_u4(rec + (4 * u + 2 * p + 1) * 512 + lane * 16);  // weights 16..31
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int jj = 2 * p + h;  // sub-block within the unit: low nibbles (h = 0) or high
+            uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a0 = dot4_codes((word(q0, i) >> (4 * h)) & 0x0F0F0F0Fu, x4[8 * jj + i], 0.0f, a0);
+                a1 = dot4_codes((word(q1, i) >> (4 * h)) & 0x0F0F0F0Fu, x4[8 * jj + 4 + i], 0.0f, a1);
+            }
+            const float qx = (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1));
+            qacc = fmaf((float)((scw >> (8 * jj)) & 0xFFu), qx, qacc);
+            macc = fmaf((float)((mnw >> (8 * jj)) & 0xFFu), xsum[jj], macc);
+        }
     }
-    const float qx = (f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1));
-    return (d * (float)sc) * qx - (dmin * (float)mn) * xsum[0];
+    return d * qacc - dmin * macc;
 }
 
 template <>
@@ -241,7 +254,7 @@ __global__ void __launch_bounds__(kFmtThreads) fmt_gemv_kernel(FmtArgs a) {
                 for (int v = warp; v < kUnitsPerStage; v += kFmtCWarps) {
                     const int r = v / F::kUnits, u = v % F::kUnits;
                     if (r < nbs) {
-                        const int w0 = (j * F::kStageRecs + r) * F::kW + u * 32;  // relative to the slice
+                        const int w0 = (j * F::kStageRecs + r) * F::kW + u * F::kUnitW;  // relative to the slice
                         acc += unit_dot<T>(st + r * F::kRec, u, lane, xs + w0, xsum + w0 / 32);
                     }
                 }
