@@ -624,35 +624,29 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
             const float acc = tile_blocks_dot(tw, nbx, warp, kCaWarps, nbx, lane, XN);
             RED2[warp * 33 + lane] = acc;
             named_bar_sync(1, kCaCT);
-            if (warp == 0) {
-                float v = 0.0f;
+            // every warp sums the eight partials (same order, same result) and
+            // sends the rows to its share of the cluster's CTAs: ranks warp,
+            // warp + 8; warp 0 also writes the cache
+            float v = 0.0f;
 #pragma unroll
-                for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
-                v *= r_norm;
-                const float other = __shfl_xor_sync(0xffffffffu, v, 1);
-                const int row = qkv_tile_row0(i) + lane;  // row of [Wq;Wk;Wv]
-                if (i < nq + nkt) {
-                    // q or k row: rotate the pair (2m, 2m+1) of its head
-                    const int d = row % HD;
-                    const float cs = cosr[d >> 1], sn = sinr[d >> 1];
-                    const float rot = (lane & 1) ? other * sn + v * cs : v * cs - other * sn;
-                    if (i < nq) {
-                        float* dst = &Q[row - kh * G * HD];
-#pragma unroll 4
-                        for (int r = 0; r < CL; ++r) st_async_f32(dst, (uint32_t)r, rot, &rows_bar);
-                    } else {
-                        fa.kc[((int64_t)kh * fa.stride + pos) * HD + d] = rot;
-#pragma unroll 4
-                        for (int r = 0; r < CL; ++r) st_async_f32(&KNEW[d], (uint32_t)r, rot, &rows_bar);
-                    }
-                } else {
-                    const int d = row % HD;
-                    fa.vc[((int64_t)kh * fa.stride + pos) * HD + d] = v;
-#pragma unroll 4
-                    for (int r = 0; r < CL; ++r) st_async_f32(&VNEW[d], (uint32_t)r, v, &rows_bar);
-                }
+            for (int w = 0; w < kCaWarps; ++w) v += RED2[w * 33 + lane];
+            v *= r_norm;
+            const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+            const int row = qkv_tile_row0(i) + lane;  // row of [Wq;Wk;Wv]
+            const int d = row % HD;
+            float val = v;
+            float* dst = &VNEW[d];
+            if (i < nq + nkt) {
+                // q or k row: rotate the pair (2m, 2m+1) of its head
+                const float cs = cosr[d >> 1], sn = sinr[d >> 1];
+                val = (lane & 1) ? other * sn + v * cs : v * cs - other * sn;
+                dst = i < nq ? &Q[row - kh * G * HD] : &KNEW[d];
+                if (i >= nq && warp == 0) fa.kc[((int64_t)kh * fa.stride + pos) * HD + d] = val;
+            } else if (warp == 0) {
+                fa.vc[((int64_t)kh * fa.stride + pos) * HD + d] = v;
             }
-            named_bar_sync(1, kCaCT);
+            for (int r = warp; r < CL; r += kCaWarps) st_async_f32(dst, (uint32_t)r, val, &rows_bar);
+            if (i + CL < n_qkv) named_bar_sync(1, kCaCT);  // RED2 is refilled by the next tile
         }
     }
     mbar_wait_bounded(&rows_bar, 0, fa.err, 26);  // q, k and v of the new position are here
@@ -741,7 +735,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) layer_front_cluster_kernel(Fron
             const int r = t * 32 + lane;
             if (r < fa.wo.rows) fa.part[(int64_t)kh * fa.part_stride + r] = v;
         }
-        named_bar_sync(1, kCaCT);
+        if (t + CL < o_tiles) named_bar_sync(1, kCaCT);  // RED2 is refilled by the next tile
     }
 }
 

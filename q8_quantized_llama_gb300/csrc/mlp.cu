@@ -23,7 +23,7 @@ constexpr int kMlpCT = kMlpWarps * 32;
 constexpr int kMlpThreads = kMlpCT + 32;
 
 struct MlpPlan {
-    int gu, wd, wds, xs, a, part, red_in, red, floats;  // offsets in floats
+    int gu, wd, wds, xs, red_in, red, floats;  // offsets in floats
 };
 __host__ __device__ inline int mlp_round(int n) { return (n + 31) / 32 * 32; }
 __host__ __device__ inline int mlp_rows_per_owner(int h) { return (h / kMlpCl + 3) / 4 * 4; }
@@ -36,8 +36,6 @@ __host__ __device__ inline MlpPlan mlp_plan(int h) {
     p.wd = take(tiles_h * 512 / 4);     // W_down: this CTA's 16-code chunk of each row tile
     p.wds = take(tiles_h * 64 / 4);     // and the scales of its block
     p.xs = take(h);                     // x * g
-    p.a = take(kMlpProd);               // this CTA's SiLU products
-    p.part = take(h);                   // this CTA's partial of W_down a
     p.red_in = take(kMlpCl * mlp_rows_per_owner(h));  // partials of the rows this CTA owns
     p.red = take(kMlpWarps * 33);
     p.floats = o;
@@ -60,8 +58,6 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
     uint8_t* WD = reinterpret_cast<uint8_t*>(smf + pl.wd);
     uint8_t* WDS = reinterpret_cast<uint8_t*>(smf + pl.wds);
     float* XS = smf + pl.xs;
-    float* A = smf + pl.a;
-    float* PART = smf + pl.part;
     float* RIN = smf + pl.red_in;
     float* RED = smf + pl.red;
     const int own0 = q * rpo, own1 = min(h, own0 + rpo);  // rows this CTA reduces
@@ -150,38 +146,40 @@ __global__ void __launch_bounds__(kMlpThreads, 1) decode_mlp_kernel(MlpArgs ma) 
     mbar_wait_bounded(&w_bar, 0, ma.err, 51);
 
     // ---- gate/up: tile c, its blocks over the eight warps; lane = row ----------------------
+    // Every warp sums the eight warp partials and forms the 16 SiLU products
+    // itself (the same sums in the same order in every warp), so the down
+    // projection needs no further barrier.
+    float4 a4[4];
     {
         const float acc = tile_blocks_dot(GU, nbx, warp, kMlpWarps, nbx, lane, XS);
         RED[warp * 33 + lane] = acc;
         named_bar_sync(1, kMlpCT);
-        if (warp == 0) {
-            float v = 0.0f;
+        float v = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kMlpWarps; ++w) v += RED[w * 33 + lane];
-            v *= r_norm;
-            const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-            if (!(lane & 1)) A[lane >> 1] = silu_f32(v) * up;
-        }
-        named_bar_sync(1, kMlpCT);
+        for (int w = 0; w < kMlpWarps; ++w) v += RED[w * 33 + lane];
+        v *= r_norm;
+        const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+        const float prod = silu_f32(v) * up;  // valid in even lanes: entry lane / 2
+        float e[kMlpProd];
+#pragma unroll
+        for (int i = 0; i < kMlpProd; ++i) e[i] = __shfl_sync(0xffffffffu, prod, 2 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a4[i] = make_float4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
     }
 
     // ---- down: this CTA's 16 columns of W_down times a, every row tile; lane = row ---------
+    // each row's partial goes straight to the cluster CTA owning the row:
+    // RIN[source rank][r - owner's first row]
 #pragma unroll 2
     for (int t = warp; t < tiles_h; t += kMlpWarps) {
         const uint4 q0 = *reinterpret_cast<const uint4*>(WD + (size_t)t * 512 + lane * 16);
         const float d = __half2float(reinterpret_cast<const __half*>(WDS + (size_t)t * 64)[lane]);
-        const float4* a4 = reinterpret_cast<const float4*>(A);
         uint64_t a0 = 0, a1 = 0;
         a0 = dot4_acc(q0.x, a4[0], a0); a1 = dot4_acc(q0.y, a4[1], a1);
         a0 = dot4_acc(q0.z, a4[2], a0); a1 = dot4_acc(q0.w, a4[3], a1);
-        PART[t * 32 + lane] = d * ((f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)));
-    }
-    named_bar_sync(1, kMlpCT);
-    // rows r go to the cluster CTA owning them: RIN[source rank][r - owner's first row]
-    for (int f = tid; f < h / 4; f += kMlpCT) {
-        const int r = f * 4, owner = r / rpo;
-        const float4 v = *reinterpret_cast<const float4*>(PART + r);
-        st_async_f32x4(&RIN[q * rpo + (r - owner * rpo)], (uint32_t)owner, v, &red_bar);
+        const float p = d * ((f2_lo(a0) + f2_hi(a0)) + (f2_lo(a1) + f2_hi(a1)));
+        const int r = t * 32 + lane, owner = r / rpo;
+        st_async_f32(&RIN[q * rpo + (r - owner * rpo)], (uint32_t)owner, p, &red_bar);
     }
     mbar_wait_bounded(&red_bar, 0, ma.err, 52);  // the 8 partials of the rows this CTA owns
     for (int r = own0 + tid; r < own1; r += kMlpCT) {
