@@ -311,10 +311,13 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
  * kernel_mul_mv_q8_0_f32 / kernel_mul_mm_q8_0_f32): up to 16 rows on the CUDA
  * cores with f32 accumulation (each 32-row weight tile streamed once and
  * multiplied with every row of x), more rows on the tcgen05 tensor cores: per
- * Q8_0 block the int8 codes (exact in tf32) times x split into tf32 hi and lo
- * parts (two TF32 products per step, f32 accumulation in tensor memory), the
- * block sums scaled by d and added in f32; less than 2^-19 relative error per
- * product. packed and x must be 16-byte aligned (LQ8_ERR_ARG otherwise). */
+ * Q8_0 block the int8 codes (exact in f16) times x, each token row scaled by
+ * a power of two (its largest |x| into [2^14, 2^15), found by a short pass
+ * before the product) and split into f16 hi and lo parts (two f16 products
+ * per step, f32 accumulation in tensor memory), the block sums scaled by d and
+ * added in f32, the row scale undone exactly; at most 2^-22 relative error per
+ * product, plus 2^-39 of the row's largest |x| times the weight. packed and x
+ * must be 16-byte aligned (LQ8_ERR_ARG otherwise). */
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
                                 int64_t m, float* y, void* stream);
 

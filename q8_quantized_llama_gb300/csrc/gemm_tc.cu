@@ -4,14 +4,18 @@
 // token", prefill 和 decode：同一个 forward，不同的路: many rows go to the
 // matrix-matrix kernel).
 //
-// Precision: the int8 codes q of a Q8_0 block are exact in tf32, and the
+// Precision: the int8 codes q of a Q8_0 block are exact in f16, and the
 // block scale d is one number per (row, k-block), so the tensor cores compute
-// per k-block the block partial P = sum_k q.x with the activation split as
-// x = x_hi + x_lo (x_hi = the tensor core's truncated tf32 reading of x, x_lo
-// = x - x_hi exact in f32, of which the MMA keeps the top 11 bits): two MMAs
-// per k-step, f32 accumulation in TMEM. Accumulator warps then add d.P to the
-// running sums in registers. Each product q.x is off by less than 2^-20
-// relative (the truncated x_lo), plus one f32 rounding per block partial.
+// per k-block the block partial P = sum_k q.x' in f16 x f16 -> f32 MMAs
+// (kind::f16), with each token's activations scaled by a power of two 2^s
+// (the row's largest magnitude, found by a short pass before the product,
+// brought into [2^14, 2^15)) and split as x' = x 2^s = hi + lo (hi = x'
+// rounded to f16, lo = x' - hi rounded to f16): two MMAs per 16-wide k-step,
+// f32 accumulation in TMEM. Accumulator warps add d.P to the running sums in
+// registers; the epilogue multiplies each token's sums by 2^-s (exact). Each
+// product q.x is off by at most 2^-22 relative, plus 2^-39 of the row's
+// largest |x| times |q| where lo falls below the f16 normal range, then one
+// f32 rounding per block partial.
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
 // Q8_0 block; one 128-byte swizzle row of f32). Warp roles (18 warps):
@@ -21,10 +25,11 @@
 //    views [tile][k-block][1 KiB or 64 B] of the packed weights, one box each;
 //    tiles past the matrix read as zeros);
 //  - two groups of 4 converter warps, taking k-blocks in turn: write each
-//    row's 32 codes as f32 into tensor memory (tcgen05.st; A operand, row r in
-//    lane r) and x_lo beside the activation tile in shared memory (generic
-//    stores, then a proxy fence for the tensor core);
-//  - MMA warp: one thread issues the 8 MMAs of a k-block (A from tensor
+//    row's 32 codes as f16 pairs into tensor memory (tcgen05.st; A operand,
+//    row r in lane r) and, one thread per token, the token's scaled hi and lo
+//    rows as f16 K-major tiles with the 64-byte swizzle beside the activation
+//    tile (generic stores, then a proxy fence for the tensor core);
+//  - MMA warp: one thread issues the 4 MMAs of a k-block (A from tensor
 //    memory) into one of two block-partial buffers and commits them to the
 //    stage's "done" barrier (frees the stage for the producer) and to the
 //    buffer's "full" barrier;
@@ -62,8 +67,11 @@ static_assert(kTcStagesMax % kTcConvGroups == 0 && kTcStagesSplit % kTcConvGroup
               "each stage is converted by one group");
 constexpr int kTcProducerWarp = kTcConvWarps + kTcAccWarps, kTcMmaWarp = kTcProducerWarp + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
-// one stage: x tile (hi as loaded), x_lo tile, codes of 4 row tiles, their scales
-constexpr int kStXlo = kTileBytes, kStCodes = 2 * kTileBytes, kStScales = kStCodes + 4096;
+// one stage: x tile (f32, as loaded), its hi and lo f16 tiles (128 tokens x
+// 64 bytes each), codes of 4 row tiles, their scales
+constexpr int kHalfTileBytes = 128 * 64;
+constexpr int kStHi = kTileBytes, kStLo = kStHi + kHalfTileBytes, kStCodes = kStLo + kHalfTileBytes;
+constexpr int kStScales = kStCodes + 4096;
 constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
 constexpr int kTcSmem = kTcStagesMax * kStageBytes + 1024;  // + alignment slack
 constexpr int kPartStride = kTcBN + 4;                   // floats per row of a partial tile in shared memory
@@ -72,10 +80,11 @@ constexpr int kRecvBytes = kTcBM * kPartStride * 4;
 constexpr int kTcSmemSplit = kTcStagesSplit * kStageBytes + 1024 + kRecvBytes;
 static_assert(kTcSmem <= 227 * 1024 && kTcSmemSplit <= 227 * 1024, "shared memory per CTA");
 // tensor memory: two block-partial buffers of 128 columns, then per stage the
-// 32 codes of each row (A operand)
+// 32 codes of each row as 16 f16 pairs (A operand)
 constexpr int kTmemCols = 512;
 constexpr int kTmemA = 2 * kTcBN;
-static_assert(kTmemA + kTcStagesMax * 32 <= kTmemCols, "tensor memory columns");
+constexpr int kTmemACols = 16;  // columns of one stage's A
+static_assert(kTmemA + kTcStagesMax * kTmemACols <= kTmemCols, "tensor memory columns");
 
 // ---- tcgen05 wrappers ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
@@ -93,29 +102,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle (rows of
+// 64 bytes; 16-byte chunk c of row r stored at chunk c ^ ((r / 2) % 4)), 8-row
+// groups 512 bytes apart.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFF) >> 4);         // start address
     d |= (uint64_t)(16 >> 4) << 16;                   // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
+    d |= (uint64_t)(512 >> 4) << 32;                  // stride byte offset
     d |= (uint64_t)1 << 46;                           // descriptor version
-    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    d |= (uint64_t)4 << 61;                           // 64-byte swizzle
     return d;
 }
 
-// Instruction descriptor: D f32, A/B tf32, both K-major, M = 128, N = 128.
-constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kTcBN >> 3) << 17) |
-                                ((uint32_t)(kTcBM >> 4) << 24);
+// Instruction descriptor: D f32, A and B f16, both K-major, M = 128, N = 128.
+constexpr uint32_t kIdescF16 = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcBN >> 3) << 17) |
+                               ((uint32_t)(kTcBM >> 4) << 24);
 
 // D (tensor memory) += A (tensor memory, row i in lane i, k along columns) * B (shared memory)
-__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(kIdescTf32), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(kIdescF16), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -164,21 +174,25 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// Exact f32 values of 16 codes (4 words) times the block scale.
-__device__ __forceinline__ void dequant16(const uint4& q, float d, float (&w)[16]) {
-    const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t u = ws[i] ^ 0x80808080u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float biased = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 + j));
-            w[4 * i + j] = d * (biased - 8388736.0f);
-        }
-    }
+// Four codes (one word) as two f16 pairs, exactly: each byte u = q + 128
+// becomes the f16 1024 + u (exponent 10, u in the mantissa), minus 1152.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t q, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = q ^ 0x80808080u;
+    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480u), __ushort_as_half((unsigned short)0x6480u));
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&ha);
+    hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // sign, exponent and the 10 mantissa bits of tf32
+// Exponent s of the power of two that brings a row's largest magnitude mx
+// into [2^14, 2^15), clamped so that 2^s and 2^-s are normal f32 numbers.
+__device__ __forceinline__ int row_shift(float mx) {
+    const int e = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+    return max(-126, min(126, 14 - e));
+}
+__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
 
 // Epilogue of one output element pair/element (row r of W, token t).
 template <int EPI>
@@ -212,12 +226,14 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     q8_gemm_tc_kernel(PackedQ8 W, const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap dmap, int m, EpiArgs e, int* err) {
+                      const __grid_constant__ CUtensorMap dmap, int m, const float* __restrict__ rowmax, EpiArgs e,
+                      int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int kTcStages = SPLIT ? kTcStagesSplit : kTcStagesMax;
     __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
-    __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and x_lo
+    __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and the hi / lo tiles
+    __shared__ float row_inv[kTcBN];                        // each token's 2^-s, for the epilogue
     __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
     __shared__ __align__(8) uint64_t part_full[2];          // a block partial is in tensor memory
     __shared__ __align__(8) uint64_t part_empty[2];         // the accumulator warps have read it
@@ -301,13 +317,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (kb >= 2 && alive) alive = mbar_wait_bounded(&part_empty[p], ((kb >> 1) - 1) & 1, err, 17);
                 tc_fence_after();
                 const uint32_t xs = smem_u32(smem + s * kStageBytes);
-                const uint32_t a = tmem + (uint32_t)(kTmemA + s * 32);
+                const uint32_t a = tmem + (uint32_t)(kTmemA + s * kTmemACols);
                 const uint32_t d = tmem + (uint32_t)(p * kTcBN);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t b_hi = sw128_desc(xs + kk * 32), b_lo = sw128_desc(xs + kStXlo + kk * 32);
-                    mma_tf32_ts(d, a + kk * 8, b_hi, kk != 0);
-                    mma_tf32_ts(d, a + kk * 8, b_lo, 1u);
+                for (int kk = 0; kk < 2; ++kk) {  // two 16-wide k-steps, 32 bytes apart in the rows
+                    const uint64_t b_hi = sw64_desc(xs + kStHi + kk * 32), b_lo = sw64_desc(xs + kStLo + kk * 32);
+                    mma_f16_ts(d, a + kk * 8, b_hi, kk != 0);
+                    mma_f16_ts(d, a + kk * 8, b_lo, 1u);
                 }
                 mma_commit(&done_bar[s]);
                 mma_commit(&part_full[p]);
@@ -320,39 +336,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pdl_wait();
         if (tid == 0) pdl_launch_dependents();
         // converter group g takes k-blocks g, g + G, ...; warp w of the group
-        // writes the 32 codes (as exact f32) of row r = 32 * (w % 4) + lane
+        // writes the 32 codes (as exact f16) of row r = 32 * (w % 4) + lane,
+        // and thread gtid converts token row gtid of the activation tile
         const int group = warp / kTcGroupWarps, gtid = tid - group * kTcGroupWarps * 32;
         const int quarter = warp & 3;
         const bool row_ok = quarter < valid_tiles;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        // this token's scale 2^s from its row maximum (rows past m: any scale, x is zero)
+        const int tok = t0 + gtid;
+        const int sh = row_shift(tok < m ? rowmax[tok] : 0.0f);
+        const float sc = pow2f(sh);
+        if (group == 0) row_inv[gtid] = pow2f(-sh);
         for (int kb = group; kb < nb; kb += kTcConvGroups) {
             const int s = kb % kTcStages;
             if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 11);
             tc_fence_after();
             uint8_t* st = smem + s * kStageBytes;
-            const uint32_t a = tmem + lane_base + (uint32_t)(kTmemA + s * 32);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint4 qa = make_uint4(0u, 0u, 0u, 0u);
-                if (row_ok) qa = *reinterpret_cast<const uint4*>(st + kStCodes + quarter * 1024 + h * 512 + lane * 16);
-                float w[16];
-                dequant16(qa, 1.0f, w);  // the codes themselves: exact in tf32
+            const uint32_t a = tmem + lane_base + (uint32_t)(kTmemA + s * kTmemACols);
+            {
                 uint32_t u[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(w[i]);
-                tmem_st16(a + h * 16, u);
+                for (int h = 0; h < 2; ++h) {
+                    uint4 qa = make_uint4(0u, 0u, 0u, 0u);
+                    if (row_ok) qa = *reinterpret_cast<const uint4*>(st + kStCodes + quarter * 1024 + h * 512 + lane * 16);
+                    codes_to_f16x2(qa.x, u[8 * h + 0], u[8 * h + 1]);
+                    codes_to_f16x2(qa.y, u[8 * h + 2], u[8 * h + 3]);
+                    codes_to_f16x2(qa.z, u[8 * h + 4], u[8 * h + 5]);
+                    codes_to_f16x2(qa.w, u[8 * h + 6], u[8 * h + 7]);
+                }
+                tmem_st16(a, u);  // column c: codes 2c, 2c + 1
             }
-            // x_lo: elementwise, so the swizzled positions of the x tile carry over
+            // token row gtid: its 32 f32 in 16-byte chunks c at chunk c ^ (r % 8) of the
+            // 128-byte row (the copy's 128-byte swizzle); hi and lo into 64-byte rows,
+            // chunk c (k = 8c .. 8c + 7) at chunk c ^ ((r / 2) % 4)
+            const int r = gtid;
 #pragma unroll
-            for (int i = 0; i < kTileBytes / (kTcGroupWarps * 32 * 16); ++i) {
-                const int off = (gtid + i * kTcGroupWarps * 32) * 16;
-                const float4 x = *reinterpret_cast<const float4*>(st + off);
-                float4 xl;
-                xl.x = x.x - __uint_as_float(__float_as_uint(x.x) & kTf32Mask);
-                xl.y = x.y - __uint_as_float(__float_as_uint(x.y) & kTf32Mask);
-                xl.z = x.z - __uint_as_float(__float_as_uint(x.z) & kTf32Mask);
-                xl.w = x.w - __uint_as_float(__float_as_uint(x.w) & kTf32Mask);
-                *reinterpret_cast<float4*>(st + kStXlo + off) = xl;
+            for (int c = 0; c < 4; ++c) {
+                const float4 xa = *reinterpret_cast<const float4*>(st + r * 128 + (((2 * c) ^ (r & 7)) << 4));
+                const float4 xb = *reinterpret_cast<const float4*>(st + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4));
+                const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float x0 = xv[2 * i] * sc, x1 = xv[2 * i + 1] * sc;
+                    const __half2 hi = __floats2half2_rn(x0, x1);
+                    const float2 hf = __half22float2(hi);
+                    const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+                    hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
+                    lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
+                }
+                const int off = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+                *reinterpret_cast<uint4*>(st + kStHi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(st + kStLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             tmem_wait_st();
             fence_proxy_async_smem();
@@ -423,6 +458,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c0 = part * 32; c0 < part * 32 + 32; c0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(eq * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] *= row_inv[c0 + j];
                 if (EPI == EPI_RESIDUAL) {
                     // the 16 residual reads first, then the 16 writes: no chain of dependent round trips
                     float y0[16];
@@ -479,7 +516,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 v0.x += a4.x; v0.y += a4.y; v0.z += a4.z; v0.w += a4.w;
                 v1.x += b4.x; v1.y += b4.y; v1.z += b4.z; v1.w += b4.w;
             }
-            const float e0[4] = {v0.x, v0.y, v0.z, v0.w}, e1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const float i0 = row_inv[t], i1 = row_inv[t + 1], i2 = row_inv[t + 2], i3 = row_inv[t + 3];
+            const float e0[4] = {v0.x * i0, v0.y * i1, v0.z * i2, v0.w * i3};
+            const float e1[4] = {v1.x * i0, v1.y * i1, v1.z * i2, v1.w * i3};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (EPI == EPI_QKV || EPI == EPI_SILU) {
@@ -627,9 +666,37 @@ static cudaError_t make_w_maps(CUtensorMap* qmap, CUtensorMap* dmap, const Packe
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Largest |x| of each token row (the product's per-row scale): one warp per
+// row, float4 loads; after the grid dependency wait, since X comes from the
+// preceding kernel.
+constexpr int kRowMaxWarps = 8;
+__global__ void __launch_bounds__(kRowMaxWarps * 32) row_absmax_kernel(const float* __restrict__ X, int m, int k,
+                                                                        int ldx, float* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRowMaxWarps + warp;
+    if (t >= m) return;
+    const float* row = X + (size_t)t * ldx;
+    float mx = 0.0f;
+    for (int i = lane * 4; i < k; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(row + i);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) out[t] = mx;
+}
+
 template <int EPI>
 static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
-                               int* err, cudaStream_t s) {
+                               int* err, cudaStream_t s, float* rowmax, bool rowmax_ready) {
+    if (!rowmax_ready) {
+        cudaError_t rerr = launch_ex(row_absmax_kernel, dim3((m + kRowMaxWarps - 1) / kRowMaxWarps),
+                                     dim3(kRowMaxWarps * 32), 0, s, pdl, X, m, W.k, ldx, rowmax);
+        if (rerr != cudaSuccess) return rerr;
+        pdl = true;  // the product follows its own row-maximum pass
+    }
     CUtensorMap xmap, qmap, dmap;
     cudaError_t merr = make_x_map(&xmap, X, m, W.k, ldx);
     if (merr == cudaSuccess) merr = make_w_maps(&qmap, &dmap, W);
@@ -638,7 +705,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     const int S = gemm_tc_splits(gx * gy, W.k / 32);
     if (S == 1)
         return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gy, gx), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
-                         xmap, qmap, dmap, m, e, err);
+                         xmap, qmap, dmap, m, (const float*)rowmax, e, err);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gy, gx, S);
     cfg.blockDim = dim3(kTcThreads);
@@ -657,7 +724,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, qmap, dmap, m, e, err);
+    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, qmap, dmap, m, (const float*)rowmax, e, err);
 }
 
 template <int EPI>
@@ -679,12 +746,13 @@ cudaError_t init_gemm_tc_attributes() {
 }
 
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
-                           int* err, cudaStream_t s) {
+                           int* err, cudaStream_t s, float* rowmax, bool rowmax_ready) {
+    if (!rowmax) return cudaErrorInvalidValue;
     switch (epi) {
-        case EPI_STORE: return gemm_tc_one<EPI_STORE>(W, X, m, ldx, e, pdl, err, s);
-        case EPI_RESIDUAL: return gemm_tc_one<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s);
-        case EPI_QKV: return gemm_tc_one<EPI_QKV>(W, X, m, ldx, e, pdl, err, s);
-        case EPI_SILU: return gemm_tc_one<EPI_SILU>(W, X, m, ldx, e, pdl, err, s);
+        case EPI_STORE: return gemm_tc_one<EPI_STORE>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
+        case EPI_RESIDUAL: return gemm_tc_one<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
+        case EPI_QKV: return gemm_tc_one<EPI_QKV>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
+        case EPI_SILU: return gemm_tc_one<EPI_SILU>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
     }
     return cudaErrorInvalidValue;
 }

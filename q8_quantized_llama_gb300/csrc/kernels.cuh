@@ -89,7 +89,7 @@ cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const Dev
 // returns when that kernel has completed.
 cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
-                           cudaStream_t s);
+                           cudaStream_t s, float* rowmax = nullptr);
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
 cudaError_t launch_wait_timeout(int* err, int code, cudaStream_t s);  // bounded-wait self-test
 
@@ -127,9 +127,13 @@ cudaError_t init_gemv_fmt_attributes();
 cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
                              int* err, cudaStream_t s);
 bool gemv_rows_fits(int64_t m, int64_t k);  // a chunk's x slices fit beside the ring (at most 8 splits)
-// gemm_tc.cu: tcgen05 split-TF32 kernel for many rows
+// gemm_tc.cu: tcgen05 kernel for many rows (f16 products of the codes and of
+// each token's activations scaled by a power of two and split into hi and lo);
+// rowmax: device memory of m floats for the rows' largest |x|: filled by a
+// pass launched just before the product, or (rowmax_ready) already written by
+// the kernel that produced X
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
-                           int* err, cudaStream_t s);
+                           int* err, cudaStream_t s, float* rowmax, bool rowmax_ready = false);
 cudaError_t init_gemm_tc_attributes();
 // Every kernel's attributes on the current device, once per device (runtime.cu).
 cudaError_t ensure_kernel_attributes();
@@ -148,9 +152,11 @@ inline bool matmul_on_tensor_cores(int m, int rows, int k, int path) {
     return m > kTensorCoreMinRows;
 }
 inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,
-                                      bool pdl, int* err, cudaStream_t s, int path = MATMUL_AUTO) {
-    return matmul_on_tensor_cores(m, W.rows, W.k, path) ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s)
-                                                         : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
+                                      bool pdl, int* err, cudaStream_t s, float* rowmax, int path = MATMUL_AUTO,
+                                      bool rowmax_ready = false) {
+    return matmul_on_tensor_cores(m, W.rows, W.k, path)
+               ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s, rowmax, rowmax_ready)
+               : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
 }
 
 // attention.cu

@@ -152,8 +152,10 @@ cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 // RMSNorm rows: y = x * g / sqrt(mean(x^2) + eps), f32.
 // ---------------------------------------------------------------------------
+// rowmax (optional): each output row's largest |y|, the per-row scale the
+// tensor-core product that reads y needs
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g, float eps,
-                               int k, float* __restrict__ y) {
+                               int k, float* __restrict__ y, float* __restrict__ rowmax) {
     __shared__ float red[32];
     pdl_wait();
     pdl_launch_dependents();
@@ -175,17 +177,30 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
     }
     __syncthreads();
     const float r = 1.0f / sqrtf(red[0] / (float)k + eps);
+    float mx = 0.0f;
     for (int i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
         float4 v = *reinterpret_cast<const float4*>(xr + i);
         float4 gg = *reinterpret_cast<const float4*>(g + i);
-        *reinterpret_cast<float4*>(yr + i) =
-            make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
+        const float4 o = make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
+        *reinterpret_cast<float4*>(yr + i) = o;
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
+    }
+    if (rowmax) {
+        mx = warp_max(mx);
+        __syncthreads();  // every thread has read the sum of squares from red[0]
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+            v = warp_max(v);
+            if (threadIdx.x == 0) rowmax[blockIdx.x] = v;
+        }
     }
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
-                           cudaStream_t s) {
-    return launch_ex(rmsnorm_kernel, dim3(m), dim3(256), 0, s, pdl, x, g, eps, k, y);
+                           cudaStream_t s, float* rowmax) {
+    return launch_ex(rmsnorm_kernel, dim3(m), dim3(256), 0, s, pdl, x, g, eps, k, y, rowmax);
 }
 
 __global__ void set_state_kernel(DevState* st, int pos, int token, int n_out) {

@@ -109,6 +109,7 @@ struct llama_q8_ctx {
     unsigned long long* d_best = nullptr;
     unsigned int* d_done = nullptr;
     void* d_attn_ws = nullptr;
+    float* d_rowmax = nullptr;  // prefill products on the tensor cores: each token row's largest |x|
 
     int32_t* h_ids = nullptr;
     int32_t* h_out = nullptr;
@@ -156,7 +157,7 @@ void free_ctx_memory(llama_q8_ctx* c) {
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
                    c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
                    c->d_out_ids,
-                   c->d_state, c->d_best, c->d_done, c->d_attn_ws};
+                   c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_rowmax};
     for (void* p : dev)
         if (p) cudaFree(p);
     void* host[] = {c->h_ids, c->h_out, c->h_logits, c->h_state};
@@ -374,23 +375,25 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
     cudaError_t err = launch_embed(c->embd, d_ids, T, nullptr, c->d_state, c->d_x, cfg.n_vocab, true, s);
     for (int l = 0; l < cfg.n_layer && err == cudaSuccess; ++l) {
         const LayerDev& L = c->layers[l];
-        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
+        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, true, s, c->d_rowmax);
         EpiArgs e = qkv_epi(c, l);
         e.pos0 = index_pos;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.qkv, c->d_y, T, h, EPI_QKV, e, true, &c->d_state->err, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.qkv, c->d_y, T, h, EPI_QKV, e, true, &c->d_state->err, s, c->d_rowmax,
+                                                         MATMUL_AUTO, true);
         if (err == cudaSuccess)
             err = launch_attn_prefill(c->d_q, c->kcache(l), c->vcache(l), T, index_pos, cfg.n_head, cfg.n_head_kv,
                                       cfg.head_dim, cfg.max_seq, c->d_o, true, s);
         EpiArgs r;
         r.y = c->d_x;
         r.ldy = h;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, &c->d_state->err, s);
-        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, true, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, &c->d_state->err, s, c->d_rowmax);
+        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, true, s, c->d_rowmax);
         EpiArgs g;
         g.a_out = c->d_a;
         g.lda = cfg.n_ff;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.gu, c->d_y, T, h, EPI_SILU, g, true, &c->d_state->err, s);
-        if (err == cudaSuccess) err = launch_matmul_rows(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, &c->d_state->err, s);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.gu, c->d_y, T, h, EPI_SILU, g, true, &c->d_state->err, s, c->d_rowmax,
+                                                         MATMUL_AUTO, true);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, &c->d_state->err, s, c->d_rowmax);
     }
     if (err == cudaSuccess)
         err = launch_gemv(c->head, c->d_x + (size_t)(T - 1) * h, c->out_norm, cfg.rms_eps, EPI_ARGMAX,
@@ -409,7 +412,13 @@ llama_q8_status device_status(llama_q8_ctx* c) {
     return LQ8_ERR_CUDA;
 }
 
-int prefill_kernel_count(const llama_q8_ctx* c) { return 1 + 7 * c->cfg.n_layer + 1; }
+// embed, per layer two norms, attention and four products (on the tensor
+// cores, W_o and the down projection after a row-maximum pass each; the
+// norms give Q/K/V and gate/up theirs), the lm_head
+int prefill_kernel_count(const llama_q8_ctx* c, int T) {
+    const int per_layer = 7 + (matmul_on_tensor_cores(T, 0, 0, MATMUL_AUTO) ? 2 : 0);
+    return 1 + per_layer * c->cfg.n_layer + 1;
+}
 
 constexpr int kMultiSteps = 8;
 
@@ -482,7 +491,7 @@ llama_q8_status run_forward(llama_q8_ctx* c, const int32_t* ids, int T, int inde
         LQ8_CK(c, cudaMemcpyAsync(c->d_ids, c->h_ids, sizeof(int32_t) * T, cudaMemcpyHostToDevice, c->stream));
         LQ8_CK(c, launch_set_state(c->d_state, index_pos, -1, 0, c->stream));
         LQ8_CK(c, enqueue_prefill(c, c->d_ids, T, index_pos));
-        c->launches += 1 + prefill_kernel_count(c);
+        c->launches += 1 + prefill_kernel_count(c, T);
     }
     c->len = index_pos + T;
     return LQ8_OK;
@@ -702,6 +711,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_q, sizeof(float) * T * c->q_rows));
     LOAD_CK(cudaMalloc(&c->d_o, sizeof(float) * T * c->q_rows));
     LOAD_CK(cudaMalloc(&c->d_a, sizeof(float) * T * F));
+    LOAD_CK(cudaMalloc(&c->d_rowmax, sizeof(float) * T));
     LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
     LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_xr, sizeof(float) * h));
@@ -791,7 +801,7 @@ llama_q8_status llama_q8_generate(llama_q8_ctx* ctx, const int32_t* prompt, int3
         LQ8_CK(ctx, cudaMemcpyAsync(ctx->d_ids, ctx->h_ids, sizeof(int32_t) * T, cudaMemcpyHostToDevice, ctx->stream));
         LQ8_CK(ctx, launch_set_state(ctx->d_state, 0, -1, 0, ctx->stream));
         LQ8_CK(ctx, enqueue_prefill(ctx, ctx->d_ids, T, 0));
-        ctx->launches += 1 + prefill_kernel_count(ctx);
+        ctx->launches += 1 + prefill_kernel_count(ctx, T);
     }
     LQ8_CK(ctx, launch_decode_steps(ctx, n_decode));
     ctx->launches += (int64_t)n_decode * ctx->decode_kernels;
@@ -820,7 +830,7 @@ llama_q8_status llama_q8_prefill_async(llama_q8_ctx* ctx, const int32_t* d_ids, 
         ctx->launches += 1 + ctx->decode_kernels;
     } else {
         LQ8_CK(ctx, enqueue_prefill(ctx, d_ids, T, index_pos));
-        ctx->launches += 1 + prefill_kernel_count(ctx);
+        ctx->launches += 1 + prefill_kernel_count(ctx, T);
     }
     LQ8_CK(ctx, cudaMemcpyAsync(d_next, ctx->d_out_ids, sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
     ctx->len = index_pos + T;
@@ -1063,8 +1073,18 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
         if ((size_t)k > gemv_max_k()) return LQ8_ERR_UNSUPPORTED;
         err = launch_gemv(W, x, nullptr, 0.f, EPI_STORE, e, early, nullptr, (cudaStream_t)stream);
     } else {
-        if (!matmul_on_tensor_cores((int)m, (int)rows, (int)k, path) && !gemv_rows_fits(m, k)) return LQ8_ERR_UNSUPPORTED;
-        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream, path);
+        const bool tc = matmul_on_tensor_cores((int)m, (int)rows, (int)k, path);
+        if (!tc && !gemv_rows_fits(m, k)) return LQ8_ERR_UNSUPPORTED;
+        float* rowmax = nullptr;  // the rows' largest |x| (tensor cores), stream-ordered scratch
+        if (tc && cudaMallocAsync(reinterpret_cast<void**>(&rowmax), sizeof(float) * (size_t)m,
+                                  (cudaStream_t)stream) != cudaSuccess)
+            return LQ8_ERR_OOM;
+        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream, rowmax,
+                                 path);
+        if (rowmax) {
+            const cudaError_t ferr = cudaFreeAsync(rowmax, (cudaStream_t)stream);
+            if (err == cudaSuccess) err = ferr;
+        }
     }
     return err == cudaSuccess ? LQ8_OK : LQ8_ERR_CUDA;
 }
