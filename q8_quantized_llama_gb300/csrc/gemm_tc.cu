@@ -27,8 +27,9 @@
 //  - two groups of 4 converter warps, taking k-blocks in turn: write each
 //    row's 32 codes as f16 pairs into tensor memory (tcgen05.st; A operand,
 //    row r in lane r) and, one thread per token, the token's scaled hi and lo
-//    rows as f16 K-major tiles with the 64-byte swizzle beside the activation
-//    tile (generic stores, then a proxy fence for the tensor core);
+//    as one f16 K-major tile (hi then lo in each 128-byte row, 128-byte
+//    swizzle) beside the activation tile (generic stores, then a proxy fence
+//    for the tensor core);
 //  - MMA warp: one thread issues the 4 MMAs of a k-block (A from tensor
 //    memory) into one of two block-partial buffers and commits them to the
 //    stage's "done" barrier (frees the stage for the producer) and to the
@@ -67,10 +68,10 @@ static_assert(kTcStagesMax % kTcConvGroups == 0 && kTcStagesSplit % kTcConvGroup
               "each stage is converted by one group");
 constexpr int kTcProducerWarp = kTcConvWarps + kTcAccWarps, kTcMmaWarp = kTcProducerWarp + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
-// one stage: x tile (f32, as loaded), its hi and lo f16 tiles (128 tokens x
-// 64 bytes each), codes of 4 row tiles, their scales
-constexpr int kHalfTileBytes = 128 * 64;
-constexpr int kStHi = kTileBytes, kStLo = kStHi + kHalfTileBytes, kStCodes = kStLo + kHalfTileBytes;
+// one stage: x tile (f32, as loaded), its f16 hi and lo (128 tokens x 128
+// bytes: hi in the first 64 bytes of each row, lo in the second), codes of 4
+// row tiles, their scales
+constexpr int kStHiLo = kTileBytes, kStCodes = 2 * kTileBytes;
 constexpr int kStScales = kStCodes + 4096;
 constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
 constexpr int kTcSmem = kTcStagesMax * kStageBytes + 1024;  // + alignment slack
@@ -102,16 +103,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle (rows of
-// 64 bytes; 16-byte chunk c of row r stored at chunk c ^ ((r / 2) % 4)), 8-row
-// groups 512 bytes apart.
-__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (16-byte
+// chunk c of row r stored at chunk c ^ (r % 8)), 8-row groups 1024 bytes
+// apart. A start address 32 or 64 bytes into the row selects the next 16
+// k-values or the lo half.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFF) >> 4);         // start address
     d |= (uint64_t)(16 >> 4) << 16;                   // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(512 >> 4) << 32;                  // stride byte offset
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
     d |= (uint64_t)1 << 46;                           // descriptor version
-    d |= (uint64_t)4 << 61;                           // 64-byte swizzle
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
     return d;
 }
 
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d = tmem + (uint32_t)(p * kTcBN);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {  // two 16-wide k-steps, 32 bytes apart in the rows
-                    const uint64_t b_hi = sw64_desc(xs + kStHi + kk * 32), b_lo = sw64_desc(xs + kStLo + kk * 32);
+                    const uint64_t b_hi = sw128_desc(xs + kStHiLo + kk * 32), b_lo = sw128_desc(xs + kStHiLo + 64 + kk * 32);
                     mma_f16_ts(d, a + kk * 8, b_hi, kk != 0);
                     mma_f16_ts(d, a + kk * 8, b_lo, 1u);
                 }
@@ -367,8 +369,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_st16(a, u);  // column c: codes 2c, 2c + 1
             }
             // token row gtid: its 32 f32 in 16-byte chunks c at chunk c ^ (r % 8) of the
-            // 128-byte row (the copy's 128-byte swizzle); hi and lo into 64-byte rows,
-            // chunk c (k = 8c .. 8c + 7) at chunk c ^ ((r / 2) % 4)
+            // 128-byte row (the copy's 128-byte swizzle); hi chunk c (k = 8c .. 8c + 7)
+            // and lo chunk c of the hi/lo row at chunks c ^ (r % 8) and (c + 4) ^ (r % 8)
             const int r = gtid;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -385,9 +387,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
                     lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
                 }
-                const int off = r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-                *reinterpret_cast<uint4*>(st + kStHi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(st + kStLo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                uint8_t* hl = st + kStHiLo + r * 128;
+                *reinterpret_cast<uint4*>(hl + ((c ^ (r & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(hl + (((c + 4) ^ (r & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             tmem_wait_st();
             fence_proxy_async_smem();
