@@ -45,8 +45,8 @@ FALLBACK_HBM_GBS = 6800.0
 # (135M model, decode steps after the 203-token prompt, kv_len stated); the
 # K/V part grows by n_kv * head_dim * 8 bytes per cached position.
 NCU_TRAFFIC = {
-    # 3 launches (layers 0-2 of decode step 21, kv_len 224), mean of 1,343,232 / 1,356,288 / 1,356,544 B read, 0 written
-    "layer_front_qkv_attn_o": {"bytes": 1352021, "kv_len": 224, "kv_bytes_per_pos": 1536},
+    # 3 launches (layers 0-2 of decode step 21, kv_len 224), mean of 1,344,768 / 1,358,592 / 1,358,336 B read, 0 written
+    "layer_front_qkv_attn_o": {"bytes": 1353899, "kv_len": 224, "kv_bytes_per_pos": 1536},
 }
 FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x 2 flops x max SM clock
 L2_BYTES = 126 * 2 ** 20
