@@ -312,11 +312,13 @@ llama_q8_status llama_q8_pack(const void* q8, int64_t rows, int64_t k, void* pac
  * cores with f32 accumulation (each 32-row weight tile streamed once and
  * multiplied with every row of x), more rows on the tcgen05 tensor cores: per
  * Q8_0 block the int8 codes (exact in f16) times x, each token row scaled by
- * a power of two (its largest |x| into [2^14, 2^15), found by a short pass
- * before the product) and split into f16 hi and lo parts (two f16 products
- * per step, f32 accumulation in tensor memory), the block sums scaled by d and
+ * a power of two (its largest |x| into [2^14, 2^15)) and split into f16 hi
+ * and lo parts by a short pass before the product (two f16 products per
+ * step, f32 accumulation in tensor memory), the block sums scaled by d and
  * added in f32, the row scale undone exactly; at most 2^-22 relative error per
- * product, plus 2^-39 of the row's largest |x| times the weight. packed and x
+ * product, plus 2^-39 of the row's largest |x| times the weight. The tensor-core
+ * path takes stream-ordered scratch of 4 m + 4 m k bytes (cudaMallocAsync on
+ * `stream`, freed after the product; LQ8_ERR_OOM if it fails). packed and x
  * must be 16-byte aligned (LQ8_ERR_ARG otherwise). */
 llama_q8_status llama_q8_matmul(const void* packed, int64_t rows, int64_t k, const float* x,
                                 int64_t m, float* y, void* stream);

@@ -137,6 +137,37 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core operand of prefill rows: each token row x is scaled by 2^s, s
+// the exponent that brings the row's largest |x| into [2^14, 2^15) (clamped so
+// that 2^s and 2^-s are normal f32 numbers), and x 2^s = hi + lo is split into
+// two f16 numbers (hi = x 2^s rounded to f16, lo = the remainder rounded to
+// f16). Row layout: per 32-wide k-block the 32 hi values, then the 32 lo
+// values (2k halves per row; one 128-byte row per k-block, the MMA's K-major
+// operand row).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int row_shift(float mx) {
+    const int e = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+    return max(-126, min(126, 14 - e));
+}
+__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
+
+// Elements i .. i + 3 (i a multiple of 4) of a row, already multiplied by the
+// row's 2^s, into the row's hi / lo halves (hl = the row's first half).
+__device__ __forceinline__ void store_split4(__half* hl, int i, float a, float b, float c, float d) {
+    const __half2 h0 = __floats2half2_rn(a, b), h1 = __floats2half2_rn(c, d);
+    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+    const __half2 l0 = __floats2half2_rn(a - f0.x, b - f0.y), l1 = __floats2half2_rn(c - f1.x, d - f1.y);
+    __half* blk = hl + (size_t)(i >> 5) * 64 + (i & 31);
+    uint2 hw, lw;
+    hw.x = *reinterpret_cast<const uint32_t*>(&h0);
+    hw.y = *reinterpret_cast<const uint32_t*>(&h1);
+    lw.x = *reinterpret_cast<const uint32_t*>(&l0);
+    lw.y = *reinterpret_cast<const uint32_t*>(&l1);
+    *reinterpret_cast<uint2*>(blk) = hw;
+    *reinterpret_cast<uint2*>(blk + 32) = lw;
+}
+
 // Streaming 128-bit load that does not allocate in L1 (weights are read once).
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
     uint4 r;

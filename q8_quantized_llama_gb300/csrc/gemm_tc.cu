@@ -8,28 +8,28 @@
 // block scale d is one number per (row, k-block), so the tensor cores compute
 // per k-block the block partial P = sum_k q.x' in f16 x f16 -> f32 MMAs
 // (kind::f16), with each token's activations scaled by a power of two 2^s
-// (the row's largest magnitude, found by a short pass before the product,
-// brought into [2^14, 2^15)) and split as x' = x 2^s = hi + lo (hi = x'
-// rounded to f16, lo = x' - hi rounded to f16): two MMAs per 16-wide k-step,
-// f32 accumulation in TMEM. Accumulator warps add d.P to the running sums in
+// (the row's largest magnitude brought into [2^14, 2^15)) and split as
+// x' = x 2^s = hi + lo (hi = x' rounded to f16, lo = x' - hi rounded to f16):
+// two MMAs per 16-wide k-step, f32 accumulation in TMEM. The scaling and the
+// split are done once per token row, before the product, by the kernel that
+// finds the row's maximum (the RMSNorm that produced x, or a short pass), which
+// writes the split rows in the MMA's operand layout: per k-block one 128-byte
+// row of 32 hi then 32 lo halves. Accumulator warps add d.P to the running sums in
 // registers; the epilogue multiplies each token's sums by 2^-s (exact). Each
 // product q.x is off by at most 2^-22 relative, plus 2^-39 of the row's
 // largest |x| times |q| where lo falls below the f16 normal range, then one
 // f32 rounding per block partial.
 //
 // CTA tile: 128 weight rows (MMA M) x 128 tokens (MMA N), k-block 32 (one
-// Q8_0 block; one 128-byte swizzle row of f32). Warp roles (18 warps):
-//  - producer warp: per k-block three tensor copies: the activation tile
-//    (2-D, 128 token rows x 128 bytes, 128-byte swizzle: the MMA's K-major B
-//    layout), and the codes and scales of the CTA's four 32-row tiles (3-D
-//    views [tile][k-block][1 KiB or 64 B] of the packed weights, one box each;
-//    tiles past the matrix read as zeros);
+// Q8_0 block). Warp roles (18 warps):
+//  - producer warp: per k-block three tensor copies: the split activation
+//    tile (2-D, 128 token rows x 128 bytes of hi and lo, 128-byte swizzle:
+//    the MMA's K-major B layout, used in place), and the codes and scales of
+//    the CTA's four 32-row tiles (3-D views [tile][k-block][1 KiB or 64 B] of
+//    the packed weights, one box each; tiles past the matrix read as zeros);
 //  - two groups of 4 converter warps, taking k-blocks in turn: write each
 //    row's 32 codes as f16 pairs into tensor memory (tcgen05.st; A operand,
-//    row r in lane r) and, one thread per token, the token's scaled hi and lo
-//    as one f16 K-major tile (hi then lo in each 128-byte row, 128-byte
-//    swizzle) beside the activation tile (generic stores, then a proxy fence
-//    for the tensor core);
+//    row r in lane r);
 //  - MMA warp: one thread issues the 4 MMAs of a k-block (A from tensor
 //    memory) into one of two block-partial buffers and commits them to the
 //    stage's "done" barrier (frees the stage for the producer) and to the
@@ -68,10 +68,10 @@ static_assert(kTcStagesMax % kTcConvGroups == 0 && kTcStagesSplit % kTcConvGroup
               "each stage is converted by one group");
 constexpr int kTcProducerWarp = kTcConvWarps + kTcAccWarps, kTcMmaWarp = kTcProducerWarp + 1;
 constexpr int kTileBytes = 128 * 128;                 // 128 rows x 128 bytes
-// one stage: x tile (f32, as loaded), its f16 hi and lo (128 tokens x 128
-// bytes: hi in the first 64 bytes of each row, lo in the second), codes of 4
+// one stage: the split activation tile (128 tokens x 128 bytes: hi in the
+// first 64 bytes of each row, lo in the second, 128-byte swizzle), codes of 4
 // row tiles, their scales
-constexpr int kStHiLo = kTileBytes, kStCodes = 2 * kTileBytes;
+constexpr int kStHiLo = 0, kStCodes = kTileBytes;
 constexpr int kStScales = kStCodes + 4096;
 constexpr int kStageBytes = (kStScales + 256 + 1023) / 1024 * 1024;
 constexpr int kTcSmem = kTcStagesMax * kStageBytes + 1024;  // + alignment slack
@@ -99,9 +99,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (16-byte
 // chunk c of row r stored at chunk c ^ (r % 8)), 8-row groups 1024 bytes
@@ -188,14 +185,6 @@ __device__ __forceinline__ void codes_to_f16x2(uint32_t q, uint32_t& lo, uint32_
     hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
-// Exponent s of the power of two that brings a row's largest magnitude mx
-// into [2^14, 2^15), clamped so that 2^s and 2^-s are normal f32 numbers.
-__device__ __forceinline__ int row_shift(float mx) {
-    const int e = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
-    return max(-126, min(126, 14 - e));
-}
-__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
-
 // Epilogue of one output element pair/element (row r of W, token t).
 template <int EPI>
 __device__ __forceinline__ void tc_epilogue_one(const EpiArgs& e, int m, int rows, int t, int r, float val,
@@ -234,7 +223,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int kTcStages = SPLIT ? kTcStagesSplit : kTcStagesMax;
     __shared__ __align__(8) uint64_t full_bar[kTcStages];  // producer's copies landed
-    __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM) and the hi / lo tiles
+    __shared__ __align__(8) uint64_t conv_bar[kTcStages];  // converters wrote A (TMEM)
     __shared__ float row_inv[kTcBN];                        // each token's 2^-s, for the epilogue
     __shared__ __align__(8) uint64_t done_bar[kTcStages];  // MMAs of the stage complete
     __shared__ __align__(8) uint64_t part_full[2];          // a block partial is in tensor memory
@@ -276,8 +265,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcProducerWarp) {
         // lane 0 registers a stage's bytes (full boxes: tiles past the matrix
-        // arrive as zeros), then lane 17 copies the codes of the four tiles,
-        // lane 18 their scales and lane 16 the x tile
+        // and token rows past m arrive as zeros), then lane 17 copies the codes
+        // of the four tiles, lane 18 their scales and lane 16 the split
+        // activation tile
         constexpr uint32_t stage_tx = (uint32_t)kTileBytes + 4u * (1024u + 64u);
         auto issue_weights = [&](int kb) {
             uint8_t* st = smem + (kb % kTcStages) * kStageBytes;
@@ -289,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         auto issue_x = [&](int kb) {
             if (lane == 16)
-                tma_load_2d(smem + (kb % kTcStages) * kStageBytes, &xmap, (kb0 + kb) * 32, t0,
+                tma_load_2d(smem + (kb % kTcStages) * kStageBytes + kStHiLo, &xmap, (kb0 + kb) * 64, t0,
                             &full_bar[kb % kTcStages]);
         };
         // the first stages' weights stream before the dependency on the previous kernel
@@ -314,6 +304,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             for (int kb = 0; kb < nb; ++kb) {
                 const int s = kb % kTcStages, p = kb & 1;
+                // the activation tile has landed (tensor copy) and A is in tensor memory
+                if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 18);
                 if (alive) alive = mbar_wait_bounded(&conv_bar[s], (kb / kTcStages) & 1, err, 15);
                 // the partial buffer of k-block kb - 2 has been read by the accumulator warps
                 if (kb >= 2 && alive) alive = mbar_wait_bounded(&part_empty[p], ((kb >> 1) - 1) & 1, err, 17);
@@ -338,17 +330,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pdl_wait();
         if (tid == 0) pdl_launch_dependents();
         // converter group g takes k-blocks g, g + G, ...; warp w of the group
-        // writes the 32 codes (as exact f16) of row r = 32 * (w % 4) + lane,
-        // and thread gtid converts token row gtid of the activation tile
+        // writes the 32 codes (as exact f16) of row r = 32 * (w % 4) + lane
         const int group = warp / kTcGroupWarps, gtid = tid - group * kTcGroupWarps * 32;
         const int quarter = warp & 3;
         const bool row_ok = quarter < valid_tiles;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        // this token's scale 2^s from its row maximum (rows past m: any scale, x is zero)
+        // token gtid's 2^-s for the epilogue, from its row maximum (rows past m: any)
         const int tok = t0 + gtid;
-        const int sh = row_shift(tok < m ? rowmax[tok] : 0.0f);
-        const float sc = pow2f(sh);
-        if (group == 0) row_inv[gtid] = pow2f(-sh);
+        if (group == 0) row_inv[gtid] = pow2f(-row_shift(tok < m ? rowmax[tok] : 0.0f));
         for (int kb = group; kb < nb; kb += kTcConvGroups) {
             const int s = kb % kTcStages;
             if (alive) alive = mbar_wait_bounded(&full_bar[s], (kb / kTcStages) & 1, err, 11);
@@ -368,31 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tmem_st16(a, u);  // column c: codes 2c, 2c + 1
             }
-            // token row gtid: its 32 f32 in 16-byte chunks c at chunk c ^ (r % 8) of the
-            // 128-byte row (the copy's 128-byte swizzle); hi chunk c (k = 8c .. 8c + 7)
-            // and lo chunk c of the hi/lo row at chunks c ^ (r % 8) and (c + 4) ^ (r % 8)
-            const int r = gtid;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float4 xa = *reinterpret_cast<const float4*>(st + r * 128 + (((2 * c) ^ (r & 7)) << 4));
-                const float4 xb = *reinterpret_cast<const float4*>(st + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4));
-                const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float x0 = xv[2 * i] * sc, x1 = xv[2 * i + 1] * sc;
-                    const __half2 hi = __floats2half2_rn(x0, x1);
-                    const float2 hf = __half22float2(hi);
-                    const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-                    hw[i] = *reinterpret_cast<const uint32_t*>(&hi);
-                    lw[i] = *reinterpret_cast<const uint32_t*>(&lo);
-                }
-                uint8_t* hl = st + kStHiLo + r * 128;
-                *reinterpret_cast<uint4*>(hl + ((c ^ (r & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(hl + (((c + 4) ^ (r & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&conv_bar[s]);
@@ -627,17 +592,19 @@ static cudaError_t get_encode_tiled() {
     return cudaSuccess;
 }
 
-// Tensor map of the activations X[m][ldx] (f32, k columns used): boxes of 32
-// columns x 128 rows with the 128-byte swizzle; rows past m read as zeros.
-static cudaError_t make_x_map(CUtensorMap* map, const float* X, int m, int k, int ldx) {
-    if (((uintptr_t)X & 15) || (ldx & 3) || ldx < k) return cudaErrorInvalidValue;
+// Tensor map of the split activations hl[m][2k] (f16): boxes of one k-block
+// (64 halves = 128 bytes: 32 hi, 32 lo) x 128 rows with the 128-byte swizzle;
+// rows past m read as zeros. The box's x coordinate is 64 kb: 128 bytes, a
+// multiple of 16.
+static cudaError_t make_hl_map(CUtensorMap* map, const __half* hl, int m, int k) {
+    if ((uintptr_t)hl & 15) return cudaErrorInvalidValue;
     cudaError_t e = get_encode_tiled();
     if (e != cudaSuccess) return e;
-    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
-    const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
-    const cuuint32_t box[2] = {32, (cuuint32_t)kTcBN};
+    const cuuint64_t dims[2] = {(cuuint64_t)2 * k, (cuuint64_t)m};
+    const cuuint64_t strides[1] = {(cuuint64_t)2 * k * sizeof(__half)};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTcBN};
     const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides,
+    const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(hl), dims, strides,
                                       box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -668,46 +635,62 @@ static cudaError_t make_w_maps(CUtensorMap* qmap, CUtensorMap* dmap, const Packe
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Largest |x| of each token row (the product's per-row scale): one warp per
-// row, float4 loads; after the grid dependency wait, since X comes from the
-// preceding kernel.
-constexpr int kRowMaxWarps = 8;
-__global__ void __launch_bounds__(kRowMaxWarps * 32) row_absmax_kernel(const float* __restrict__ X, int m, int k,
-                                                                        int ldx, float* __restrict__ out) {
+// The product's operand from X[m][ldx] (k columns): each row's largest |x|
+// into rowmax, then the row scaled by its power of two and split into hi / lo
+// (common.cuh) into hl. One CTA per row (enough CTAs to stream the widest
+// inputs, 14336 columns, at HBM speed), float4 loads; the second pass reads
+// the row again from L1. After the grid dependency wait, since X comes from
+// the preceding kernel.
+constexpr int kRowSplitThreads = 256;
+__global__ void __launch_bounds__(kRowSplitThreads) row_split_kernel(const float* __restrict__ X, int k, int ldx,
+                                                                     float* __restrict__ rowmax,
+                                                                     __half* __restrict__ hl) {
+    __shared__ float red[kRowSplitThreads / 32];
     pdl_wait();
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kRowMaxWarps + warp;
-    if (t >= m) return;
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* row = X + (size_t)t * ldx;
     float mx = 0.0f;
-    for (int i = lane * 4; i < k; i += 128) {
+    for (int i = threadIdx.x * 4; i < k; i += kRowSplitThreads * 4) {
         const float4 v = *reinterpret_cast<const float4*>(row + i);
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) out[t] = mx;
+    for (int w = 0; w < kRowSplitThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    if (threadIdx.x == 0) rowmax[t] = mx;
+    const float sc = pow2f(row_shift(mx));
+    __half* hr = hl + (size_t)t * 2 * k;
+    for (int i = threadIdx.x * 4; i < k; i += kRowSplitThreads * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(row + i);
+        store_split4(hr, i, v.x * sc, v.y * sc, v.z * sc, v.w * sc);
+    }
 }
 
 template <int EPI>
 static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx, const EpiArgs& e, bool pdl,
-                               int* err, cudaStream_t s, float* rowmax, bool rowmax_ready) {
-    if (!rowmax_ready) {
-        cudaError_t rerr = launch_ex(row_absmax_kernel, dim3((m + kRowMaxWarps - 1) / kRowMaxWarps),
-                                     dim3(kRowMaxWarps * 32), 0, s, pdl, X, m, W.k, ldx, rowmax);
+                               int* err, cudaStream_t s, const SplitRows& split, bool split_ready) {
+    if (!split.rowmax || !split.hl) return cudaErrorInvalidValue;
+    if (!split_ready) {
+        if (((uintptr_t)X & 15) || (ldx & 3) || ldx < W.k) return cudaErrorInvalidValue;
+        cudaError_t rerr = launch_ex(row_split_kernel, dim3(m), dim3(kRowSplitThreads), 0, s, pdl, X, W.k, ldx,
+                                     split.rowmax, split.hl);
         if (rerr != cudaSuccess) return rerr;
-        pdl = true;  // the product follows its own row-maximum pass
+        pdl = true;  // the product follows its own operand pass
     }
     CUtensorMap xmap, qmap, dmap;
-    cudaError_t merr = make_x_map(&xmap, X, m, W.k, ldx);
+    cudaError_t merr = make_hl_map(&xmap, split.hl, m, W.k);
     if (merr == cudaSuccess) merr = make_w_maps(&qmap, &dmap, W);
     if (merr != cudaSuccess) return merr;
+    const float* rowmax = split.rowmax;
     const int gx = (W.rows_pad + kTcBM - 1) / kTcBM, gy = (m + kTcBN - 1) / kTcBN;
     const int S = gemm_tc_splits(gx * gy, W.k / 32);
     if (S == 1)
         return launch_ex(q8_gemm_tc_kernel<EPI, false>, dim3(gy, gx), dim3(kTcThreads), (size_t)kTcSmem, s, pdl, W,
-                         xmap, qmap, dmap, m, (const float*)rowmax, e, err);
+                         xmap, qmap, dmap, m, rowmax, e, err);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gy, gx, S);
     cfg.blockDim = dim3(kTcThreads);
@@ -726,7 +709,7 @@ static cudaError_t gemm_tc_one(const PackedQ8& W, const float* X, int m, int ldx
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, qmap, dmap, m, (const float*)rowmax, e, err);
+    return cudaLaunchKernelEx(&cfg, q8_gemm_tc_kernel<EPI, true>, W, xmap, qmap, dmap, m, rowmax, e, err);
 }
 
 template <int EPI>
@@ -748,13 +731,12 @@ cudaError_t init_gemm_tc_attributes() {
 }
 
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
-                           int* err, cudaStream_t s, float* rowmax, bool rowmax_ready) {
-    if (!rowmax) return cudaErrorInvalidValue;
+                           int* err, cudaStream_t s, const SplitRows& split, bool split_ready) {
     switch (epi) {
-        case EPI_STORE: return gemm_tc_one<EPI_STORE>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
-        case EPI_RESIDUAL: return gemm_tc_one<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
-        case EPI_QKV: return gemm_tc_one<EPI_QKV>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
-        case EPI_SILU: return gemm_tc_one<EPI_SILU>(W, X, m, ldx, e, pdl, err, s, rowmax, rowmax_ready);
+        case EPI_STORE: return gemm_tc_one<EPI_STORE>(W, X, m, ldx, e, pdl, err, s, split, split_ready);
+        case EPI_RESIDUAL: return gemm_tc_one<EPI_RESIDUAL>(W, X, m, ldx, e, pdl, err, s, split, split_ready);
+        case EPI_QKV: return gemm_tc_one<EPI_QKV>(W, X, m, ldx, e, pdl, err, s, split, split_ready);
+        case EPI_SILU: return gemm_tc_one<EPI_SILU>(W, X, m, ldx, e, pdl, err, s, split, split_ready);
     }
     return cudaErrorInvalidValue;
 }

@@ -88,8 +88,18 @@ cudaError_t launch_embed(const PackedQ8& E, const int32_t* ids, int T, const Dev
 // wait: placed after the last kernel of the instrumented decode graph, its wait
 // returns when that kernel has completed.
 cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s);
+// The operand of a tensor-core product of m token rows of k activations (the
+// row scaling and hi / lo split of common.cuh): rowmax[m] holds each row's
+// largest |x| (the product's epilogue undoes the row's scale from it), hl[m][2k]
+// the split rows.
+struct SplitRows {
+    float* rowmax = nullptr;
+    __half* hl = nullptr;
+};
+// y = RMSNorm rows of x (written when y is non-null); with split, also the
+// tensor-core operand of y (split->rowmax and split->hl)
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
-                           cudaStream_t s, float* rowmax = nullptr);
+                           cudaStream_t s, const SplitRows* split = nullptr);
 cudaError_t launch_set_state(DevState* st, int pos, int token, int n_out, cudaStream_t s);
 cudaError_t launch_wait_timeout(int* err, int code, cudaStream_t s);  // bounded-wait self-test
 
@@ -128,12 +138,12 @@ cudaError_t launch_gemv_rows(const PackedQ8& W, const float* X, int m, int ldx, 
                              int* err, cudaStream_t s);
 bool gemv_rows_fits(int64_t m, int64_t k);  // a chunk's x slices fit beside the ring (at most 8 splits)
 // gemm_tc.cu: tcgen05 kernel for many rows (f16 products of the codes and of
-// each token's activations scaled by a power of two and split into hi and lo);
-// rowmax: device memory of m floats for the rows' largest |x|: filled by a
-// pass launched just before the product, or (rowmax_ready) already written by
-// the kernel that produced X
+// each token's activations scaled by a power of two and split into hi and lo).
+// split: device memory for the operand of X (m floats, m x 2k halves): filled
+// from X by a pass launched just before the product, or (split_ready) already
+// written by the kernel that produced X, in which case X is not read.
 cudaError_t launch_gemm_tc(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e, bool pdl,
-                           int* err, cudaStream_t s, float* rowmax, bool rowmax_ready = false);
+                           int* err, cudaStream_t s, const SplitRows& split, bool split_ready = false);
 cudaError_t init_gemm_tc_attributes();
 // Every kernel's attributes on the current device, once per device (runtime.cu).
 cudaError_t ensure_kernel_attributes();
@@ -151,11 +161,13 @@ inline bool matmul_on_tensor_cores(int m, int rows, int k, int path) {
     if (path == MATMUL_CUDA_CORES) return false;
     return m > kTensorCoreMinRows;
 }
+// split / split_ready: the tensor-core operand (launch_gemm_tc); the CUDA-core
+// kernel reads X and ignores them
 inline cudaError_t launch_matmul_rows(const PackedQ8& W, const float* X, int m, int ldx, int epi, const EpiArgs& e,
-                                      bool pdl, int* err, cudaStream_t s, float* rowmax, int path = MATMUL_AUTO,
-                                      bool rowmax_ready = false) {
+                                      bool pdl, int* err, cudaStream_t s, const SplitRows& split,
+                                      int path = MATMUL_AUTO, bool split_ready = false) {
     return matmul_on_tensor_cores(m, W.rows, W.k, path)
-               ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s, rowmax, rowmax_ready)
+               ? launch_gemm_tc(W, X, m, ldx, epi, e, pdl, err, s, split, split_ready)
                : launch_gemv_rows(W, X, m, ldx, epi, e, pdl, err, s);
 }
 

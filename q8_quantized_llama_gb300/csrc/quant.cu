@@ -152,15 +152,16 @@ cudaError_t launch_stamp(unsigned long long* stamp, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 // RMSNorm rows: y = x * g / sqrt(mean(x^2) + eps), f32.
 // ---------------------------------------------------------------------------
-// rowmax (optional): each output row's largest |y|, the per-row scale the
-// tensor-core product that reads y needs
+// y is written when non-null. With hl, the kernel also writes the operand of
+// the tensor-core product that reads the normalised rows: rowmax[row] = the
+// row's largest |y| and hl[row] = y scaled by the row's power of two and split
+// into f16 hi / lo (common.cuh), from the same f32 values y holds.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g, float eps,
-                               int k, float* __restrict__ y, float* __restrict__ rowmax) {
+                               int k, float* __restrict__ y, float* __restrict__ rowmax, __half* __restrict__ hl) {
     __shared__ float red[32];
     pdl_wait();
     pdl_launch_dependents();
     const float* xr = x + (int64_t)blockIdx.x * k;
-    float* yr = y + (int64_t)blockIdx.x * k;
     float ss = 0.0f;
     for (int i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
         float4 v = *reinterpret_cast<const float4*>(xr + i);
@@ -177,30 +178,43 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
     }
     __syncthreads();
     const float r = 1.0f / sqrtf(red[0] / (float)k + eps);
+    auto norm4 = [&](int i) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + i);
+        const float4 gg = *reinterpret_cast<const float4*>(g + i);
+        return make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
+    };
     float mx = 0.0f;
     for (int i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
-        float4 v = *reinterpret_cast<const float4*>(xr + i);
-        float4 gg = *reinterpret_cast<const float4*>(g + i);
-        const float4 o = make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w);
-        *reinterpret_cast<float4*>(yr + i) = o;
+        const float4 o = norm4(i);
+        if (y) *reinterpret_cast<float4*>(y + (int64_t)blockIdx.x * k + i) = o;
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
     }
-    if (rowmax) {
-        mx = warp_max(mx);
-        __syncthreads();  // every thread has read the sum of squares from red[0]
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
-            v = warp_max(v);
-            if (threadIdx.x == 0) rowmax[blockIdx.x] = v;
+    if (!hl) return;
+    mx = warp_max(mx);
+    __syncthreads();  // every thread has read the sum of squares from red[0]
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+        v = warp_max(v);
+        if (threadIdx.x == 0) {
+            rowmax[blockIdx.x] = v;
+            red[0] = v;
         }
+    }
+    __syncthreads();
+    const float sc = pow2f(row_shift(red[0]));
+    __half* hr = hl + (int64_t)blockIdx.x * 2 * k;
+    for (int i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
+        const float4 o = norm4(i);  // the same products as above: the same f32 values
+        store_split4(hr, i, o.x * sc, o.y * sc, o.z * sc, o.w * sc);
     }
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* g, float eps, int m, int k, float* y, bool pdl,
-                           cudaStream_t s, float* rowmax) {
-    return launch_ex(rmsnorm_kernel, dim3(m), dim3(256), 0, s, pdl, x, g, eps, k, y, rowmax);
+                           cudaStream_t s, const SplitRows* split) {
+    return launch_ex(rmsnorm_kernel, dim3(m), dim3(256), 0, s, pdl, x, g, eps, k, y,
+                     split ? split->rowmax : nullptr, split ? split->hl : nullptr);
 }
 
 __global__ void set_state_kernel(DevState* st, int pos, int token, int n_out) {

@@ -9,6 +9,7 @@
 // row-interleaved projection, RoPE and the KV append run in the projection
 // epilogue, the cache is preallocated and written in place, and the decode
 // step is one CUDA graph whose position and input token live in device memory.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -110,6 +111,7 @@ struct llama_q8_ctx {
     unsigned int* d_done = nullptr;
     void* d_attn_ws = nullptr;
     float* d_rowmax = nullptr;  // prefill products on the tensor cores: each token row's largest |x|
+    __half* d_hl = nullptr;     // and its rows scaled and split into f16 hi / lo (max_seq x 2 x widest k)
 
     int32_t* h_ids = nullptr;
     int32_t* h_out = nullptr;
@@ -157,7 +159,7 @@ void free_ctx_memory(llama_q8_ctx* c) {
     void* dev[] = {c->d_weights, c->d_norms, c->d_rope_cos, c->d_rope_sin, c->d_kcache, c->d_vcache,
                    c->d_x, c->d_y, c->d_q, c->d_o, c->d_a, c->d_part, c->d_xsum, c->d_xr, c->d_mlp, c->d_logits, c->d_ids,
                    c->d_out_ids,
-                   c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_rowmax};
+                   c->d_state, c->d_best, c->d_done, c->d_attn_ws, c->d_rowmax, c->d_hl};
     for (void* p : dev)
         if (p) cudaFree(p);
     void* host[] = {c->h_ids, c->h_out, c->h_logits, c->h_state};
@@ -373,12 +375,19 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
     cudaStream_t s = c->stream;
     const int h = cfg.n_embd;
     cudaError_t err = launch_embed(c->embd, d_ids, T, nullptr, c->d_state, c->d_x, cfg.n_vocab, true, s);
+    // the tensor-core operand of every product (rows scaled and split), one
+    // buffer reused in stream order; the RMSNorms write it for the Q/K/V and
+    // gate/up products in place of y when those run on the tensor cores
+    const SplitRows sp{c->d_rowmax, c->d_hl};
+    const bool tc_norm = matmul_on_tensor_cores(T, 0, h, MATMUL_AUTO);
+    float* y = tc_norm ? nullptr : c->d_y;
+    const SplitRows* norm_split = tc_norm ? &sp : nullptr;
     for (int l = 0; l < cfg.n_layer && err == cudaSuccess; ++l) {
         const LayerDev& L = c->layers[l];
-        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, c->d_y, true, s, c->d_rowmax);
+        err = launch_rmsnorm(c->d_x, L.attn_norm, cfg.rms_eps, T, h, y, true, s, norm_split);
         EpiArgs e = qkv_epi(c, l);
         e.pos0 = index_pos;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.qkv, c->d_y, T, h, EPI_QKV, e, true, &c->d_state->err, s, c->d_rowmax,
+        if (err == cudaSuccess) err = launch_matmul_rows(L.qkv, c->d_y, T, h, EPI_QKV, e, true, &c->d_state->err, s, sp,
                                                          MATMUL_AUTO, true);
         if (err == cudaSuccess)
             err = launch_attn_prefill(c->d_q, c->kcache(l), c->vcache(l), T, index_pos, cfg.n_head, cfg.n_head_kv,
@@ -386,14 +395,14 @@ cudaError_t enqueue_prefill(llama_q8_ctx* c, const int32_t* d_ids, int T, int in
         EpiArgs r;
         r.y = c->d_x;
         r.ldy = h;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, &c->d_state->err, s, c->d_rowmax);
-        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, c->d_y, true, s, c->d_rowmax);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.o, c->d_o, T, c->q_rows, EPI_RESIDUAL, r, true, &c->d_state->err, s, sp);
+        if (err == cudaSuccess) err = launch_rmsnorm(c->d_x, L.ffn_norm, cfg.rms_eps, T, h, y, true, s, norm_split);
         EpiArgs g;
         g.a_out = c->d_a;
         g.lda = cfg.n_ff;
-        if (err == cudaSuccess) err = launch_matmul_rows(L.gu, c->d_y, T, h, EPI_SILU, g, true, &c->d_state->err, s, c->d_rowmax,
+        if (err == cudaSuccess) err = launch_matmul_rows(L.gu, c->d_y, T, h, EPI_SILU, g, true, &c->d_state->err, s, sp,
                                                          MATMUL_AUTO, true);
-        if (err == cudaSuccess) err = launch_matmul_rows(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, &c->d_state->err, s, c->d_rowmax);
+        if (err == cudaSuccess) err = launch_matmul_rows(L.down, c->d_a, T, cfg.n_ff, EPI_RESIDUAL, r, true, &c->d_state->err, s, sp);
     }
     if (err == cudaSuccess)
         err = launch_gemv(c->head, c->d_x + (size_t)(T - 1) * h, c->out_norm, cfg.rms_eps, EPI_ARGMAX,
@@ -712,6 +721,7 @@ llama_q8_status llama_q8_load(const llama_q8_config* cfg, const llama_q8_weights
     LOAD_CK(cudaMalloc(&c->d_o, sizeof(float) * T * c->q_rows));
     LOAD_CK(cudaMalloc(&c->d_a, sizeof(float) * T * F));
     LOAD_CK(cudaMalloc(&c->d_rowmax, sizeof(float) * T));
+    LOAD_CK(cudaMalloc(&c->d_hl, sizeof(__half) * T * 2 * std::max({(size_t)h, (size_t)c->q_rows, (size_t)F})));
     LOAD_CK(cudaMalloc(&c->d_part, sizeof(float) * C.n_head_kv * h));
     LOAD_CK(cudaMalloc(&c->d_xsum, sizeof(float) * h));
     LOAD_CK(cudaMalloc(&c->d_xr, sizeof(float) * h));
@@ -1075,14 +1085,21 @@ llama_q8_status llama_q8_matmul_ex(const void* packed, int64_t rows, int64_t k, 
     } else {
         const bool tc = matmul_on_tensor_cores((int)m, (int)rows, (int)k, path);
         if (!tc && !gemv_rows_fits(m, k)) return LQ8_ERR_UNSUPPORTED;
-        float* rowmax = nullptr;  // the rows' largest |x| (tensor cores), stream-ordered scratch
-        if (tc && cudaMallocAsync(reinterpret_cast<void**>(&rowmax), sizeof(float) * (size_t)m,
-                                  (cudaStream_t)stream) != cudaSuccess)
-            return LQ8_ERR_OOM;
-        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream, rowmax,
-                                 path);
-        if (rowmax) {
-            const cudaError_t ferr = cudaFreeAsync(rowmax, (cudaStream_t)stream);
+        // tensor cores: the rows' largest |x| and the scaled, split rows, in
+        // stream-ordered scratch (one allocation: m floats, then m x 2k halves)
+        SplitRows sp;
+        void* scratch = nullptr;
+        const size_t rm_bytes = ((size_t)m * sizeof(float) + 255) / 256 * 256;
+        if (tc) {
+            if (cudaMallocAsync(&scratch, rm_bytes + (size_t)m * 2 * (size_t)k * sizeof(__half),
+                                (cudaStream_t)stream) != cudaSuccess)
+                return LQ8_ERR_OOM;
+            sp.rowmax = reinterpret_cast<float*>(scratch);
+            sp.hl = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(scratch) + rm_bytes);
+        }
+        err = launch_matmul_rows(W, x, (int)m, (int)k, EPI_STORE, e, early, nullptr, (cudaStream_t)stream, sp, path);
+        if (scratch) {
+            const cudaError_t ferr = cudaFreeAsync(scratch, (cudaStream_t)stream);
             if (err == cudaSuccess) err = ferr;
         }
     }
