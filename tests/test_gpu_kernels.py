@@ -230,6 +230,36 @@ def test_matmul_tensor_core_split_precision_one_hot(rows, k, m):
     assert np.mean(err <= 2.0 ** -21 * np.abs(ref)) > 0.999  # the bulk to 2^-21 relative
 
 
+def test_matmul_tensor_core_row_scales():
+    """Token rows whose magnitudes span 1e-30 .. 1e30, and an all-zero row, in
+    one product: each row's power of two comes from its own largest |x|, so
+    every row keeps the same relative accuracy (the bound of the other
+    tensor-core cases, relative to that row's sum |w x|) and the zero row
+    gives exact zeros. A scale taken from another row, or one not undone,
+    would put rows off by many orders of magnitude or overflow the f16 split."""
+    B = binding()
+    rows, k, m = 192, 1024, 40
+    w = synth.weight_matrix_f32(rows, k, 12, stream=rows + k)
+    x = synth.normal_f32((m, k), 12, 1)
+    row_scale = np.array([1e-30, 1e-12, 1e-3, 1.0, 1e3, 1e12, 1e30, 0.0], np.float32)
+    x = (x * row_scale[np.arange(m) % row_scale.size][:, None]).astype(np.float32)
+    wq = gpu_quantize(w)
+    packed = _packed(wq, rows, k)
+    dy = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    B.llama_q8_matmul_ex(packed, rows, k, to_dev(x), m, dy, B.LQ8_MATMUL_TENSOR_CORES)
+    torch.cuda.synchronize()
+    got = dy.cpu().numpy().astype(np.float64)
+    wd = O.dequantize_q8_0(O.quantize_q8_0(w), rows, k).astype(np.float64)
+    ref = x.astype(np.float64) @ wd.T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(wd).T
+    tol = ((k + 16) * U + 2.0 ** -19) * mag
+    assert np.all(np.isfinite(got))
+    zero_rows = np.arange(m) % row_scale.size == row_scale.size - 1
+    assert np.all(got[zero_rows] == 0.0)
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} elements off"
+
+
 # ------------------------------------------------------------------ attention
 
 def _attention_case(T, index_pos, nh, nkv, hd, stride, seed, entry="attention"):
