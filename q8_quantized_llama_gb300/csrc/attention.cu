@@ -17,8 +17,11 @@
 //
 // Prefill (T > 1): attn_prefill_kernel<HD, RT, KS>, a causal flash-style
 // kernel, one CTA per (query head, 16*RT query rows) with 256 threads as a
-// 16 x 16 grid (or a cluster of KS CTAs splitting the keys, for short
-// prompts), register-blocked scores, K/V tiles of 64 positions (head_dim 64)
+// 16 x 16 grid (or a cluster of KS CTAs splitting the keys: for short
+// prompts, and for 64-row tiles when the grid is at most two waves, where the
+// causal mask would leave the last row tiles' CTAs alone setting the time;
+// the row tiles with the most visible keys are scheduled first),
+// register-blocked scores, K/V tiles of 64 positions (head_dim 64)
 // or 32 (head_dim 128) double-buffered in shared memory, online softmax; query
 // t sees positions <= index_pos + t ("量化 llama 的一次前向", forward：mask
 // 什么时候建 — the mask is a predicate here, never built).
@@ -1043,9 +1046,11 @@ struct PfCfg {
     static constexpr int LDP = KT + 4;             // floats per P row
     static constexpr int kQ = 0, kK = R * LD, kV = kK + 2 * KT * LD, kP = kV + 2 * KT * LD;
     static constexpr size_t kSmem = (size_t)(kP + R * LDP) * sizeof(float);
-    // key split: this CTA's unnormalised output rows, row maxima and row sums
-    static constexpr int kMO = kP + R * LDP, kMM = kMO + R * HD, kML = kMM + R;
-    static constexpr size_t kSmemSplit = (size_t)(kML + R) * sizeof(float);
+    // key split: this CTA's unnormalised output rows, row maxima and row sums,
+    // in the K/V stages (free once the last key tile has been used)
+    static constexpr int kMO = kK, kMM = kMO + R * HD, kML = kMM + R;
+    static_assert(kML + R <= kP, "the merge buffers fit in the K/V stages");
+    static constexpr size_t kSmemSplit = kSmem;
 };
 constexpr int kPfThreads = 256;
 
@@ -1062,7 +1067,8 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
     float* Qs = pf_smem + C::kQ;
     float* Ps = pf_smem + C::kP;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int h = blockIdx.x / KS, z = blockIdx.x % KS, t0 = blockIdx.y * R;  // z: rank in the key split
+    // z: rank in the key split; the last row tiles (the most visible keys) first
+    const int h = blockIdx.x / KS, z = blockIdx.x % KS, t0 = (gridDim.y - 1 - blockIdx.y) * R;
     const int kh = h / (n_head / n_kv);
     const float* kbase = kc + (int64_t)kh * cache_stride * HD;
     const float* vbase = vc + (int64_t)kh * cache_stride * HD;
@@ -1210,6 +1216,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) attn_prefill_kernel(const float
         float* MO = pf_smem + C::kMO;
         float* MM = pf_smem + C::kMM;
         float* ML = pf_smem + C::kML;
+        __syncthreads();  // every thread is done with the stages the buffers reuse
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
             const int row = ty * RT + i;
@@ -1283,6 +1290,7 @@ static cudaError_t pf_attr() {
 template <int HD>
 static cudaError_t pf_attr_hd() {
     cudaError_t err = pf_attr<HD, 4, 1>();
+    if (err == cudaSuccess) err = pf_attr<HD, 4, 2>();
     if (err == cudaSuccess) err = pf_attr<HD, 1, 1>();
     if (err == cudaSuccess) err = pf_attr<HD, 1, 2>();
     if (err == cudaSuccess) err = pf_attr<HD, 1, 4>();
@@ -1330,12 +1338,20 @@ template <int HD>
 static cudaError_t pf_dispatch(const float* q, const float* k_cache, const float* v_cache, int T, int index_pos,
                                int n_head, int n_head_kv, int cache_stride, float* out, bool pdl, cudaStream_t s,
                                int sms) {
-    // 64 rows per CTA when that still gives every SM a CTA; else 16 rows, and
-    // when even those leave SMs idle, each row tile's keys split over a
+    // 64 rows per CTA when that still gives every SM a CTA; their keys split
+    // over a cluster of 2 when the doubled grid stays within two waves of two
+    // resident CTAs per SM (under a causal mask the last row tiles see the
+    // most keys: in one wave they alone would set the time). Else 16 rows,
+    // and when even those leave SMs idle, each row tile's keys split over a
     // cluster of 2, 4 or 8 CTAs (two resident per SM, at least one key tile
     // each)
-    if ((int64_t)n_head * ((T + 63) / 64) >= sms)
+    const int64_t ctas64 = (int64_t)n_head * ((T + 63) / 64);
+    if (ctas64 >= sms) {
+        const int tiles64 = (index_pos + T + PfCfg<HD, 4>::KT - 1) / PfCfg<HD, 4>::KT;
+        if (ctas64 * 2 <= 4 * (int64_t)sms && tiles64 >= 4)
+            return pf_launch<HD, 4, 2>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
         return pf_launch<HD, 4, 1>(q, k_cache, v_cache, T, index_pos, n_head, n_head_kv, cache_stride, out, pdl, s);
+    }
     const int64_t ctas = (int64_t)n_head * ((T + 15) / 16);
     const int tiles = (index_pos + T + PfCfg<HD, 1>::KT - 1) / PfCfg<HD, 1>::KT;
     int ks = 1;
