@@ -640,7 +640,8 @@ def linear_sweep(torch, B, synth, device, peak):
 
 def attention_prefill_bench(torch, B, synth, device):
     """Causal prefill attention (llama_q8_attention, T > 1): T = 203 at
-    position 0 and T = 64 at position 512, at the 135M shape (9/3 heads of 64)
+    position 0, T = 64 at position 512 and T = 512 at position 0 (the 7B
+    prefill's length), at the 135M shape (9/3 heads of 64)
     and the 7B shape (32/8 heads of 128), cache stride 4096. Algorithmic
     FLOP = 4 * n_head * head_dim * sum over queries of the visible positions
     (q k^T and p v); the kernel runs on the FP32 CUDA cores, so the fraction is
@@ -651,7 +652,7 @@ def attention_prefill_bench(torch, B, synth, device):
         stride = 4096
         kc = torch.from_numpy(synth.normal_f32((nkv, stride, hd), 3, 1)).to(device)
         vc = torch.from_numpy(synth.normal_f32((nkv, stride, hd), 3, 2)).to(device)
-        for T, pos in ((203, 0), (64, 512)):
+        for T, pos in ((203, 0), (64, 512), (512, 0)):
             q = torch.from_numpy(synth.normal_f32((T, nh, hd), 3, 3)).to(device)
             o = torch.empty((T, nh, hd), dtype=torch.float32, device=device)
             for _ in range(3):
