@@ -52,7 +52,7 @@ namespace lq8 {
 
 constexpr int kTcBM = 128;
 constexpr int kTcBN = 128;
-// Stages in flight (6 measured no faster: the MMA issue is the pacing step).
+// Stages in flight (6 or 8 measured no faster).
 // The count stays a multiple of the converter groups: each stage is always
 // converted by the same group, whose parity waits then never see a barrier
 // two phases behind.
