@@ -104,17 +104,21 @@ __device__ __forceinline__ void gemv_epilogue(const EpiArgs& e, int rows, int ti
     }
 }
 
-// Greedy token: every publishing CTA adds its best key; the last one to arrive
-// (ticket) reads the maximum, resets the accumulators for the next launch and
-// writes the token and position to the step state. One thread.
+// Greedy token: every publishing CTA raises the shared maximum key, then takes
+// a ticket with release semantics (ordering its maximum before the ticket, no
+// separate fence); the CTA holding the last ticket (acquire: it sees every
+// maximum) reads the key, resets both accumulators for the next launch with
+// plain stores (the kernel boundary orders them before it) and writes the
+// token and position to the step state. One thread.
 __device__ __forceinline__ void argmax_publish(const EpiArgs& e, unsigned long long best, unsigned int n_pub) {
     atomicMax(e.best_key, best);
-    __threadfence();
-    const unsigned int ticket = atomicAdd(e.done_count, 1u);
+    unsigned int ticket;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(e.done_count) : "memory");
     if (ticket == n_pub - 1) {
-        __threadfence();
-        const unsigned long long key = atomicExch(e.best_key, 0ull);
-        atomicExch(e.done_count, 0u);
+        unsigned long long key;
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(key) : "l"(e.best_key) : "memory");
+        *e.best_key = 0ull;
+        *e.done_count = 0u;
         const int tok = argmax_key_index(key);
         DevState* st = e.st;
         st->token = tok;
