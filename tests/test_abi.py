@@ -95,3 +95,20 @@ def test_rope_style_by_architecture_name(B):
     for arch in ("llama", "Qwen2", "qwen3moe", "", "mistral"):
         assert B.rope_style_for_arch(arch) == 0, arch
     assert B.rope_style_for_arch(None) == -1
+
+
+def test_matmul_argument_checks_without_a_gpu(B):
+    """llama_q8_matmul_ex refuses bad arguments on the host, before any CUDA
+    call: the pointers below are never dereferenced (16-byte aligned stand-in
+    addresses, or misaligned ones where the check is the alignment)."""
+    L = B.lib()
+    p, x, y = C.c_void_p(1 << 20), C.c_void_p(1 << 21), C.c_void_p(1 << 22)
+    tc, cc = B.LQ8_MATMUL_TENSOR_CORES, B.LQ8_MATMUL_CUDA_CORES
+    assert L.llama_q8_matmul_ex(p, 64, 33, x, 20, y, 0, None) == B.LQ8_ERR_ARG       # k % 32
+    assert L.llama_q8_matmul_ex(p, 0, 64, x, 20, y, 0, None) == B.LQ8_ERR_ARG        # rows
+    assert L.llama_q8_matmul_ex(p, 64, 64, x, 0, y, 0, None) == B.LQ8_ERR_ARG        # m
+    assert L.llama_q8_matmul_ex(p, 64, 64, x, 20, y, 8, None) == B.LQ8_ERR_ARG       # unknown flag bit
+    assert L.llama_q8_matmul_ex(p, 64, 64, x, 20, y, tc | cc, None) == B.LQ8_ERR_ARG  # both kernels forced
+    assert L.llama_q8_matmul_ex(C.c_void_p((1 << 20) + 4), 64, 64, x, 20, y, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_matmul_ex(p, 64, 64, C.c_void_p((1 << 21) + 8), 20, y, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_matmul_ex(p, (1 << 30) + 1, 64, x, 20, y, 0, None) == B.LQ8_ERR_UNSUPPORTED
