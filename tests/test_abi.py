@@ -112,3 +112,20 @@ def test_matmul_argument_checks_without_a_gpu(B):
     assert L.llama_q8_matmul_ex(C.c_void_p((1 << 20) + 4), 64, 64, x, 20, y, 0, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_matmul_ex(p, 64, 64, C.c_void_p((1 << 21) + 8), 20, y, 0, None) == B.LQ8_ERR_ARG
     assert L.llama_q8_matmul_ex(p, (1 << 30) + 1, 64, x, 20, y, 0, None) == B.LQ8_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("entry", ["llama_q8_attention_decode", "llama_q8_attention_decode_noalloc"])
+def test_decode_attention_argument_checks_without_a_gpu(B, entry):
+    """The decode attention entries refuse bad shapes and misaligned buffers on
+    the host, before any CUDA call (stand-in addresses, never dereferenced)."""
+    f = getattr(B.lib(), entry)
+    q, k, v, o = (C.c_void_p(a << 20) for a in (1, 2, 3, 4))
+    assert f(q, k, v, 0, 9, 3, 64, 4096, o, None) == B.LQ8_ERR_ARG           # kv_len
+    assert f(q, k, v, 100, 9, 4, 64, 4096, o, None) == B.LQ8_ERR_ARG         # heads not grouped evenly
+    assert f(q, k, v, 4097, 9, 3, 64, 4096, o, None) == B.LQ8_ERR_CTX        # past the cache
+    assert f(q, k, v, 100, 9, 3, 96, 4096, o, None) == B.LQ8_ERR_UNSUPPORTED  # head_dim
+    assert f(q, k, v, 100, 18, 1, 64, 4096, o, None) == B.LQ8_ERR_UNSUPPORTED  # group of 18 > 8
+    for bad in range(4):
+        ptrs = [q, k, v, o]
+        ptrs[bad] = C.c_void_p(((bad + 1) << 20) + 4)                        # misaligned buffer
+        assert f(ptrs[0], ptrs[1], ptrs[2], 100, 9, 3, 64, 4096, ptrs[3], None) == B.LQ8_ERR_ARG, bad
