@@ -129,3 +129,34 @@ def test_decode_attention_argument_checks_without_a_gpu(B, entry):
         ptrs = [q, k, v, o]
         ptrs[bad] = C.c_void_p(((bad + 1) << 20) + 4)                        # misaligned buffer
         assert f(ptrs[0], ptrs[1], ptrs[2], 100, 9, 3, 64, 4096, ptrs[3], None) == B.LQ8_ERR_ARG, bad
+
+
+def test_prefill_attention_argument_checks_without_a_gpu(B):
+    """llama_q8_attention (T > 1) refuses bad shapes, a prompt past the cache
+    and misaligned buffers on the host, before any CUDA call."""
+    f = B.lib().llama_q8_attention
+    q, k, v, o = (C.c_void_p(a << 20) for a in (1, 2, 3, 4))
+    assert f(q, k, v, 0, 0, 9, 3, 64, 4096, o, None, 0, None) == B.LQ8_ERR_ARG            # T
+    assert f(q, k, v, 8, -1, 9, 3, 64, 4096, o, None, 0, None) == B.LQ8_ERR_ARG           # index_pos
+    assert f(q, k, v, 8, 0, 9, 2, 64, 4096, o, None, 0, None) == B.LQ8_ERR_ARG            # 9 heads over 2
+    assert f(q, k, v, 8, 4090, 9, 3, 64, 4096, o, None, 0, None) == B.LQ8_ERR_CTX         # index_pos + T > 4096
+    assert f(q, k, v, 8, 0, 9, 3, 32, 4096, o, None, 0, None) == B.LQ8_ERR_UNSUPPORTED    # head_dim
+    assert f(q, k, v, 8, 0, 32, 2, 64, 4096, o, None, 0, None) == B.LQ8_ERR_UNSUPPORTED   # group of 16
+    assert f(q, k, C.c_void_p((3 << 20) + 8), 8, 0, 9, 3, 64, 4096, o, None, 0, None) == B.LQ8_ERR_ARG
+
+
+def test_block_format_matvec_argument_checks_without_a_gpu(B):
+    """llama_q8_matvec_fmt refuses unsupported types, k off the block size,
+    unknown flags and misaligned buffers on the host; the packed size query
+    is 0 for those shapes."""
+    L = B.lib()
+    p, x, y = C.c_void_p(1 << 20), C.c_void_p(1 << 21), C.c_void_p(1 << 22)
+    q4_k, q5_0 = 12, 6
+    assert L.llama_q8_matvec_fmt(q4_k, p, 64, 128, x, y, 0, None) == B.LQ8_ERR_ARG         # k % 256
+    assert L.llama_q8_matvec_fmt(q5_0, p, 64, 48, x, y, 0, None) == B.LQ8_ERR_ARG          # k % 32
+    assert L.llama_q8_matvec_fmt(2, p, 64, 256, x, y, 0, None) == B.LQ8_ERR_UNSUPPORTED    # Q4_0: not built
+    assert L.llama_q8_matvec_fmt(q4_k, p, 64, 256, x, y, 4, None) == B.LQ8_ERR_ARG         # unknown flag
+    assert L.llama_q8_matvec_fmt(q4_k, C.c_void_p((1 << 20) + 4), 64, 256, x, y, 0, None) == B.LQ8_ERR_ARG
+    assert L.llama_q8_packed_bytes_fmt(q4_k, 64, 128) == 0
+    assert L.llama_q8_packed_bytes_fmt(2, 64, 256) == 0
+    assert L.llama_q8_packed_bytes_fmt(q4_k, 64, 256) > 0
